@@ -1,0 +1,238 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: attention over a paged KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow three FlashInfer API pages:
+ *   [append]  flashinfer.page.append_paged_kv_cache (signature, parameters,
+ *             worked example, note that the space is reserved beforehand);
+ *   [decode]  flashinfer.decode.trtllm_batch_decode_with_kv_cache
+ *             (signature and parameter list);
+ *   [prefill] flashinfer.prefill.cudnn_batch_prefill_with_kv_cache
+ *             (signature, parameter list, returns, note on head sizes).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is caller-owned.  Tensor arguments are DEVICE
+ *    pointers on the current CUDA device; scalars are passed by value.  The
+ *    library allocates and frees no memory and keeps no per-call state; the
+ *    only global is a launch counter for diagnostics.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All device work is enqueued on it and the call returns without
+ *    synchronising.  Argument errors are detected on the host and returned
+ *    before anything is launched.
+ *  - Return value: a pkv_status.  PKV_ERR_CUDA means a launch failed; the
+ *    CUDA error is left for cudaGetLastError-style inspection by the caller.
+ *  - `err_word` (optional, may be NULL) is one device int32.  Kernels OR
+ *    PKV_DEV_ERR_* bits into it when an index read from device memory is out
+ *    of range; the offending read or write is skipped and nothing traps.  The
+ *    caller clears it.
+ *  - 16-bit elements: dtype PKV_F16 (IEEE half) or PKV_BF16.  Attention
+ *    accumulates in fp32 and rounds the output to nearest-even in the input
+ *    dtype; LSE is fp32, natural log.
+ *  - Layouts (both pages list the same two):
+ *      PKV_HND: a page is [num_kv_heads][page_size][head_dim];
+ *      PKV_NHD: a page is [page_size][num_kv_heads][head_dim].
+ *    There is no default: the decode page defaults to HND, the append page
+ *    to NHD, so the caller always says which.
+ *  - A cache is passed as two base pointers (K pages, V pages) and a page
+ *    stride in elements.  The 5-D form [pages, 2, ...] is k = base,
+ *    v = base + num_kv_heads * page_size * head_dim, stride = 2 * that; the
+ *    tuple form is two tensors with stride num_kv_heads*page_size*head_dim.
+ *    Element (page, head, slot, d) lives at
+ *      HND: page * stride + (head * page_size + slot) * head_dim + d
+ *      NHD: page * stride + (slot * num_kv_heads + head) * head_dim + d.
+ *  - Alignment: every 16-bit tensor base and page stride must be a multiple
+ *    of 16 bytes (8 elements), else PKV_ERR_INVALID_ARG.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_NULL = 1,        /* a required pointer is NULL                   */
+    PKV_ERR_INVALID_ARG = 2, /* bad enum, size, ratio or alignment           */
+    PKV_ERR_UNSUPPORTED = 3, /* valid but not compiled (head dim, page size) */
+    PKV_ERR_WORKSPACE = 4,   /* workspace smaller than the size query says   */
+    PKV_ERR_CUDA = 5         /* a kernel launch failed                       */
+} pkv_status;
+
+enum { PKV_NHD = 0, PKV_HND = 1 };
+enum { PKV_F16 = 0, PKV_BF16 = 1 };
+
+/* bits of the device error word */
+#define PKV_DEV_ERR_PAGE 1    /* physical page id outside [0, max_num_pages)        */
+#define PKV_DEV_ERR_POS 2     /* append position outside the request's reserved pages */
+#define PKV_DEV_ERR_BATCH 4   /* append batch index outside [0, batch_size)         */
+#define PKV_DEV_ERR_QLEN 8    /* kv length shorter than the query length            */
+#define PKV_DEV_ERR_TIMEOUT 16 /* a bounded pipeline wait gave up; output invalid   */
+
+/* Human-readable name of a pkv_status value (static string). */
+const char *pkv_status_string(int status);
+
+/* Number of kernels this library has launched in this process. */
+unsigned long long pkv_kernel_launches(void);
+
+/*
+ * paged_seq_lens -- [append] worked example, `get_seq_lens` and the comments
+ * "45 = (3 - 1) * 16 + 13" ...: the kv length of each request from its page
+ * count and the fill of its last page,
+ *   seq_lens[b] = (kv_indptr[b+1] - kv_indptr[b] - 1) * page_size
+ *                 + kv_last_page_len[b]          (0 for a request with no page).
+ *   kv_indptr [batch_size+1], kv_last_page_len [batch_size], seq_lens
+ *   [batch_size] (output); all int32, device.
+ */
+int paged_seq_lens(const int32_t *kv_indptr, const int32_t *kv_last_page_len,
+                   int32_t batch_size, int32_t page_size, int32_t *seq_lens,
+                   void *stream);
+
+/*
+ * paged_batch_indices_positions -- [append] worked example,
+ * `get_batch_indices_positions` and its printed output: for appended entry
+ * i of request b (append_indptr[b] <= i < append_indptr[b+1]),
+ *   batch_indices[i] = b,
+ *   positions[i] = seq_lens[b] - (append_indptr[b+1] - append_indptr[b])
+ *                  + (i - append_indptr[b]),
+ * i.e. the new tokens are the last ones of each sequence because seq_lens
+ * already counts them ([append] note).  Entries i >= append_indptr[batch_size]
+ * get -1 in both outputs.  append_indptr must be non-decreasing.
+ *   append_indptr [batch_size+1], seq_lens [batch_size]; outputs [nnz];
+ *   int32, device.
+ */
+int paged_batch_indices_positions(const int32_t *append_indptr,
+                                  const int32_t *seq_lens, int32_t batch_size,
+                                  int64_t nnz, int32_t *batch_indices,
+                                  int32_t *positions, void *stream);
+
+/*
+ * paged_append -- [append] signature and parameters: scatter nnz new tokens
+ * into their reserved page slots.  For entry i with b = batch_indices[i],
+ * p = positions[i]:
+ *   page = kv_indices[kv_indptr[b] + p / page_size], slot = p % page_size,
+ *   k_cache[page, head, slot, :] = append_key[i, head, :]  (HND indexing; NHD
+ *   analogous), and the same for append_value into v_cache.
+ * Bits are copied unchanged (dtype only fixes the element size; both 16-bit
+ * types are accepted).  Nothing else in the pool is written.
+ *   append_key/value: [nnz, num_kv_heads, head_dim], contiguous.
+ *   batch_indices, positions: [nnz] int32 (from the helper above or the caller).
+ *   kv_indices [kv_indptr[batch_size]], kv_indptr [batch_size+1],
+ *   kv_last_page_len [batch_size]: int32.
+ * Device errors: b outside [0, batch_size) -> PKV_DEV_ERR_BATCH; p outside
+ * [0, seq_len(b)) -> PKV_DEV_ERR_POS; page outside [0, max_num_pages) ->
+ * PKV_DEV_ERR_PAGE; the entry is skipped.  Duplicate (b, p) pairs race.
+ * Host errors: head_dim % 8 != 0 or page_size <= 0 -> PKV_ERR_INVALID_ARG.
+ */
+int paged_append(const void *append_key, const void *append_value, int64_t nnz,
+                 const int32_t *batch_indices, const int32_t *positions,
+                 void *k_cache, void *v_cache, int64_t page_stride,
+                 int64_t max_num_pages, const int32_t *kv_indices,
+                 const int32_t *kv_indptr, const int32_t *kv_last_page_len,
+                 int32_t batch_size, int32_t num_kv_heads, int32_t head_dim,
+                 int32_t page_size, int32_t layout, int32_t dtype,
+                 int32_t *err_word, void *stream);
+
+/*
+ * paged_decode_workspace_size -- bytes of device workspace paged_decode needs
+ * for these sizes (split-KV partial outputs and their LSEs).  The decode
+ * page asks for a caller-provided workspace; this query sizes it exactly.
+ * Returns 0 for invalid sizes.
+ */
+size_t paged_decode_workspace_size(int32_t batch_size, int32_t q_len_per_req,
+                                   int32_t num_qo_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_seq_len,
+                                   int32_t page_size, int32_t window_left);
+
+/*
+ * paged_decode -- [decode] signature and parameters (query, kv_cache,
+ * workspace_buffer, block_tables, seq_lens, max_seq_len, bmm1_scale,
+ * bmm2_scale, window_left, sinks, kv_layout, q_len_per_req).  For request b
+ * with L = seq_lens[b] keys, query token t < Q = q_len_per_req (row b*Q + t
+ * of query/out) and qo head h:
+ *   kv head   = h / (num_qo_heads / num_kv_heads)      (consecutive groups)
+ *   position  p = L - Q + t        (the Q tokens are the last Q of the
+ *             sequence, causal among themselves)
+ *   keys      j with max(0, p - window_left) <= j <= p; window_left = -1
+ *             means all j <= p ("left, inclusive" window)
+ *   logits    s_j = bmm1_scale * <q, k_j>   (natural-exp softmax)
+ *   out       bmm2_scale * sum_j e^{s_j} v_j / (sum_j e^{s_j} + e^{sinks[h]})
+ *             (the sink term only when sinks != NULL; it has no value row)
+ *   lse       log(sum_j e^{s_j} + e^{sinks[h]})      (optional output)
+ * Key j of request b lives in page block_tables[b * block_table_stride +
+ * j / page_size], slot j % page_size; table entries at or beyond
+ * ceil(L / page_size) are never read.  An empty key set gives out = 0 and
+ * lse = -inf (lse = sink with a sink).
+ *   query/out: [batch_size*Q, num_qo_heads, head_dim] contiguous, dtype.
+ *   seq_lens: [batch_size] uint32 (decode page: "uint32 1D tensor"), each
+ *   <= max_seq_len.  sinks: [num_qo_heads] fp32 or NULL.  lse:
+ *   [batch_size*Q, num_qo_heads] fp32 or NULL.
+ *   workspace: >= paged_decode_workspace_size(...) bytes, 256-byte aligned.
+ * Supported: head_dim 128; page_size a power of two in [8, 256];
+ * num_qo_heads % num_kv_heads == 0 with (num_qo_heads/num_kv_heads) * Q <= 64.
+ * Device errors: bad page id -> PKV_DEV_ERR_PAGE (key treated as absent);
+ * L < Q -> PKV_DEV_ERR_QLEN (rows with p < 0 see no key).
+ */
+int paged_decode(const void *query, const void *k_cache, const void *v_cache,
+                 int64_t page_stride, int64_t max_num_pages, void *workspace,
+                 size_t workspace_bytes, const int32_t *block_tables,
+                 int32_t block_table_stride, const uint32_t *seq_lens,
+                 int32_t batch_size, int32_t max_seq_len, float bmm1_scale,
+                 float bmm2_scale, int32_t window_left, const float *sinks,
+                 int32_t q_len_per_req, int32_t num_qo_heads,
+                 int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                 int32_t layout, int32_t dtype, void *out, float *lse,
+                 int32_t *err_word, void *stream);
+
+/*
+ * paged_prefill_workspace_size -- bytes of device workspace paged_prefill
+ * needs (packed query offsets and the work list of query tiles).  The
+ * prefill page's workspace_buffer plays the same role.
+ */
+size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_qo_heads,
+                                    int32_t max_token_per_sequence,
+                                    int32_t max_sequence_kv);
+
+/*
+ * paged_prefill -- [prefill] signature, parameters and returns (q, k_cache,
+ * v_cache, scale, workspace_buffer, max_token_per_sequence, max_sequence_kv,
+ * actual_seq_lens_q, actual_seq_lens_kv, block_tables, causal, return_lse
+ * = true, out, lse).  Request b has q_b = actual_seq_lens_q[b] query tokens,
+ * packed at rows cu_q[b] .. cu_q[b] + q_b - 1 of q/out/lse (cu_q the
+ * exclusive prefix sum of the q lengths), and kv_b = actual_seq_lens_kv[b]
+ * keys.  Query i sits at position kv_b - q_b + i (the queries are the last
+ * q_b tokens); with causal it sees keys j <= that position, otherwise all
+ * j < kv_b.  With kvh = h / (num_qo_heads / num_kv_heads):
+ *   out[row, h, :] = softmax_j(scale * <q[row, h], k_j>) v_j
+ *   lse[row, h]    = log sum_j e^{scale * <q[row, h], k_j>}   (natural log)
+ *   q: [total_q, num_qo_heads, d_qk]; out: [total_q, num_qo_heads, d_vo];
+ *   lse: [total_q, num_qo_heads] fp32 (required: the page says return_lse
+ *   must be true).  k_cache pages hold d_qk-wide rows, v_cache pages d_vo-wide
+ *   rows, each with its own page stride.  actual_seq_lens_q/kv: [batch_size]
+ *   int32 on the device.  max_token_per_sequence / max_sequence_kv bound them.
+ *   workspace: >= paged_prefill_workspace_size(...) bytes, 256-byte aligned.
+ * Supported (prefill page note): d_qk in {128, 192}, d_vo = 128; page_size a
+ * power of two in [8, 256]; num_qo_heads % num_kv_heads == 0.
+ * Device errors: bad page id -> PKV_DEV_ERR_PAGE; kv_b < q_b ->
+ * PKV_DEV_ERR_QLEN (rows that see no key get out = 0, lse = -inf).
+ */
+int paged_prefill(const void *q, const void *k_cache, const void *v_cache,
+                  int64_t k_page_stride, int64_t v_page_stride,
+                  int64_t max_num_pages, float scale, void *workspace,
+                  size_t workspace_bytes, int32_t max_token_per_sequence,
+                  int32_t max_sequence_kv, const int32_t *actual_seq_lens_q,
+                  const int32_t *actual_seq_lens_kv, const int32_t *block_tables,
+                  int32_t block_table_stride, int32_t batch_size, int32_t causal,
+                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                  int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
+                  void *out, float *lse, int32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

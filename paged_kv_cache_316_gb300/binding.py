@@ -1,0 +1,255 @@
+"""Thin Python binding of libpagedkv.so (``include/pagedkv.h``).
+
+Argument marshalling only: every function derives sizes and strides from
+torch tensor shapes, passes device pointers and the current CUDA stream to
+the C entry point of the same name, and raises on a non-zero status.  No
+step of the computation happens here, and there is no CPU fallback: when the
+library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+NHD, HND = 0, 1
+F16, BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libpagedkv.so"
+_lib = None
+
+_c_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "pkv_kernel_launches": ([], ctypes.c_ulonglong),
+    "paged_seq_lens": ([_c_p, _c_p, _i32, _i32, _c_p, _c_p], ctypes.c_int),
+    "paged_batch_indices_positions": ([_c_p, _c_p, _i32, _i64, _c_p, _c_p, _c_p],
+                                      ctypes.c_int),
+    "paged_append": ([_c_p, _c_p, _i64, _c_p, _c_p, _c_p, _c_p, _i64, _i64, _c_p,
+                      _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32, _c_p, _c_p],
+                     ctypes.c_int),
+    "paged_decode_workspace_size": ([_i32] * 8, _sz),
+    "paged_decode": ([_c_p, _c_p, _c_p, _i64, _i64, _c_p, _sz, _c_p, _i32, _c_p,
+                      _i32, _i32, _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32,
+                      _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
+    "paged_prefill_workspace_size": ([_i32] * 4, _sz),
+    "paged_prefill": ([_c_p, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _sz, _i32,
+                       _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
+                       _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
+}
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load_library():
+    """Load libpagedkv.so from the package directory (raises if missing)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise PagedKVError(
+                f"{path} is not built: run `python -m paged_kv_cache_316_gb300.build` "
+                "(nvcc, sm_103a) first; there is no fallback implementation")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def kernel_launches() -> int:
+    return int(load_library().pkv_kernel_launches())
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load_library().pkv_status_string(status).decode()
+        raise PagedKVError(f"libpagedkv status {status}: {msg}")
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise PagedKVError("tensor arguments must live on a CUDA device")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise PagedKVError(f"unsupported element type {t.dtype}")
+
+
+def _layout_code(kv_layout) -> int:
+    if kv_layout in (NHD, "NHD"):
+        return NHD
+    if kv_layout in (HND, "HND"):
+        return HND
+    raise PagedKVError(f"kv_layout must be NHD or HND, got {kv_layout!r}")
+
+
+def split_cache(kv_cache, layout: int):
+    """(k_ptr, v_ptr, page_stride, num_pages, num_heads, page_size, head_dim)
+    for a 5-D [P, 2, ...] tensor or a (k, v) tuple of 4-D tensors."""
+    if isinstance(kv_cache, (tuple, list)):
+        k, v = kv_cache
+        if k.shape != v.shape or k.stride(0) != v.stride(0):
+            raise PagedKVError("K and V caches must have the same shape and page stride")
+        base = k
+        kp, vp = k.data_ptr(), v.data_ptr()
+        for t in (k, v):
+            if not t[0].is_contiguous():
+                raise PagedKVError("each page must be contiguous")
+        shape = k.shape[1:]
+    else:
+        if kv_cache.dim() != 5 or kv_cache.shape[1] != 2:
+            raise PagedKVError("a single kv_cache tensor must be [pages, 2, ...]")
+        if not kv_cache[0].is_contiguous():
+            raise PagedKVError("each page must be contiguous")
+        base = kv_cache
+        kp = kv_cache.data_ptr()
+        vp = kv_cache[:, 1].data_ptr()
+        shape = kv_cache.shape[2:]
+    _ptr(base)
+    if layout == HND:
+        H, S, D = shape
+    else:
+        S, H, D = shape
+    return kp, vp, base.stride(0), base.shape[0], H, S, D, base
+
+
+# ---- index helpers ------------------------------------------------------------------
+
+def paged_seq_lens(kv_indptr, kv_last_page_len, page_size: int, seq_lens=None,
+                   stream=None):
+    B = kv_last_page_len.shape[0]
+    if seq_lens is None:
+        seq_lens = torch.empty(B, dtype=torch.int32, device=kv_indptr.device)
+    _check(load_library().paged_seq_lens(_ptr(kv_indptr), _ptr(kv_last_page_len), B,
+                                         page_size, _ptr(seq_lens), _stream(stream)))
+    return seq_lens
+
+
+def paged_batch_indices_positions(append_indptr, seq_lens, nnz: int,
+                                  batch_indices=None, positions=None, stream=None):
+    B = seq_lens.shape[0]
+    dev = append_indptr.device
+    if batch_indices is None:
+        batch_indices = torch.empty(nnz, dtype=torch.int32, device=dev)
+    if positions is None:
+        positions = torch.empty(nnz, dtype=torch.int32, device=dev)
+    _check(load_library().paged_batch_indices_positions(
+        _ptr(append_indptr), _ptr(seq_lens), B, nnz, _ptr(batch_indices),
+        _ptr(positions), _stream(stream)))
+    return batch_indices, positions
+
+
+# ---- append -----------------------------------------------------------------------------
+
+def paged_append(append_key, append_value, batch_indices, positions, paged_kv_cache,
+                 kv_indices, kv_indptr, kv_last_page_len, kv_layout="NHD",
+                 err_word=None, stream=None) -> None:
+    layout = _layout_code(kv_layout)
+    kp, vp, stride, P, H, S, D, _ = split_cache(paged_kv_cache, layout)
+    nnz = append_key.shape[0]
+    if not (append_key.is_contiguous() and append_value.is_contiguous()):
+        raise PagedKVError("append_key/append_value must be contiguous")
+    _check(load_library().paged_append(
+        _ptr(append_key), _ptr(append_value), nnz, _ptr(batch_indices),
+        _ptr(positions), kp, vp, stride, P, _ptr(kv_indices), _ptr(kv_indptr),
+        _ptr(kv_last_page_len), kv_last_page_len.shape[0], H, D, S, layout,
+        _dtype_code(append_key), _ptr(err_word), _stream(stream)))
+
+
+# ---- decode -------------------------------------------------------------------------------
+
+def paged_decode_workspace_size(batch_size, q_len_per_req, num_qo_heads, num_kv_heads,
+                                head_dim, max_seq_len, page_size, window_left=-1) -> int:
+    return int(load_library().paged_decode_workspace_size(
+        batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
+        max_seq_len, page_size, window_left))
+
+
+def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len: int,
+                 bmm1_scale: float = 1.0, bmm2_scale: float = 1.0, window_left: int = -1,
+                 sinks=None, kv_layout="HND", q_len_per_req: int = 1, out=None,
+                 lse=None, err_word=None, stream=None):
+    """seq_lens: int32 (or uint32) tensor holding the unsigned kv lengths."""
+    layout = _layout_code(kv_layout)
+    kp, vp, stride, P, Hkv, S, D, _ = split_cache(kv_cache, layout)
+    rows, Hqo, Dq = query.shape
+    if Dq != D:
+        raise PagedKVError("query head_dim differs from the cache's")
+    B = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(query)
+    _check(load_library().paged_decode(
+        _ptr(query), kp, vp, stride, P, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(block_tables),
+        block_tables.stride(0), _ptr(seq_lens), B, max_seq_len, bmm1_scale,
+        bmm2_scale, window_left, _ptr(sinks), q_len_per_req, Hqo, Hkv, D, S,
+        layout, _dtype_code(query), _ptr(out), _ptr(lse), _ptr(err_word),
+        _stream(stream)))
+    return out
+
+
+# ---- prefill ---------------------------------------------------------------------------------
+
+def paged_prefill_workspace_size(batch_size, num_qo_heads, max_token_per_sequence,
+                                 max_sequence_kv) -> int:
+    return int(load_library().paged_prefill_workspace_size(
+        batch_size, num_qo_heads, max_token_per_sequence, max_sequence_kv))
+
+
+def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
+                  max_token_per_sequence: int, max_sequence_kv: int,
+                  actual_seq_lens_q, actual_seq_lens_kv, block_tables,
+                  causal: bool = True, out=None, lse=None, kv_layout="HND",
+                  err_word=None, stream=None):
+    layout = _layout_code(kv_layout)
+    total_q, Hqo, d_qk = q.shape
+    if layout == HND:
+        P, Hkv, S, dk = k_cache.shape
+        dv = v_cache.shape[3]
+    else:
+        P, S, Hkv, dk = k_cache.shape
+        dv = v_cache.shape[3]
+    if dk != d_qk:
+        raise PagedKVError("q head_dim differs from the key cache's")
+    if out is None:
+        out = torch.empty((total_q, Hqo, dv), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((total_q, Hqo), dtype=torch.float32, device=q.device)
+    B = actual_seq_lens_q.shape[0]
+    _check(load_library().paged_prefill(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
+        P, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        max_token_per_sequence, max_sequence_kv, _ptr(actual_seq_lens_q),
+        _ptr(actual_seq_lens_kv), _ptr(block_tables), block_tables.stride(0), B,
+        int(causal), Hqo, Hkv, d_qk, dv, S, layout, _dtype_code(q), _ptr(out),
+        _ptr(lse), _ptr(err_word), _stream(stream)))
+    return out, lse
