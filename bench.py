@@ -1,0 +1,520 @@
+"""Benchmark of the paged-KV hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step runs every operation of the path once, each on its own synthetic
+workload resident in HBM (inputs larger than L2, so no flush is needed):
+
+  index helpers + append  4096 requests, prefix U[0,256], append U[1,128],
+                          32 kv heads, head_dim 128, page 16, fp16, NHD
+  decode (Llama-shaped)   batch 64, kv U[512,8192], page 16, 32/8 heads, bf16, HND
+  decode (long context)   batch 256, lognormal kv (median 4096, cap 32768),
+                          page 64, 64/8 heads, window 4095, sinks, 4 query tokens
+  prefill d128 / d192     batch 16, q U[128,2048], prefix U[0,2048], page 32,
+                          32/8 heads, causal, LSE
+
+Each operation is bracketed by CUDA events on the launching stream.  The
+headline value is the Llama-shaped decode's algorithmic HBM bandwidth; the
+JSON line also carries every part's throughput, the roofline of the kernel
+that dominates the step, the oracle's CPU throughput on a bounded sample
+(cpu_baseline), and an end-to-end number through the public API with the
+query copied from pinned host memory and the output copied back.
+
+With --impl reference the same metric is measured for the fp64 CPU oracle
+on the host cores (bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = ("paged-KV attn: decode HBM GB/s, prefill TFLOP/s, append GB/s; "
+          "% of GB300 roofline")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD = ("hot-path step: helpers+append (4096 req, 32 kv heads, fp16, NHD) + "
+            "Llama-3-8B-shaped decode (B=64, kv U[512,8192], 32/8 heads, d128, page 16, HND) + "
+            "long-context decode (B=256, 64/8 heads, window 4095, sinks, Q=4, page 64) + "
+            "causal ragged prefill (B=16, 32/8 heads, page 32; d128 and d192/128); "
+            "headline = Llama-shaped decode")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---- algorithmic work per part ----------------------------------------------------------
+
+def decode_bytes(c) -> int:
+    """K and V rows each visible query row set needs (read once per kv head),
+    query, output, the block-table entries used and the lengths."""
+    Q, S = c.q_len_per_req, c.pool.page_size
+    kv_tok = 0
+    pages = 0
+    for L in c.pt.lengths:
+        lo = max(0, L - Q - c.window_left) if c.window_left >= 0 else 0
+        kv_tok += L - lo
+        pages += (L + S - 1) // S - lo // S
+    row = c.num_kv_heads * c.head_dim * 2
+    qo = 2 * c.query.numel() * 2
+    return kv_tok * row * 2 + qo + pages * 4 + len(c.pt.lengths) * 4
+
+
+def append_bytes(c) -> int:
+    nnz, H, D = c.append_key.shape
+    return nnz * (2 * 2 * H * D * 2 + 8)
+
+
+def prefill_flops(c) -> int:
+    tot = 0
+    for q, kv in zip(c.seq_lens_q.tolist(), c.seq_lens_kv.tolist()):
+        pre = kv - q
+        pairs = q * pre + q * (q + 1) // 2 if c.causal else q * kv
+        tot += pairs
+    return 2 * (c.d_qk + c.d_vo) * c.num_qo_heads * tot
+
+
+# ---- clocks ---------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = sorted({n for _, _, fl in rows for n, f in zip(names, fl) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows), "reasons": seen}
+
+
+# ---- distributed plumbing -----------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, ws: int, dev) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(x: float, ws: int, dev) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- our arm ----------------------------------------------------------------------------------------
+
+class Part:
+    def __init__(self, name, fn, work, unit, bound, kernel):
+        self.name, self.fn, self.work, self.unit, self.bound = name, fn, work, unit, bound
+        self.kernel = kernel  # source file of the dominant kernel of this part
+        self.ms = []
+
+
+def make_parts(rank: int, dev):
+    import paged_kv_cache_316_gb300 as pk
+    from paged_kv_cache_316_gb300 import workloads as wl
+    parts = []
+    seed_off = 1000 * rank
+
+    # index helpers + append
+    ap = wl.append_sweep(4096, seed=1 + seed_off, layout=wl.NHD, device=dev, fill="empty")
+    ak, av = ap.append_key, ap.append_value
+    kvi, kvp, last = (x.to(dev) for x in (ap.kv_indices, ap.kv_indptr, ap.kv_last_page_len))
+    aind = ap.append_indptr.to(dev)
+    nnz = ak.shape[0]
+    seq = torch.empty(4096, dtype=torch.int32, device=dev)
+    bi = torch.empty(nnz, dtype=torch.int32, device=dev)
+    pos = torch.empty(nnz, dtype=torch.int32, device=dev)
+    pool = ap.pool.storage[0]
+
+    def run_helpers():
+        pk.paged_seq_lens(kvp, last, 16, seq)
+        pk.paged_batch_indices_positions(aind, seq, nnz, bi, pos)
+
+    def run_append():
+        pk.paged_append(ak, av, bi, pos, pool, kvi, kvp, last, kv_layout="NHD")
+
+    run_helpers()
+    parts.append(Part("index_helpers", run_helpers, 4096 * 12 + nnz * 8 + 4097 * 4, "GB/s",
+                      "hbm", "append.cu"))
+    parts.append(Part("append", run_append, append_bytes(ap), "GB/s", "hbm", "append.cu"))
+
+    def decode_part(name, c):
+        kv = c.pool.storage[0]
+        B = len(c.pt.lengths)
+        ws = torch.zeros(max(1, pk.paged_decode_workspace_size(
+            B, c.q_len_per_req, c.num_qo_heads, c.num_kv_heads, 128, c.max_seq_len,
+            c.pool.page_size, c.window_left)), dtype=torch.uint8, device=dev)
+        bt, sl = c.block_tables.to(dev), c.seq_lens.to(dev)
+        sinks = None if c.sinks is None else c.sinks.to(dev)
+        out = torch.empty_like(c.query)
+
+        def run():
+            pk.paged_decode(c.query, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=c.bmm1_scale,
+                            bmm2_scale=c.bmm2_scale, window_left=c.window_left, sinks=sinks,
+                            kv_layout="HND", q_len_per_req=c.q_len_per_req, out=out)
+        p = Part(name, run, decode_bytes(c), "GB/s", "hbm", "decode.cu")
+        p.case, p.ws, p.bt, p.sl, p.sinks = c, ws, bt, sl, sinks
+        return p
+
+    llama = wl.llama_decode(seed=0 + seed_off, device=dev)
+    parts.append(decode_part("decode_llama", llama))
+    parts.append(decode_part("decode_long", wl.long_decode(seed=0 + seed_off, device=dev)))
+
+    for dqk in (128, 192):
+        c = wl.ragged_prefill(seed=0 + seed_off, d_qk=dqk, device=dev)
+        ws = torch.zeros(pk.paged_prefill_workspace_size(16, 32, c.max_q, c.max_kv),
+                         dtype=torch.uint8, device=dev)
+        lq, lkv, bt = c.seq_lens_q.to(dev), c.seq_lens_kv.to(dev), c.block_tables.to(dev)
+        out = torch.empty((c.q.shape[0], 32, 128), dtype=c.q.dtype, device=dev)
+        lse = torch.empty((c.q.shape[0], 32), dtype=torch.float32, device=dev)
+
+        def run(c=c, ws=ws, lq=lq, lkv=lkv, bt=bt, out=out, lse=lse):
+            pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv,
+                             bt, causal=True, out=out, lse=lse, kv_layout="HND")
+        parts.append(Part(f"prefill_d{dqk}", run, prefill_flops(c), "TFLOP/s", "tensor",
+                          "prefill.cu"))
+    return parts
+
+
+def traffic_for(kernel_file: str, part: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(path))
+        e = d[part]
+        src = os.path.join(ROOT, "paged_kv_cache_316_gb300", "csrc", kernel_file)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return e["dram_bytes_per_launch"] if e.get("src_sha") == sha else None
+    except Exception:
+        return None
+
+
+def cpu_baseline_decode(llama_part, budget_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the Llama-shaped
+    decode (a few requests, all heads), repeated until ~budget_s of CPU work."""
+    import oracle
+    from paged_kv_cache_316_gb300 import workloads as wl
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    c = llama_part.case
+    requests = [0, 1, 2, 3]
+    subs = []
+    for b in requests:
+        pages = c.pt.pages[b]
+        idx = torch.tensor(pages, dtype=torch.long, device=c.pool.k.device)
+        k = c.pool.k.index_select(0, idx).cpu().contiguous()
+        v = c.pool.v.index_select(0, idx).cpu().contiguous()
+        L = c.pt.lengths[b]
+        q = c.query[b:b + 1].cpu().contiguous()
+        bt = np.arange(len(pages), dtype=np.int32)[None, :]
+        subs.append((q, k, v, L, bt))
+    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    nbytes = 0
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        for q, k, v, L, bt in subs:
+            oracle.decode(u16(q), u16(k), u16(v), k[0].numel(), k.shape[0], bt,
+                          np.array([L], np.uint32), L, c.bmm1_scale, 1.0, -1, None, 1, 32, 8,
+                          128, 16, wl.HND, wl.BF16)
+            nbytes += L * 8 * 128 * 2 * 2 + 2 * 32 * 128 * 2 + ((L + 15) // 16) * 4 + 4
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle decode of requests {requests} (all 32 heads, full kv length) "
+                      f"of the Llama-shaped decode, {reps} repetitions, {el:.1f} s"}
+
+
+def e2e_decode(part, steps: int, dev):
+    """Decode through the public API with the query copied from pinned host
+    memory and the output copied back to pinned host memory, every step."""
+    import paged_kv_cache_316_gb300 as pk
+    c = part.case
+    hq = c.query.cpu().pin_memory()
+    hbt = c.block_tables.cpu().pin_memory()
+    hsl = c.seq_lens.cpu().pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    dq = torch.empty_like(c.query)
+    dbt, dsl = torch.empty_like(part.bt), torch.empty_like(part.sl)
+    kv = c.pool.storage[0]
+    dout = torch.empty_like(c.query)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dsl.copy_(hsl, non_blocking=True)
+        pk.paged_decode(dq, kv, part.ws, dbt, dsl, c.max_seq_len, bmm1_scale=c.bmm1_scale,
+                        kv_layout="HND", out=dout)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
+    return ms, h2d, hout.numel() * 2
+
+
+def run_ours(args):
+    ws, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from paged_kv_cache_316_gb300 import build as _build
+    if rank == 0 or ws == 1:
+        _build.build()
+    barrier(ws)
+    import paged_kv_cache_316_gb300 as pk
+
+    parts = make_parts(rank, dev)
+    st = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for p in parts:
+            p.fn()
+    torch.cuda.synchronize()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in parts] for _ in range(args.steps)]
+    launches0 = pk.kernel_launches()
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(st)
+        for s in range(args.steps):
+            for i, p in enumerate(parts):
+                ev[s][i][0].record(st)
+                p.fn()
+                ev[s][i][1].record(st)
+        t1.record(st)
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = pk.kernel_launches() - launches0
+    total_ms = t0.elapsed_time(t1)
+    for i, p in enumerate(parts):
+        p.ms = [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
+    total_ms = allreduce_max(total_ms, ws, dev)
+
+    pk_peaks, peak_src = peaks()
+    out_parts = {}
+    for p in parts:
+        mean_ms = allreduce_max(sum(p.ms) / len(p.ms), ws, dev)
+        work = allreduce_sum(float(p.work), ws, dev)
+        if p.unit == "GB/s":
+            val = work / (mean_ms * 1e-3) / 1e9
+            peak = pk_peaks["hbm_gbs"]
+        else:
+            val = work / (mean_ms * 1e-3) / 1e12
+            peak = pk_peaks["bf16_tflops"]
+        out_parts[p.name] = {"value": round(val, 2), "unit": p.unit, "ms": round(mean_ms, 4),
+                             "work": int(work), "roofline_frac": round(val / peak / ws, 4)}
+    step_ms = total_ms / args.steps
+    dom = max(parts, key=lambda p: sum(p.ms))
+    d = out_parts[dom.name]
+    per_launch_work = dom.work
+    ach = (per_launch_work / (d["ms"] * 1e-3)) / (1e9 if dom.unit == "GB/s" else 1e12)
+    peak = pk_peaks["hbm_gbs"] if dom.unit == "GB/s" else pk_peaks["bf16_tflops"]
+    roofline = {"kernel": dom.name, "bound": dom.bound, "achieved": round(ach, 2), "peak": peak,
+                "unit": dom.unit, "frac": round(ach / peak, 4),
+                "peak_source": f"{peak_src} ({'hbm_gbs' if dom.unit == 'GB/s' else 'bf16_tflops'})",
+                "traffic": traffic_for(dom.kernel, dom.name)}
+
+    llama = next(p for p in parts if p.name == "decode_llama")
+    e2e_ms, h2d, d2h = e2e_decode(llama, max(10, args.steps // 4), dev)
+    e2e_ms = allreduce_max(e2e_ms, ws, dev)
+    value = out_parts["decode_llama"]["value"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{ws} (independent requests)",
+                   "l2": "no flush: every part's inputs exceed the 129 MB L2",
+                   "headline_part": "decode_llama"},
+        "parts": out_parts, "roofline": roofline,
+        "e2e": {"value": round(allreduce_sum(float(llama.work), ws, dev) / (e2e_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4),
+                "what": "paged_decode through the Python API; query, block table and lengths "
+                        "copied from pinned host memory and the output copied back each step"},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(llama)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores, on bounded samples of
+    the Llama-shaped decode (2 requests, all heads, per step)."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_316_gb300 import workloads as wl
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    c = wl.llama_decode(seed=0, device=dev)
+    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    samples = []
+    for b in range(len(c.pt.lengths)):
+        pages = c.pt.pages[b]
+        idx = torch.tensor(pages, dtype=torch.long, device=c.pool.k.device)
+        k = c.pool.k.index_select(0, idx).cpu().contiguous()
+        v = c.pool.v.index_select(0, idx).cpu().contiguous()
+        samples.append((c.query[b:b + 1].cpu().contiguous(), k, v, c.pt.lengths[b]))
+
+    def step(i):
+        nb = 0
+        for j in range(2):
+            q, k, v, L = samples[(2 * i + j) % len(samples)]
+            bt = np.arange(k.shape[0], dtype=np.int32)[None, :]
+            oracle.decode(u16(q), u16(k), u16(v), k[0].numel(), k.shape[0], bt,
+                          np.array([L], np.uint32), L, c.bmm1_scale, 1.0, -1, None, 1, 32, 8,
+                          128, 16, wl.HND, wl.BF16)
+            nb += L * 8 * 128 * 2 * 2 + 2 * 32 * 128 * 2 + ((L + 15) // 16) * 4 + 4
+        return nb
+
+    for i in range(args.warmup):
+        step(i)
+    tot_b, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        tot_b += step(args.warmup + i)
+    el = time.perf_counter() - t0
+    val = tot_b / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "headline_part": "decode_llama",
+                       "reference": "fp64 CPU oracle (the pages ship no code to run)"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "kind": "oracle",
+                             "cores": oracle.max_threads(),
+                             "sample": "per step: 2 requests of the Llama-shaped decode "
+                                       "(all 32 heads, full kv length), fp64 oracle"},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

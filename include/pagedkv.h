@@ -72,6 +72,7 @@ enum { PKV_F16 = 0, PKV_BF16 = 1 };
 #define PKV_DEV_ERR_BATCH 4   /* append batch index outside [0, batch_size)         */
 #define PKV_DEV_ERR_QLEN 8    /* kv length shorter than the query length            */
 #define PKV_DEV_ERR_TIMEOUT 16 /* a bounded pipeline wait gave up; output invalid   */
+#define PKV_DEV_ERR_LEN 32    /* a length exceeds the stated maximum; it is clamped  */
 
 /* Human-readable name of a pkv_status value (static string). */
 const char *pkv_status_string(int status);
@@ -172,6 +173,9 @@ size_t paged_decode_workspace_size(int32_t batch_size, int32_t q_len_per_req,
  *   <= max_seq_len.  sinks: [num_qo_heads] fp32 or NULL.  lse:
  *   [batch_size*Q, num_qo_heads] fp32 or NULL.
  *   workspace: >= paged_decode_workspace_size(...) bytes, 256-byte aligned.
+ *   block_table_stride >= ceil(max_seq_len / page_size), else
+ *   PKV_ERR_INVALID_ARG.  A seq_lens entry above max_seq_len sets
+ *   PKV_DEV_ERR_LEN and is treated as max_seq_len.
  * Supported: head_dim 128; page_size a power of two in [8, 256];
  * num_qo_heads % num_kv_heads == 0 with (num_qo_heads/num_kv_heads) * Q <= 64.
  * Device errors: bad page id -> PKV_DEV_ERR_PAGE (key treated as absent);
@@ -215,6 +219,9 @@ size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_qo_heads,
  *   rows, each with its own page stride.  actual_seq_lens_q/kv: [batch_size]
  *   int32 on the device.  max_token_per_sequence / max_sequence_kv bound them.
  *   workspace: >= paged_prefill_workspace_size(...) bytes, 256-byte aligned.
+ *   block_table_stride >= ceil(max_sequence_kv / page_size), else
+ *   PKV_ERR_INVALID_ARG.  A length above its maximum sets PKV_DEV_ERR_LEN
+ *   and is clamped to it.
  * Supported (prefill page note): d_qk in {128, 192}, d_vo = 128; page_size a
  * power of two in [8, 256]; num_qo_heads % num_kv_heads == 0.
  * Device errors: bad page id -> PKV_DEV_ERR_PAGE; kv_b < q_b ->

@@ -1,0 +1,557 @@
+// decode.cu -- split-KV GQA batch decode over a paged KV cache.
+//
+// Computes what flashinfer.decode.trtllm_batch_decode_with_kv_cache
+// documents (parameters query, kv_cache, workspace_buffer, block_tables,
+// seq_lens, max_seq_len, bmm1_scale, bmm2_scale, window_left, sinks,
+// kv_layout, q_len_per_req): for every request, kv head and split of its
+// visible key range, one CTA streams the split's K/V rows through a
+// cp.async ring in shared memory and keeps an online softmax; a second
+// kernel merges the splits by their log-sum-exp and adds the sink term.
+//
+// Row packing: the group = Hqo / Hkv query heads that share a kv head and
+// the Q query tokens of a request form R = group * Q rows, padded to
+// 16 * MT rows of one mma.sync m16n8k16 A operand, so each K/V row read
+// from HBM feeds every query row that needs it.
+#include <math.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+constexpr int kDecD = 128;                        // head_dim
+constexpr int kDecTile = 64;                      // keys per pipeline stage
+constexpr int kDecStages = 3;
+constexpr int kDecThreads = 128;
+constexpr int kDecRowBytes = kDecD * 2;           // one K or V row
+constexpr int kDecTileBytes = kDecTile * kDecRowBytes;
+constexpr int kDecStageBytes = 2 * kDecTileBytes; // K tile then V tile
+
+struct DecodeParams {
+    const void *q;
+    const void *k;
+    const void *v;
+    int64_t page_stride;
+    int64_t max_num_pages;
+    const int32_t *block_tables;
+    int64_t bt_stride;
+    const uint32_t *seq_lens;
+    int B;
+    int max_seq_len;
+    float scale_log2;  // bmm1_scale * log2(e): logits in base-2 units
+    float bmm2;
+    int window_left;
+    const float *sinks;
+    int Q, Hqo, Hkv, group, R;
+    int page_shift;
+    int chunk;        // keys per split
+    int n_split_max;  // split slots per (request, kv head) in the workspace
+    void *out;
+    float *lse;
+    float *ws_o;      // [B][Hkv][n_split_max][R][128] normalised partial outputs
+    float *ws_lse;    // [B][Hkv][n_split_max][R] partial log2-sum-exp
+    int32_t *err;
+};
+
+// Lowest visible key `lo` of a request and how its range [lo, L) is cut into
+// splits: split s covers keys [max(lo, (first + s) * chunk), min(L, (first +
+// s + 1) * chunk)).  An empty request keeps one split so its rows are written.
+__host__ __device__ inline void decode_split_geometry(int L, int Q, int window_left, int chunk,
+                                                      int &lo, int &first, int &n_split) {
+    lo = 0;
+    if (window_left >= 0) {
+        lo = L - Q - window_left;
+        if (lo < 0) lo = 0;
+    }
+    if (L <= lo) {
+        first = 0;
+        n_split = 1;
+        return;
+    }
+    first = lo / chunk;
+    n_split = (L + chunk - 1) / chunk - first;
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T *dst, float a, float b, float c, float d) {
+    uint2 v;
+    v.x = pack2<T>(a, b);
+    v.y = pack2<T>(c, d);
+    *reinterpret_cast<uint2 *>(dst) = v;
+}
+
+template <typename T, int MT, int LAYOUT>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const DecodeParams p) {
+    constexpr int NKG = 4 / MT;          // warps that split the keys of a tile
+    constexpr int KPW = kDecTile / NKG;  // keys per warp per tile
+    constexpr int NT = KPW / 8;          // 8-key score tiles per warp
+    constexpr int ROWS = 16 * MT;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *q_s = smem + kDecStages * kDecStageBytes;
+    uint8_t *kvalid = q_s + ROWS * kDecRowBytes;
+    float *comb_m = reinterpret_cast<float *>(kvalid + kDecStages * kDecTile);
+    float *comb_l = comb_m + NKG * ROWS;
+    __shared__ int any_bad;
+
+    const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int mt = warp % MT, kg = warp / MT;
+    const uint32_t L_in = p.seq_lens[b];
+    const int L = L_in > static_cast<uint32_t>(p.max_seq_len) ? p.max_seq_len : static_cast<int>(L_in);
+    if (L_in > static_cast<uint32_t>(p.max_seq_len) && s == 0 && kvh == 0 && threadIdx.x == 0)
+        set_err(p.err, PKV_DEV_ERR_LEN);
+    const int Q = p.Q;
+    int lo, first, n_split;
+    decode_split_geometry(L, Q, p.window_left, p.chunk, lo, first, n_split);
+    if (s >= n_split) return;
+    if (L < Q && s == 0 && kvh == 0 && tid == 0) set_err(p.err, PKV_DEV_ERR_QLEN);
+    const int k_begin = max(lo, (first + s) * p.chunk);
+    const int k_end = min(L, (first + s + 1) * p.chunk);
+    const int n_tiles = k_end > k_begin ? (k_end - k_begin + kDecTile - 1) / kDecTile : 0;
+
+    const T *kc = static_cast<const T *>(p.k);
+    const T *vc = static_cast<const T *>(p.v);
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
+    const int S = 1 << p.page_shift;
+    if (tid == 0) any_bad = 0;
+    __syncthreads();
+
+    // Two threads per key row, 8 x 16 B each, for K and V.  Rows past the
+    // split end or on an out-of-range page are zero-filled and never read
+    // from global memory; kvalid records which rows hold a key.
+    auto load_tile = [&](int stage, int j0) {
+        const int r = tid >> 1;
+        const int c0 = (tid & 1) * 8;
+        const int j = j0 + r;
+        bool ok = j < k_end;
+        const T *ks = kc, *vs = vc;
+        if (ok) {
+            int page = bt[j >> p.page_shift];
+            if (page < 0 || page >= p.max_num_pages) {
+                ok = false;
+                set_err(p.err, PKV_DEV_ERR_PAGE);
+                any_bad = 1;
+            } else {
+                int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
+                                                    S, kDecD);
+                ks = kc + off;
+                vs = vc + off;
+            }
+        }
+        if ((tid & 1) == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
+        const uint32_t dst = smem_u32(smem + stage * kDecStageBytes);
+#pragma unroll
+        for (int c = c0; c < c0 + 8; ++c) {
+            uint32_t o = swz(r, c, kDecRowBytes);
+            cp_async_16(dst + o, ks + c * 8, ok);
+            cp_async_16(dst + kDecTileBytes + o, vs + c * 8, ok);
+        }
+    };
+
+    // query rows r = t * group + i  ->  query[(b*Q + t), kvh*group + i, :]
+    const T *qp = static_cast<const T *>(p.q);
+    for (int idx = tid; idx < ROWS * 16; idx += kDecThreads) {
+        int r = idx >> 4, c = idx & 15;
+        bool ok = r < p.R;
+        const T *src = qp;
+        if (ok) {
+            int t = r / p.group, i = r - t * p.group;
+            src = qp + (static_cast<int64_t>(b * Q + t) * p.Hqo + kvh * p.group + i) * kDecD + c * 8;
+        }
+        cp_async_16(smem_u32(q_s) + swz(r, c, kDecRowBytes), src, ok);
+    }
+    cp_async_commit();
+#pragma unroll
+    for (int st = 0; st < kDecStages - 1; ++st) {
+        if (st < n_tiles) load_tile(st, k_begin + st * kDecTile);
+        cp_async_commit();
+    }
+    cp_async_wait<kDecStages - 1>();
+    __syncthreads();
+
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        ldsm_x4(qa[kk], smem_u32(q_s) + swz(16 * mt + (lane & 15), 2 * kk + (lane >> 4), kDecRowBytes));
+
+    // the two rows this lane holds in every accumulator fragment
+    const int r0 = 16 * mt + (lane >> 2), r1 = r0 + 8;
+    const int t0 = min(r0 / p.group, Q - 1), t1 = min(r1 / p.group, Q - 1);
+    const int pos0 = L - Q + t0, pos1 = L - Q + t1;
+    const int lo0 = p.window_left >= 0 ? max(0, pos0 - p.window_left) : 0;
+    const int lo1 = p.window_left >= 0 ? max(0, pos1 - p.window_left) : 0;
+    const int lo_max = p.window_left >= 0 ? max(0, L - 1 - p.window_left) : 0;
+    const int hi_min = min(L - Q, k_end - 1);
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int kw0 = kg * KPW;
+
+    for (int it = 0; it < n_tiles; ++it) {
+        cp_async_wait<kDecStages - 2>();
+        __syncthreads();
+        {
+            int nxt = it + kDecStages - 1;
+            if (nxt < n_tiles) load_tile(nxt % kDecStages, k_begin + nxt * kDecTile);
+            cp_async_commit();
+        }
+        const int stage = it % kDecStages;
+        const int j0 = k_begin + it * kDecTile;
+        const uint32_t kb = smem_u32(smem + stage * kDecStageBytes);
+        const uint32_t vb = kb + kDecTileBytes;
+
+        float sc[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                uint32_t bf[4];
+                int key = kw0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                ldsm_x4(bf, kb + swz(key, 2 * kk + ((lane >> 3) & 1), kDecRowBytes));
+                mma16816<T>(sc[2 * np], qa[kk], bf[0], bf[1]);
+                mma16816<T>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
+            }
+        }
+
+        const bool interior = !any_bad && j0 >= lo_max && j0 + kDecTile - 1 <= hi_min;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float x = sc[nt][e] * p.scale_log2;
+                if (!interior) {
+                    int jj = kw0 + nt * 8 + 2 * (lane & 3) + (e & 1);
+                    int j = j0 + jj;
+                    bool vis = kvalid[stage * kDecTile + jj] &&
+                               (e < 2 ? (j >= lo0 && j <= pos0) : (j >= lo1 && j <= pos1));
+                    if (!vis) x = -INFINITY;
+                }
+                sc[nt][e] = x;
+            }
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+            mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
+        float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][0] = fast_exp2(sc[nt][0] - base0);
+            sc[nt][1] = fast_exp2(sc[nt][1] - base0);
+            sc[nt][2] = fast_exp2(sc[nt][2] - base1);
+            sc[nt][3] = fast_exp2(sc[nt][3] - base1);
+            rs0 += sc[nt][0] + sc[nt][1];
+            rs1 += sc[nt][2] + sc[nt][3];
+        }
+        l0 = l0 * al0 + rs0;
+        l1 = l1 * al1 + rs1;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            o[i][0] *= al0;
+            o[i][1] *= al0;
+            o[i][2] *= al1;
+            o[i][3] *= al1;
+        }
+#pragma unroll
+        for (int ks = 0; ks < NT / 2; ++ks) {
+            uint32_t a[4];
+            a[0] = pack2<T>(sc[2 * ks][0], sc[2 * ks][1]);
+            a[1] = pack2<T>(sc[2 * ks][2], sc[2 * ks][3]);
+            a[2] = pack2<T>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+            a[3] = pack2<T>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+            const int key = kw0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int dp = 0; dp < 8; ++dp) {
+                uint32_t vf[4];
+                ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), kDecRowBytes));
+                mma16816<T>(o[2 * dp], a, vf[0], vf[1]);
+                mma16816<T>(o[2 * dp + 1], a, vf[2], vf[3]);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // combine the key groups of this CTA through shared memory
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    float *comb_o = reinterpret_cast<float *>(smem);  // [NKG][ROWS][128]
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+        int d = nd * 8 + 2 * (lane & 3);
+        *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r0) * kDecD + d]) = make_float2(o[nd][0], o[nd][1]);
+        *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r1) * kDecD + d]) = make_float2(o[nd][2], o[nd][3]);
+    }
+    if ((lane & 3) == 0) {
+        comb_m[kg * ROWS + r0] = m0;
+        comb_l[kg * ROWS + r0] = l0;
+        comb_m[kg * ROWS + r1] = m1;
+        comb_l[kg * ROWS + r1] = l1;
+    }
+    __syncthreads();
+
+    for (int idx = tid; idx < p.R * 32; idx += kDecThreads) {
+        const int r = idx >> 5, d = (idx & 31) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < NKG; ++g) M = fmaxf(M, comb_m[g * ROWS + r]);
+        const float Mb = M == -INFINITY ? 0.f : M;
+        float lsum = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int g = 0; g < NKG; ++g) {
+            float w = fast_exp2(comb_m[g * ROWS + r] - Mb);
+            lsum += w * comb_l[g * ROWS + r];
+            float4 x = *reinterpret_cast<const float4 *>(&comb_o[(g * ROWS + r) * kDecD + d]);
+            a0 += w * x.x;
+            a1 += w * x.y;
+            a2 += w * x.z;
+            a3 += w * x.w;
+        }
+        const int t = r / p.group, i = r - t * p.group, h = kvh * p.group + i;
+        if (n_split == 1) {
+            float sc_o, lse_v;
+            if (p.sinks) {
+                const float sk = p.sinks[h] * kLog2e;
+                const float Mf = fmaxf(M, sk);
+                const float wk = fast_exp2(M - Mf);
+                const float den = lsum * wk + fast_exp2(sk - Mf);
+                sc_o = p.bmm2 * wk / den;
+                lse_v = (Mf + fast_log2(den)) * kLn2;
+            } else if (lsum > 0.f) {
+                sc_o = p.bmm2 / lsum;
+                lse_v = (M + fast_log2(lsum)) * kLn2;
+            } else {
+                sc_o = 0.f;
+                lse_v = -INFINITY;
+            }
+            const int64_t orow = static_cast<int64_t>(b * Q + t) * p.Hqo + h;
+            store4(static_cast<T *>(p.out) + orow * kDecD + d, a0 * sc_o, a1 * sc_o, a2 * sc_o, a3 * sc_o);
+            if (p.lse && d == 0) p.lse[orow] = lse_v;
+        } else {
+            const int64_t prow =
+                (static_cast<int64_t>(b * p.Hkv + kvh) * p.n_split_max + s) * p.R + r;
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            *reinterpret_cast<float4 *>(p.ws_o + prow * kDecD + d) =
+                make_float4(a0 * inv, a1 * inv, a2 * inv, a3 * inv);
+            if (d == 0) p.ws_lse[prow] = lsum > 0.f ? M + fast_log2(lsum) : -INFINITY;
+        }
+    }
+}
+
+// One warp per output row (b*Q + t, h): weights the split partials by
+// 2^lse_s, adds the sink to the denominator, applies bmm2_scale.
+template <typename T>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+    if (row >= static_cast<int64_t>(p.B) * p.Q * p.Hqo) return;
+    const int h = static_cast<int>(row % p.Hqo);
+    const int64_t bq = row / p.Hqo;
+    const int t = static_cast<int>(bq % p.Q), b = static_cast<int>(bq / p.Q);
+    const uint32_t L_in = p.seq_lens[b];
+    const int L = L_in > static_cast<uint32_t>(p.max_seq_len) ? p.max_seq_len : static_cast<int>(L_in);
+    int lo, first, n_split;
+    decode_split_geometry(L, p.Q, p.window_left, p.chunk, lo, first, n_split);
+    if (n_split <= 1) return;  // the split kernel wrote this row itself
+    const int kvh = h / p.group;
+    const int r = t * p.group + (h - kvh * p.group);
+    const int64_t base = static_cast<int64_t>(b * p.Hkv + kvh) * p.n_split_max * p.R + r;
+    float M = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, p.ws_lse[base + static_cast<int64_t>(s) * p.R]);
+    const int d = lane * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < n_split; ++s) {
+            const int64_t prow = base + static_cast<int64_t>(s) * p.R;
+            const float w = fast_exp2(p.ws_lse[prow] - M);
+            const float4 x = *reinterpret_cast<const float4 *>(p.ws_o + prow * kDecD + d);
+            den += w;
+            acc.x += w * x.x;
+            acc.y += w * x.y;
+            acc.z += w * x.z;
+            acc.w += w * x.w;
+        }
+        if (p.sinks) den += fast_exp2(p.sinks[h] * kLog2e - M);
+    }
+    const float sc = den > 0.f ? p.bmm2 / den : 0.f;
+    store4(static_cast<T *>(p.out) + row * kDecD + d, acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+    if (p.lse && lane == 0) p.lse[row] = den > 0.f ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+}
+
+struct DecodePlan {
+    int R, MT, chunk, n_split_max;
+    size_t ws_o_bytes, ws_bytes;
+};
+
+static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, int page_size,
+                       int window_left, DecodePlan &pl) {
+    if (B < 0 || Q < 1 || Hqo < 1 || Hkv < 1 || max_seq_len < 0 || window_left < -1)
+        return PKV_ERR_INVALID_ARG;
+    if (Hqo % Hkv) return PKV_ERR_INVALID_ARG;
+    if (B > 65535 || Hkv > 65535) return PKV_ERR_UNSUPPORTED;
+    if (D != kDecD) return PKV_ERR_UNSUPPORTED;
+    if (ilog2_exact(page_size) < 0 || page_size > 1024) return PKV_ERR_UNSUPPORTED;
+    const int group = Hqo / Hkv;
+    pl.R = group * Q;
+    if (pl.R > 64) return PKV_ERR_UNSUPPORTED;
+    pl.MT = pl.R <= 16 ? 1 : (pl.R <= 32 ? 2 : 4);
+    const int64_t span = window_left >= 0
+                             ? (static_cast<int64_t>(window_left) + Q < max_seq_len
+                                    ? static_cast<int64_t>(window_left) + Q
+                                    : max_seq_len)
+                             : max_seq_len;
+    // Larger row groups write larger partials: scale the chunk with R so the
+    // partial traffic stays a few percent of the K/V bytes; then shrink it
+    // while the grid would leave SMs idle.
+    int chunk = 64 * pl.R;
+    chunk = chunk < 512 ? 512 : (chunk > 4096 ? 4096 : chunk);
+    chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+    const int64_t want = 2LL * num_sms();
+    while (chunk > 4 * kDecTile &&
+           static_cast<int64_t>(B) * Hkv * ((span + chunk - 1) / chunk) < want)
+        chunk /= 2;
+    pl.chunk = chunk;
+    int64_t ns = span > 0 ? (span + chunk - 1) / chunk : 1;
+    if (window_left >= 0 && span > 0) ns += 1;  // a window start need not sit on a chunk edge
+    if (ns > 65535) return PKV_ERR_UNSUPPORTED;
+    pl.n_split_max = static_cast<int>(ns);
+    if (pl.n_split_max > 1) {
+        const size_t slots = static_cast<size_t>(B) * Hkv * pl.n_split_max * pl.R;
+        pl.ws_o_bytes = round_up(slots * kDecD * sizeof(float), 256);
+        pl.ws_bytes = pl.ws_o_bytes + round_up(slots * sizeof(float), 256);
+    } else {
+        pl.ws_o_bytes = pl.ws_bytes = 0;
+    }
+    return PKV_OK;
+}
+
+template <typename T, int MT, int LAYOUT>
+static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
+    constexpr int ROWS = 16 * MT, NKG = 4 / MT;
+    const size_t smem = kDecStages * kDecStageBytes + ROWS * kDecRowBytes + kDecStages * kDecTile +
+                        2 * NKG * ROWS * sizeof(float);
+    auto kern = decode_split_kernel<T, MT, LAYOUT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    kern<<<grid, kDecThreads, smem, st>>>(p);
+    return PKV_OK;
+}
+
+template <typename T, int LAYOUT>
+static int launch_split_mt(int MT, const DecodeParams &p, dim3 grid, cudaStream_t st) {
+    if (MT == 1) return launch_split<T, 1, LAYOUT>(p, grid, st);
+    if (MT == 2) return launch_split<T, 2, LAYOUT>(p, grid, st);
+    return launch_split<T, 4, LAYOUT>(p, grid, st);
+}
+
+template <typename T>
+static int run_decode(const DecodeParams &p, const DecodePlan &pl, int layout, cudaStream_t st) {
+    dim3 grid(pl.n_split_max, p.Hkv, p.B);
+    int rc = layout == PKV_HND ? launch_split_mt<T, PKV_HND>(pl.MT, p, grid, st)
+                               : launch_split_mt<T, PKV_NHD>(pl.MT, p, grid, st);
+    if (rc != PKV_OK) return rc;
+    int launches = 1;
+    if (pl.n_split_max > 1) {
+        int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hqo;
+        decode_merge_kernel<T><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(p);
+        ++launches;
+    }
+    note_launches(launches);
+    return launch_status();
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t paged_decode_workspace_size(int32_t batch_size, int32_t q_len_per_req,
+                                              int32_t num_qo_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t max_seq_len,
+                                              int32_t page_size, int32_t window_left) {
+    DecodePlan pl;
+    if (plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim, max_seq_len,
+                    page_size, window_left, pl) != PKV_OK)
+        return 0;
+    return pl.ws_bytes;
+}
+
+extern "C" int paged_decode(const void *query, const void *k_cache, const void *v_cache,
+                            int64_t page_stride, int64_t max_num_pages, void *workspace,
+                            size_t workspace_bytes, const int32_t *block_tables,
+                            int32_t block_table_stride, const uint32_t *seq_lens,
+                            int32_t batch_size, int32_t max_seq_len, float bmm1_scale,
+                            float bmm2_scale, int32_t window_left, const float *sinks,
+                            int32_t q_len_per_req, int32_t num_qo_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
+                            void *out, float *lse, int32_t *err_word, void *stream) {
+    if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    DecodePlan pl;
+    int rc = plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
+                         max_seq_len, page_size, window_left, pl);
+    if (rc != PKV_OK) return rc;
+    if (page_stride < static_cast<int64_t>(num_kv_heads) * page_size * head_dim || max_num_pages < 0 ||
+        static_cast<int64_t>(block_table_stride) * page_size < max_seq_len)
+        return PKV_ERR_INVALID_ARG;
+    if (batch_size == 0) return PKV_OK;
+    if (!query || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_NULL;
+    if (!aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (page_stride % 8))
+        return PKV_ERR_INVALID_ARG;
+    if (pl.ws_bytes > 0) {
+        if (!workspace) return PKV_ERR_NULL;
+        if (workspace_bytes < pl.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+            return PKV_ERR_WORKSPACE;
+    }
+    DecodeParams p;
+    p.q = query;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.page_stride = page_stride;
+    p.max_num_pages = max_num_pages;
+    p.block_tables = block_tables;
+    p.bt_stride = block_table_stride;
+    p.seq_lens = seq_lens;
+    p.B = batch_size;
+    p.max_seq_len = max_seq_len;
+    p.scale_log2 = bmm1_scale * kLog2e;
+    p.bmm2 = bmm2_scale;
+    p.window_left = window_left;
+    p.sinks = sinks;
+    p.Q = q_len_per_req;
+    p.Hqo = num_qo_heads;
+    p.Hkv = num_kv_heads;
+    p.group = num_qo_heads / num_kv_heads;
+    p.R = pl.R;
+    p.page_shift = ilog2_exact(page_size);
+    p.chunk = pl.chunk;
+    p.n_split_max = pl.n_split_max;
+    p.out = out;
+    p.lse = lse;
+    p.ws_o = pl.ws_bytes ? static_cast<float *>(workspace) : nullptr;
+    p.ws_lse = pl.ws_bytes ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.ws_o_bytes)
+                           : nullptr;
+    p.err = err_word;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return dtype == PKV_BF16 ? run_decode<__nv_bfloat16>(p, pl, layout, st)
+                             : run_decode<__half>(p, pl, layout, st);
+}

@@ -1,0 +1,125 @@
+"""The C ABI on a machine without a GPU: the library builds for sm_103a,
+loads, exports every entry point the header declares, and rejects bad
+arguments on the host before any launch.  Every call below is rejected by
+host validation (or has nothing to do), so the fake pointers it carries are
+never dereferenced and no kernel is launched, on any machine."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_316_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*?[\s\*]+(\w+)\s*\(",
+                                 text, flags=re.M)) - {"if", "defined"})
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ["paged_seq_lens", "paged_batch_indices_positions", "paged_append",
+              "paged_decode_workspace_size", "paged_decode", "paged_prefill_workspace_size",
+              "paged_prefill", "pkv_status_string", "pkv_kernel_launches"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libpagedkv.so does not export {name}"
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"ok"
+    assert b"workspace" in lib.pkv_status_string(4)
+
+
+def _append(lib, **over):
+    good = 0x1000  # any 16-byte aligned non-null value: these calls fail before use
+    args = dict(append_key=good, append_value=good, nnz=4, batch_indices=good, positions=good,
+                k_cache=good, v_cache=good, page_stride=2 * 8 * 16 * 128, max_num_pages=10,
+                kv_indices=good, kv_indptr=good, kv_last_page_len=good, batch_size=2,
+                num_kv_heads=8, head_dim=128, page_size=16, layout=0, dtype=0,
+                err_word=None, stream=None)
+    args.update(over)
+    return lib.paged_append(*args.values())
+
+
+def test_append_rejects_bad_arguments(lib):
+    assert _append(lib, layout=2) == 2
+    assert _append(lib, dtype=5) == 2
+    assert _append(lib, head_dim=12) == 2
+    assert _append(lib, page_stride=100) == 2
+    assert _append(lib, append_key=None) == 1
+    assert _append(lib, k_cache=0x1004) == 2      # misaligned
+    assert _append(lib, nnz=0, append_key=None) == 0  # nothing to do
+
+
+def test_decode_rejects_bad_arguments(lib):
+    good = 0x1000
+
+    def call(**over):
+        a = dict(query=good, k=good, v=good, stride=2 * 8 * 16 * 128, pages=64, ws=good,
+                 ws_bytes=1 << 30, bt=good, bt_stride=10000, seq=good, B=4, max_len=100, s1=0.1,
+                 s2=1.0, win=-1, sinks=None, Q=1, hqo=32, hkv=8, D=128, S=16, layout=1,
+                 dtype=1, out=good, lse=None, err=None, stream=None)
+        a.update(over)
+        return lib.paged_decode(*a.values())
+
+    assert call(layout=3) == 2
+    assert call(hqo=30) == 2          # 30 % 8 != 0
+    assert call(D=64) == 3            # head_dim 128 only
+    assert call(S=24) == 3            # page size must be a power of two
+    assert call(Q=9, hqo=64) == 3     # group 8 x 9 tokens = 72 rows > 64
+    assert call(query=None) == 1
+    assert call(ws_bytes=16, max_len=100000) == 4
+    assert call(bt_stride=2) == 2     # block-table row narrower than max_seq_len
+    assert call(B=0) == 0
+
+
+def test_decode_workspace_size_grows_with_length(lib):
+    f = lib.paged_decode_workspace_size
+    small = f(64, 1, 32, 8, 128, 512, 16, -1)
+    big = f(64, 1, 32, 8, 128, 8192, 16, -1)
+    assert 0 <= small <= big and big > 0
+    # a window bounds the work per request, so the workspace stops growing
+    assert f(256, 4, 64, 8, 128, 32768, 64, 4095) == f(256, 4, 64, 8, 128, 65536, 64, 4095)
+    assert f(4, 1, 30, 8, 128, 100, 16, -1) == 0  # invalid sizes
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    good = 0x1000
+
+    def call(**over):
+        a = dict(q=good, k=good, v=good, ks=8 * 32 * 128, vs=8 * 32 * 128, pages=100,
+                 scale=0.08, ws=good, ws_bytes=4096, maxq=100, maxkv=200, lq=good, lkv=good,
+                 bt=good, bt_stride=8, B=2, causal=1, hqo=32, hkv=8, dqk=128, dvo=128, S=32,
+                 layout=1, dtype=1, out=good, lse=good, err=None, stream=None)
+        a.update(over)
+        return lib.paged_prefill(*a.values())
+
+    assert call(dqk=64) == 3
+    assert call(dvo=192) == 3
+    assert call(hkv=5) == 2
+    assert call(lse=None) == 1        # the LSE output is required
+    assert call(ws_bytes=8) == 4
+    assert call(bt_stride=3) == 2     # 3 pages of 32 < max_sequence_kv 200
+    assert call(B=0) == 0

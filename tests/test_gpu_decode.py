@@ -1,0 +1,152 @@
+"""GPU parity for paged GQA decode against the fp64 oracle: every output
+element within |err| <= 2e-2 + 1e-2 |ref| and LSE within 1e-3, over small
+shapes that span several tiles, splits and ragged tails, the configurations
+at full size (sampled requests), guards and edge cases."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_316_gb300 import workloads as wl
+from _gpu import (DEV, assert_attn_close, assert_lse_close, compact_request, decode_on_gpu,
+                  err_word)
+from _util import oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(c, **kw):
+    out, lse = decode_on_gpu(c, **kw)
+    ro, rl, _ = oracle_decode(c)
+    assert_attn_close(out, ro)
+    assert_lse_close(lse, rl)
+    return out, lse
+
+
+@pytest.mark.parametrize("layout", [wl.HND, wl.NHD])
+def test_pr1_config(layout):
+    _check(wl.pr1_decode(layout=layout))
+
+
+CASES = [
+    # lengths, page, Hqo, Hkv, Q, window, sinks, dtype, layout, seed
+    ([1, 63, 64, 65, 700], 16, 32, 8, 1, -1, False, wl.BF16, wl.HND, 1),
+    ([1500, 3, 1029, 511], 16, 32, 8, 1, -1, True, wl.BF16, wl.NHD, 2),
+    ([2100, 777, 40], 64, 64, 8, 4, 300, True, wl.BF16, wl.HND, 3),
+    ([900, 4, 130], 8, 16, 16, 1, -1, False, wl.F16, wl.HND, 4),      # MHA, group 1
+    ([333, 1200], 32, 32, 2, 2, -1, False, wl.BF16, wl.NHD, 5),       # group 16, 32 rows
+    ([257, 1025, 64], 16, 32, 4, 8, 100, False, wl.F16, wl.NHD, 6),   # 64 rows
+    ([5000, 10, 2049], 128, 8, 1, 3, 1000, True, wl.BF16, wl.HND, 7),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_small_shapes(case):
+    L, S, hq, hk, Q, w, sk, dt, lay, seed = case
+    c = wl.decode_case(L, S, hq, hk, 128, lay, dt, q_len_per_req=Q, window_left=w,
+                       with_sinks=sk, seed=seed, bmm2_scale=0.8, slack=0.3)
+    _check(c)
+
+
+def test_bmm_scales_and_window_zero():
+    c = wl.decode_case([300, 45], 16, 32, 8, 128, wl.HND, q_len_per_req=1, window_left=0,
+                       seed=9, bmm1_scale=0.05, bmm2_scale=2.5)
+    _check(c)
+
+
+def test_page_permutation_bit_identical():
+    a = wl.decode_case([700, 1300], 16, 32, 8, 128, wl.HND, seed=3, pool_pages=200)
+    b = wl.decode_case([700, 1300], 16, 32, 8, 128, wl.HND, seed=4, pool_pages=200)
+    b.query.copy_(a.query)
+    for r in range(2):
+        k, v = wl.read_tokens(a.pool, a.pt, r)
+        wl.write_tokens(b.pool, b.pt, r, k, v)
+    assert a.pt.pages != b.pt.pages
+    oa, la = decode_on_gpu(a)
+    ob, lb = decode_on_gpu(b)
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(la, lb)
+
+
+def test_never_reads_padding_or_unused_slots():
+    # block-table padding holds a huge page id and every slot outside the
+    # sequences holds NaN: neither may reach the output
+    L = [45, 8, 25, 22]
+    c = wl.decode_case(L, 16, 32, 8, 128, wl.HND, seed=5, pool_pages=64, fill="nan",
+                       bt_width=12)
+    for b, n in enumerate(L):
+        kv = wl.randn((n, 8, 128), torch.bfloat16, wl.generator(100 + b))
+        vv = wl.randn((n, 8, 128), torch.bfloat16, wl.generator(200 + b))
+        wl.write_tokens(c.pool, c.pt, b, kv, vv)
+    assert int(c.block_tables[1, 5]) == wl.POISON
+    err = err_word()
+    _check(c, err_word=err)
+    assert int(err.item()) == 0
+
+
+def test_empty_and_short_requests():
+    c = wl.decode_case([0, 1, 2, 600], 16, 32, 8, 128, wl.HND, q_len_per_req=2,
+                       with_sinks=True, seed=6)
+    err = err_word()
+    out, lse = decode_on_gpu(c, err_word=err)
+    ro, rl, oerr = oracle_decode(c)
+    assert int(err.item()) == oerr == oracle.E_QLEN
+    assert_attn_close(out, ro)
+    assert_lse_close(lse, rl)
+    c2 = dataclasses.replace(c, sinks=None)
+    out, lse = decode_on_gpu(c2)
+    ro, rl, _ = oracle_decode(c2)
+    assert_attn_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_bad_page_flagged_and_treated_as_absent():
+    c = wl.decode_case([100, 50], 16, 32, 8, 128, wl.HND, seed=8, slack=0.5)
+    c.block_tables[0, 2] = c.pool.num_pages + 10
+    err = err_word()
+    out, lse = decode_on_gpu(c, err_word=err)
+    ro, rl, oerr = oracle_decode(c)
+    assert int(err.item()) & oracle.E_PAGE and oerr & oracle.E_PAGE
+    assert_attn_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_without_lse_output():
+    c = wl.decode_case([500, 20], 16, 32, 8, 128, wl.NHD, seed=10)
+    out, _ = decode_on_gpu(c, with_lse=False)
+    assert_attn_close(out, oracle_decode(c)[0])
+
+
+def _sampled_full_size(c, requests):
+    """Run the full case on the GPU; check the sampled requests' rows against
+    the oracle run on a compact copy of just those requests' pages."""
+    out, lse = decode_on_gpu(c)
+    Q = c.q_len_per_req
+    for b in requests:
+        pool, pt = compact_request(c.pool, c.pt, b)
+        sub = dataclasses.replace(
+            c, query=c.query[b * Q:(b + 1) * Q].cpu(), pool=pool, pt=pt,
+            block_tables=pt.block_tables(), seq_lens=torch.tensor([pt.lengths[0]], dtype=torch.int32),
+            max_seq_len=pt.lengths[0],
+            sinks=None if c.sinks is None else c.sinks.cpu())
+        ro, rl, _ = oracle_decode(sub)
+        assert_attn_close(out[b * Q:(b + 1) * Q], ro, f"request {b}")
+        assert_lse_close(lse[b * Q:(b + 1) * Q], rl, f"request {b} lse")
+
+
+def test_llama_config_full_size_sampled():
+    c = wl.llama_decode(device=DEV)
+    lengths = np.array(c.pt.lengths)
+    pick = sorted({int(lengths.argmin()), int(lengths.argmax()), 0, 17, 63})
+    _sampled_full_size(c, pick)
+
+
+def test_long_context_config_full_size_sampled():
+    c = wl.long_decode(device=DEV)
+    lengths = np.array(c.pt.lengths)
+    pick = sorted({int(lengths.argmin()), int(lengths.argmax()), 1, 100, 255})
+    _sampled_full_size(c, pick)
