@@ -70,6 +70,15 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
 
 
+def _check_pool(arr, page_stride: int, num_pages: int):
+    """The C code addresses page p at p * page_stride elements from the
+    array's first element: refuse views whose layout says otherwise."""
+    assert arr.dtype == np.uint16, "pass uint16 views of the pool"
+    assert arr.ndim >= 2 and arr.shape[0] >= num_pages, (arr.shape, num_pages)
+    assert arr.strides[0] == 2 * page_stride, (arr.strides, page_stride)
+    assert arr[0].size <= page_stride and arr[0].flags.c_contiguous, "pages must be contiguous"
+
+
 def max_threads() -> int:
     """OpenMP threads the oracle can use (1 when built without OpenMP)."""
     return max(1, _load().orc_has_openmp())
@@ -105,7 +114,7 @@ def append(append_key, append_value, batch_indices, positions, k_cache, v_cache,
     bi, pos = _i32(batch_indices), _i32(positions)
     ind, ptr, last = _i32(kv_indices), _i32(kv_indptr), _i32(kv_last_page_len)
     for c in (k_cache, v_cache):
-        assert c.dtype == np.uint16, "pass uint16 views of the pool"
+        _check_pool(c, page_stride, max_num_pages)
     return int(_load().orc_append(
         _p(ak), _p(av), ctypes.c_int64(bi.shape[0]), _p(bi), _p(pos),
         ctypes.c_void_p(k_cache.ctypes.data), ctypes.c_void_p(v_cache.ctypes.data),
@@ -122,6 +131,8 @@ def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
     """Returns (out [B*Q, Hqo, D] float64, lse [B*Q, Hqo] float64, err)."""
     q = _u16(query)
     kc, vc = k_cache, v_cache
+    _check_pool(kc, page_stride, max_num_pages)
+    _check_pool(vc, page_stride, max_num_pages)
     bt = _i32(block_tables)
     sl = np.ascontiguousarray(np.asarray(seq_lens_), dtype=np.uint32)
     B = sl.shape[0]
@@ -154,6 +165,8 @@ def prefill(q, k_cache, v_cache, k_page_stride: int, v_page_stride: int,
     """Returns (out [total_q, Hqo, d_vo], lse [total_q, Hqo], err), float64."""
     qq = _u16(q)
     lq, lkv = _i32(seq_lens_q), _i32(seq_lens_kv)
+    _check_pool(k_cache, k_page_stride, max_num_pages)
+    _check_pool(v_cache, v_page_stride, max_num_pages)
     bt = _i32(block_tables)
     B = lq.shape[0]
     total_q = int(lq.sum())
