@@ -193,6 +193,41 @@ int paged_decode(const void *query, const void *k_cache, const void *v_cache,
                  int32_t *err_word, void *stream);
 
 /*
+ * paged_decode_noalloc -- paged_decode without a caller workspace.  The API
+ * pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory where they call decode (a plugin inside another
+ * runtime's execution step, which owns the device memory and forbids
+ * allocation there; a latency-critical loop that cannot take cudaMalloc's
+ * device-wide synchronisation; a process that reserves all device memory up
+ * front).  Arguments, results and device errors are those of paged_decode
+ * minus `workspace` / `workspace_bytes`; it allocates and frees nothing.
+ *  - The split partials go to a fixed array of PKV_NOALLOC_SCRATCH_BYTES in
+ *    the library's device image; every GPU that loads the library holds one
+ *    copy until the process exits.  Sizes whose
+ *    paged_decode_workspace_size(...) exceeds it are rejected with
+ *    PKV_ERR_WORKSPACE before anything is launched (use paged_decode then).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero.  Calls that overlap on the GPU
+ *    (concurrent streams, or host threads on one device) race on it:
+ *    serialise them.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+int paged_decode_noalloc(const void *query, const void *k_cache,
+                         const void *v_cache, int64_t page_stride,
+                         int64_t max_num_pages, const int32_t *block_tables,
+                         int32_t block_table_stride, const uint32_t *seq_lens,
+                         int32_t batch_size, int32_t max_seq_len,
+                         float bmm1_scale, float bmm2_scale, int32_t window_left,
+                         const float *sinks, int32_t q_len_per_req,
+                         int32_t num_qo_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t page_size, int32_t layout,
+                         int32_t dtype, void *out, float *lse, int32_t *err_word,
+                         void *stream);
+
+/*
  * paged_prefill_workspace_size -- bytes of device workspace paged_prefill
  * needs (packed query offsets and the work list of query tiles).  The
  * prefill page's workspace_buffer plays the same role.

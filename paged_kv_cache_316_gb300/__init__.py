@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     paged_append,
     paged_decode_workspace_size,
     paged_decode,
+    paged_decode_noalloc,
     paged_prefill_workspace_size,
     paged_prefill,
     kernel_launches,

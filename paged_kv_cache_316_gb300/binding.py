@@ -39,6 +39,9 @@ _SIGNATURES = {
     "paged_decode": ([_c_p, _c_p, _c_p, _i64, _i64, _c_p, _sz, _c_p, _i32, _c_p,
                       _i32, _i32, _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32,
                       _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
+    "paged_decode_noalloc": ([_c_p, _c_p, _c_p, _i64, _i64, _c_p, _i32, _c_p, _i32, _i32,
+                              _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
+                              _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
     "paged_prefill_workspace_size": ([_i32] * 4, _sz),
     "paged_prefill": ([_c_p, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _sz, _i32,
                        _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
@@ -214,6 +217,31 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
         bmm2_scale, window_left, _ptr(sinks), q_len_per_req, Hqo, Hkv, D, S,
         layout, _dtype_code(query), _ptr(out), _ptr(lse), _ptr(err_word),
         _stream(stream)))
+    return out
+
+
+def paged_decode_noalloc(query, kv_cache, block_tables, seq_lens, max_seq_len: int,
+                         bmm1_scale: float = 1.0, bmm2_scale: float = 1.0,
+                         window_left: int = -1, sinks=None, kv_layout="HND",
+                         q_len_per_req: int = 1, out=None, lse=None, err_word=None,
+                         stream=None):
+    """paged_decode for callers that cannot allocate device memory at the
+    call: the split partials use the library's fixed device scratch array
+    (PKV_NOALLOC_SCRATCH_BYTES) instead of a workspace tensor.  Calls that
+    overlap on the GPU share that array and race."""
+    layout = _layout_code(kv_layout)
+    kp, vp, stride, P, Hkv, S, D, _ = split_cache(kv_cache, layout)
+    rows, Hqo, Dq = query.shape
+    if Dq != D:
+        raise PagedKVError("query head_dim differs from the cache's")
+    B = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(query)
+    _check(load_library().paged_decode_noalloc(
+        _ptr(query), kp, vp, stride, P, _ptr(block_tables), block_tables.stride(0),
+        _ptr(seq_lens), B, max_seq_len, bmm1_scale, bmm2_scale, window_left, _ptr(sinks),
+        q_len_per_req, Hqo, Hkv, D, S, layout, _dtype_code(query), _ptr(out), _ptr(lse),
+        _ptr(err_word), _stream(stream)))
     return out
 
 

@@ -555,3 +555,68 @@ extern "C" int paged_decode(const void *query, const void *k_cache, const void *
     return dtype == PKV_BF16 ? run_decode<__nv_bfloat16>(p, pl, layout, st)
                              : run_decode<__half>(p, pl, layout, st);
 }
+
+// ---- decode with a library-owned scratch array ------------------------------
+//
+// For callers that cannot allocate device memory where they call decode: a
+// plugin running inside another runtime's execution step (that runtime owns
+// the device memory and forbids allocation there), a latency-critical loop
+// that cannot afford cudaMalloc's implicit device-wide synchronisation, or
+// a process that reserves all device memory up front.  The split partials
+// live in a fixed array in this library's own device image instead of a
+// caller workspace.
+#include <mutex>
+
+namespace pkv {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES);
+constexpr int kNoAllocMaxDevices = 64;
+
+// One copy per device that loads the library, held until the process exits.
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of g_decode_scratch on the current device.  In host code
+// the symbol is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static void *noalloc_scratch_ptr() {
+    static std::mutex mu;
+    static void *ptrs[kNoAllocMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return nullptr;
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+}  // namespace pkv
+
+extern "C" int paged_decode_noalloc(const void *query, const void *k_cache, const void *v_cache,
+                                    int64_t page_stride, int64_t max_num_pages,
+                                    const int32_t *block_tables, int32_t block_table_stride,
+                                    const uint32_t *seq_lens, int32_t batch_size,
+                                    int32_t max_seq_len, float bmm1_scale, float bmm2_scale,
+                                    int32_t window_left, const float *sinks,
+                                    int32_t q_len_per_req, int32_t num_qo_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                    int32_t layout, int32_t dtype, void *out, float *lse,
+                                    int32_t *err_word, void *stream) {
+    DecodePlan pl;
+    int rc = plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
+                         max_seq_len, page_size, window_left, pl);
+    if (rc != PKV_OK) return rc;
+    if (pl.ws_bytes > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (pl.ws_bytes > 0) {
+        scratch = noalloc_scratch_ptr();
+        if (!scratch) return PKV_ERR_CUDA;
+    }
+    return paged_decode(query, k_cache, v_cache, page_stride, max_num_pages, scratch,
+                        scratch ? kNoAllocScratchBytes : 0, block_tables, block_table_stride,
+                        seq_lens, batch_size, max_seq_len, bmm1_scale, bmm2_scale, window_left,
+                        sinks, q_len_per_req, num_qo_heads, num_kv_heads, head_dim, page_size,
+                        layout, dtype, out, lse, err_word, stream);
+}
