@@ -249,6 +249,8 @@ size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_qo_heads,
  *   out[row, h, :] = softmax_j(scale * <q[row, h], k_j>) v_j
  *   lse[row, h]    = log sum_j e^{scale * <q[row, h], k_j>}   (natural log)
  *   q: [total_q, num_qo_heads, d_qk]; out: [total_q, num_qo_heads, d_vo];
+ *   total_q is the row count of q/out/lse (rows past it are neither read
+ *   nor written even if the lengths say otherwise);
  *   lse: [total_q, num_qo_heads] fp32 (required: the page says return_lse
  *   must be true).  k_cache pages hold d_qk-wide rows, v_cache pages d_vo-wide
  *   rows, each with its own page stride.  actual_seq_lens_q/kv: [batch_size]
@@ -259,10 +261,14 @@ size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_qo_heads,
  *   and is clamped to it.
  * Supported (prefill page note): d_qk in {128, 192}, d_vo = 128; page_size a
  * power of two in [8, 256]; num_qo_heads % num_kv_heads == 0.
+ * Errors: PKV_ERR_CUDA also when the driver rejects a TMA tensor map.
+ * Device errors additionally include PKV_DEV_ERR_TIMEOUT if a pipeline wait
+ * gave up (the affected rows are then zero).
  * Device errors: bad page id -> PKV_DEV_ERR_PAGE; kv_b < q_b ->
  * PKV_DEV_ERR_QLEN (rows that see no key get out = 0, lse = -inf).
  */
-int paged_prefill(const void *q, const void *k_cache, const void *v_cache,
+int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
+                  const void *v_cache,
                   int64_t k_page_stride, int64_t v_page_stride,
                   int64_t max_num_pages, float scale, void *workspace,
                   size_t workspace_bytes, int32_t max_token_per_sequence,

@@ -43,7 +43,7 @@ _SIGNATURES = {
                               _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
                               _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
     "paged_prefill_workspace_size": ([_i32] * 4, _sz),
-    "paged_prefill": ([_c_p, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _sz, _i32,
+    "paged_prefill": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _sz, _i32,
                        _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
                        _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
 }
@@ -274,7 +274,7 @@ def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
         lse = torch.empty((total_q, Hqo), dtype=torch.float32, device=q.device)
     B = actual_seq_lens_q.shape[0]
     _check(load_library().paged_prefill(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
+        _ptr(q), total_q, _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
         P, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
         max_token_per_sequence, max_sequence_kv, _ptr(actual_seq_lens_q),
         _ptr(actual_seq_lens_kv), _ptr(block_tables), block_tables.stride(0), B,

@@ -3,27 +3,49 @@
 // Computes what flashinfer.prefill.cudnn_batch_prefill_with_kv_cache
 // documents (q, k_cache, v_cache, scale, workspace_buffer,
 // max_token_per_sequence, max_sequence_kv, actual_seq_lens_q/kv,
-// block_tables, causal, return_lse): queries of request b are the last
-// q_b of its kv_b positions; each CTA owns 128 query rows of one qo head and
-// streams the keys it can see through a cp.async ring, with an online
-// softmax in registers.
+// block_tables, causal, return_lse): the queries of request b are the last
+// q_b of its kv_b positions; softmax(scale q k^T) v over the visible keys
+// and the natural-log LSE of the scaled logits.
+//
+// One CTA owns 128 query rows of one qo head and walks the key tiles they
+// can see.  Warp roles (192 threads):
+//   warp 4  TMA producer: Q once, then K and V tiles of BN keys, page by
+//           page, through a ring of STAGES shared-memory stages;
+//   warp 5  allocates tensor memory and issues the tcgen05 MMAs from one
+//           thread: S = Q K^T into one of two TMEM score buffers, then
+//           O += P V into the TMEM output accumulator;
+//   warps 0-3  one thread per query row: read its S row from TMEM, mask,
+//           online softmax in base 2, write P (bf16/fp16) back to shared
+//           memory for the PV MMA, rescale O in TMEM when the running max
+//           grows by more than 2^8, and finally normalise O and write out
+//           and lse.
+// Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
+// other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
 
 #include "pkv_common.cuh"
+#include "sm103_ptx.cuh"
 
 namespace pkv {
 
-constexpr int kPfRows = 128;   // query rows per CTA (8 warps x 16)
-constexpr int kPfTile = 64;    // keys per pipeline stage
-constexpr int kPfStages = 2;
-constexpr int kPfThreads = 256;
+constexpr int kPfRows = 128;     // query rows per CTA
+constexpr int kPfThreads = 192;  // 4 softmax warps + TMA warp + MMA warp
 constexpr int kPfDV = 128;
 
+template <int DQK>
+struct PfCfg;
+template <>
+struct PfCfg<128> {
+    static constexpr int BN = 128, STAGES = 2;
+};
+template <>
+struct PfCfg<192> {
+    static constexpr int BN = 64, STAGES = 3;
+};
+
 struct PrefillParams {
-    const void *q;
-    const void *k;
-    const void *v;
-    int64_t k_page_stride, v_page_stride, max_num_pages;
+    int64_t max_num_pages;
+    int64_t total_q;
     float scale_log2;
     const int32_t *seq_lens_q;
     const int32_t *seq_lens_kv;
@@ -37,7 +59,7 @@ struct PrefillParams {
 };
 
 // cu_q = exclusive prefix sum of the query lengths (one warp, 32 at a time);
-// flags requests with fewer keys than queries.
+// flags lengths above their maxima and requests with fewer keys than queries.
 __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_t *__restrict__ lkv,
                                     int B, int max_q, int max_kv, int32_t *__restrict__ cu_q,
                                     int32_t *err) {
@@ -61,243 +83,378 @@ __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_
     if (lane == 0) cu_q[B] = carry;
 }
 
-template <typename T, int DQK, int LAYOUT>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_mma_kernel(const PrefillParams p) {
-    constexpr int KROW = DQK * 2, VROW = kPfDV * 2;
-    constexpr int KCH = DQK / 8, VCH = kPfDV / 8;  // 16-byte chunks per row
-    constexpr int KTILE = kPfTile * KROW, VTILE = kPfTile * VROW;
-    constexpr int STAGE = KTILE + VTILE;
-    constexpr int NT = kPfTile / 8;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *q_s = smem + kPfStages * STAGE;
-    uint8_t *kvalid = q_s + kPfRows * KROW;
-    __shared__ int any_bad;
+template <typename T>
+struct IsBf16 {
+    static constexpr bool value = false;
+};
+template <>
+struct IsBf16<__nv_bfloat16> {
+    static constexpr bool value = true;
+};
 
-    const int b = blockIdx.z, h = blockIdx.y;
+template <typename T, int DQK, int LAYOUT>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+    constexpr int BN = PfCfg<DQK>::BN;
+    constexpr int STAGES = PfCfg<DQK>::STAGES;
+    constexpr int QA = DQK / 64;                 // 64-column atoms of a Q / K row
+    constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of the Q tile
+    constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
+    constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
+    constexpr uint32_t PB = kPfRows * BN * 2;    // bytes of the P tile
+    constexpr uint32_t TMEM_COLS = (kPfDV + 2 * BN) <= 256 ? 256 : 512;
+    constexpr uint32_t S_COL = kPfDV;            // S buffers follow the O accumulator
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t q_s = smem_u32(smem);
+    const uint32_t k_s = q_s + QB;
+    const uint32_t v_s = k_s + STAGES * KB;
+    const uint32_t p_s = v_s + STAGES * VB;
+    const uint32_t bar0 = p_s + PB;
+    uint8_t *v_gen = smem + QB + STAGES * KB;  // generic pointers to V stages and P
+    uint8_t *p_gen = smem + QB + STAGES * (KB + VB);
+    const uint32_t b_qfull = bar0;
+    auto b_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto b_vfull = [&](int s) { return bar0 + 8u * (1 + STAGES + s); };
+    auto b_kvempty = [&](int s) { return bar0 + 8u * (1 + 2 * STAGES + s); };
+    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + 3 * STAGES + i); };
+    auto b_sfree = [&](int i) { return bar0 + 8u * (3 + 3 * STAGES + i); };
+    const uint32_t b_pfull = bar0 + 8u * (5 + 3 * STAGES);
+    const uint32_t b_oready = bar0 + 8u * (6 + 3 * STAGES);
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
     const int qb = min(max(p.seq_lens_q[b], 0), p.max_q);
     const int kvb = min(max(p.seq_lens_kv[b], 0), p.max_kv);
     const int n_qt = (qb + kPfRows - 1) / kPfRows;
-    if (static_cast<int>(blockIdx.x) >= n_qt) return;
-    const int qt = n_qt - 1 - blockIdx.x;  // most keys first
+    if (static_cast<int>(blockIdx.x) >= n_qt) return;  // uniform: before any barrier or TMEM use
+    const int qt = n_qt - 1 - blockIdx.x;              // the tiles that see most keys first
     const int i0 = qt * kPfRows;
     const int row_base = p.cu_q[b] + i0;
     const int kvh = h / p.group;
-    const int shift = kvb - qb;  // position of query i is shift + i
+    const int shift = kvb - qb;  // query i sits at position shift + i
     int k_hi = p.causal ? min(kvb, shift + i0 + kPfRows) : kvb;
     if (k_hi < 0) k_hi = 0;
-    const int n_tiles = (k_hi + kPfTile - 1) / kPfTile;
+    const int n_tiles = (k_hi + BN - 1) / BN;
 
-    const T *kc = static_cast<const T *>(p.k);
-    const T *vc = static_cast<const T *>(p.v);
-    const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
-    const int S = 1 << p.page_shift;
-    if (tid == 0) any_bad = 0;
-    __syncthreads();
-
-    auto load_tile = [&](int stage, int j0) {
-        uint8_t *base = smem + stage * STAGE;
-        for (int idx = tid; idx < kPfTile * (KCH + VCH); idx += kPfThreads) {
-            const bool is_v = idx >= kPfTile * KCH;
-            const int li = is_v ? idx - kPfTile * KCH : idx;
-            const int nch = is_v ? VCH : KCH;
-            const int r = li / nch, c = li - r * nch;
-            const int j = j0 + r;
-            bool ok = j < k_hi;
-            const T *src = kc;
-            if (ok) {
-                int page = bt[j >> p.page_shift];
-                if (page < 0 || page >= p.max_num_pages) {
-                    ok = false;
-                    if (c == 0 && !is_v) {
-                        set_err(p.err, PKV_DEV_ERR_PAGE);
-                        any_bad = 1;
-                    }
-                } else if (is_v) {
-                    src = vc + kv_row_offset<LAYOUT>(page, p.v_page_stride, kvh, j & (S - 1), p.Hkv,
-                                                     S, kPfDV) + c * 8;
-                } else {
-                    src = kc + kv_row_offset<LAYOUT>(page, p.k_page_stride, kvh, j & (S - 1), p.Hkv,
-                                                     S, DQK) + c * 8;
-                }
-            }
-            if (!is_v && c == 0) kvalid[stage * kPfTile + r] = ok ? 1 : 0;
-            uint32_t dst = smem_u32(base + (is_v ? KTILE : 0)) + swz(r, c, is_v ? VROW : KROW);
-            cp_async_16(dst, src, ok);
+    if (tid == 0) {
+        mbar_init(b_qfull, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(b_kfull(s), 1);
+            mbar_init(b_vfull(s), 1);
+            mbar_init(b_kvempty(s), 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(b_sfull(i), 1);
+            mbar_init(b_sfree(i), 128);
+        }
+        mbar_init(b_pfull, 128);
+        mbar_init(b_oready, 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    volatile int *abort_flag = &abort_s;
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        set_err(p.err, PKV_DEV_ERR_TIMEOUT);
     };
 
-    const T *qp = static_cast<const T *>(p.q);
-    for (int idx = tid; idx < kPfRows * KCH; idx += kPfThreads) {
-        const int r = idx / KCH, c = idx - r * KCH;
-        const bool ok = i0 + r < qb;
-        const T *src = ok ? qp + (static_cast<int64_t>(row_base + r) * p.Hqo + h) * DQK + c * 8 : qp;
-        cp_async_16(smem_u32(q_s) + swz(r, c, KROW), src, ok);
-    }
-    cp_async_commit();
-#pragma unroll
-    for (int st = 0; st < kPfStages - 1; ++st) {
-        if (st < n_tiles) load_tile(st, st * kPfTile);
-        cp_async_commit();
-    }
-    cp_async_wait<kPfStages - 1>();
-    __syncthreads();
-
-    uint32_t qa[DQK / 16][4];
-#pragma unroll
-    for (int kk = 0; kk < DQK / 16; ++kk)
-        ldsm_x4(qa[kk], smem_u32(q_s) + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), KROW));
-
-    const int ra = 16 * warp + (lane >> 2), rb = ra + 8;  // rows of this lane (tile-local)
-    const int posa = shift + i0 + ra, posb = shift + i0 + rb;
-    const int lim_a = p.causal ? min(posa, kvb - 1) : kvb - 1;  // last visible key
-    const int lim_b = p.causal ? min(posb, kvb - 1) : kvb - 1;
-    // last key visible to the warp's first / last row (warp-uniform)
-    const int warp_lim_lo = p.causal ? min(shift + i0 + 16 * warp, kvb - 1) : kvb - 1;
-    const int warp_lim_hi = p.causal ? min(shift + i0 + 16 * warp + 15, kvb - 1) : kvb - 1;
-
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int it = 0; it < n_tiles; ++it) {
-        cp_async_wait<kPfStages - 2>();
-        __syncthreads();
-        {
-            int nxt = it + kPfStages - 1;
-            if (nxt < n_tiles) load_tile(nxt % kPfStages, nxt * kPfTile);
-            cp_async_commit();
-        }
-        const int stage = it % kPfStages;
-        const int j0 = it * kPfTile;
-        const uint32_t kb = smem_u32(smem + stage * STAGE);
-        const uint32_t vb = kb + KTILE;
-        if (j0 > warp_lim_hi) continue;  // no key of this tile is visible to this warp
-
-        float sc[NT][4];
-#pragma unroll
-        for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t bf[4];
-                int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(bf, kb + swz(key, 2 * kk + ((lane >> 3) & 1), KROW));
-                mma16816<T>(sc[2 * np], qa[kk], bf[0], bf[1]);
-                mma16816<T>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
-            }
-        }
-        const bool interior = !any_bad && j0 + kPfTile - 1 <= warp_lim_lo;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float x = sc[nt][e] * p.scale_log2;
-                if (!interior) {
-                    int jj = nt * 8 + 2 * (lane & 3) + (e & 1);
-                    int j = j0 + jj;
-                    bool vis = kvalid[stage * kPfTile + jj] && j <= (e < 2 ? lim_a : lim_b);
-                    if (!vis) x = -INFINITY;
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(b_qfull, QB);
+            for (int c = 0; c < QA; ++c)
+                tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, h, row_base);
+            const int S = 1 << p.page_shift;
+            const int RB = S < BN ? S : BN;  // rows per TMA box
+            const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
+            const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % STAGES, u = j / STAGES;
+                if (u > 0 && !mbar_wait(b_kvempty(s), (u - 1) & 1, abort_flag)) {
+                    give_up();
+                    break;
                 }
-                sc[nt][e] = x;
+                const int j0 = j * BN;
+                mbar_expect_tx(b_kfull(s), KB);
+                mbar_expect_tx(b_vfull(s), VB);
+                for (int r0 = 0; r0 < BN; r0 += RB) {
+                    const int key = j0 + r0;
+                    const int slot0 = key & (S - 1);
+                    int page = oob;
+                    if (key < kvb) {
+                        page = bt[key >> p.page_shift];
+                        if (page < 0 || page >= p.max_num_pages) {
+                            set_err(p.err, PKV_DEV_ERR_PAGE);
+                            page = oob;
+                        }
+                    }
+                    const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
+                    const int cb = LAYOUT == PKV_HND ? kvh : slot0;
+                    for (int c = 0; c < QA; ++c)
+                        tma_load_4d(k_s + s * KB + c * (BN * 128) + r0 * 128, &tm_k, b_kfull(s), c * 64,
+                                    ca, cb, page);
+                    for (int c = 0; c < kPfDV / 64; ++c)
+                        tma_load_4d(v_s + s * VB + c * (BN * 128) + r0 * 128, &tm_v, b_vfull(s), c * 64,
+                                    ca, cb, page);
+                }
             }
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
+            constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
+            bool ok = mbar_wait(b_qfull, 0, abort_flag);
+            auto issue_pv = [&](int jj) -> bool {
+                const int s = jj % STAGES, u = jj / STAGES;
+                if (!mbar_wait(b_pfull, jj & 1, abort_flag)) return false;
+                if (!mbar_wait(b_vfull(s), u & 1, abort_flag)) return false;
+                tc_fence_after();
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
-        float rs0 = 0.f, rs1 = 0.f;
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    uint64_t a = umma_sdesc_sw128(p_s + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
+                    uint64_t bd = umma_sdesc_sw128(v_s + s * VB + kk * 16 * 128, BN * 128, 1024);
+                    umma_ss(tmem, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(b_oready);
+                umma_commit(b_kvempty(s));
+                return true;
+            };
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int s = j % STAGES, u = j / STAGES, bb = j & 1;
+                if (!mbar_wait(b_kfull(s), u & 1, abort_flag)) { ok = false; break; }
+                if (j >= 2 && !mbar_wait(b_sfree(bb), ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            sc[nt][0] = fast_exp2(sc[nt][0] - base0);
-            sc[nt][1] = fast_exp2(sc[nt][1] - base0);
-            sc[nt][2] = fast_exp2(sc[nt][2] - base1);
-            sc[nt][3] = fast_exp2(sc[nt][3] - base1);
-            rs0 += sc[nt][0] + sc[nt][1];
-            rs1 += sc[nt][2] + sc[nt][3];
-        }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            o[i][0] *= al0;
-            o[i][1] *= al0;
-            o[i][2] *= al1;
-            o[i][3] *= al1;
-        }
-#pragma unroll
-        for (int ks = 0; ks < NT / 2; ++ks) {
-            uint32_t a[4];
-            a[0] = pack2<T>(sc[2 * ks][0], sc[2 * ks][1]);
-            a[1] = pack2<T>(sc[2 * ks][2], sc[2 * ks][3]);
-            a[2] = pack2<T>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-            a[3] = pack2<T>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
-            const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {
-                uint32_t vf[4];
-                ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), VROW));
-                mma16816<T>(o[2 * dp], a, vf[0], vf[1]);
-                mma16816<T>(o[2 * dp + 1], a, vf[2], vf[3]);
+                for (int kk = 0; kk < DQK / 16; ++kk) {
+                    uint64_t a = umma_sdesc_sw128(q_s + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
+                    uint64_t bd = umma_sdesc_sw128(k_s + s * KB + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+                    umma_ss(tmem + S_COL + bb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(b_sfull(bb));
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
+            if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
+            if (!ok) give_up();
         }
-    }
-    cp_async_wait<0>();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int r = tid;  // query row of this thread inside the tile
+        const int pos = shift + i0 + r;
+        const int lim = p.causal ? min(pos, kvb - 1) : kvb - 1;  // last visible key
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        // the TMEM loads below are warp-collective: a lane that gave up
+        // waiting takes its whole warp out of the loop
+        auto wait_warp = [&](uint32_t bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+        };
+        for (int j = 0; j < n_tiles; ++j) {
+            const int bb = j & 1, s = j % STAGES, u = j / STAGES;
+            const int j0 = j * BN;
+            if (!wait_warp(b_sfull(bb), (j >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            float x[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(t_lane + S_COL + bb * BN + c * 32, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(rr[e]);
+            }
+            tc_fence_before();
+            mbar_arrive(b_sfree(bb));
 
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    T *outp = static_cast<T *>(p.out);
-    const bool va = i0 + ra < qb, vb_ = i0 + rb < qb;
-    const int64_t orow_a = static_cast<int64_t>(row_base + ra) * p.Hqo + h;
-    const int64_t orow_b = static_cast<int64_t>(row_base + rb) * p.Hqo + h;
+            const bool full = j0 + BN - 1 <= lim;
+            float mx = -INFINITY;
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-        const int d = nd * 8 + 2 * (lane & 3);
-        if (va) *reinterpret_cast<uint32_t *>(outp + orow_a * kPfDV + d) = pack2<T>(o[nd][0] * inv0, o[nd][1] * inv0);
-        if (vb_) *reinterpret_cast<uint32_t *>(outp + orow_b * kPfDV + d) = pack2<T>(o[nd][2] * inv1, o[nd][3] * inv1);
+            for (int c = 0; c < BN; ++c) {
+                float v = x[c] * p.scale_log2;
+                if (!full && j0 + c > lim) v = -INFINITY;
+                x[c] = v;
+                mx = fmaxf(mx, v);
+            }
+            float alpha = 1.f;
+            bool need = false;
+            if (mx != -INFINITY) {
+                if (m_used == -INFINITY) {
+                    m_used = mx;
+                } else if (mx > m_used + 8.f) {
+                    alpha = fast_exp2(m_used - mx);
+                    m_used = mx;
+                    l *= alpha;
+                    need = true;
+                }
+            }
+            const float base = m_used == -INFINITY ? 0.f : m_used;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+                x[c] = fast_exp2(x[c] - base);
+                rs += x[c];
+            }
+            l += rs;
+
+            // the previous PV must be complete before O or the P buffer is touched
+            if (j >= 1 && !wait_warp(b_oready, (j - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int c = 0; c < kPfDV / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(t_lane + c * 32, rr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                    tmem_st32(t_lane + c * 32, rr);
+                }
+                tmem_wait_st();
+            }
+            // rows of V past the sequence end may hold anything (even NaN):
+            // zero them so that P = 0 there cannot produce 0 * NaN
+            if (j0 < kvb && j0 + BN > kvb) {
+                if (!wait_warp(b_vfull(s), u & 1)) { ok = false; break; }
+                const int z0 = kvb - j0;
+                uint8_t *vbase = v_gen + s * VB;
+                for (int idx = tid; idx < (BN - z0) * 16; idx += 128) {
+                    const int row = z0 + (idx >> 4), chunk = idx & 15;
+                    *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // P row -> shared memory, 128-byte swizzled K-major (A operand of PV)
+#pragma unroll
+            for (int a = 0; a < BN / 64; ++a) {
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const float *xv = x + a * 64 + cc * 8;
+                    uint4 w = make_uint4(pack2<T>(xv[0], xv[1]), pack2<T>(xv[2], xv[3]),
+                                         pack2<T>(xv[4], xv[5]), pack2<T>(xv[6], xv[7]));
+                    *reinterpret_cast<uint4 *>(p_gen + a * (kPfRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(b_pfull);
+        }
+        // epilogue: O / l -> out, lse
+        if (ok && n_tiles > 0 && !wait_warp(b_oready, (n_tiles - 1) & 1)) ok = false;
+        if (!ok) give_up();
+        const bool have_o = __all_sync(0xffffffffu, ok) && n_tiles > 0;
+        tc_fence_after();
+        const int qi = i0 + r;
+        const int64_t grow = static_cast<int64_t>(row_base) + r;
+        const bool valid = qi < qb && grow < p.total_q;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV;
+#pragma unroll
+        for (int c = 0; c < kPfDV / 32; ++c) {
+            uint32_t rr[32];
+            if (have_o) {
+                tmem_ld32(t_lane + c * 32, rr);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) rr[e] = 0u;
+            }
+            if (valid) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint4 w;
+                    w.x = pack2<T>(__uint_as_float(rr[g * 8 + 0]) * inv, __uint_as_float(rr[g * 8 + 1]) * inv);
+                    w.y = pack2<T>(__uint_as_float(rr[g * 8 + 2]) * inv, __uint_as_float(rr[g * 8 + 3]) * inv);
+                    w.z = pack2<T>(__uint_as_float(rr[g * 8 + 4]) * inv, __uint_as_float(rr[g * 8 + 5]) * inv);
+                    w.w = pack2<T>(__uint_as_float(rr[g * 8 + 6]) * inv, __uint_as_float(rr[g * 8 + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(orow + c * 32 + g * 8) = w;
+                }
+            }
+        }
+        if (valid) p.lse[grow * p.Hqo + h] = l > 0.f ? (m_used + fast_log2(l)) * kLn2 : -INFINITY;
     }
-    if ((lane & 3) == 0) {
-        if (va) p.lse[orow_a] = l0 > 0.f ? (m0 + fast_log2(l0)) * kLn2 : -INFINITY;
-        if (vb_) p.lse[orow_b] = l1 > 0.f ? (m1 + fast_log2(l1)) * kLn2 : -INFINITY;
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
+template <int DQK>
+static size_t prefill_smem_bytes() {
+    constexpr int BN = PfCfg<DQK>::BN, STAGES = PfCfg<DQK>::STAGES;
+    return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + kPfRows * BN * 2 +
+           8 * (7 + 3 * STAGES);
+}
+
 template <typename T, int DQK, int LAYOUT>
-static int launch_prefill(const PrefillParams &p, dim3 grid, cudaStream_t st) {
-    const size_t smem = kPfStages * (kPfTile * DQK * 2 + kPfTile * kPfDV * 2) + kPfRows * DQK * 2 +
-                        kPfStages * kPfTile;
-    auto kern = prefill_mma_kernel<T, DQK, LAYOUT>;
+static int launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const PrefillParams &p, dim3 grid, cudaStream_t st) {
+    const size_t smem = prefill_smem_bytes<DQK>();
+    auto kern = prefill_tc_kernel<T, DQK, LAYOUT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
-    kern<<<grid, kPfThreads, smem, st>>>(p);
+    kern<<<grid, kPfThreads, smem, st>>>(tq, tk, tv, p);
     return PKV_OK;
 }
 
 template <typename T>
-static int dispatch_prefill(int d_qk, int layout, const PrefillParams &p, dim3 grid, cudaStream_t st) {
+static int dispatch_prefill(int d_qk, int layout, const CUtensorMap &tq, const CUtensorMap &tk,
+                            const CUtensorMap &tv, const PrefillParams &p, dim3 grid, cudaStream_t st) {
     if (d_qk == 128)
-        return layout == PKV_HND ? launch_prefill<T, 128, PKV_HND>(p, grid, st)
-                                 : launch_prefill<T, 128, PKV_NHD>(p, grid, st);
-    return layout == PKV_HND ? launch_prefill<T, 192, PKV_HND>(p, grid, st)
-                             : launch_prefill<T, 192, PKV_NHD>(p, grid, st);
+        return layout == PKV_HND ? launch_prefill<T, 128, PKV_HND>(tq, tk, tv, p, grid, st)
+                                 : launch_prefill<T, 128, PKV_NHD>(tq, tk, tv, p, grid, st);
+    return layout == PKV_HND ? launch_prefill<T, 192, PKV_HND>(tq, tk, tv, p, grid, st)
+                             : launch_prefill<T, 192, PKV_NHD>(tq, tk, tv, p, grid, st);
+}
+
+// K or V cache as a 4-D tensor map whose box is one 64-element d-atom of
+// `rows` consecutive slots of one (page, kv head).
+static bool cache_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int layout, int d,
+                       int page_size, int num_kv_heads, int64_t page_stride, int64_t num_pages,
+                       int rows) {
+    uint64_t dims[4], strides[3];
+    uint32_t box[4];
+    dims[0] = d;
+    box[0] = 64;
+    strides[0] = static_cast<uint64_t>(d) * 2;
+    if (layout == PKV_HND) {
+        dims[1] = page_size;
+        dims[2] = num_kv_heads;
+        strides[1] = static_cast<uint64_t>(page_size) * d * 2;
+        box[1] = rows;
+        box[2] = 1;
+    } else {
+        dims[1] = num_kv_heads;
+        dims[2] = page_size;
+        strides[1] = static_cast<uint64_t>(num_kv_heads) * d * 2;
+        box[1] = 1;
+        box[2] = rows;
+    }
+    dims[3] = static_cast<uint64_t>(num_pages);
+    strides[2] = static_cast<uint64_t>(page_stride) * 2;
+    box[3] = 1;
+    return encode_tmap(m, base, dt, 4, dims, strides, box);
 }
 
 static size_t prefill_ws_bytes(int B) { return round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256); }
@@ -314,30 +471,32 @@ extern "C" size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_q
     return prefill_ws_bytes(batch_size);
 }
 
-extern "C" int paged_prefill(const void *q, const void *k_cache, const void *v_cache,
-                             int64_t k_page_stride, int64_t v_page_stride, int64_t max_num_pages,
-                             float scale, void *workspace, size_t workspace_bytes,
-                             int32_t max_token_per_sequence, int32_t max_sequence_kv,
-                             const int32_t *actual_seq_lens_q, const int32_t *actual_seq_lens_kv,
-                             const int32_t *block_tables, int32_t block_table_stride,
-                             int32_t batch_size, int32_t causal, int32_t num_qo_heads,
-                             int32_t num_kv_heads, int32_t d_qk, int32_t d_vo, int32_t page_size,
-                             int32_t layout, int32_t dtype, void *out, float *lse,
-                             int32_t *err_word, void *stream) {
+extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
+                             const void *v_cache, int64_t k_page_stride, int64_t v_page_stride,
+                             int64_t max_num_pages, float scale, void *workspace,
+                             size_t workspace_bytes, int32_t max_token_per_sequence,
+                             int32_t max_sequence_kv, const int32_t *actual_seq_lens_q,
+                             const int32_t *actual_seq_lens_kv, const int32_t *block_tables,
+                             int32_t block_table_stride, int32_t batch_size, int32_t causal,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                             int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
+                             void *out, float *lse, int32_t *err_word, void *stream) {
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
     if (batch_size < 0 || num_qo_heads < 1 || num_kv_heads < 1 || max_token_per_sequence < 0 ||
-        max_sequence_kv < 0 || max_num_pages < 0 || block_table_stride < 0)
+        max_sequence_kv < 0 || max_num_pages < 0 || block_table_stride < 0 || total_q < 0)
         return PKV_ERR_INVALID_ARG;
     if (num_qo_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
     if ((d_qk != 128 && d_qk != 192) || d_vo != 128) return PKV_ERR_UNSUPPORTED;
-    if (ilog2_exact(page_size) < 0 || page_size > 1024) return PKV_ERR_UNSUPPORTED;
-    if (batch_size > 65535 || num_qo_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (ilog2_exact(page_size) < 3 || page_size > 256) return PKV_ERR_UNSUPPORTED;
+    if (batch_size > 65535 || num_qo_heads > 65535 || max_num_pages > 0x7fffffff ||
+        total_q > 0x7fffffff)
+        return PKV_ERR_UNSUPPORTED;
     if (k_page_stride < static_cast<int64_t>(num_kv_heads) * page_size * d_qk ||
         v_page_stride < static_cast<int64_t>(num_kv_heads) * page_size * d_vo ||
         static_cast<int64_t>(block_table_stride) * page_size < max_sequence_kv)
         return PKV_ERR_INVALID_ARG;
-    if (batch_size == 0) return PKV_OK;
+    if (batch_size == 0 || total_q == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !actual_seq_lens_q || !actual_seq_lens_kv || !block_tables ||
         !out || !lse)
         return PKV_ERR_NULL;
@@ -349,17 +508,32 @@ extern "C" int paged_prefill(const void *q, const void *k_cache, const void *v_c
         (reinterpret_cast<uintptr_t>(workspace) & 255))
         return PKV_ERR_WORKSPACE;
 
+    const CUtensorMapDataType tdt =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int BN = d_qk == 128 ? PfCfg<128>::BN : PfCfg<192>::BN;
+    const int rows = page_size < BN ? page_size : BN;
+    CUtensorMap tq, tk, tv;
+    {
+        uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),
+                            static_cast<uint64_t>(total_q)};
+        uint64_t strides[2] = {static_cast<uint64_t>(d_qk) * 2,
+                               static_cast<uint64_t>(num_qo_heads) * d_qk * 2};
+        uint32_t box[3] = {64, 1, static_cast<uint32_t>(kPfRows)};
+        if (!encode_tmap(&tq, q, tdt, 3, dims, strides, box)) return PKV_ERR_CUDA;
+    }
+    if (!cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride,
+                    max_num_pages, rows) ||
+        !cache_tmap(&tv, v_cache, tdt, layout, d_vo, page_size, num_kv_heads, v_page_stride,
+                    max_num_pages, rows))
+        return PKV_ERR_CUDA;
+
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int32_t *cu_q = static_cast<int32_t *>(workspace);
     prefill_plan_kernel<<<1, 32, 0, st>>>(actual_seq_lens_q, actual_seq_lens_kv, batch_size,
                                           max_token_per_sequence, max_sequence_kv, cu_q, err_word);
     PrefillParams p;
-    p.q = q;
-    p.k = k_cache;
-    p.v = v_cache;
-    p.k_page_stride = k_page_stride;
-    p.v_page_stride = v_page_stride;
     p.max_num_pages = max_num_pages;
+    p.total_q = total_q;
     p.scale_log2 = scale * kLog2e;
     p.seq_lens_q = actual_seq_lens_q;
     p.seq_lens_kv = actual_seq_lens_kv;
@@ -381,8 +555,8 @@ extern "C" int paged_prefill(const void *q, const void *k_cache, const void *v_c
     int launches = 1;
     if (n_qt > 0) {
         dim3 grid(n_qt, num_qo_heads, batch_size);
-        int rc = dtype == PKV_BF16 ? dispatch_prefill<__nv_bfloat16>(d_qk, layout, p, grid, st)
-                                   : dispatch_prefill<__half>(d_qk, layout, p, grid, st);
+        int rc = dtype == PKV_BF16 ? dispatch_prefill<__nv_bfloat16>(d_qk, layout, tq, tk, tv, p, grid, st)
+                                   : dispatch_prefill<__half>(d_qk, layout, tq, tk, tv, p, grid, st);
         if (rc != PKV_OK) return rc;
         ++launches;
     }

@@ -21,3 +21,44 @@ extern "C" const char *pkv_status_string(int status) {
 }
 
 extern "C" unsigned long long pkv_kernel_launches(void) { return pkv::g_launches.load(); }
+
+// ---- tensor-map encoding through the driver entry point (no libcuda link) ----
+#include <mutex>
+
+#include "sm103_ptx.cuh"
+
+namespace pkv {
+
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_tmap(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int rank,
+                 const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box) {
+    auto fn = tmap_encoder();
+    if (!fn) return false;
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t bdim[5], estride[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estride[i] = 1;
+        if (i < rank - 1) gstride[i] = strides_bytes[i];
+    }
+    CUresult r = fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(base), gdim, gstride,
+                    bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace pkv

@@ -109,7 +109,7 @@ def test_prefill_rejects_bad_arguments(lib):
     good = 0x1000
 
     def call(**over):
-        a = dict(q=good, k=good, v=good, ks=8 * 32 * 128, vs=8 * 32 * 128, pages=100,
+        a = dict(q=good, total_q=150, k=good, v=good, ks=8 * 32 * 128, vs=8 * 32 * 128, pages=100,
                  scale=0.08, ws=good, ws_bytes=4096, maxq=100, maxkv=200, lq=good, lkv=good,
                  bt=good, bt_stride=8, B=2, causal=1, hqo=32, hkv=8, dqk=128, dvo=128, S=32,
                  layout=1, dtype=1, out=good, lse=good, err=None, stream=None)
@@ -122,4 +122,6 @@ def test_prefill_rejects_bad_arguments(lib):
     assert call(lse=None) == 1        # the LSE output is required
     assert call(ws_bytes=8) == 4
     assert call(bt_stride=3) == 2     # 3 pages of 32 < max_sequence_kv 200
+    assert call(S=4) == 3             # TMA boxes need pages of >= 8 slots
+    assert call(total_q=0) == 0       # no query rows: nothing to do
     assert call(B=0) == 0
