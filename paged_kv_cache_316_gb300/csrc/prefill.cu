@@ -8,17 +8,18 @@
 // and the natural-log LSE of the scaled logits.
 //
 // One CTA owns 128 query rows of one qo head and walks the key tiles they
-// can see.  Warp roles (192 threads):
-//   warp 4  TMA producer: Q once, then K and V tiles of BN keys, page by
+// can see.  Warp roles (320 threads):
+//   warp 8  TMA producer: Q once, then K and V tiles of BN keys, page by
 //           page, through a ring of STAGES shared-memory stages;
-//   warp 5  allocates tensor memory and issues the tcgen05 MMAs from one
+//   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
 //           thread: S = Q K^T into one of two TMEM score buffers, then
 //           O += P V into the TMEM output accumulator;
-//   warps 0-3  one thread per query row: read its S row from TMEM, mask,
-//           online softmax in base 2, write P (bf16/fp16) back to shared
-//           memory for the PV MMA, rescale O in TMEM when the running max
-//           grows by more than 2^8, and finally normalise O and write out
-//           and lse.
+//   warps 0-7  two threads per query row, each owning half of its columns:
+//           read S from TMEM, mask, online softmax in base 2 (the pair
+//           agrees on the row max through shared memory), write P
+//           (bf16/fp16) back to shared memory for the PV MMA, rescale O in
+//           TMEM when the running max grows by more than 2^8, and finally
+//           normalise O and write out and lse.
 // Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
 // other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
@@ -29,7 +30,8 @@
 namespace pkv {
 
 constexpr int kPfRows = 128;     // query rows per CTA
-constexpr int kPfThreads = 192;  // 4 softmax warps + TMA warp + MMA warp
+constexpr int kPfThreads = 320;  // 8 softmax warps + TMA warp + MMA warp
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr int kPfDV = 128;
 
 template <int DQK>
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t b_oready = bar0 + 8u * (6 + 3 * STAGES);
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
+    __shared__ float xchg[3][2][kPfRows];  // partial row maxima (2 tiles in flight) and sums
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, h = blockIdx.y;
@@ -151,14 +154,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sfull(i), 1);
-            mbar_init(b_sfree(i), 128);
+            mbar_init(b_sfree(i), 256);
         }
-        mbar_init(b_pfull, 128);
+        mbar_init(b_pfull, 256);
         mbar_init(b_oready, 1);
         abort_s = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&tmem_base_s), TMEM_COLS);
         tmem_relinquish();
     }
@@ -171,8 +174,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         *abort_flag = 1;
         set_err(p.err, PKV_DEV_ERR_TIMEOUT);
     };
+    auto give_up_quiet = [&]() { set_err(p.err, PKV_DEV_ERR_TIMEOUT); };
 
-    if (warp == 4) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
@@ -256,43 +260,57 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        const int r = tid;  // query row of this thread inside the tile
+        // warp w: query rows 32*(w%4) .. +31 (its TMEM lane quarter), key /
+        // output columns [hf*BN/2, (hf+1)*BN/2) of S and [hf*64, hf*64+64)
+        // of O, hf = w/4.  The two threads of a row trade their partial
+        // maxima (and at the end their partial sums) through shared memory.
+        constexpr int HC = BN / 2;  // S columns per thread
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = 32 * q4 + lane;  // query row of this thread inside the tile
+        const int c0 = hf * HC;
         const int pos = shift + i0 + r;
         const int lim = p.causal ? min(pos, kvb - 1) : kvb - 1;  // last visible key
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+        const uint32_t o_col = hf * (kPfDV / 2);
         float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        // the TMEM loads below are warp-collective: a lane that gave up
-        // waiting takes its whole warp out of the loop
+        // A warp whose wait gave up is dead: it skips all TMEM and barrier
+        // traffic but still meets its partner at the named barriers, so no
+        // thread of the CTA waits forever.
+        bool dead = false;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
         for (int j = 0; j < n_tiles; ++j) {
             const int bb = j & 1, s = j % STAGES, u = j / STAGES;
             const int j0 = j * BN;
-            if (!wait_warp(b_sfull(bb), (j >> 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-            float x[BN];
+            float x[HC];
+            float mloc = -INFINITY;
+            if (!dead && !wait_warp(b_sfull(bb), (j >> 1) & 1)) dead = true;
+            if (!dead) {
+                tc_fence_after();
+                uint32_t rr[HC];
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(t_lane + S_COL + bb * BN + c * 32, rr);
+                for (int c = 0; c < HC / 32; ++c)
+                    tmem_ld32(t_lane + S_COL + bb * BN + c0 + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(rr + c * 32));
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(b_sfree(bb));
+                const bool full = j0 + BN - 1 <= lim;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(rr[e]);
+                for (int c = 0; c < HC; ++c) {
+                    float v = __uint_as_float(rr[c]) * p.scale_log2;
+                    if (!full && j0 + c0 + c > lim) v = -INFINITY;
+                    x[c] = v;
+                    m4[c & 3] = fmaxf(m4[c & 3], v);
+                }
+                mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            tc_fence_before();
-            mbar_arrive(b_sfree(bb));
-
-            const bool full = j0 + BN - 1 <= lim;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                float v = x[c] * p.scale_log2;
-                if (!full && j0 + c > lim) v = -INFINITY;
-                x[c] = v;
-                mx = fmaxf(mx, v);
-            }
+            xchg[j & 1][hf][r] = mloc;
+            named_bar_sync(1, 256);
+            if (dead) continue;
+            const float mx = fmaxf(mloc, xchg[j & 1][hf ^ 1][r]);
             float alpha = 1.f;
             bool need = false;
             if (mx != -INFINITY) {
@@ -306,71 +324,74 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
             }
             const float base = m_used == -INFINITY ? 0.f : m_used;
-            float rs = 0.f;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
+            for (int c = 0; c < HC; ++c) {
                 x[c] = fast_exp2(x[c] - base);
-                rs += x[c];
+                s4[c & 3] += x[c];
             }
-            l += rs;
+            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
 
             // the previous PV must be complete before O or the P buffer is touched
-            if (j >= 1 && !wait_warp(b_oready, (j - 1) & 1)) { ok = false; break; }
+            if (j >= 1 && !wait_warp(b_oready, (j - 1) & 1)) { dead = true; continue; }
             tc_fence_after();
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int c = 0; c < kPfDV / 32; ++c) {
+                for (int c = 0; c < kPfDV / 64; ++c) {
                     uint32_t rr[32];
-                    tmem_ld32(t_lane + c * 32, rr);
+                    tmem_ld32(t_lane + o_col + c * 32, rr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                    tmem_st32(t_lane + c * 32, rr);
+                    tmem_st32(t_lane + o_col + c * 32, rr);
                 }
                 tmem_wait_st();
             }
             // rows of V past the sequence end may hold anything (even NaN):
             // zero them so that P = 0 there cannot produce 0 * NaN
             if (j0 < kvb && j0 + BN > kvb) {
-                if (!wait_warp(b_vfull(s), u & 1)) { ok = false; break; }
+                if (!wait_warp(b_vfull(s), u & 1)) { dead = true; continue; }
                 const int z0 = kvb - j0;
                 uint8_t *vbase = v_gen + s * VB;
-                for (int idx = tid; idx < (BN - z0) * 16; idx += 128) {
+                for (int idx = tid; idx < (BN - z0) * 16; idx += 256) {
                     const int row = z0 + (idx >> 4), chunk = idx & 15;
                     *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // P row -> shared memory, 128-byte swizzled K-major (A operand of PV)
+            // my part of the P row -> shared memory, 128-byte swizzled K-major
+            // (A operand of PV): columns c0 .. c0+HC-1
 #pragma unroll
-            for (int a = 0; a < BN / 64; ++a) {
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const float *xv = x + a * 64 + cc * 8;
-                    uint4 w = make_uint4(pack2<T>(xv[0], xv[1]), pack2<T>(xv[2], xv[3]),
-                                         pack2<T>(xv[4], xv[5]), pack2<T>(xv[6], xv[7]));
-                    *reinterpret_cast<uint4 *>(p_gen + a * (kPfRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
-                }
+            for (int cc = 0; cc < HC / 8; ++cc) {
+                const int col = c0 + cc * 8;
+                const int atom = col >> 6, chunk = (col & 63) >> 3;
+                const float *xv = x + cc * 8;
+                uint4 w = make_uint4(pack2<T>(xv[0], xv[1]), pack2<T>(xv[2], xv[3]),
+                                     pack2<T>(xv[4], xv[5]), pack2<T>(xv[6], xv[7]));
+                *reinterpret_cast<uint4 *>(p_gen + atom * (kPfRows * 128) + r * 128 + ((chunk ^ (r & 7)) << 4)) = w;
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(b_pfull);
         }
         // epilogue: O / l -> out, lse
-        if (ok && n_tiles > 0 && !wait_warp(b_oready, (n_tiles - 1) & 1)) ok = false;
-        if (!ok) give_up();
-        const bool have_o = __all_sync(0xffffffffu, ok) && n_tiles > 0;
+        if (!dead && n_tiles > 0 && !wait_warp(b_oready, (n_tiles - 1) & 1)) dead = true;
+        xchg[2][hf][r] = l;
+        named_bar_sync(1, 256);
+        if (dead || __any_sync(0xffffffffu, *abort_flag != 0)) give_up_quiet();
+        const bool have_o = !dead && n_tiles > 0;
+        const float lt = l + xchg[2][hf ^ 1][r];
         tc_fence_after();
         const int qi = i0 + r;
         const int64_t grow = static_cast<int64_t>(row_base) + r;
         const bool valid = qi < qb && grow < p.total_q;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + o_col;
 #pragma unroll
-        for (int c = 0; c < kPfDV / 32; ++c) {
+        for (int c = 0; c < kPfDV / 64; ++c) {
             uint32_t rr[32];
             if (have_o) {
-                tmem_ld32(t_lane + c * 32, rr);
+                tmem_ld32(t_lane + o_col + c * 32, rr);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -388,12 +409,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
             }
         }
-        if (valid) p.lse[grow * p.Hqo + h] = l > 0.f ? (m_used + fast_log2(l)) * kLn2 : -INFINITY;
+        if (valid && hf == 0) p.lse[grow * p.Hqo + h] = lt > 0.f ? (m_used + fast_log2(lt)) * kLn2 : -INFINITY;
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
