@@ -17,7 +17,8 @@
 //   warps 0-7  two threads per query row, each owning half of its columns:
 //           read S from TMEM, mask, online softmax in base 2 (the pair
 //           agrees on the row max through shared memory), write P
-//           (bf16/fp16) back to shared memory for the PV MMA, rescale O in
+//           (bf16/fp16) to one of two shared-memory buffers for the PV MMA
+//           (so the next tile's softmax need not wait for it), rescale O in
 //           TMEM when the running max grows by more than 2^8, and finally
 //           normalise O and write out and lse.
 // Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
@@ -38,7 +39,7 @@ template <int DQK>
 struct PfCfg;
 template <>
 struct PfCfg<128> {
-    static constexpr int BN = 128, STAGES = 2;
+    static constexpr int BN = 64, STAGES = 4;
 };
 template <>
 struct PfCfg<192> {
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of the Q tile
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
-    constexpr uint32_t PB = kPfRows * BN * 2;    // bytes of the P tile
+    constexpr uint32_t PB = kPfRows * BN * 2;    // bytes of one P tile (two of them)
     constexpr uint32_t TMEM_COLS = (kPfDV + 2 * BN) <= 256 ? 256 : 512;
     constexpr uint32_t S_COL = kPfDV;            // S buffers follow the O accumulator
 
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t k_s = q_s + QB;
     const uint32_t v_s = k_s + STAGES * KB;
     const uint32_t p_s = v_s + STAGES * VB;
-    const uint32_t bar0 = p_s + PB;
+    const uint32_t bar0 = p_s + 2 * PB;
     uint8_t *v_gen = smem + QB + STAGES * KB;  // generic pointers to V stages and P
     uint8_t *p_gen = smem + QB + STAGES * (KB + VB);
     const uint32_t b_qfull = bar0;
@@ -125,7 +126,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     auto b_sfull = [&](int i) { return bar0 + 8u * (1 + 3 * STAGES + i); };
     auto b_sfree = [&](int i) { return bar0 + 8u * (3 + 3 * STAGES + i); };
     const uint32_t b_pfull = bar0 + 8u * (5 + 3 * STAGES);
-    const uint32_t b_oready = bar0 + 8u * (6 + 3 * STAGES);
+    // completion of the PV that read P buffer i (and of every MMA before it)
+    auto b_pvdone = [&](int i) { return bar0 + 8u * (6 + 3 * STAGES + i); };
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ float xchg[3][2][kPfRows];  // partial row maxima (2 tiles in flight) and sums
@@ -157,7 +159,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(b_sfree(i), 256);
         }
         mbar_init(b_pfull, 256);
-        mbar_init(b_oready, 1);
+        mbar_init(b_pvdone(0), 1);
+        mbar_init(b_pvdone(1), 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -233,11 +236,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    uint64_t a = umma_sdesc_sw128(p_s + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
+                    uint64_t a = umma_sdesc_sw128(p_s + (jj & 1) * PB + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32,
+                                                  16, 1024);
                     uint64_t bd = umma_sdesc_sw128(v_s + s * VB + kk * 16 * 128, BN * 128, 1024);
                     umma_ss(tmem, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(b_oready);
+                umma_commit(b_pvdone(jj & 1));
                 umma_commit(b_kvempty(s));
                 return true;
             };
@@ -332,10 +336,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
 
-            // the previous PV must be complete before O or the P buffer is touched
-            if (j >= 1 && !wait_warp(b_oready, (j - 1) & 1)) { dead = true; continue; }
+            // P buffer j&1 was last read by PV_{j-2}; the O rescale needs PV_{j-1}
+            // complete.  Each pv_done barrier is only ever waited at its newest
+            // possible phase, so the parity waits are exact.
+            if (j >= 2 && !wait_warp(b_pvdone(j & 1), ((j >> 1) - 1) & 1)) { dead = true; continue; }
+            const bool rescale = __any_sync(0xffffffffu, need);
+            if (rescale && j >= 1 && !wait_warp(b_pvdone((j - 1) & 1), ((j - 1) >> 1) & 1)) { dead = true; continue; }
             tc_fence_after();
-            if (__any_sync(0xffffffffu, need)) {
+            if (rescale) {
 #pragma unroll
                 for (int c = 0; c < kPfDV / 64; ++c) {
                     uint32_t rr[32];
@@ -368,14 +376,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const float *xv = x + cc * 8;
                 uint4 w = make_uint4(pack2<T>(xv[0], xv[1]), pack2<T>(xv[2], xv[3]),
                                      pack2<T>(xv[4], xv[5]), pack2<T>(xv[6], xv[7]));
-                *reinterpret_cast<uint4 *>(p_gen + atom * (kPfRows * 128) + r * 128 + ((chunk ^ (r & 7)) << 4)) = w;
+                *reinterpret_cast<uint4 *>(p_gen + (j & 1) * PB + atom * (kPfRows * 128) + r * 128 +
+                                           ((chunk ^ (r & 7)) << 4)) = w;
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(b_pfull);
         }
         // epilogue: O / l -> out, lse
-        if (!dead && n_tiles > 0 && !wait_warp(b_oready, (n_tiles - 1) & 1)) dead = true;
+        if (!dead && n_tiles > 0 &&
+            !wait_warp(b_pvdone((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1))
+            dead = true;
         xchg[2][hf][r] = l;
         named_bar_sync(1, 256);
         if (dead || __any_sync(0xffffffffu, *abort_flag != 0)) give_up_quiet();
@@ -423,8 +434,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 template <int DQK>
 static size_t prefill_smem_bytes() {
     constexpr int BN = PfCfg<DQK>::BN, STAGES = PfCfg<DQK>::STAGES;
-    return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + kPfRows * BN * 2 +
-           8 * (7 + 3 * STAGES);
+    return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + 2 * kPfRows * BN * 2 +
+           8 * (8 + 3 * STAGES);
 }
 
 template <typename T, int DQK, int LAYOUT>
