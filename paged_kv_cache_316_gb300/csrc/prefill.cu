@@ -14,13 +14,13 @@
 //   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
 //           thread: S = Q K^T into one of two TMEM score buffers, then
 //           O += P V into the TMEM output accumulator;
-//   warps 0-7  two threads per query row, each owning half of its columns:
-//           read S from TMEM, mask, online softmax in base 2 (the pair
-//           agrees on the row max through shared memory), write P
-//           (bf16/fp16) to one of two shared-memory buffers for the PV MMA
-//           (so the next tile's softmax need not wait for it), rescale O in
-//           TMEM when the running max grows by more than 2^8, and finally
-//           normalise O and write out and lse.
+//   warps 0-7  two groups of four warps, one thread per query row each;
+//           group g takes the key tiles j = g, g+2, ...: read S from TMEM,
+//           mask, online softmax in base 2, write P (bf16/fp16) to its own
+//           shared-memory buffer for the PV MMA, which accumulates into the
+//           group's own O in TMEM (rescaled there when the running max grows
+//           by more than 2^8).  At the end the two partial (O, max, sum)
+//           are merged, normalised and written with the LSE.
 // Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
 // other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
@@ -106,8 +106,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
     constexpr uint32_t PB = kPfRows * BN * 2;    // bytes of one P tile (two of them)
-    constexpr uint32_t TMEM_COLS = (kPfDV + 2 * BN) <= 256 ? 256 : 512;
-    constexpr uint32_t S_COL = kPfDV;            // S buffers follow the O accumulator
+    // TMEM columns: O of group 0, O of group 1, then the two S buffers
+    constexpr uint32_t TMEM_COLS = 512;
+    constexpr uint32_t S_COL = 2 * kPfDV;
+    static_assert(2 * kPfDV + 2 * BN <= 512, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -125,12 +127,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     auto b_kvempty = [&](int s) { return bar0 + 8u * (1 + 2 * STAGES + s); };
     auto b_sfull = [&](int i) { return bar0 + 8u * (1 + 3 * STAGES + i); };
     auto b_sfree = [&](int i) { return bar0 + 8u * (3 + 3 * STAGES + i); };
-    const uint32_t b_pfull = bar0 + 8u * (5 + 3 * STAGES);
+    auto b_pfull = [&](int i) { return bar0 + 8u * (5 + 3 * STAGES + i); };
     // completion of the PV that read P buffer i (and of every MMA before it)
-    auto b_pvdone = [&](int i) { return bar0 + 8u * (6 + 3 * STAGES + i); };
+    auto b_pvdone = [&](int i) { return bar0 + 8u * (7 + 3 * STAGES + i); };
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
-    __shared__ float xchg[3][2][kPfRows];  // partial row maxima (2 tiles in flight) and sums
+    __shared__ float xchg[2][2][kPfRows];  // per group: final row max and row sum
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, h = blockIdx.y;
@@ -156,11 +158,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sfull(i), 1);
-            mbar_init(b_sfree(i), 256);
+            mbar_init(b_sfree(i), 128);
+            mbar_init(b_pfull(i), 128);
+            mbar_init(b_pvdone(i), 1);
         }
-        mbar_init(b_pfull, 256);
-        mbar_init(b_pvdone(0), 1);
-        mbar_init(b_pvdone(1), 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             bool ok = mbar_wait(b_qfull, 0, abort_flag);
             auto issue_pv = [&](int jj) -> bool {
                 const int s = jj % STAGES, u = jj / STAGES;
-                if (!mbar_wait(b_pfull, jj & 1, abort_flag)) return false;
+                if (!mbar_wait(b_pfull(jj & 1), (jj >> 1) & 1, abort_flag)) return false;
                 if (!mbar_wait(b_vfull(s), u & 1, abort_flag)) return false;
                 tc_fence_after();
 #pragma unroll
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     uint64_t a = umma_sdesc_sw128(p_s + (jj & 1) * PB + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32,
                                                   16, 1024);
                     uint64_t bd = umma_sdesc_sw128(v_s + s * VB + kk * 16 * 128, BN * 128, 1024);
-                    umma_ss(tmem, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                    umma_ss(tmem + (jj & 1) * kPfDV, a, bd, idesc_pv, (jj > 1 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(b_pvdone(jj & 1));
                 umma_commit(b_kvempty(s));
@@ -264,163 +265,164 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        // warp w: query rows 32*(w%4) .. +31 (its TMEM lane quarter), key /
-        // output columns [hf*BN/2, (hf+1)*BN/2) of S and [hf*64, hf*64+64)
-        // of O, hf = w/4.  The two threads of a row trade their partial
-        // maxima (and at the end their partial sums) through shared memory.
-        constexpr int HC = BN / 2;  // S columns per thread
-        const int q4 = warp & 3, hf = warp >> 2;
-        const int r = 32 * q4 + lane;  // query row of this thread inside the tile
-        const int c0 = hf * HC;
+        // Two independent groups of four warps: group g takes the key tiles
+        // j with j % 2 == g and keeps its own running max, sum, P buffer and
+        // O accumulator (TMEM columns g*128 ..), so the groups never wait
+        // for each other inside the loop and run out of phase (one does its
+        // exponentials while the other loads S or writes P).  Warp w owns
+        // TMEM lanes / query rows 32*(w%4) .. +31, one thread per row.  The
+        // two partial results are merged once at the end.
+        const int g = warp >> 2;
+        const int r = 32 * (warp & 3) + lane;  // query row of this thread inside the tile
         const int pos = shift + i0 + r;
         const int lim = p.causal ? min(pos, kvb - 1) : kvb - 1;  // last visible key
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-        const uint32_t o_col = hf * (kPfDV / 2);
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        const uint32_t o_g = g * kPfDV;  // this group's O columns
+        const int my_tiles = n_tiles > g ? (n_tiles - g + 1) / 2 : 0;
         float m_used = -INFINITY, l = 0.f;
-        // A warp whose wait gave up is dead: it skips all TMEM and barrier
-        // traffic but still meets its partner at the named barriers, so no
-        // thread of the CTA waits forever.
+        // A warp whose wait gave up is dead: it skips the rest of the work but
+        // still meets the others at the final named barrier.
         bool dead = false;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
-        for (int j = 0; j < n_tiles; ++j) {
-            const int bb = j & 1, s = j % STAGES, u = j / STAGES;
+        for (int k = 0; k < my_tiles && !dead; ++k) {
+            const int j = 2 * k + g;
+            const int s = j % STAGES, u = j / STAGES;
             const int j0 = j * BN;
-            float x[HC];
-            float mloc = -INFINITY;
-            if (!dead && !wait_warp(b_sfull(bb), (j >> 1) & 1)) dead = true;
-            if (!dead) {
-                tc_fence_after();
-                uint32_t rr[HC];
+            if (!wait_warp(b_sfull(g), k & 1)) { dead = true; break; }
+            tc_fence_after();
+            float x[BN];
+            {
+                uint32_t rr[BN];
 #pragma unroll
-                for (int c = 0; c < HC / 32; ++c)
-                    tmem_ld32(t_lane + S_COL + bb * BN + c0 + c * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(rr + c * 32));
+                for (int c = 0; c < BN / 32; ++c)
+                    tmem_ld32(t_lane + S_COL + g * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(rr + c * 32));
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(b_sfree(bb));
+                mbar_arrive(b_sfree(g));
                 const bool full = j0 + BN - 1 <= lim;
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < HC; ++c) {
+                for (int c = 0; c < BN; ++c) {
                     float v = __uint_as_float(rr[c]) * p.scale_log2;
-                    if (!full && j0 + c0 + c > lim) v = -INFINITY;
+                    if (!full && j0 + c > lim) v = -INFINITY;
                     x[c] = v;
                     m4[c & 3] = fmaxf(m4[c & 3], v);
                 }
-                mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            }
-            xchg[j & 1][hf][r] = mloc;
-            named_bar_sync(1, 256);
-            if (dead) continue;
-            const float mx = fmaxf(mloc, xchg[j & 1][hf ^ 1][r]);
-            float alpha = 1.f;
-            bool need = false;
-            if (mx != -INFINITY) {
-                if (m_used == -INFINITY) {
-                    m_used = mx;
-                } else if (mx > m_used + 8.f) {
-                    alpha = fast_exp2(m_used - mx);
-                    m_used = mx;
-                    l *= alpha;
-                    need = true;
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                float alpha = 1.f;
+                bool need = false;
+                if (mx != -INFINITY) {
+                    if (m_used == -INFINITY) {
+                        m_used = mx;
+                    } else if (mx > m_used + 8.f) {
+                        alpha = fast_exp2(m_used - mx);
+                        m_used = mx;
+                        l *= alpha;
+                        need = true;
+                    }
                 }
-            }
-            const float base = m_used == -INFINITY ? 0.f : m_used;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                const float base = m_used == -INFINITY ? 0.f : m_used;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < HC; ++c) {
-                x[c] = fast_exp2(x[c] - base);
-                s4[c & 3] += x[c];
-            }
-            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                for (int c = 0; c < BN; ++c) {
+                    x[c] = fast_exp2(x[c] - base);
+                    s4[c & 3] += x[c];
+                }
+                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
 
-            // P buffer j&1 was last read by PV_{j-2}; the O rescale needs PV_{j-1}
-            // complete.  Each pv_done barrier is only ever waited at its newest
-            // possible phase, so the parity waits are exact.
-            if (j >= 2 && !wait_warp(b_pvdone(j & 1), ((j >> 1) - 1) & 1)) { dead = true; continue; }
-            const bool rescale = __any_sync(0xffffffffu, need);
-            if (rescale && j >= 1 && !wait_warp(b_pvdone((j - 1) & 1), ((j - 1) >> 1) & 1)) { dead = true; continue; }
-            tc_fence_after();
-            if (rescale) {
+                // PV_{j-2} (this group's previous PV) must be complete before P
+                // buffer g is rewritten or O_g rescaled; pv_done[g] is only ever
+                // waited at its newest possible phase, so the parity wait is exact.
+                if (k >= 1 && !wait_warp(b_pvdone(g), (k - 1) & 1)) { dead = true; break; }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int c = 0; c < kPfDV / 64; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(t_lane + o_col + c * 32, rr);
-                    tmem_wait_ld();
+                    for (int c = 0; c < kPfDV / 32; ++c) {
+                        uint32_t ro[32];
+                        tmem_ld32(t_lane + o_g + c * 32, ro);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                    tmem_st32(t_lane + o_col + c * 32, rr);
+                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+                        tmem_st32(t_lane + o_g + c * 32, ro);
+                    }
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
             }
             // rows of V past the sequence end may hold anything (even NaN):
             // zero them so that P = 0 there cannot produce 0 * NaN
             if (j0 < kvb && j0 + BN > kvb) {
-                if (!wait_warp(b_vfull(s), u & 1)) { dead = true; continue; }
+                if (!wait_warp(b_vfull(s), u & 1)) { dead = true; break; }
                 const int z0 = kvb - j0;
                 uint8_t *vbase = v_gen + s * VB;
-                for (int idx = tid; idx < (BN - z0) * 16; idx += 256) {
+                for (int idx = r; idx < (BN - z0) * 16; idx += 128) {
                     const int row = z0 + (idx >> 4), chunk = idx & 15;
                     *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // my part of the P row -> shared memory, 128-byte swizzled K-major
-            // (A operand of PV): columns c0 .. c0+HC-1
+            // P row -> P buffer g, 128-byte swizzled K-major (A operand of PV)
 #pragma unroll
-            for (int cc = 0; cc < HC / 8; ++cc) {
-                const int col = c0 + cc * 8;
-                const int atom = col >> 6, chunk = (col & 63) >> 3;
+            for (int cc = 0; cc < BN / 8; ++cc) {
+                const int atom = cc >> 3, chunk = cc & 7;
                 const float *xv = x + cc * 8;
                 uint4 w = make_uint4(pack2<T>(xv[0], xv[1]), pack2<T>(xv[2], xv[3]),
                                      pack2<T>(xv[4], xv[5]), pack2<T>(xv[6], xv[7]));
-                *reinterpret_cast<uint4 *>(p_gen + (j & 1) * PB + atom * (kPfRows * 128) + r * 128 +
+                *reinterpret_cast<uint4 *>(p_gen + g * PB + atom * (kPfRows * 128) + r * 128 +
                                            ((chunk ^ (r & 7)) << 4)) = w;
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(b_pfull);
+            mbar_arrive(b_pfull(g));
         }
-        // epilogue: O / l -> out, lse
-        if (!dead && n_tiles > 0 &&
-            !wait_warp(b_pvdone((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1))
-            dead = true;
-        xchg[2][hf][r] = l;
+        // epilogue: wait for this group's last PV, trade (max, sum) with the
+        // other group, merge the two partial O rows; group g writes output
+        // columns [g*64, g*64+64) and group 0 the LSE
+        if (!dead && my_tiles > 0 && !wait_warp(b_pvdone(g), (my_tiles - 1) & 1)) dead = true;
+        xchg[0][g][r] = m_used;
+        xchg[1][g][r] = l;
         named_bar_sync(1, 256);
         if (dead || __any_sync(0xffffffffu, *abort_flag != 0)) give_up_quiet();
-        const bool have_o = !dead && n_tiles > 0;
-        const float lt = l + xchg[2][hf ^ 1][r];
+        const float m0 = xchg[0][0][r], m1 = xchg[0][1][r];
+        const float M = fmaxf(m0, m1);
+        const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+        const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+        const float lt = xchg[1][0][r] * w0 + xchg[1][1][r] * w1;
+        // O_h holds data only if group h had a tile and nobody gave up
+        const bool ok_all = !__any_sync(0xffffffffu, dead) && *abort_flag == 0;
+        const bool have0 = ok_all && n_tiles > 0, have1 = ok_all && n_tiles > 1;
         tc_fence_after();
         const int qi = i0 + r;
         const int64_t grow = static_cast<int64_t>(row_base) + r;
         const bool valid = qi < qb && grow < p.total_q;
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + o_col;
+        const uint32_t ocol = g * (kPfDV / 2);
+        T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + ocol;
 #pragma unroll
         for (int c = 0; c < kPfDV / 64; ++c) {
-            uint32_t rr[32];
-            if (have_o) {
-                tmem_ld32(t_lane + o_col + c * 32, rr);
-                tmem_wait_ld();
-            } else {
+            uint32_t ra[32], rb[32];
+            if (have0) tmem_ld32(t_lane + ocol + c * 32, ra);
+            if (have1) tmem_ld32(t_lane + kPfDV + ocol + c * 32, rb);
+            if (have0 || have1) tmem_wait_ld();
+            float o[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) rr[e] = 0u;
+            for (int e = 0; e < 32; ++e) {
+                float v = 0.f;
+                if (have0 && w0 != 0.f) v += __uint_as_float(ra[e]) * w0;
+                if (have1 && w1 != 0.f) v += __uint_as_float(rb[e]) * w1;
+                o[e] = v * inv;
             }
             if (valid) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint4 w;
-                    w.x = pack2<T>(__uint_as_float(rr[g * 8 + 0]) * inv, __uint_as_float(rr[g * 8 + 1]) * inv);
-                    w.y = pack2<T>(__uint_as_float(rr[g * 8 + 2]) * inv, __uint_as_float(rr[g * 8 + 3]) * inv);
-                    w.z = pack2<T>(__uint_as_float(rr[g * 8 + 4]) * inv, __uint_as_float(rr[g * 8 + 5]) * inv);
-                    w.w = pack2<T>(__uint_as_float(rr[g * 8 + 6]) * inv, __uint_as_float(rr[g * 8 + 7]) * inv);
-                    *reinterpret_cast<uint4 *>(orow + c * 32 + g * 8) = w;
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w = make_uint4(pack2<T>(o[q * 8 + 0], o[q * 8 + 1]), pack2<T>(o[q * 8 + 2], o[q * 8 + 3]),
+                                         pack2<T>(o[q * 8 + 4], o[q * 8 + 5]), pack2<T>(o[q * 8 + 6], o[q * 8 + 7]));
+                    *reinterpret_cast<uint4 *>(orow + c * 32 + q * 8) = w;
                 }
             }
         }
-        if (valid && hf == 0) p.lse[grow * p.Hqo + h] = lt > 0.f ? (m_used + fast_log2(lt)) * kLn2 : -INFINITY;
+        if (valid && g == 0) p.lse[grow * p.Hqo + h] = lt > 0.f ? (M + fast_log2(lt)) * kLn2 : -INFINITY;
     }
 
     tc_fence_before();
@@ -435,7 +437,7 @@ template <int DQK>
 static size_t prefill_smem_bytes() {
     constexpr int BN = PfCfg<DQK>::BN, STAGES = PfCfg<DQK>::STAGES;
     return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + 2 * kPfRows * BN * 2 +
-           8 * (8 + 3 * STAGES);
+           8 * (9 + 3 * STAGES);
 }
 
 template <typename T, int DQK, int LAYOUT>
