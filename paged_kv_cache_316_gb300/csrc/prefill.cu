@@ -12,12 +12,13 @@
 //   warp 8  TMA producer: Q once, then K and V tiles of BN keys, page by
 //           page, through a ring of STAGES shared-memory stages;
 //   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
-//           thread: S = Q K^T into one of two TMEM score buffers, then
-//           O += P V into the TMEM output accumulator;
+//           thread: S = Q K^T into one of two TMEM score buffers (Q read
+//           from TMEM at d_qk 128, from shared memory at 192), then
+//           O += P V with P read from TMEM;
 //   warps 0-7  two groups of four warps, one thread per query row each;
 //           group g takes the key tiles j = g, g+2, ...: read S from TMEM,
 //           mask, online softmax in base 2, write P (bf16/fp16) to its own
-//           shared-memory buffer for the PV MMA, which accumulates into the
+//           TMEM tile, the A operand of the PV MMA, which accumulates into the
 //           group's own O in TMEM (rescaled there when the running max grows
 //           by more than 2^8).  At the end the two partial (O, max, sum)
 //           are merged, normalised and written with the LSE.
@@ -37,13 +38,18 @@ constexpr int kPfDV = 128;
 
 template <int DQK>
 struct PfCfg;
+// Q_TMEM: Q is copied once into tensor memory and read from there by the QK
+// MMA (no shared-memory operand traffic for it); at d_qk 192 it does not fit
+// next to the two O accumulators and stays in shared memory.
 template <>
 struct PfCfg<128> {
-    static constexpr int BN = 64, STAGES = 4;
+    static constexpr int BN = 64, STAGES = 5;
+    static constexpr bool Q_TMEM = true;
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int BN = 64, STAGES = 3;
+    static constexpr int BN = 64, STAGES = 4;
+    static constexpr bool Q_TMEM = false;
 };
 
 struct PrefillParams {
@@ -105,11 +111,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of the Q tile
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
-    constexpr uint32_t PB = kPfRows * BN * 2;    // bytes of one P tile (two of them)
-    // TMEM columns: O of group 0, O of group 1, then the two S buffers
+    constexpr bool Q_TMEM = PfCfg<DQK>::Q_TMEM;
+    // TMEM columns: O of group 0 and 1, the two S buffers, the two P tiles
+    // (bf16/fp16 packed in pairs), then Q (packed in pairs) when it lives there
     constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t S_COL = 2 * kPfDV;
-    static_assert(2 * kPfDV + 2 * BN <= 512, "TMEM budget");
+    constexpr uint32_t P_COL = S_COL + 2 * BN;
+    constexpr uint32_t Q_COL = P_COL + 2 * (BN / 2);
+    static_assert(Q_COL + (Q_TMEM ? DQK / 2 : 0) <= TMEM_COLS, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -117,10 +126,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t q_s = smem_u32(smem);
     const uint32_t k_s = q_s + QB;
     const uint32_t v_s = k_s + STAGES * KB;
-    const uint32_t p_s = v_s + STAGES * VB;
-    const uint32_t bar0 = p_s + 2 * PB;
-    uint8_t *v_gen = smem + QB + STAGES * KB;  // generic pointers to V stages and P
-    uint8_t *p_gen = smem + QB + STAGES * (KB + VB);
+    const uint32_t bar0 = v_s + STAGES * VB;
+    uint8_t *v_gen = smem + QB + STAGES * KB;  // generic pointers to the V stages and Q
+    const uint8_t *q_gen = smem;
     const uint32_t b_qfull = bar0;
     auto b_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
     auto b_vfull = [&](int s) { return bar0 + 8u * (1 + STAGES + s); };
@@ -130,6 +138,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     auto b_pfull = [&](int i) { return bar0 + 8u * (5 + 3 * STAGES + i); };
     // completion of the PV that read P buffer i (and of every MMA before it)
     auto b_pvdone = [&](int i) { return bar0 + 8u * (7 + 3 * STAGES + i); };
+    const uint32_t b_qtmem = bar0 + 8u * (9 + 3 * STAGES);  // Q copied into TMEM
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ float xchg[2][2][kPfRows];  // per group: final row max and row sum
@@ -162,6 +171,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(b_pfull(i), 128);
             mbar_init(b_pvdone(i), 1);
         }
+        mbar_init(b_qtmem, 128);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -229,7 +239,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
             constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
-            bool ok = mbar_wait(b_qfull, 0, abort_flag);
+            bool ok = Q_TMEM ? mbar_wait(b_qtmem, 0, abort_flag) : mbar_wait(b_qfull, 0, abort_flag);
             auto issue_pv = [&](int jj) -> bool {
                 const int s = jj % STAGES, u = jj / STAGES;
                 if (!mbar_wait(b_pfull(jj & 1), (jj >> 1) & 1, abort_flag)) return false;
@@ -237,10 +247,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    uint64_t a = umma_sdesc_sw128(p_s + (jj & 1) * PB + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32,
-                                                  16, 1024);
                     uint64_t bd = umma_sdesc_sw128(v_s + s * VB + kk * 16 * 128, BN * 128, 1024);
-                    umma_ss(tmem + (jj & 1) * kPfDV, a, bd, idesc_pv, (jj > 1 || kk > 0) ? 1u : 0u);
+                    umma_ts(tmem + (jj & 1) * kPfDV, tmem + P_COL + (jj & 1) * (BN / 2) + kk * 8, bd, idesc_pv,
+                            (jj > 1 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(b_pvdone(jj & 1));
                 umma_commit(b_kvempty(s));
@@ -253,9 +262,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk) {
-                    uint64_t a = umma_sdesc_sw128(q_s + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
                     uint64_t bd = umma_sdesc_sw128(k_s + s * KB + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-                    umma_ss(tmem + S_COL + bb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    if (Q_TMEM) {
+                        umma_ts(tmem + S_COL + bb * BN, tmem + Q_COL + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    } else {
+                        uint64_t a = umma_sdesc_sw128(q_s + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
+                        umma_ss(tmem + S_COL + bb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                 }
                 umma_commit(b_sfull(bb));
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
@@ -286,6 +299,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
+        if (Q_TMEM && g == 0) {
+            // Q row r (128-byte swizzled in shared memory) -> TMEM lane r,
+            // two elements per column: the A operand of every QK MMA
+            if (!wait_warp(b_qfull, 0)) {
+                dead = true;
+            } else {
+#pragma unroll
+                for (int c = 0; c < DQK / 64; ++c) {
+                    uint32_t qr[32];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            q_gen + c * (kPfRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4));
+                        qr[ch * 4 + 0] = v.x;
+                        qr[ch * 4 + 1] = v.y;
+                        qr[ch * 4 + 2] = v.z;
+                        qr[ch * 4 + 3] = v.w;
+                    }
+                    tmem_st32(t_lane + Q_COL + c * 32, qr);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_qtmem);
+            }
+        }
         for (int k = 0; k < my_tiles && !dead; ++k) {
             const int j = 2 * k + g;
             const int s = j % STAGES, u = j / STAGES;
@@ -362,17 +400,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // P row -> P buffer g, 128-byte swizzled K-major (A operand of PV)
+            // P row -> TMEM P tile g (two elements per column): the A operand of PV
 #pragma unroll
-            for (int cc = 0; cc < BN / 8; ++cc) {
-                const int atom = cc >> 3, chunk = cc & 7;
-                const float *xv = x + cc * 8;
-                uint4 w = make_uint4(pack2<T>(xv[0], xv[1]), pack2<T>(xv[2], xv[3]),
-                                     pack2<T>(xv[4], xv[5]), pack2<T>(xv[6], xv[7]));
-                *reinterpret_cast<uint4 *>(p_gen + g * PB + atom * (kPfRows * 128) + r * 128 +
-                                           ((chunk ^ (r & 7)) << 4)) = w;
+            for (int c = 0; c < BN / 64; ++c) {
+                uint32_t pw[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pw[e] = pack2<T>(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1]);
+                tmem_st32(t_lane + P_COL + g * (BN / 2) + c * 32, pw);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
+            fence_proxy_async_smem();  // the zeroed V rows, if any
             tc_fence_before();
             mbar_arrive(b_pfull(g));
         }
@@ -436,8 +473,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 template <int DQK>
 static size_t prefill_smem_bytes() {
     constexpr int BN = PfCfg<DQK>::BN, STAGES = PfCfg<DQK>::STAGES;
-    return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + 2 * kPfRows * BN * 2 +
-           8 * (9 + 3 * STAGES);
+    return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + 8 * (10 + 3 * STAGES);
 }
 
 template <typename T, int DQK, int LAYOUT>
