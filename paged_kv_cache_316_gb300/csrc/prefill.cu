@@ -9,16 +9,16 @@
 //
 // One CTA owns 128 query rows of one qo head and walks the key tiles they
 // can see.  Warp roles (320 threads):
-//   warp 8  TMA producer: Q once, then K and V tiles of BN keys, page by
-//           page, through a ring of STAGES shared-memory stages;
+//   warp 8  TMA producer: Q once, then K and V tiles of 128 keys, page by
+//           page, through separate K and V rings of shared-memory stages;
 //   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
-//           thread: S = Q K^T into one of two TMEM score buffers (Q read
-//           from TMEM at d_qk 128, from shared memory at 192), then
-//           O += P V with P read from TMEM;
+//           thread: S = Q K^T into one of two TMEM score buffers, then
+//           O += P V with P read from TMEM (it overwrites half of its S
+//           buffer);
 //   warps 0-7  two groups of four warps, one thread per query row each;
 //           group g takes the key tiles j = g, g+2, ...: read S from TMEM,
-//           mask, online softmax in base 2, write P (bf16/fp16) to its own
-//           TMEM tile, the A operand of the PV MMA, which accumulates into the
+//           mask, online softmax in base 2, write P (bf16/fp16) into its S
+//           buffer, the A operand of the PV MMA, which accumulates into the
 //           group's own O in TMEM (rescaled there when the running max grows
 //           by more than 2^8).  At the end the two partial (O, max, sum)
 //           are merged, normalised and written with the LSE.
@@ -36,21 +36,19 @@ constexpr int kPfThreads = 320;  // 8 softmax warps + TMA warp + MMA warp
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr int kPfDV = 128;
 
+// Key tiles of BN = 128; separate K and V rings (a K stage is released by
+// its QK, a V stage by its PV).
 template <int DQK>
 struct PfCfg;
-// Q_TMEM: Q is copied once into tensor memory and read from there by the QK
-// MMA (no shared-memory operand traffic for it); at d_qk 192 it does not fit
-// next to the two O accumulators and stays in shared memory.
 template <>
 struct PfCfg<128> {
-    static constexpr int BN = 64, STAGES = 5;
-    static constexpr bool Q_TMEM = true;
+    static constexpr int SK = 3, SV = 2;
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int BN = 64, STAGES = 4;
-    static constexpr bool Q_TMEM = false;
+    static constexpr int SK = 2, SV = 2;
 };
+constexpr int kPfBN = 128;
 
 struct PrefillParams {
     int64_t max_num_pages;
@@ -92,6 +90,7 @@ __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_
     if (lane == 0) cu_q[B] = carry;
 }
 
+
 template <typename T>
 struct IsBf16 {
     static constexpr bool value = false;
@@ -105,40 +104,34 @@ template <typename T, int DQK, int LAYOUT>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    constexpr int BN = PfCfg<DQK>::BN;
-    constexpr int STAGES = PfCfg<DQK>::STAGES;
+    constexpr int BN = kPfBN;
+    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
     constexpr int QA = DQK / 64;                 // 64-column atoms of a Q / K row
     constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of the Q tile
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
-    constexpr bool Q_TMEM = PfCfg<DQK>::Q_TMEM;
-    // TMEM columns: O of group 0 and 1, the two S buffers, the two P tiles
-    // (bf16/fp16 packed in pairs), then Q (packed in pairs) when it lives there
+    // TMEM columns: O of group 0 and 1, then the two S buffers; P of a tile
+    // (16-bit pairs, BN/2 columns) overwrites the first half of its S buffer
     constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t S_COL = 2 * kPfDV;
-    constexpr uint32_t P_COL = S_COL + 2 * BN;
-    constexpr uint32_t Q_COL = P_COL + 2 * (BN / 2);
-    static_assert(Q_COL + (Q_TMEM ? DQK / 2 : 0) <= TMEM_COLS, "TMEM budget");
+    static_assert(S_COL + 2 * BN <= TMEM_COLS, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t q_s = smem_u32(smem);
     const uint32_t k_s = q_s + QB;
-    const uint32_t v_s = k_s + STAGES * KB;
-    const uint32_t bar0 = v_s + STAGES * VB;
-    uint8_t *v_gen = smem + QB + STAGES * KB;  // generic pointers to the V stages and Q
-    const uint8_t *q_gen = smem;
+    const uint32_t v_s = k_s + SK * KB;
+    const uint32_t bar0 = v_s + SV * VB;
+    uint8_t *v_gen = smem + QB + SK * KB;  // generic pointer to the V stages
     const uint32_t b_qfull = bar0;
     auto b_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto b_vfull = [&](int s) { return bar0 + 8u * (1 + STAGES + s); };
-    auto b_kvempty = [&](int s) { return bar0 + 8u * (1 + 2 * STAGES + s); };
-    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + 3 * STAGES + i); };
-    auto b_sfree = [&](int i) { return bar0 + 8u * (3 + 3 * STAGES + i); };
-    auto b_pfull = [&](int i) { return bar0 + 8u * (5 + 3 * STAGES + i); };
-    // completion of the PV that read P buffer i (and of every MMA before it)
-    auto b_pvdone = [&](int i) { return bar0 + 8u * (7 + 3 * STAGES + i); };
-    const uint32_t b_qtmem = bar0 + 8u * (9 + 3 * STAGES);  // Q copied into TMEM
+    auto b_kempty = [&](int s) { return bar0 + 8u * (1 + SK + s); };
+    auto b_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * SK + s); };
+    auto b_vempty = [&](int s) { return bar0 + 8u * (1 + 2 * SK + SV + s); };
+    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + 2 * SK + 2 * SV + i); };
+    auto b_pfull = [&](int i) { return bar0 + 8u * (3 + 2 * SK + 2 * SV + i); };
+    auto b_pvdone = [&](int i) { return bar0 + 8u * (5 + 2 * SK + 2 * SV + i); };
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ float xchg[2][2][kPfRows];  // per group: final row max and row sum
@@ -160,18 +153,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     if (tid == 0) {
         mbar_init(b_qfull, 1);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < SK; ++s) {
             mbar_init(b_kfull(s), 1);
+            mbar_init(b_kempty(s), 1);
+        }
+        for (int s = 0; s < SV; ++s) {
             mbar_init(b_vfull(s), 1);
-            mbar_init(b_kvempty(s), 1);
+            mbar_init(b_vempty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sfull(i), 1);
-            mbar_init(b_sfree(i), 128);
             mbar_init(b_pfull(i), 128);
             mbar_init(b_pvdone(i), 1);
         }
-        mbar_init(b_qtmem, 128);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -204,73 +198,88 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
             const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
             for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % STAGES, u = j / STAGES;
-                if (u > 0 && !mbar_wait(b_kvempty(s), (u - 1) & 1, abort_flag)) {
-                    give_up();
-                    break;
-                }
                 const int j0 = j * BN;
-                mbar_expect_tx(b_kfull(s), KB);
-                mbar_expect_tx(b_vfull(s), VB);
-                for (int r0 = 0; r0 < BN; r0 += RB) {
-                    const int key = j0 + r0;
-                    const int slot0 = key & (S - 1);
+                int pages[BN / 8];  // one entry per TMA box of the tile (page_size >= 8)
+#pragma unroll
+                for (int i = 0; i < BN / 8; ++i) {
+                    const int key = j0 + i * RB;
                     int page = oob;
-                    if (key < kvb) {
+                    if (i * RB < BN && key < kvb) {
                         page = bt[key >> p.page_shift];
                         if (page < 0 || page >= p.max_num_pages) {
                             set_err(p.err, PKV_DEV_ERR_PAGE);
                             page = oob;
                         }
                     }
+                    pages[i] = page;
+                }
+                const int sk = j % SK, uk = j / SK;
+                if (uk > 0 && !mbar_wait(b_kempty(sk), (uk - 1) & 1, abort_flag)) { give_up(); break; }
+                mbar_expect_tx(b_kfull(sk), KB);
+#pragma unroll
+                for (int i = 0; i < BN / 8; ++i) {
+                    if (i * RB >= BN) break;
+                    const int r0 = i * RB;
+                    const int slot0 = (j0 + r0) & (S - 1);
                     const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
                     const int cb = LAYOUT == PKV_HND ? kvh : slot0;
                     for (int c = 0; c < QA; ++c)
-                        tma_load_4d(k_s + s * KB + c * (BN * 128) + r0 * 128, &tm_k, b_kfull(s), c * 64,
-                                    ca, cb, page);
+                        tma_load_4d(k_s + sk * KB + c * (BN * 128) + r0 * 128, &tm_k, b_kfull(sk), c * 64,
+                                    ca, cb, pages[i]);
+                }
+                const int sv = j % SV, uv = j / SV;
+                if (uv > 0 && !mbar_wait(b_vempty(sv), (uv - 1) & 1, abort_flag)) { give_up(); break; }
+                mbar_expect_tx(b_vfull(sv), VB);
+#pragma unroll
+                for (int i = 0; i < BN / 8; ++i) {
+                    if (i * RB >= BN) break;
+                    const int r0 = i * RB;
+                    const int slot0 = (j0 + r0) & (S - 1);
+                    const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
+                    const int cb = LAYOUT == PKV_HND ? kvh : slot0;
                     for (int c = 0; c < kPfDV / 64; ++c)
-                        tma_load_4d(v_s + s * VB + c * (BN * 128) + r0 * 128, &tm_v, b_vfull(s), c * 64,
-                                    ca, cb, page);
+                        tma_load_4d(v_s + sv * VB + c * (BN * 128) + r0 * 128, &tm_v, b_vfull(sv), c * 64,
+                                    ca, cb, pages[i]);
                 }
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
+        // Issue order QK_0, [QK_j, PV_{j-1}] for j >= 1, PV_last.  tcgen05 MMAs
+        // execute in issue order, so QK_{j+2}, which overwrites S buffer j&1,
+        // cannot disturb PV_j reading P_j from the same columns.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
             constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
-            bool ok = Q_TMEM ? mbar_wait(b_qtmem, 0, abort_flag) : mbar_wait(b_qfull, 0, abort_flag);
+            const uint64_t qdesc0 = umma_sdesc_sw128(q_s, 16, 1024);
+            const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
+            const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
+            bool ok = mbar_wait(b_qfull, 0, abort_flag);
             auto issue_pv = [&](int jj) -> bool {
-                const int s = jj % STAGES, u = jj / STAGES;
-                if (!mbar_wait(b_pfull(jj & 1), (jj >> 1) & 1, abort_flag)) return false;
-                if (!mbar_wait(b_vfull(s), u & 1, abort_flag)) return false;
+                const int g = jj & 1, sv = jj % SV, uv = jj / SV;
+                if (!mbar_wait(b_pfull(g), (jj >> 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(b_vfull(sv), uv & 1, abort_flag)) return false;
                 tc_fence_after();
+                const uint64_t vd = vdesc0 + ((sv * VB) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    uint64_t bd = umma_sdesc_sw128(v_s + s * VB + kk * 16 * 128, BN * 128, 1024);
-                    umma_ts(tmem + (jj & 1) * kPfDV, tmem + P_COL + (jj & 1) * (BN / 2) + kk * 8, bd, idesc_pv,
-                            (jj > 1 || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(b_pvdone(jj & 1));
-                umma_commit(b_kvempty(s));
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ts(tmem + g * kPfDV, tmem + S_COL + g * BN + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                            idesc_pv, (jj > 1 || kk > 0) ? 1u : 0u);
+                umma_commit(b_pvdone(g));
+                umma_commit(b_vempty(sv));
                 return true;
             };
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int s = j % STAGES, u = j / STAGES, bb = j & 1;
-                if (!mbar_wait(b_kfull(s), u & 1, abort_flag)) { ok = false; break; }
-                if (j >= 2 && !mbar_wait(b_sfree(bb), ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                const int g = j & 1, sk = j % SK, uk = j / SK;
+                if (!mbar_wait(b_kfull(sk), uk & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                const uint64_t kd = kdesc0 + ((sk * KB) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < DQK / 16; ++kk) {
-                    uint64_t bd = umma_sdesc_sw128(k_s + s * KB + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-                    if (Q_TMEM) {
-                        umma_ts(tmem + S_COL + bb * BN, tmem + Q_COL + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
-                    } else {
-                        uint64_t a = umma_sdesc_sw128(q_s + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
-                        umma_ss(tmem + S_COL + bb * BN, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
-                    }
-                }
-                umma_commit(b_sfull(bb));
+                for (int kk = 0; kk < DQK / 16; ++kk)
+                    umma_ss(tmem + S_COL + g * BN, qdesc0 + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
+                            kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+                umma_commit(b_sfull(g));
+                umma_commit(b_kempty(sk));
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
             if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
@@ -279,18 +288,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax warps
         // Two independent groups of four warps: group g takes the key tiles
-        // j with j % 2 == g and keeps its own running max, sum, P buffer and
-        // O accumulator (TMEM columns g*128 ..), so the groups never wait
-        // for each other inside the loop and run out of phase (one does its
-        // exponentials while the other loads S or writes P).  Warp w owns
-        // TMEM lanes / query rows 32*(w%4) .. +31, one thread per row.  The
-        // two partial results are merged once at the end.
+        // j with j % 2 == g and keeps its own running max, sum and O
+        // accumulator (TMEM columns g*128 ..), so the groups never wait for
+        // each other inside the loop and run out of phase.  Warp w owns TMEM
+        // lanes / query rows 32*(w%4) .. +31, one thread per row.  The two
+        // partial results are merged once at the end.
         const int g = warp >> 2;
         const int r = 32 * (warp & 3) + lane;  // query row of this thread inside the tile
         const int pos = shift + i0 + r;
         const int lim = p.causal ? min(pos, kvb - 1) : kvb - 1;  // last visible key
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        const uint32_t o_g = g * kPfDV;  // this group's O columns
+        const uint32_t t_s = t_lane + S_COL + g * BN;  // this group's S buffer (and P)
+        const uint32_t o_g = g * kPfDV;               // this group's O columns
         const int my_tiles = n_tiles > g ? (n_tiles - g + 1) / 2 : 0;
         float m_used = -INFINITY, l = 0.f;
         // A warp whose wait gave up is dead: it skips the rest of the work but
@@ -299,123 +308,101 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
-        if (Q_TMEM && g == 0) {
-            // Q row r (128-byte swizzled in shared memory) -> TMEM lane r,
-            // two elements per column: the A operand of every QK MMA
-            if (!wait_warp(b_qfull, 0)) {
-                dead = true;
-            } else {
-#pragma unroll
-                for (int c = 0; c < DQK / 64; ++c) {
-                    uint32_t qr[32];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(
-                            q_gen + c * (kPfRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4));
-                        qr[ch * 4 + 0] = v.x;
-                        qr[ch * 4 + 1] = v.y;
-                        qr[ch * 4 + 2] = v.z;
-                        qr[ch * 4 + 3] = v.w;
-                    }
-                    tmem_st32(t_lane + Q_COL + c * 32, qr);
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(b_qtmem);
-            }
-        }
-        for (int k = 0; k < my_tiles && !dead; ++k) {
+        for (int k = 0; k < my_tiles; ++k) {
             const int j = 2 * k + g;
-            const int s = j % STAGES, u = j / STAGES;
             const int j0 = j * BN;
+            // S_j complete; by commit order so is this group's previous PV,
+            // so O_g may be rescaled and the P columns rewritten
             if (!wait_warp(b_sfull(g), k & 1)) { dead = true; break; }
             tc_fence_after();
-            float x[BN];
-            {
-                uint32_t rr[BN];
+            // Two passes over the S row in TMEM, 32 columns at a time (cheap
+            // reads, few live registers): the row max, then the exponentials,
+            // their sum and the packed P, written into the columns the pass has
+            // already consumed (P column e holds keys 2e and 2e+1).
+            const bool full = j0 + BN - 1 <= lim;
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    tmem_ld32(t_lane + S_COL + g * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(rr + c * 32));
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t sr[32];
+                tmem_ld32(t_s + c * 32, sr);
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(b_sfree(g));
-                const bool full = j0 + BN - 1 <= lim;
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    float v = __uint_as_float(rr[c]) * p.scale_log2;
-                    if (!full && j0 + c > lim) v = -INFINITY;
-                    x[c] = v;
-                    m4[c & 3] = fmaxf(m4[c & 3], v);
-                }
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                float alpha = 1.f;
-                bool need = false;
-                if (mx != -INFINITY) {
-                    if (m_used == -INFINITY) {
-                        m_used = mx;
-                    } else if (mx > m_used + 8.f) {
-                        alpha = fast_exp2(m_used - mx);
-                        m_used = mx;
-                        l *= alpha;
-                        need = true;
-                    }
-                }
-                const float base = m_used == -INFINITY ? 0.f : m_used;
-                float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    x[c] = fast_exp2(x[c] - base);
-                    s4[c & 3] += x[c];
-                }
-                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-
-                // PV_{j-2} (this group's previous PV) must be complete before P
-                // buffer g is rewritten or O_g rescaled; pv_done[g] is only ever
-                // waited at its newest possible phase, so the parity wait is exact.
-                if (k >= 1 && !wait_warp(b_pvdone(g), (k - 1) & 1)) { dead = true; break; }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-                    for (int c = 0; c < kPfDV / 32; ++c) {
-                        uint32_t ro[32];
-                        tmem_ld32(t_lane + o_g + c * 32, ro);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
-                        tmem_st32(t_lane + o_g + c * 32, ro);
-                    }
-                    tmem_wait_st();
+                for (int e = 0; e < 32; ++e) {
+                    float v = __uint_as_float(sr[e]) * p.scale_log2;
+                    if (!full && j0 + c * 32 + e > lim) v = -INFINITY;
+                    m4[e & 3] = fmaxf(m4[e & 3], v);
                 }
             }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            float alpha = 1.f;
+            bool need = false;
+            if (mx != -INFINITY) {
+                if (m_used == -INFINITY) {
+                    m_used = mx;
+                } else if (mx > m_used + 8.f) {
+                    alpha = fast_exp2(m_used - mx);
+                    m_used = mx;
+                    l *= alpha;
+                    need = true;
+                }
+            }
+            const float base = m_used == -INFINITY ? 0.f : m_used;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t sr[32], pw[16];
+                tmem_ld32(t_s + c * 32, sr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float v0 = __uint_as_float(sr[2 * e]) * p.scale_log2;
+                    float v1 = __uint_as_float(sr[2 * e + 1]) * p.scale_log2;
+                    if (!full && j0 + c * 32 + 2 * e > lim) v0 = -INFINITY;
+                    if (!full && j0 + c * 32 + 2 * e + 1 > lim) v1 = -INFINITY;
+                    const float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
+                    s4[e & 3] += p0;
+                    s4[(e + 2) & 3] += p1;
+                    pw[e] = pack2<T>(p0, p1);
+                }
+                tmem_st16(t_s + c * 16, pw);
+            }
+            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            const float alpha_keep = alpha;
+            const bool need_keep = need;
             // rows of V past the sequence end may hold anything (even NaN):
             // zero them so that P = 0 there cannot produce 0 * NaN
             if (j0 < kvb && j0 + BN > kvb) {
-                if (!wait_warp(b_vfull(s), u & 1)) { dead = true; break; }
+                const int sv = j % SV, uv = j / SV;
+                if (!wait_warp(b_vfull(sv), uv & 1)) { dead = true; break; }
                 const int z0 = kvb - j0;
-                uint8_t *vbase = v_gen + s * VB;
+                uint8_t *vbase = v_gen + sv * VB;
                 for (int idx = r; idx < (BN - z0) * 16; idx += 128) {
                     const int row = z0 + (idx >> 4), chunk = idx & 15;
                     *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
             }
-            // P row -> TMEM P tile g (two elements per column): the A operand of PV
+            // O_g *= alpha when the running max moved (rare: threshold 2^8)
+            if (__any_sync(0xffffffffu, need_keep)) {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
-                uint32_t pw[32];
+                for (int c = 0; c < kPfDV / 32; ++c) {
+                    uint32_t ro[32];
+                    tmem_ld32(t_lane + o_g + c * 32, ro);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pw[e] = pack2<T>(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1]);
-                tmem_st32(t_lane + P_COL + g * (BN / 2) + c * 32, pw);
+                    for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha_keep);
+                    tmem_st32(t_lane + o_g + c * 32, ro);
+                }
             }
             tmem_wait_st();
-            fence_proxy_async_smem();  // the zeroed V rows, if any
             tc_fence_before();
             mbar_arrive(b_pfull(g));
         }
-        // epilogue: wait for this group's last PV, trade (max, sum) with the
-        // other group, merge the two partial O rows; group g writes output
-        // columns [g*64, g*64+64) and group 0 the LSE
+        // epilogue: wait for this group's last PV (the newest phase of its
+        // pv_done barrier), trade (max, sum) with the other group, merge the
+        // two partial O rows; group g writes output columns [g*64, g*64+64)
+        // and group 0 the LSE
         if (!dead && my_tiles > 0 && !wait_warp(b_pvdone(g), (my_tiles - 1) & 1)) dead = true;
         xchg[0][g][r] = m_used;
         xchg[1][g][r] = l;
@@ -472,8 +459,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 template <int DQK>
 static size_t prefill_smem_bytes() {
-    constexpr int BN = PfCfg<DQK>::BN, STAGES = PfCfg<DQK>::STAGES;
-    return 1024 + kPfRows * DQK * 2 + STAGES * (BN * DQK * 2 + BN * kPfDV * 2) + 8 * (10 + 3 * STAGES);
+    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
+    return 1024 + kPfRows * DQK * 2 + SK * kPfBN * DQK * 2 + SV * kPfBN * kPfDV * 2 + 8 * (7 + 2 * SK + 2 * SV);
 }
 
 template <typename T, int DQK, int LAYOUT>
@@ -580,8 +567,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
 
     const CUtensorMapDataType tdt =
         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const int BN = d_qk == 128 ? PfCfg<128>::BN : PfCfg<192>::BN;
-    const int rows = page_size < BN ? page_size : BN;
+    const int rows = page_size < kPfBN ? page_size : kPfBN;
     CUtensorMap tq, tk, tv;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),
