@@ -8,9 +8,10 @@
 // and the natural-log LSE of the scaled logits.
 //
 // One CTA owns 128 query rows of one qo head and walks the key tiles they
-// can see.  Warp roles (320 threads):
-//   warp 8  TMA producer: Q once, then K and V tiles of 128 keys, page by
-//           page, through separate K and V rings of shared-memory stages;
+// can see.  Warp roles (352 threads):
+//   warps 8, 10  TMA producers: Q once and the K tiles (warp 8), the V tiles
+//           (warp 10), 128 keys page by page, through separate K and V rings
+//           of shared-memory stages;
 //   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
 //           thread: S = Q K^T into one of two TMEM score buffers, then
 //           O += P V with P read from TMEM (it overwrites half of its S
@@ -32,8 +33,8 @@
 namespace pkv {
 
 constexpr int kPfRows = 128;     // query rows per CTA
-constexpr int kPfThreads = 320;  // 8 softmax warps + TMA warp + MMA warp
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kPfThreads = 352;  // 8 softmax warps + K-load warp + MMA warp + V-load warp
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kTmaVWarp = 10;
 constexpr int kPfDV = 128;
 
 // Key tiles of BN = 128; separate K and V rings (a K stage is released by
@@ -184,62 +185,59 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     };
     auto give_up_quiet = [&]() { set_err(p.err, PKV_DEV_ERR_TIMEOUT); };
 
-    if (warp == kTmaWarp) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == kTmaWarp || warp == kTmaVWarp) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 8 loads Q and the K tiles, warp 10 the V tiles: a K stage is
+        // released by its QK and a V stage by its (much later) PV, so the two
+        // rings advance independently and K runs ahead of the MMA.
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            mbar_expect_tx(b_qfull, QB);
-            for (int c = 0; c < QA; ++c)
-                tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, h, row_base);
+            const bool is_k = warp == kTmaWarp;
+            if (is_k) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                mbar_expect_tx(b_qfull, QB);
+                for (int c = 0; c < QA; ++c)
+                    tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, h, row_base);
+            } else {
+                prefetch_tmap(&tm_v);
+            }
             const int S = 1 << p.page_shift;
             const int RB = S < BN ? S : BN;  // rows per TMA box
             const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
             const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
+            const int NS = is_k ? SK : SV;
             for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % NS, us = j / NS;
+                if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag)) {
+                    give_up();
+                    break;
+                }
+                const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
+                mbar_expect_tx(full, is_k ? KB : VB);
                 const int j0 = j * BN;
-                int pages[BN / 8];  // one entry per TMA box of the tile (page_size >= 8)
-#pragma unroll
-                for (int i = 0; i < BN / 8; ++i) {
-                    const int key = j0 + i * RB;
+#pragma unroll 1
+                for (int r0 = 0; r0 < BN; r0 += RB) {
+                    const int key = j0 + r0;
                     int page = oob;
-                    if (i * RB < BN && key < kvb) {
+                    if (key < kvb) {
                         page = bt[key >> p.page_shift];
                         if (page < 0 || page >= p.max_num_pages) {
-                            set_err(p.err, PKV_DEV_ERR_PAGE);
+                            if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
                             page = oob;
                         }
                     }
-                    pages[i] = page;
-                }
-                const int sk = j % SK, uk = j / SK;
-                if (uk > 0 && !mbar_wait(b_kempty(sk), (uk - 1) & 1, abort_flag)) { give_up(); break; }
-                mbar_expect_tx(b_kfull(sk), KB);
-#pragma unroll
-                for (int i = 0; i < BN / 8; ++i) {
-                    if (i * RB >= BN) break;
-                    const int r0 = i * RB;
-                    const int slot0 = (j0 + r0) & (S - 1);
+                    const int slot0 = key & (S - 1);
                     const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
                     const int cb = LAYOUT == PKV_HND ? kvh : slot0;
-                    for (int c = 0; c < QA; ++c)
-                        tma_load_4d(k_s + sk * KB + c * (BN * 128) + r0 * 128, &tm_k, b_kfull(sk), c * 64,
-                                    ca, cb, pages[i]);
-                }
-                const int sv = j % SV, uv = j / SV;
-                if (uv > 0 && !mbar_wait(b_vempty(sv), (uv - 1) & 1, abort_flag)) { give_up(); break; }
-                mbar_expect_tx(b_vfull(sv), VB);
-#pragma unroll
-                for (int i = 0; i < BN / 8; ++i) {
-                    if (i * RB >= BN) break;
-                    const int r0 = i * RB;
-                    const int slot0 = (j0 + r0) & (S - 1);
-                    const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
-                    const int cb = LAYOUT == PKV_HND ? kvh : slot0;
-                    for (int c = 0; c < kPfDV / 64; ++c)
-                        tma_load_4d(v_s + sv * VB + c * (BN * 128) + r0 * 128, &tm_v, b_vfull(sv), c * 64,
-                                    ca, cb, pages[i]);
+                    if (is_k) {
+                        for (int c = 0; c < QA; ++c)
+                            tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca, cb,
+                                        page);
+                    } else {
+                        for (int c = 0; c < kPfDV / 64; ++c)
+                            tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca, cb,
+                                        page);
+                    }
                 }
             }
         }
@@ -315,23 +313,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             // so O_g may be rescaled and the P columns rewritten
             if (!wait_warp(b_sfull(g), k & 1)) { dead = true; break; }
             tc_fence_after();
-            // Two passes over the S row in TMEM, 32 columns at a time (cheap
-            // reads, few live registers): the row max, then the exponentials,
-            // their sum and the packed P, written into the columns the pass has
-            // already consumed (P column e holds keys 2e and 2e+1).
+            // The S row: all BN columns in one batch of TMEM loads and a single
+            // wait (TMEM latency is high while the tensor core is busy), then
+            // mask, max, exponentials and the packed P row, all in place.
+            uint32_t sx[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+                tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
+            tmem_wait_ld();
             const bool full = j0 + BN - 1 <= lim;
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t sr[32];
-                tmem_ld32(t_s + c * 32, sr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float v = __uint_as_float(sr[e]) * p.scale_log2;
-                    if (!full && j0 + c * 32 + e > lim) v = -INFINITY;
-                    m4[e & 3] = fmaxf(m4[e & 3], v);
-                }
+            for (int c = 0; c < BN; ++c) {
+                float v = __uint_as_float(sx[c]) * p.scale_log2;
+                if (!full && j0 + c > lim) v = -INFINITY;
+                sx[c] = __float_as_uint(v);
+                m4[c & 3] = fmaxf(m4[c & 3], v);
             }
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             float alpha = 1.f;
@@ -349,23 +346,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const float base = m_used == -INFINITY ? 0.f : m_used;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t sr[32], pw[16];
-                tmem_ld32(t_s + c * 32, sr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float v0 = __uint_as_float(sr[2 * e]) * p.scale_log2;
-                    float v1 = __uint_as_float(sr[2 * e + 1]) * p.scale_log2;
-                    if (!full && j0 + c * 32 + 2 * e > lim) v0 = -INFINITY;
-                    if (!full && j0 + c * 32 + 2 * e + 1 > lim) v1 = -INFINITY;
-                    const float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
-                    s4[e & 3] += p0;
-                    s4[(e + 2) & 3] += p1;
-                    pw[e] = pack2<T>(p0, p1);
-                }
-                tmem_st16(t_s + c * 16, pw);
+            for (int e = 0; e < BN / 2; ++e) {
+                const float p0 = fast_exp2(__uint_as_float(sx[2 * e]) - base);
+                const float p1 = fast_exp2(__uint_as_float(sx[2 * e + 1]) - base);
+                s4[e & 3] += p0;
+                s4[(e + 2) & 3] += p1;
+                sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1
             }
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+                tmem_st32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             const float alpha_keep = alpha;
             const bool need_keep = need;
