@@ -92,6 +92,24 @@ __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_
 }
 
 
+// 2^x on the FMA pipe, for part of the softmax exponentials (the rest use
+// the special-function unit): x = n + f with n = round(x) taken from the
+// low mantissa bits of x + 1.5*2^23, f in [-1/2, 1/2]; 2^f from the degree-4
+// polynomial interpolating 2^f at the Chebyshev nodes of [-1/2, 1/2]
+// (coefficients from exp2_poly_fit.py beside this file, max relative error
+// 3.6e-6); 2^n added to the exponent bits.  x = -inf (a masked key) gives 0.
+__device__ __forceinline__ float exp2_fma(float x) {
+    const float xc = fmaxf(x, -126.f);
+    const float t = xc + 12582912.f;
+    const float f = xc - (t - 12582912.f);
+    float q = fmaf(9.666368365e-03f, f, 5.592197552e-02f);
+    q = fmaf(q, f, 2.402234972e-01f);
+    q = fmaf(q, f, 6.931210160e-01f);
+    q = fmaf(q, f, 1.0f);
+    const float r = __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+    return x < -126.f ? 0.f : r;
+}
+
 template <typename T>
 struct IsBf16 {
     static constexpr bool value = false;
@@ -322,15 +340,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
             tmem_wait_ld();
             const bool full = j0 + BN - 1 <= lim;
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            // row max: on the raw scores when the scale is positive (then
+            // max(scale * s) = scale * max(s) and one FFMA per element later
+            // does both the scaling and the shift), else on the scaled ones
+            const float sc = p.scale_log2;
+            const bool pos_scale = sc > 0.f;
+            float m8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
+                           -INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
-                float v = __uint_as_float(sx[c]) * p.scale_log2;
+                float v = __uint_as_float(sx[c]);
+                if (!pos_scale) v *= sc;
                 if (!full && j0 + c > lim) v = -INFINITY;
                 sx[c] = __float_as_uint(v);
-                m4[c & 3] = fmaxf(m4[c & 3], v);
+                m8[c & 7] = fmaxf(m8[c & 7], v);
             }
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            if (pos_scale) mx *= sc;
+            const float k_mul = pos_scale ? sc : 1.f;  // x = s * k_mul - base
             float alpha = 1.f;
             bool need = false;
             if (mx != -INFINITY) {
@@ -347,8 +375,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < BN / 2; ++e) {
-                const float p0 = fast_exp2(__uint_as_float(sx[2 * e]) - base);
-                const float p1 = fast_exp2(__uint_as_float(sx[2 * e + 1]) - base);
+                const float x0 = fmaf(__uint_as_float(sx[2 * e]), k_mul, -base);
+                const float x1 = fmaf(__uint_as_float(sx[2 * e + 1]), k_mul, -base);
+                // one pair in four on the FMA pipe, the rest on the SFU
+                const float p0 = (e & 3) == 3 ? exp2_fma(x0) : fast_exp2(x0);
+                const float p1 = (e & 3) == 3 ? exp2_fma(x1) : fast_exp2(x1);
                 s4[e & 3] += p0;
                 s4[(e + 2) & 3] += p1;
                 sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1
