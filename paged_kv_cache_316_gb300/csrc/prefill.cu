@@ -13,16 +13,17 @@
 //           (warp 10), 128 keys page by page, through separate K and V rings
 //           of shared-memory stages;
 //   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
-//           thread: S = Q K^T into one of two TMEM score buffers, then
-//           O += P V with P read from TMEM (it overwrites half of its S
-//           buffer);
+//           thread: S = Q K^T into one of two TMEM score buffers (so the
+//           next tile's QK overlaps this tile's softmax), then per group
+//           O_g += P_g V_g with P read from TMEM;
 //   warps 0-7  two groups of four warps, one thread per query row each;
-//           group g takes the key tiles j = g, g+2, ...: read S from TMEM,
-//           mask, online softmax in base 2, write P (bf16/fp16) into its S
-//           buffer, the A operand of the PV MMA, which accumulates into the
-//           group's own O in TMEM (rescaled there when the running max grows
-//           by more than 2^8).  At the end the two partial (O, max, sum)
-//           are merged, normalised and written with the LSE.
+//           group g owns keys [64g, 64g+64) of every tile: read its S
+//           columns from TMEM, mask, online softmax in base 2, write P
+//           (bf16/fp16) over the consumed S columns as the A operand of its
+//           PV MMA, which accumulates into the group's own O in TMEM
+//           (rescaled there when the running max grows by more than 2^8).
+//           At the end the two partial (O, max, sum) are merged, normalised
+//           and written with the LSE.
 // Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
 // other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
@@ -109,6 +110,12 @@ __device__ __forceinline__ float exp2_fma(float x) {
     const float r = __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
     return x < -126.f ? 0.f : r;
 }
+
+// Share of the softmax exponentials computed by exp2_fma (one pair in
+// kExpFmaEvery; 0 = none).  Measured on GB300 with the ragged-prefill
+// workload: the special-function unit is not the bottleneck of this kernel,
+// and moving work to the FMA pipe costs issue slots, so it is off.
+constexpr int kExpFmaEvery = 0;
 
 template <typename T>
 struct IsBf16 {
@@ -261,9 +268,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Issue order QK_0, [QK_j, PV_{j-1}] for j >= 1, PV_last.  tcgen05 MMAs
-        // execute in issue order, so QK_{j+2}, which overwrites S buffer j&1,
-        // cannot disturb PV_j reading P_j from the same columns.
+        // Issue order QK_0, then for every tile j: QK_{j+1}, PV_{j,0}, PV_{j,1}.
+        // QK_{j+1} runs on the tensor core while the softmax works on S_j.
+        // tcgen05 MMAs execute in issue order, so QK_{j+2}, which overwrites
+        // S buffer j&1, cannot disturb PV_j reading P_j from it.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
             constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
@@ -271,52 +279,59 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
             const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
             bool ok = mbar_wait(b_qfull, 0, abort_flag);
-            auto issue_pv = [&](int jj) -> bool {
-                const int g = jj & 1, sv = jj % SV, uv = jj / SV;
-                if (!mbar_wait(b_pfull(g), (jj >> 1) & 1, abort_flag)) return false;
-                if (!mbar_wait(b_vfull(sv), uv & 1, abort_flag)) return false;
-                tc_fence_after();
-                const uint64_t vd = vdesc0 + ((sv * VB) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(tmem + g * kPfDV, tmem + S_COL + g * BN + kk * 8, vd + ((kk * 16 * 128) >> 4),
-                            idesc_pv, (jj > 1 || kk > 0) ? 1u : 0u);
-                umma_commit(b_pvdone(g));
-                umma_commit(b_vempty(sv));
-                return true;
-            };
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int g = j & 1, sk = j % SK, uk = j / SK;
-                if (!mbar_wait(b_kfull(sk), uk & 1, abort_flag)) { ok = false; break; }
+            auto issue_qk = [&](int j) -> bool {
+                const int sk = j % SK, uk = j / SK;
+                if (!mbar_wait(b_kfull(sk), uk & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t kd = kdesc0 + ((sk * KB) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk)
-                    umma_ss(tmem + S_COL + g * BN, qdesc0 + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
+                    umma_ss(tmem + S_COL + (j & 1) * BN,
+                            qdesc0 + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
                             kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-                umma_commit(b_sfull(g));
+                umma_commit(b_sfull(j & 1));
                 umma_commit(b_kempty(sk));
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                const int sv = j % SV, uv = j / SV;
+                const uint64_t vd = vdesc0 + ((sv * VB) >> 4);
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait(b_pfull(hh), j & 1, abort_flag)) return false;
+                    if (hh == 0 && !mbar_wait(b_vfull(sv), uv & 1, abort_flag)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BN / 32; ++kk)
+                        umma_ts(tmem + hh * kPfDV, tmem + S_COL + (j & 1) * BN + hh * (BN / 2) + kk * 8,
+                                vd + (((hh * (BN / 2) + kk * 16) * 128) >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(b_pvdone(hh));
+                }
+                umma_commit(b_vempty(sv));
+                return true;
+            };
+            if (ok && n_tiles > 0) ok = issue_qk(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
+                if (!issue_pv(j)) { ok = false; break; }
             }
-            if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
             if (!ok) give_up();
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Two independent groups of four warps: group g takes the key tiles
-        // j with j % 2 == g and keeps its own running max, sum and O
-        // accumulator (TMEM columns g*128 ..), so the groups never wait for
-        // each other inside the loop and run out of phase.  Warp w owns TMEM
-        // lanes / query rows 32*(w%4) .. +31, one thread per row.  The two
-        // partial results are merged once at the end.
+        // Two groups of four warps split every key tile by columns: group g
+        // owns keys [64g, 64g+64) of each tile and keeps its own running max,
+        // sum and O accumulator (TMEM columns g*128 ..), so the groups never
+        // exchange anything inside the loop.  Warp w owns TMEM lanes / query
+        // rows 32*(w%4) .. +31, one thread per (row, group).  The two partial
+        // results are merged once at the end.
+        constexpr int HC = BN / 2;  // S columns per thread
         const int g = warp >> 2;
         const int r = 32 * (warp & 3) + lane;  // query row of this thread inside the tile
         const int pos = shift + i0 + r;
         const int lim = p.causal ? min(pos, kvb - 1) : kvb - 1;  // last visible key
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        const uint32_t t_s = t_lane + S_COL + g * BN;  // this group's S buffer (and P)
-        const uint32_t o_g = g * kPfDV;               // this group's O columns
-        const int my_tiles = n_tiles > g ? (n_tiles - g + 1) / 2 : 0;
+        const uint32_t o_g = g * kPfDV;  // this group's O columns
+        const int my_tiles = n_tiles;
         float m_used = -INFINITY, l = 0.f;
         // A warp whose wait gave up is dead: it skips the rest of the work but
         // still meets the others at the final named barrier.
@@ -324,22 +339,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
-        for (int k = 0; k < my_tiles; ++k) {
-            const int j = 2 * k + g;
-            const int j0 = j * BN;
-            // S_j complete; by commit order so is this group's previous PV,
-            // so O_g may be rescaled and the P columns rewritten
-            if (!wait_warp(b_sfull(g), k & 1)) { dead = true; break; }
+        for (int j = 0; j < n_tiles; ++j) {
+            const int j0 = j * BN + g * HC;  // first key of this thread's columns
+            const uint32_t t_s = t_lane + S_COL + (j & 1) * BN + g * HC;
+            // S_j complete; by commit order so is PV_{j-2}, the last reader of
+            // the P columns about to be rewritten
+            if (!wait_warp(b_sfull(j & 1), (j >> 1) & 1)) { dead = true; break; }
             tc_fence_after();
-            // The S row: all BN columns in one batch of TMEM loads and a single
-            // wait (TMEM latency is high while the tensor core is busy), then
-            // mask, max, exponentials and the packed P row, all in place.
-            uint32_t sx[BN];
+            uint32_t sx[HC];
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
+            for (int c = 0; c < HC / 32; ++c)
                 tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
             tmem_wait_ld();
-            const bool full = j0 + BN - 1 <= lim;
+            const bool full = j0 + HC - 1 <= lim;
             // row max: on the raw scores when the scale is positive (then
             // max(scale * s) = scale * max(s) and one FFMA per element later
             // does both the scaling and the shift), else on the scaled ones
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             float m8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
                            -INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
+            for (int c = 0; c < HC; ++c) {
                 float v = __uint_as_float(sx[c]);
                 if (!pos_scale) v *= sc;
                 if (!full && j0 + c > lim) v = -INFINITY;
@@ -374,45 +386,48 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const float base = m_used == -INFINITY ? 0.f : m_used;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < BN / 2; ++e) {
+            for (int e = 0; e < HC / 2; ++e) {
                 const float x0 = fmaf(__uint_as_float(sx[2 * e]), k_mul, -base);
                 const float x1 = fmaf(__uint_as_float(sx[2 * e + 1]), k_mul, -base);
-                // one pair in four on the FMA pipe, the rest on the SFU
-                const float p0 = (e & 3) == 3 ? exp2_fma(x0) : fast_exp2(x0);
-                const float p1 = (e & 3) == 3 ? exp2_fma(x1) : fast_exp2(x1);
+                // pairs e with e % kExpFmaEvery == kExpFmaEvery - 1 on the FMA
+                // pipe, the rest on the special-function unit
+                const bool on_fma = kExpFmaEvery > 0 && (e % (kExpFmaEvery > 0 ? kExpFmaEvery : 1)) == kExpFmaEvery - 1;
+                const float p0 = on_fma ? exp2_fma(x0) : fast_exp2(x0);
+                const float p1 = on_fma ? exp2_fma(x1) : fast_exp2(x1);
                 s4[e & 3] += p0;
                 s4[(e + 2) & 3] += p1;
-                sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1
+                sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1 of this half
             }
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-                tmem_st32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
+            // P (HC keys, HC/2 columns) over the consumed first half of my S columns
+            tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(sx));
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-            const float alpha_keep = alpha;
-            const bool need_keep = need;
             // rows of V past the sequence end may hold anything (even NaN):
-            // zero them so that P = 0 there cannot produce 0 * NaN
-            if (j0 < kvb && j0 + BN > kvb) {
+            // zero the ones this group's PV reads so that P = 0 there cannot
+            // produce 0 * NaN
+            if (j0 + HC > kvb) {  // some of this group's keys lie past the end
                 const int sv = j % SV, uv = j / SV;
                 if (!wait_warp(b_vfull(sv), uv & 1)) { dead = true; break; }
-                const int z0 = kvb - j0;
+                const int zs = max(kvb - j * BN, g * HC), ze = (g + 1) * HC;  // stage rows to zero
                 uint8_t *vbase = v_gen + sv * VB;
-                for (int idx = r; idx < (BN - z0) * 16; idx += 128) {
-                    const int row = z0 + (idx >> 4), chunk = idx & 15;
+                for (int idx = r; idx < (ze - zs) * 16; idx += 128) {
+                    const int row = zs + (idx >> 4), chunk = idx & 15;
                     *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
-            // O_g *= alpha when the running max moved (rare: threshold 2^8)
-            if (__any_sync(0xffffffffu, need_keep)) {
+            // O_g *= alpha when the running max moved (rare: threshold 2^8);
+            // PV_{j-1} of this group must be complete first
+            if (__any_sync(0xffffffffu, need)) {
+                if (j >= 1 && !wait_warp(b_pvdone(g), (j - 1) & 1)) { dead = true; break; }
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < kPfDV / 32; ++c) {
                     uint32_t ro[32];
                     tmem_ld32(t_lane + o_g + c * 32, ro);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha_keep);
+                    for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
                     tmem_st32(t_lane + o_g + c * 32, ro);
                 }
             }
@@ -436,7 +451,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float lt = xchg[1][0][r] * w0 + xchg[1][1][r] * w1;
         // O_h holds data only if group h had a tile and nobody gave up
         const bool ok_all = !__any_sync(0xffffffffu, dead) && *abort_flag == 0;
-        const bool have0 = ok_all && n_tiles > 0, have1 = ok_all && n_tiles > 1;
+        const bool have0 = ok_all && n_tiles > 0, have1 = ok_all && n_tiles > 0;
         tc_fence_after();
         const int qi = i0 + r;
         const int64_t grow = static_cast<int64_t>(row_base) + r;
