@@ -214,9 +214,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // ------------------------------------------------------------ TMA producers
         // warp 8 loads Q and the K tiles, warp 10 the V tiles: a K stage is
         // released by its QK and a V stage by its (much later) PV, so the two
-        // rings advance independently and K runs ahead of the MMA.
+        // rings advance independently and K runs ahead of the MMA.  The
+        // whole warp looks up a tile's page ids in one coalesced load, one
+        // tile ahead; lane 0 issues the copies.
+        const bool is_k = warp == kTmaWarp;
         if (lane == 0) {
-            const bool is_k = warp == kTmaWarp;
             if (is_k) {
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
@@ -226,45 +228,62 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             } else {
                 prefetch_tmap(&tm_v);
             }
-            const int S = 1 << p.page_shift;
-            const int RB = S < BN ? S : BN;  // rows per TMA box
-            const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
-            const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
-            const int NS = is_k ? SK : SV;
-            for (int j = 0; j < n_tiles; ++j) {
+        }
+        const int S = 1 << p.page_shift;
+        const int RB = S < BN ? S : BN;  // rows per TMA box
+        const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
+        const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
+        const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
+        const int NS = is_k ? SK : SV;
+        auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
+            const int key = j * BN + lane * RB;
+            int page = oob;
+            if (lane < nbox && key < kvb) {
+                page = bt[key >> p.page_shift];
+                if (page < 0 || page >= p.max_num_pages) {
+                    if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
+                    page = oob;
+                }
+            }
+            return page;
+        };
+        int pg_next = n_tiles > 0 ? lookup(0) : oob;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int pg = pg_next;
+            if (j + 1 < n_tiles) pg_next = lookup(j + 1);
+            int pages[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
+            if (lane == 0) {
                 const int st = j % NS, us = j / NS;
                 if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag)) {
                     give_up();
-                    break;
-                }
-                const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
-                mbar_expect_tx(full, is_k ? KB : VB);
-                const int j0 = j * BN;
-#pragma unroll 1
-                for (int r0 = 0; r0 < BN; r0 += RB) {
-                    const int key = j0 + r0;
-                    int page = oob;
-                    if (key < kvb) {
-                        page = bt[key >> p.page_shift];
-                        if (page < 0 || page >= p.max_num_pages) {
-                            if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
-                            page = oob;
+                    ok = false;
+                } else {
+                    const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
+                    mbar_expect_tx(full, is_k ? KB : VB);
+                    const int j0 = j * BN;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (i >= nbox) break;
+                        const int r0 = i * RB;
+                        const int slot0 = (j0 + r0) & (S - 1);
+                        const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
+                        const int cb = LAYOUT == PKV_HND ? kvh : slot0;
+                        if (is_k) {
+                            for (int c = 0; c < QA; ++c)
+                                tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca, cb,
+                                            pages[i]);
+                        } else {
+                            for (int c = 0; c < kPfDV / 64; ++c)
+                                tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca, cb,
+                                            pages[i]);
                         }
-                    }
-                    const int slot0 = key & (S - 1);
-                    const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
-                    const int cb = LAYOUT == PKV_HND ? kvh : slot0;
-                    if (is_k) {
-                        for (int c = 0; c < QA; ++c)
-                            tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca, cb,
-                                        page);
-                    } else {
-                        for (int c = 0; c < kPfDV / 64; ++c)
-                            tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca, cb,
-                                        page);
                     }
                 }
             }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
