@@ -25,6 +25,9 @@ constexpr int kDecThreads = 128;
 constexpr int kDecRowBytes = kDecD * 2;           // one K or V row
 constexpr int kDecTileBytes = kDecTile * kDecRowBytes;
 constexpr int kDecStageBytes = 2 * kDecTileBytes; // K tile then V tile
+constexpr int kDecMinPage = 8;                    // smallest supported page size
+constexpr int kDecMaxChunk = 4096;                // largest split (keys)
+constexpr int kDecMaxPages = kDecMaxChunk / kDecMinPage + 2;  // page ids one split can touch
 
 struct DecodeParams {
     const void *q;
@@ -90,6 +93,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const Deco
     uint8_t *kvalid = q_s + ROWS * kDecRowBytes;
     float *comb_m = reinterpret_cast<float *>(kvalid + kDecStages * kDecTile);
     float *comb_l = comb_m + NKG * ROWS;
+    int *pages_s = reinterpret_cast<int *>(comb_l + NKG * ROWS);  // the split's page ids
     __shared__ int any_bad;
 
     const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -113,6 +117,19 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const Deco
     const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
     const int S = 1 << p.page_shift;
     if (tid == 0) any_bad = 0;
+    // page ids of the split, fetched once (coalesced) so that the per-tile
+    // address computation does not wait on global memory; -1 marks an id
+    // outside the pool
+    const int first_page = k_begin >> p.page_shift;
+    const int n_pages = k_end > k_begin ? ((k_end - 1) >> p.page_shift) - first_page + 1 : 0;
+    for (int i = tid; i < n_pages; i += kDecThreads) {
+        int page = bt[first_page + i];
+        if (page < 0 || page >= p.max_num_pages) {
+            set_err(p.err, PKV_DEV_ERR_PAGE);
+            page = -1;
+        }
+        pages_s[i] = page;
+    }
     __syncthreads();
 
     // Two threads per key row, 8 x 16 B each, for K and V.  Rows past the
@@ -125,10 +142,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const Deco
         bool ok = j < k_end;
         const T *ks = kc, *vs = vc;
         if (ok) {
-            int page = bt[j >> p.page_shift];
-            if (page < 0 || page >= p.max_num_pages) {
+            const int page = pages_s[(j >> p.page_shift) - first_page];
+            if (page < 0) {
                 ok = false;
-                set_err(p.err, PKV_DEV_ERR_PAGE);
                 any_bad = 1;
             } else {
                 int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
@@ -408,7 +424,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     if (Hqo % Hkv) return PKV_ERR_INVALID_ARG;
     if (B > 65535 || Hkv > 65535) return PKV_ERR_UNSUPPORTED;
     if (D != kDecD) return PKV_ERR_UNSUPPORTED;
-    if (ilog2_exact(page_size) < 0 || page_size > 1024) return PKV_ERR_UNSUPPORTED;
+    if (ilog2_exact(page_size) < 0 || page_size < kDecMinPage || page_size > 256) return PKV_ERR_UNSUPPORTED;
     const int group = Hqo / Hkv;
     pl.R = group * Q;
     if (pl.R > 64) return PKV_ERR_UNSUPPORTED;
@@ -422,7 +438,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     // partial traffic stays a few percent of the K/V bytes; then shrink it
     // while the grid would leave SMs idle.
     int chunk = 64 * pl.R;
-    chunk = chunk < 512 ? 512 : (chunk > 4096 ? 4096 : chunk);
+    chunk = chunk < 512 ? 512 : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
     chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
     const int64_t want = 2LL * num_sms();
     while (chunk > 4 * kDecTile &&
@@ -447,7 +463,7 @@ template <typename T, int MT, int LAYOUT>
 static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
     const size_t smem = kDecStages * kDecStageBytes + ROWS * kDecRowBytes + kDecStages * kDecTile +
-                        2 * NKG * ROWS * sizeof(float);
+                        2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
     auto kern = decode_split_kernel<T, MT, LAYOUT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
