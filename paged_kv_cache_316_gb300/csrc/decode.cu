@@ -132,34 +132,35 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const Deco
     }
     __syncthreads();
 
-    // Two threads per key row, 8 x 16 B each, for K and V.  Rows past the
-    // split end or on an out-of-range page are zero-filled and never read
-    // from global memory; kvalid records which rows hold a key.
+    // K and V rows of a tile: 16 consecutive lanes copy one 256-byte row,
+    // so every warp instruction moves two whole rows.  Rows past the split
+    // end or on an out-of-range page are zero-filled and never read from
+    // global memory; kvalid records which rows hold a key.
     auto load_tile = [&](int stage, int j0) {
-        const int r = tid >> 1;
-        const int c0 = (tid & 1) * 8;
-        const int j = j0 + r;
-        bool ok = j < k_end;
-        const T *ks = kc, *vs = vc;
-        if (ok) {
-            const int page = pages_s[(j >> p.page_shift) - first_page];
-            if (page < 0) {
-                ok = false;
-                any_bad = 1;
-            } else {
-                int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
-                                                    S, kDecD);
-                ks = kc + off;
-                vs = vc + off;
-            }
-        }
-        if ((tid & 1) == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
         const uint32_t dst = smem_u32(smem + stage * kDecStageBytes);
 #pragma unroll
-        for (int c = c0; c < c0 + 8; ++c) {
-            uint32_t o = swz(r, c, kDecRowBytes);
-            cp_async_16(dst + o, ks + c * 8, ok);
-            cp_async_16(dst + kDecTileBytes + o, vs + c * 8, ok);
+        for (int k = 0; k < kDecTile * 16 / kDecThreads; ++k) {
+            const int idx = k * kDecThreads + tid;
+            const int r = idx >> 4, c = idx & 15;
+            const int j = j0 + r;
+            bool ok = j < k_end;
+            const T *ks = kc, *vs = vc;
+            if (ok) {
+                const int page = pages_s[(j >> p.page_shift) - first_page];
+                if (page < 0) {
+                    ok = false;
+                    any_bad = 1;
+                } else {
+                    const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
+                                                              S, kDecD) + c * 8;
+                    ks = kc + off;
+                    vs = vc + off;
+                }
+            }
+            if (c == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
+            const uint32_t o = swz(r, c, kDecRowBytes);
+            cp_async_16(dst + o, ks, ok);
+            cp_async_16(dst + kDecTileBytes + o, vs, ok);
         }
     };
 
