@@ -20,7 +20,13 @@ namespace pkv {
 
 constexpr int kDecD = 128;                        // head_dim
 constexpr int kDecTile = 64;                      // keys per pipeline stage
-constexpr int kDecStages = 3;
+// One row tile (up to 16 packed query rows): 3 CTAs per SM with a 2-stage
+// ring; more row tiles need more registers: 2 CTAs per SM, 3 stages.
+template <int MT>
+struct DecCfg {
+    static constexpr int STAGES = MT == 1 ? 2 : 3;
+    static constexpr int CTAS = MT == 1 ? 3 : 2;
+};
 constexpr int kDecThreads = 128;
 constexpr int kDecRowBytes = kDecD * 2;           // one K or V row
 constexpr int kDecTileBytes = kDecTile * kDecRowBytes;
@@ -83,7 +89,8 @@ __device__ __forceinline__ void store4(T *dst, float a, float b, float c, float 
 }
 
 template <typename T, int MT, int LAYOUT>
-__global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_kernel(const DecodeParams p) {
+    constexpr int kDecStages = DecCfg<MT>::STAGES;
     constexpr int NKG = 4 / MT;          // warps that split the keys of a tile
     constexpr int KPW = kDecTile / NKG;  // keys per warp per tile
     constexpr int NT = KPW / 8;          // 8-key score tiles per warp
@@ -439,7 +446,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     // partial traffic stays a few percent of the K/V bytes; then shrink it
     // while the grid would leave SMs idle.
     int chunk = 64 * pl.R;
-    chunk = chunk < 512 ? 512 : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
+    chunk = chunk < 1024 ? 1024 : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
     chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
     const int64_t want = 2LL * num_sms();
     while (chunk > 4 * kDecTile &&
@@ -463,6 +470,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
 template <typename T, int MT, int LAYOUT>
 static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
+    constexpr int kDecStages = DecCfg<MT>::STAGES;
     const size_t smem = kDecStages * kDecStageBytes + ROWS * kDecRowBytes + kDecStages * kDecTile +
                         2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
     auto kern = decode_split_kernel<T, MT, LAYOUT>;
