@@ -7,8 +7,9 @@
 // q_b of its kv_b positions; softmax(scale q k^T) v over the visible keys
 // and the natural-log LSE of the scaled logits.
 //
-// One CTA owns 128 query rows of one qo head and walks the key tiles they
-// can see.  Warp roles (352 threads):
+// A persistent CTA per SM takes work items -- 128 query rows of one qo head
+// -- from a global counter (heaviest first) and walks the key tiles each can
+// see; the pipelines run on across items.  Warp roles (352 threads):
 //   warps 8, 10  TMA producers: Q once and the K tiles (warp 8), the V tiles
 //           (warp 10), 128 keys page by page, through separate K and V rings
 //           of shared-memory stages;
@@ -61,7 +62,8 @@ struct PrefillParams {
     const int32_t *cu_q;  // [B+1] in the workspace
     const int32_t *block_tables;
     int64_t bt_stride;
-    int B, causal, Hqo, Hkv, group, page_shift, max_q, max_kv;
+    int B, causal, Hqo, Hkv, group, page_shift, max_q, max_kv, n_qt_max;
+    int *work_counter;  // in the workspace, zeroed by the plan kernel
     void *out;
     float *lse;
     int32_t *err;
@@ -71,7 +73,7 @@ struct PrefillParams {
 // flags lengths above their maxima and requests with fewer keys than queries.
 __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_t *__restrict__ lkv,
                                     int B, int max_q, int max_kv, int32_t *__restrict__ cu_q,
-                                    int32_t *err) {
+                                    int32_t *err, int *work_counter) {
     const int lane = threadIdx.x;
     int carry = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
@@ -89,7 +91,10 @@ __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_
         if (b < B) cu_q[b] = carry + x - v;
         carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) cu_q[B] = carry;
+    if (lane == 0) {
+        cu_q[B] = carry;
+        *work_counter = 0;
+    }
 }
 
 
@@ -126,6 +131,33 @@ struct IsBf16<__nv_bfloat16> {
     static constexpr bool value = true;
 };
 
+// One query tile of one qo head of one request: the unit of work of the
+// persistent kernel.  Items are numbered x-major, x = 0 being the LAST query
+// tile of a request (the one that sees the most keys), so taking items in
+// order hands out the heaviest tiles first.
+struct PfItem {
+    int b, h, i0, row_base, kvh, shift, qb, kvb, n_tiles;
+};
+
+__device__ __forceinline__ bool pf_item(const PrefillParams &p, int idx, PfItem &it) {
+    const int per_x = p.Hqo * p.B;
+    const int x = idx / per_x, rem = idx - x * per_x;
+    it.h = rem % p.Hqo;
+    it.b = rem / p.Hqo;
+    it.qb = min(max(p.seq_lens_q[it.b], 0), p.max_q);
+    it.kvb = min(max(p.seq_lens_kv[it.b], 0), p.max_kv);
+    const int n_qt = (it.qb + kPfRows - 1) / kPfRows;
+    if (x >= n_qt) return false;
+    it.i0 = (n_qt - 1 - x) * kPfRows;
+    it.row_base = p.cu_q[it.b] + it.i0;
+    it.kvh = it.h / p.group;
+    it.shift = it.kvb - it.qb;  // query i sits at position shift + i
+    int k_hi = p.causal ? min(it.kvb, it.shift + it.i0 + kPfRows) : it.kvb;
+    if (k_hi < 0) k_hi = 0;
+    it.n_tiles = (k_hi + kPfBN - 1) / kPfBN;
+    return true;
+}
+
 template <typename T, int DQK, int LAYOUT>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -136,6 +168,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of the Q tile
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
+    constexpr int NI = 2;                        // slots of the work-item ring
     // TMEM columns: O of group 0 and 1, then the two S buffers; P of a tile
     // (16-bit pairs, BN/2 columns) overwrites the first half of its S buffer
     constexpr uint32_t TMEM_COLS = 512;
@@ -150,35 +183,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t v_s = k_s + SK * KB;
     const uint32_t bar0 = v_s + SV * VB;
     uint8_t *v_gen = smem + QB + SK * KB;  // generic pointer to the V stages
-    const uint32_t b_qfull = bar0;
-    auto b_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto b_kempty = [&](int s) { return bar0 + 8u * (1 + SK + s); };
-    auto b_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * SK + s); };
-    auto b_vempty = [&](int s) { return bar0 + 8u * (1 + 2 * SK + SV + s); };
-    auto b_sfull = [&](int i) { return bar0 + 8u * (1 + 2 * SK + 2 * SV + i); };
-    auto b_pfull = [&](int i) { return bar0 + 8u * (3 + 2 * SK + 2 * SV + i); };
-    auto b_pvdone = [&](int i) { return bar0 + 8u * (5 + 2 * SK + 2 * SV + i); };
+    // barriers
+    uint32_t nb = 0;
+    const uint32_t b_qfull = bar0 + 8u * nb++;   // Q of the current item landed
+    const uint32_t b_qempty = bar0 + 8u * nb++;  // last QK of an item done: Q buffer free
+    const uint32_t b_ofree = bar0 + 8u * nb++;   // epilogue read O: accumulators free
+    const uint32_t b_xchg = bar0 + 8u * nb++;    // both groups posted (max, sum)
+    const uint32_t b_item_full0 = bar0 + 8u * nb; nb += NI;
+    const uint32_t b_item_empty0 = bar0 + 8u * nb; nb += NI;
+    const uint32_t b_kfull0 = bar0 + 8u * nb; nb += SK;
+    const uint32_t b_kempty0 = bar0 + 8u * nb; nb += SK;
+    const uint32_t b_vfull0 = bar0 + 8u * nb; nb += SV;
+    const uint32_t b_vempty0 = bar0 + 8u * nb; nb += SV;
+    const uint32_t b_sfull0 = bar0 + 8u * nb; nb += 2;
+    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 4;  // [S buffer][group]
+    const uint32_t b_pvdone0 = bar0 + 8u * nb; nb += 4;  // [S buffer][group]
+    auto b_item_full = [&](int i) { return b_item_full0 + 8u * i; };
+    auto b_item_empty = [&](int i) { return b_item_empty0 + 8u * i; };
+    auto b_kfull = [&](int s) { return b_kfull0 + 8u * s; };
+    auto b_kempty = [&](int s) { return b_kempty0 + 8u * s; };
+    auto b_vfull = [&](int s) { return b_vfull0 + 8u * s; };
+    auto b_vempty = [&](int s) { return b_vempty0 + 8u * s; };
+    auto b_sfull = [&](int i) { return b_sfull0 + 8u * i; };
+    // P of tile t written by group g, and PV of tile t for group g done: one
+    // barrier per S buffer, so that every wait is for the newest phase that
+    // can be pending.  A wait for tile t's phase finds tile t-2's complete
+    // (S_t is written after PV_{t-2}) and tile t+2's impossible (QK_{t+2}
+    // is issued after PV_t, which needs P_t), so parity cannot alias.
+    auto b_pfull = [&](int t, int g) { return b_pfull0 + 8u * (2 * (t & 1) + g); };
+    auto b_pvdone = [&](int t, int g) { return b_pvdone0 + 8u * (2 * (t & 1) + g); };
+    static_assert(SV == 2, "the V tail wait relies on PV_{t-2} having waited for V_{t-2}");
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
-    __shared__ float xchg[2][2][kPfRows];  // per group: final row max and row sum
+    __shared__ int item_ring[NI];
+    __shared__ float xchg[2][2][2][kPfRows];  // [item parity][max|sum][group][row]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int qb = min(max(p.seq_lens_q[b], 0), p.max_q);
-    const int kvb = min(max(p.seq_lens_kv[b], 0), p.max_kv);
-    const int n_qt = (qb + kPfRows - 1) / kPfRows;
-    if (static_cast<int>(blockIdx.x) >= n_qt) return;  // uniform: before any barrier or TMEM use
-    const int qt = n_qt - 1 - blockIdx.x;              // the tiles that see most keys first
-    const int i0 = qt * kPfRows;
-    const int row_base = p.cu_q[b] + i0;
-    const int kvh = h / p.group;
-    const int shift = kvb - qb;  // query i sits at position shift + i
-    int k_hi = p.causal ? min(kvb, shift + i0 + kPfRows) : kvb;
-    if (k_hi < 0) k_hi = 0;
-    const int n_tiles = (k_hi + BN - 1) / BN;
+    const int total_items = p.n_qt_max * p.Hqo * p.B;
 
     if (tid == 0) {
         mbar_init(b_qfull, 1);
+        mbar_init(b_qempty, 1);
+        mbar_init(b_ofree, 256);
+        mbar_init(b_xchg, 256);
+        for (int i = 0; i < NI; ++i) {
+            mbar_init(b_item_full(i), 1);
+            mbar_init(b_item_empty(i), 2 + 256);  // MMA thread, V producer, 256 softmax threads
+        }
         for (int s = 0; s < SK; ++s) {
             mbar_init(b_kfull(s), 1);
             mbar_init(b_kempty(s), 1);
@@ -189,8 +240,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(b_sfull(i), 1);
-            mbar_init(b_pfull(i), 128);
-            mbar_init(b_pvdone(i), 1);
+            mbar_init(b_pfull(i, 0), 128);
+            mbar_init(b_pfull(i, 1), 128);
+            mbar_init(b_pvdone(i, 0), 1);
+            mbar_init(b_pvdone(i, 1), 1);
         }
         abort_s = 0;
         fence_mbar_init();
@@ -208,23 +261,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         *abort_flag = 1;
         set_err(p.err, PKV_DEV_ERR_TIMEOUT);
     };
-    auto give_up_quiet = [&]() { set_err(p.err, PKV_DEV_ERR_TIMEOUT); };
+    // the k-th item published by the K producer (-1: no more work); every
+    // consumer role takes every item, in order, and releases the ring slot
+    auto take_item = [&](int k, bool &ok) -> int {
+        const int slot = k % NI;
+        if (!mbar_wait(b_item_full(slot), (k / NI) & 1, abort_flag)) {
+            ok = false;
+            return -1;
+        }
+        const int idx = *reinterpret_cast<volatile int *>(&item_ring[slot]);
+        mbar_arrive(b_item_empty(slot));
+        return idx;
+    };
 
     if (warp == kTmaWarp || warp == kTmaVWarp) {
         // ------------------------------------------------------------ TMA producers
-        // warp 8 loads Q and the K tiles, warp 10 the V tiles: a K stage is
-        // released by its QK and a V stage by its (much later) PV, so the two
-        // rings advance independently and K runs ahead of the MMA.  The
-        // whole warp looks up a tile's page ids in one coalesced load, one
-        // tile ahead; lane 0 issues the copies.
+        // Warp 8 takes work items from the global counter, publishes them,
+        // and loads Q and the K tiles; warp 10 loads the V tiles.  A K stage
+        // is released by its QK and a V stage by its (later) PV, so the rings
+        // advance independently.  Both warps look up a tile's page ids in one
+        // coalesced load, one tile ahead; lane 0 issues the copies.
         const bool is_k = warp == kTmaWarp;
         if (lane == 0) {
             if (is_k) {
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
-                mbar_expect_tx(b_qfull, QB);
-                for (int c = 0; c < QA; ++c)
-                    tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, h, row_base);
             } else {
                 prefetch_tmap(&tm_v);
             }
@@ -232,106 +293,184 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int S = 1 << p.page_shift;
         const int RB = S < BN ? S : BN;  // rows per TMA box
         const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
-        const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
         const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
         const int NS = is_k ? SK : SV;
-        auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
-            const int key = j * BN + lane * RB;
-            int page = oob;
-            if (lane < nbox && key < kvb) {
-                page = bt[key >> p.page_shift];
-                if (page < 0 || page >= p.max_num_pages) {
-                    if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
-                    page = oob;
-                }
-            }
-            return page;
-        };
-        int pg_next = n_tiles > 0 ? lookup(0) : oob;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int pg = pg_next;
-            if (j + 1 < n_tiles) pg_next = lookup(j + 1);
-            int pages[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
-            if (lane == 0) {
-                const int st = j % NS, us = j / NS;
-                if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag)) {
+        int t_base = 0;  // tiles of earlier items (global tile counter)
+        for (int k = 0; ok; ++k) {
+            int idx;
+            if (is_k) {
+                // fetch the next valid item and publish it
+                idx = -1;
+                if (lane == 0) {
+                    while (true) {
+                        const int c = atomicAdd(p.work_counter, 1);
+                        if (c >= total_items) break;
+                        PfItem tmp;
+                        if (pf_item(p, c, tmp)) {
+                            idx = c;
+                            break;
+                        }
+                    }
+                    const int slot = k % NI;
+                    if (k >= NI && !mbar_wait(b_item_empty(slot), ((k / NI) - 1) & 1, abort_flag)) {
+                        give_up();
+                        ok = false;
+                    } else {
+                        item_ring[slot] = idx;
+                        mbar_arrive(b_item_full(slot));
+                    }
+                }
+                idx = __shfl_sync(0xffffffffu, idx, 0);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            } else {
+                if (lane == 0) idx = take_item(k, ok);
+                idx = __shfl_sync(0xffffffffu, idx, 0);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            if (!ok || idx < 0) break;
+            PfItem it;
+            pf_item(p, idx, it);
+            const int32_t *bt = p.block_tables + static_cast<int64_t>(it.b) * p.bt_stride;
+            // Q of this item, once the previous item's last QK is done; it is
+            // loaded after the item's first K tile so that the two overlap
+            auto load_q = [&]() {  // lane 0 of the K producer
+                if (k >= 1 && !mbar_wait(b_qempty, (k - 1) & 1, abort_flag)) {
                     give_up();
                     ok = false;
                 } else {
-                    const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
-                    mbar_expect_tx(full, is_k ? KB : VB);
-                    const int j0 = j * BN;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (i >= nbox) break;
-                        const int r0 = i * RB;
-                        const int slot0 = (j0 + r0) & (S - 1);
-                        const int ca = LAYOUT == PKV_HND ? slot0 : kvh;
-                        const int cb = LAYOUT == PKV_HND ? kvh : slot0;
-                        if (is_k) {
-                            for (int c = 0; c < QA; ++c)
-                                tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca, cb,
-                                            pages[i]);
-                        } else {
-                            for (int c = 0; c < kPfDV / 64; ++c)
-                                tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca, cb,
-                                            pages[i]);
-                        }
+                    mbar_expect_tx(b_qfull, QB);
+                    for (int c = 0; c < QA; ++c)
+                        tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.h, it.row_base);
+                }
+            };
+            if (is_k && lane == 0 && it.n_tiles == 0) load_q();
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
+                const int key = j * BN + lane * RB;
+                int page = oob;
+                if (lane < nbox && key < it.kvb) {
+                    page = bt[key >> p.page_shift];
+                    if (page < 0 || page >= p.max_num_pages) {
+                        if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
+                        page = oob;
                     }
                 }
+                return page;
+            };
+            int pg_next = it.n_tiles > 0 ? lookup(0) : oob;
+            for (int j = 0; j < it.n_tiles; ++j) {
+                const int t = t_base + j;
+                const int pg = pg_next;
+                if (j + 1 < it.n_tiles) pg_next = lookup(j + 1);
+                int pages[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
+                if (lane == 0) {
+                    const int st = t % NS, us = t / NS;
+                    if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag)) {
+                        give_up();
+                        ok = false;
+                    } else {
+                        const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
+                        mbar_expect_tx(full, is_k ? KB : VB);
+                        const int j0 = j * BN;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (i >= nbox) break;
+                            const int r0 = i * RB;
+                            const int slot0 = (j0 + r0) & (S - 1);
+                            const int ca = LAYOUT == PKV_HND ? slot0 : it.kvh;
+                            const int cb = LAYOUT == PKV_HND ? it.kvh : slot0;
+                            if (is_k) {
+                                for (int c = 0; c < QA; ++c)
+                                    tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca,
+                                                cb, pages[i]);
+                            } else {
+                                for (int c = 0; c < kPfDV / 64; ++c)
+                                    tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca,
+                                                cb, pages[i]);
+                            }
+                        }
+                        if (is_k && j == 0) load_q();
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            t_base += it.n_tiles;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Issue order QK_0, then for every tile j: QK_{j+1}, PV_{j,0}, PV_{j,1}.
+        // Per item: QK_0, then for every tile j: QK_{j+1}, PV_{j,0}, PV_{j,1}.
         // QK_{j+1} runs on the tensor core while the softmax works on S_j.
-        // tcgen05 MMAs execute in issue order, so QK_{j+2}, which overwrites
-        // S buffer j&1, cannot disturb PV_j reading P_j from it.
+        // tcgen05 MMAs execute in issue order, so a QK that overwrites an S
+        // buffer cannot disturb the PV still reading P from it.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
             constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
             const uint64_t qdesc0 = umma_sdesc_sw128(q_s, 16, 1024);
             const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
             const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
-            bool ok = mbar_wait(b_qfull, 0, abort_flag);
-            auto issue_qk = [&](int j) -> bool {
-                const int sk = j % SK, uk = j / SK;
+            bool ok = true;
+            int t_base = 0;
+            int n_tiled = 0;  // items with at least one key tile so far (o_free phases)
+            auto issue_qk = [&](int t) -> bool {
+                const int sk = t % SK, uk = t / SK;
                 if (!mbar_wait(b_kfull(sk), uk & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t kd = kdesc0 + ((sk * KB) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk)
-                    umma_ss(tmem + S_COL + (j & 1) * BN,
+                    umma_ss(tmem + S_COL + (t & 1) * BN,
                             qdesc0 + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
                             kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-                umma_commit(b_sfull(j & 1));
+                umma_commit(b_sfull(t & 1));
                 umma_commit(b_kempty(sk));
                 return true;
             };
-            auto issue_pv = [&](int j) -> bool {
-                const int sv = j % SV, uv = j / SV;
+            auto issue_pv = [&](int t, bool first) -> bool {
+                const int sv = t % SV, uv = t / SV;
                 const uint64_t vd = vdesc0 + ((sv * VB) >> 4);
                 for (int hh = 0; hh < 2; ++hh) {
-                    if (!mbar_wait(b_pfull(hh), j & 1, abort_flag)) return false;
+                    if (!mbar_wait(b_pfull(t, hh), (t >> 1) & 1, abort_flag)) return false;
                     if (hh == 0 && !mbar_wait(b_vfull(sv), uv & 1, abort_flag)) return false;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BN / 32; ++kk)
-                        umma_ts(tmem + hh * kPfDV, tmem + S_COL + (j & 1) * BN + hh * (BN / 2) + kk * 8,
-                                vd + (((hh * (BN / 2) + kk * 16) * 128) >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(b_pvdone(hh));
+                        umma_ts(tmem + hh * kPfDV, tmem + S_COL + (t & 1) * BN + hh * (BN / 2) + kk * 8,
+                                vd + (((hh * (BN / 2) + kk * 16) * 128) >> 4), idesc_pv,
+                                (!first || kk > 0) ? 1u : 0u);
+                    umma_commit(b_pvdone(t, hh));
                 }
                 umma_commit(b_vempty(sv));
                 return true;
             };
-            if (ok && n_tiles > 0) ok = issue_qk(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
-                if (!issue_pv(j)) { ok = false; break; }
+            for (int k = 0; ok; ++k) {
+                const int idx = take_item(k, ok);
+                if (!ok || idx < 0) break;
+                PfItem it;
+                pf_item(p, idx, it);
+                if (!mbar_wait(b_qfull, k & 1, abort_flag)) { ok = false; break; }
+                if (it.n_tiles > 0) ok = issue_qk(t_base);
+                if (ok && it.n_tiles == 1) umma_commit(b_qempty);
+                for (int j = 0; ok && j < it.n_tiles; ++j) {
+                    if (j + 1 < it.n_tiles) {
+                        if (!issue_qk(t_base + j + 1)) { ok = false; break; }
+                        if (j + 2 == it.n_tiles) umma_commit(b_qempty);  // last QK of the item issued
+                    }
+                    // the epilogue of the previous item with tiles must have
+                    // read O before this item's first PV overwrites it
+                    if (j == 0 && n_tiled >= 1 && !mbar_wait(b_ofree, (n_tiled - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!issue_pv(t_base + j, j == 0)) { ok = false; break; }
+                }
+                if (ok && it.n_tiles == 0) umma_commit(b_qempty);
+                t_base += it.n_tiles;
+                n_tiled += it.n_tiles > 0;
             }
             if (!ok) give_up();
         }
@@ -340,168 +479,186 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // Two groups of four warps split every key tile by columns: group g
         // owns keys [64g, 64g+64) of each tile and keeps its own running max,
         // sum and O accumulator (TMEM columns g*128 ..), so the groups never
-        // exchange anything inside the loop.  Warp w owns TMEM lanes / query
-        // rows 32*(w%4) .. +31, one thread per (row, group).  The two partial
-        // results are merged once at the end.
+        // exchange anything inside the tile loop.  Warp w owns TMEM lanes /
+        // query rows 32*(w%4) .. +31, one thread per (row, group).  The two
+        // partial results of an item are merged in its epilogue.
         constexpr int HC = BN / 2;  // S columns per thread
         const int g = warp >> 2;
         const int r = 32 * (warp & 3) + lane;  // query row of this thread inside the tile
-        const int pos = shift + i0 + r;
-        const int lim = p.causal ? min(pos, kvb - 1) : kvb - 1;  // last visible key
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const uint32_t o_g = g * kPfDV;  // this group's O columns
-        const int my_tiles = n_tiles;
-        float m_used = -INFINITY, l = 0.f;
-        // A warp whose wait gave up is dead: it skips the rest of the work but
-        // still meets the others at the final named barrier.
-        bool dead = false;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
-        for (int j = 0; j < n_tiles; ++j) {
-            const int j0 = j * BN + g * HC;  // first key of this thread's columns
-            const uint32_t t_s = t_lane + S_COL + (j & 1) * BN + g * HC;
-            // S_j complete; by commit order so is PV_{j-2}, the last reader of
-            // the P columns about to be rewritten
-            if (!wait_warp(b_sfull(j & 1), (j >> 1) & 1)) { dead = true; break; }
-            tc_fence_after();
-            uint32_t sx[HC];
-#pragma unroll
-            for (int c = 0; c < HC / 32; ++c)
-                tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
-            tmem_wait_ld();
-            const bool full = j0 + HC - 1 <= lim;
-            // row max: on the raw scores when the scale is positive (then
-            // max(scale * s) = scale * max(s) and one FFMA per element later
-            // does both the scaling and the shift), else on the scaled ones
-            const float sc = p.scale_log2;
-            const bool pos_scale = sc > 0.f;
-            float m8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
-                           -INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < HC; ++c) {
-                float v = __uint_as_float(sx[c]);
-                if (!pos_scale) v *= sc;
-                if (!full && j0 + c > lim) v = -INFINITY;
-                sx[c] = __float_as_uint(v);
-                m8[c & 7] = fmaxf(m8[c & 7], v);
-            }
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            if (pos_scale) mx *= sc;
-            const float k_mul = pos_scale ? sc : 1.f;  // x = s * k_mul - base
-            float alpha = 1.f;
-            bool need = false;
-            if (mx != -INFINITY) {
-                if (m_used == -INFINITY) {
-                    m_used = mx;
-                } else if (mx > m_used + 8.f) {
-                    alpha = fast_exp2(m_used - mx);
-                    m_used = mx;
-                    l *= alpha;
-                    need = true;
-                }
-            }
-            const float base = m_used == -INFINITY ? 0.f : m_used;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int e = 0; e < HC / 2; ++e) {
-                const float x0 = fmaf(__uint_as_float(sx[2 * e]), k_mul, -base);
-                const float x1 = fmaf(__uint_as_float(sx[2 * e + 1]), k_mul, -base);
-                // pairs e with e % kExpFmaEvery == kExpFmaEvery - 1 on the FMA
-                // pipe, the rest on the special-function unit
-                const bool on_fma = kExpFmaEvery > 0 && (e % (kExpFmaEvery > 0 ? kExpFmaEvery : 1)) == kExpFmaEvery - 1;
-                const float p0 = on_fma ? exp2_fma(x0) : fast_exp2(x0);
-                const float p1 = on_fma ? exp2_fma(x1) : fast_exp2(x1);
-                s4[e & 3] += p0;
-                s4[(e + 2) & 3] += p1;
-                sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1 of this half
-            }
-            // P (HC keys, HC/2 columns) over the consumed first half of my S columns
-            tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(sx));
-            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-            // rows of V past the sequence end may hold anything (even NaN):
-            // zero the ones this group's PV reads so that P = 0 there cannot
-            // produce 0 * NaN
-            if (j0 + HC > kvb) {  // some of this group's keys lie past the end
-                const int sv = j % SV, uv = j / SV;
-                if (!wait_warp(b_vfull(sv), uv & 1)) { dead = true; break; }
-                const int zs = max(kvb - j * BN, g * HC), ze = (g + 1) * HC;  // stage rows to zero
-                uint8_t *vbase = v_gen + sv * VB;
-                for (int idx = r; idx < (ze - zs) * 16; idx += 128) {
-                    const int row = zs + (idx >> 4), chunk = idx & 15;
-                    *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            // O_g *= alpha when the running max moved (rare: threshold 2^8);
-            // PV_{j-1} of this group must be complete first
-            if (__any_sync(0xffffffffu, need)) {
-                if (j >= 1 && !wait_warp(b_pvdone(g), (j - 1) & 1)) { dead = true; break; }
+        bool ok = true;
+        int t_base = 0;
+        for (int k = 0; ok; ++k) {
+            int idx = take_item(k, ok);
+            ok = __all_sync(0xffffffffu, ok);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            if (!ok || idx < 0) break;
+            PfItem it;
+            pf_item(p, idx, it);
+            const int pos = it.shift + it.i0 + r;
+            const int lim = p.causal ? min(pos, it.kvb - 1) : it.kvb - 1;  // last visible key
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.n_tiles; ++j) {
+                const int t = t_base + j;
+                const int j0 = j * BN + g * HC;  // first key of this thread's columns
+                const uint32_t t_s = t_lane + S_COL + (t & 1) * BN + g * HC;
+                // S_t complete; by commit order so is PV_{t-2}, the last reader
+                // of the P columns about to be rewritten
+                if (!wait_warp(b_sfull(t & 1), (t >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
+                uint32_t sx[HC];
 #pragma unroll
-                for (int c = 0; c < kPfDV / 32; ++c) {
-                    uint32_t ro[32];
-                    tmem_ld32(t_lane + o_g + c * 32, ro);
+                for (int c = 0; c < HC / 32; ++c)
+                    tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
+                tmem_wait_ld();
+                const bool full = j0 + HC - 1 <= lim;
+                // row max: on the raw scores when the scale is positive (then
+                // max(scale * s) = scale * max(s) and one FFMA per element
+                // later does both the scaling and the shift), else scaled
+                const float sc = p.scale_log2;
+                const bool pos_scale = sc > 0.f;
+                float m8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
+                               -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < HC; ++c) {
+                    float v = __uint_as_float(sx[c]);
+                    if (!pos_scale) v *= sc;
+                    if (!full && j0 + c > lim) v = -INFINITY;
+                    sx[c] = __float_as_uint(v);
+                    m8[c & 7] = fmaxf(m8[c & 7], v);
+                }
+                float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                if (pos_scale) mx *= sc;
+                const float k_mul = pos_scale ? sc : 1.f;  // x = s * k_mul - base
+                float alpha = 1.f;
+                bool need = false;
+                if (mx != -INFINITY) {
+                    if (m_used == -INFINITY) {
+                        m_used = mx;
+                    } else if (mx > m_used + 8.f) {
+                        alpha = fast_exp2(m_used - mx);
+                        m_used = mx;
+                        l *= alpha;
+                        need = true;
+                    }
+                }
+                const float base = m_used == -INFINITY ? 0.f : m_used;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < HC / 2; ++e) {
+                    const float x0 = fmaf(__uint_as_float(sx[2 * e]), k_mul, -base);
+                    const float x1 = fmaf(__uint_as_float(sx[2 * e + 1]), k_mul, -base);
+                    // pairs e with e % kExpFmaEvery == kExpFmaEvery - 1 on the
+                    // FMA pipe, the rest on the special-function unit
+                    const bool on_fma =
+                        kExpFmaEvery > 0 && (e % (kExpFmaEvery > 0 ? kExpFmaEvery : 1)) == kExpFmaEvery - 1;
+                    const float p0 = on_fma ? exp2_fma(x0) : fast_exp2(x0);
+                    const float p1 = on_fma ? exp2_fma(x1) : fast_exp2(x1);
+                    s4[e & 3] += p0;
+                    s4[(e + 2) & 3] += p1;
+                    sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1 of this half
+                }
+                // P (HC keys, HC/2 columns) over the consumed first half of my S columns
+                tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(sx));
+                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                // rows of V past the sequence end may hold anything (even NaN):
+                // zero the ones this group's PV reads so that P = 0 there
+                // cannot produce 0 * NaN
+                if (j0 + HC > it.kvb) {
+                    const int sv = t % SV, uv = t / SV;
+                    if (!wait_warp(b_vfull(sv), uv & 1)) { ok = false; break; }
+                    const int zs = max(it.kvb - j * BN, g * HC), ze = (g + 1) * HC;
+                    uint8_t *vbase = v_gen + sv * VB;
+                    for (int q = r; q < (ze - zs) * 16; q += 128) {
+                        const int row = zs + (q >> 4), chunk = q & 15;
+                        *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                // O_g *= alpha when the running max moved (rare: threshold 2^8);
+                // PV_{t-1} of this group must be complete first
+                if (__any_sync(0xffffffffu, need)) {
+                    if (j >= 1 && !wait_warp(b_pvdone(t - 1, g), ((t - 1) >> 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kPfDV / 32; ++c) {
+                        uint32_t ro[32];
+                        tmem_ld32(t_lane + o_g + c * 32, ro);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+                        tmem_st32(t_lane + o_g + c * 32, ro);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_pfull(t, g));
+            }
+            if (!ok) break;
+            // epilogue: wait for this group's last PV of the item (a commit
+            // covers every earlier MMA too), trade (max, sum) with the other
+            // group, merge the two partial O rows; group g writes output
+            // columns [g*64, g*64+64) and group 0 the LSE
+            const int tl = t_base + it.n_tiles - 1;
+            if (it.n_tiles > 0 && !wait_warp(b_pvdone(tl, g), (tl >> 1) & 1)) { ok = false; break; }
+            xchg[k & 1][0][g][r] = m_used;
+            xchg[k & 1][1][g][r] = l;
+            mbar_arrive(b_xchg);
+            if (!wait_warp(b_xchg, k & 1)) { ok = false; break; }
+            const float m0 = xchg[k & 1][0][0][r], m1 = xchg[k & 1][0][1][r];
+            const float M = fmaxf(m0, m1);
+            const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+            const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+            const float lt = xchg[k & 1][1][0][r] * w0 + xchg[k & 1][1][1][r] * w1;
+            const bool have = it.n_tiles > 0;
+            tc_fence_after();
+            const int qi = it.i0 + r;
+            const int64_t grow = static_cast<int64_t>(it.row_base) + r;
+            const bool valid = qi < it.qb && grow < p.total_q;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const uint32_t ocol = g * (kPfDV / 2);
+            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + it.h) * kPfDV + ocol;
+#pragma unroll
+            for (int c = 0; c < kPfDV / 64; ++c) {
+                uint32_t ra[32], rb[32];
+                if (have) {
+                    tmem_ld32(t_lane + ocol + c * 32, ra);
+                    tmem_ld32(t_lane + kPfDV + ocol + c * 32, rb);
                     tmem_wait_ld();
+                }
+                float o[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
-                    tmem_st32(t_lane + o_g + c * 32, ro);
+                for (int e = 0; e < 32; ++e) {
+                    float v = 0.f;
+                    if (have && w0 != 0.f) v += __uint_as_float(ra[e]) * w0;
+                    if (have && w1 != 0.f) v += __uint_as_float(rb[e]) * w1;
+                    o[e] = v * inv;
+                }
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w = make_uint4(pack2<T>(o[q * 8 + 0], o[q * 8 + 1]), pack2<T>(o[q * 8 + 2], o[q * 8 + 3]),
+                                             pack2<T>(o[q * 8 + 4], o[q * 8 + 5]), pack2<T>(o[q * 8 + 6], o[q * 8 + 7]));
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + q * 8) = w;
+                    }
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_pfull(g));
-        }
-        // epilogue: wait for this group's last PV (the newest phase of its
-        // pv_done barrier), trade (max, sum) with the other group, merge the
-        // two partial O rows; group g writes output columns [g*64, g*64+64)
-        // and group 0 the LSE
-        if (!dead && my_tiles > 0 && !wait_warp(b_pvdone(g), (my_tiles - 1) & 1)) dead = true;
-        xchg[0][g][r] = m_used;
-        xchg[1][g][r] = l;
-        named_bar_sync(1, 256);
-        if (dead || __any_sync(0xffffffffu, *abort_flag != 0)) give_up_quiet();
-        const float m0 = xchg[0][0][r], m1 = xchg[0][1][r];
-        const float M = fmaxf(m0, m1);
-        const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
-        const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
-        const float lt = xchg[1][0][r] * w0 + xchg[1][1][r] * w1;
-        // O_h holds data only if group h had a tile and nobody gave up
-        const bool ok_all = !__any_sync(0xffffffffu, dead) && *abort_flag == 0;
-        const bool have0 = ok_all && n_tiles > 0, have1 = ok_all && n_tiles > 0;
-        tc_fence_after();
-        const int qi = i0 + r;
-        const int64_t grow = static_cast<int64_t>(row_base) + r;
-        const bool valid = qi < qb && grow < p.total_q;
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const uint32_t ocol = g * (kPfDV / 2);
-        T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + ocol;
-#pragma unroll
-        for (int c = 0; c < kPfDV / 64; ++c) {
-            uint32_t ra[32], rb[32];
-            if (have0) tmem_ld32(t_lane + ocol + c * 32, ra);
-            if (have1) tmem_ld32(t_lane + kPfDV + ocol + c * 32, rb);
-            if (have0 || have1) tmem_wait_ld();
-            float o[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                float v = 0.f;
-                if (have0 && w0 != 0.f) v += __uint_as_float(ra[e]) * w0;
-                if (have1 && w1 != 0.f) v += __uint_as_float(rb[e]) * w1;
-                o[e] = v * inv;
+            if (valid && g == 0) p.lse[grow * p.Hqo + it.h] = lt > 0.f ? (M + fast_log2(lt)) * kLn2 : -INFINITY;
+            // O has been read: the next item's first PV may overwrite it (items
+            // without key tiles never touch O and are not counted)
+            if (have) {
+                tc_fence_before();
+                mbar_arrive(b_ofree);
             }
-            if (valid) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 w = make_uint4(pack2<T>(o[q * 8 + 0], o[q * 8 + 1]), pack2<T>(o[q * 8 + 2], o[q * 8 + 3]),
-                                         pack2<T>(o[q * 8 + 4], o[q * 8 + 5]), pack2<T>(o[q * 8 + 6], o[q * 8 + 7]));
-                    *reinterpret_cast<uint4 *>(orow + c * 32 + q * 8) = w;
-                }
-            }
+            t_base += it.n_tiles;
         }
-        if (valid && g == 0) p.lse[grow * p.Hqo + h] = lt > 0.f ? (M + fast_log2(lt)) * kLn2 : -INFINITY;
+        if (!ok) give_up();
     }
 
     tc_fence_before();
@@ -515,7 +672,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 template <int DQK>
 static size_t prefill_smem_bytes() {
     constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
-    return 1024 + kPfRows * DQK * 2 + SK * kPfBN * DQK * 2 + SV * kPfBN * kPfDV * 2 + 8 * (7 + 2 * SK + 2 * SV);
+    return 1024 + kPfRows * DQK * 2 + SK * kPfBN * DQK * 2 + SV * kPfBN * kPfDV * 2 + 8 * (20 + 2 * SK + 2 * SV);
 }
 
 template <typename T, int DQK, int LAYOUT>
@@ -569,7 +726,10 @@ static bool cache_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
     return encode_tmap(m, base, dt, 4, dims, strides, box);
 }
 
-static size_t prefill_ws_bytes(int B) { return round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256); }
+// workspace: cu_q[B+1], then the work-item counter of the persistent kernel
+static size_t prefill_ws_bytes(int B) {
+    return round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256) + 256;
+}
 
 }  // namespace pkv
 
@@ -609,6 +769,11 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
         static_cast<int64_t>(block_table_stride) * page_size < max_sequence_kv)
         return PKV_ERR_INVALID_ARG;
     if (batch_size == 0 || total_q == 0) return PKV_OK;
+    // work items (query tiles x heads x requests) are counted in an int that
+    // overshoots the total by one per CTA
+    if (static_cast<int64_t>((max_token_per_sequence + kPfRows - 1) / kPfRows) * num_qo_heads * batch_size >
+        0x7fffffff - 65536)
+        return PKV_ERR_UNSUPPORTED;
     if (!q || !k_cache || !v_cache || !actual_seq_lens_q || !actual_seq_lens_kv || !block_tables ||
         !out || !lse)
         return PKV_ERR_NULL;
@@ -640,8 +805,11 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int32_t *cu_q = static_cast<int32_t *>(workspace);
+    int *work_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) +
+                                                round_up(static_cast<size_t>(batch_size + 1) * sizeof(int32_t), 256));
     prefill_plan_kernel<<<1, 32, 0, st>>>(actual_seq_lens_q, actual_seq_lens_kv, batch_size,
-                                          max_token_per_sequence, max_sequence_kv, cu_q, err_word);
+                                          max_token_per_sequence, max_sequence_kv, cu_q, err_word,
+                                          work_counter);
     PrefillParams p;
     p.max_num_pages = max_num_pages;
     p.total_q = total_q;
@@ -659,13 +827,18 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     p.page_shift = ilog2_exact(page_size);
     p.max_q = max_token_per_sequence;
     p.max_kv = max_sequence_kv;
+    p.work_counter = work_counter;
     p.out = out;
     p.lse = lse;
     p.err = err_word;
     const int n_qt = (max_token_per_sequence + kPfRows - 1) / kPfRows;
+    p.n_qt_max = n_qt;
     int launches = 1;
+    const int64_t items = static_cast<int64_t>(n_qt) * num_qo_heads * batch_size;
     if (n_qt > 0) {
-        dim3 grid(n_qt, num_qo_heads, batch_size);
+        // persistent: one CTA per SM (the shared-memory footprint allows one)
+        const int64_t ctas = items < num_sms() ? items : num_sms();
+        dim3 grid(static_cast<unsigned>(ctas));
         int rc = dtype == PKV_BF16 ? dispatch_prefill<__nv_bfloat16>(d_qk, layout, tq, tk, tv, p, grid, st)
                                    : dispatch_prefill<__half>(d_qk, layout, tq, tk, tv, p, grid, st);
         if (rc != PKV_OK) return rc;
