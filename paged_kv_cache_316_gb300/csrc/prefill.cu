@@ -7,24 +7,25 @@
 // q_b of its kv_b positions; softmax(scale q k^T) v over the visible keys
 // and the natural-log LSE of the scaled logits.
 //
-// A persistent CTA per SM takes work items -- 128 query rows of one qo head
-// -- from a global counter (heaviest first) and walks the key tiles each can
-// see; the pipelines run on across items.  Warp roles (352 threads):
-//   warps 8, 10  TMA producers: Q once and the K tiles (warp 8), the V tiles
-//           (warp 10), 128 keys page by page, through separate K and V rings
-//           of shared-memory stages;
+// A persistent CTA per SM takes work items from a global counter.  An item
+// is one 128-row query tile of a request for TWO qo heads of the same kv
+// head (blocks A and B; B is absent when the group size is odd and the
+// heads run out), so every K/V tile brought into shared memory feeds two
+// 128 x BN score tiles.  Warp roles (352 threads):
+//   warps 8, 10  TMA producers: warp 8 takes the items, loads both Q blocks
+//           and the K tiles, warp 10 the V tiles, page by page, through
+//           separate K and V rings of shared-memory stages;
 //   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
-//           thread: S = Q K^T into one of two TMEM score buffers (so the
-//           next tile's QK overlaps this tile's softmax), then per group
-//           O_g += P_g V_g with P read from TMEM;
-//   warps 0-7  two groups of four warps, one thread per query row each;
-//           group g owns keys [64g, 64g+64) of every tile: read its S
-//           columns from TMEM, mask, online softmax in base 2, write P
-//           (bf16/fp16) over the consumed S columns as the A operand of its
-//           PV MMA, which accumulates into the group's own O in TMEM
-//           (rescaled there when the running max grows by more than 2^8).
-//           At the end the two partial (O, max, sum) are merged, normalised
-//           and written with the LSE.
+//           thread in the order QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1)
+//           PV_B(t) QK_B(t+1) | ..., so that while one block's softmax runs
+//           the tensor core works for the other block (ping-pong);
+//   warps 0-3 / 4-7  the softmax of block A / B, one thread per query row:
+//           read the row's S columns from TMEM 32 at a time, mask, online
+//           softmax in base 2 against a running max that is raised only
+//           when a chunk exceeds it by more than 2^8, write P (bf16/fp16)
+//           over the consumed S columns as the A operand of the block's PV
+//           MMA, which accumulates into the block's O in TMEM; at the end of
+//           the item normalise O and write it with the LSE.
 // Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
 // other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
@@ -34,24 +35,25 @@
 
 namespace pkv {
 
-constexpr int kPfRows = 128;     // query rows per CTA
+constexpr int kPfRows = 128;     // query rows per block
 constexpr int kPfThreads = 352;  // 8 softmax warps + K-load warp + MMA warp + V-load warp
 constexpr int kTmaWarp = 8, kMmaWarp = 9, kTmaVWarp = 10;
 constexpr int kPfDV = 128;
 
-// Key tiles of BN = 128; separate K and V rings (a K stage is released by
-// its QK, a V stage by its PV).
+// Keys per tile (BN) and ring depths.  TMEM holds S of both blocks (BN
+// columns each) and O of both blocks (128 columns each); shared memory holds
+// both Q blocks, SK K stages and SV V stages.
 template <int DQK>
 struct PfCfg;
 template <>
 struct PfCfg<128> {
-    static constexpr int SK = 3, SV = 2;
+    static constexpr int BN = 128, SK = 3, SV = 2;
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int SK = 2, SV = 2;
+    static constexpr int BN = 64, SK = 3, SV = 3;
 };
-constexpr int kPfBN = 128;
+static int pf_bn(int d_qk) { return d_qk == 128 ? PfCfg<128>::BN : PfCfg<192>::BN; }
 
 struct PrefillParams {
     int64_t max_num_pages;
@@ -62,65 +64,54 @@ struct PrefillParams {
     const int32_t *cu_q;  // [B+1] in the workspace
     const int32_t *block_tables;
     int64_t bt_stride;
-    int B, causal, Hqo, Hkv, group, page_shift, max_q, max_kv, n_qt_max;
+    const int32_t *cu_items;  // [B+1] in the workspace: U x prefix sum of query tiles
+    int B, causal, Hqo, Hkv, group, page_shift, max_q, max_kv;
+    int pairs;  // head pairs per kv head: (group + 1) / 2; U = Hkv * pairs items per query tile
     int *work_counter;  // in the workspace, zeroed by the plan kernel
     void *out;
     float *lse;
     int32_t *err;
 };
 
-// cu_q = exclusive prefix sum of the query lengths (one warp, 32 at a time);
-// flags lengths above their maxima and requests with fewer keys than queries.
+// cu_q = exclusive prefix sum of the query lengths and cu_items = U x the
+// exclusive prefix sum of the 128-row query tiles (one warp, 32 requests at
+// a time); flags lengths above their maxima and requests with fewer keys
+// than queries; zeroes the work-item counter.
 __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_t *__restrict__ lkv,
-                                    int B, int max_q, int max_kv, int32_t *__restrict__ cu_q,
-                                    int32_t *err, int *work_counter) {
+                                    int B, int U, int max_q, int max_kv, int32_t *__restrict__ cu_q,
+                                    int32_t *__restrict__ cu_items, int32_t *err, int *work_counter) {
     const int lane = threadIdx.x;
-    int carry = 0;
+    int carry = 0, carry_t = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         int b = b0 + lane;
         int v = b < B ? lq[b] : 0;
         if (b < B && (v > max_q || v < 0 || lkv[b] > max_kv)) set_err(err, PKV_DEV_ERR_LEN);
         v = min(max(v, 0), max_q);
         if (b < B && min(lkv[b], max_kv) < v) set_err(err, PKV_DEV_ERR_QLEN);
-        int x = v;
+        const int nt = (v + kPfRows - 1) / kPfRows;
+        int x = v, xt = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            int yt = __shfl_up_sync(0xffffffffu, xt, o);
+            if (lane >= o) {
+                x += y;
+                xt += yt;
+            }
         }
-        if (b < B) cu_q[b] = carry + x - v;
+        if (b < B) {
+            cu_q[b] = carry + x - v;
+            cu_items[b] = (carry_t + xt - nt) * U;
+        }
         carry += __shfl_sync(0xffffffffu, x, 31);
+        carry_t += __shfl_sync(0xffffffffu, xt, 31);
     }
     if (lane == 0) {
         cu_q[B] = carry;
+        cu_items[B] = carry_t * U;
         *work_counter = 0;
     }
 }
-
-
-// 2^x on the FMA pipe, for part of the softmax exponentials (the rest use
-// the special-function unit): x = n + f with n = round(x) taken from the
-// low mantissa bits of x + 1.5*2^23, f in [-1/2, 1/2]; 2^f from the degree-4
-// polynomial interpolating 2^f at the Chebyshev nodes of [-1/2, 1/2]
-// (coefficients from exp2_poly_fit.py beside this file, max relative error
-// 3.6e-6); 2^n added to the exponent bits.  x = -inf (a masked key) gives 0.
-__device__ __forceinline__ float exp2_fma(float x) {
-    const float xc = fmaxf(x, -126.f);
-    const float t = xc + 12582912.f;
-    const float f = xc - (t - 12582912.f);
-    float q = fmaf(9.666368365e-03f, f, 5.592197552e-02f);
-    q = fmaf(q, f, 2.402234972e-01f);
-    q = fmaf(q, f, 6.931210160e-01f);
-    q = fmaf(q, f, 1.0f);
-    const float r = __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
-    return x < -126.f ? 0.f : r;
-}
-
-// Share of the softmax exponentials computed by exp2_fma (one pair in
-// kExpFmaEvery; 0 = none).  Measured on GB300 with the ragged-prefill
-// workload: the special-function unit is not the bottleneck of this kernel,
-// and moving work to the FMA pipe costs issue slots, so it is off.
-constexpr int kExpFmaEvery = 0;
 
 template <typename T>
 struct IsBf16 {
@@ -131,101 +122,120 @@ struct IsBf16<__nv_bfloat16> {
     static constexpr bool value = true;
 };
 
-// One query tile of one qo head of one request: the unit of work of the
-// persistent kernel.  Items are numbered x-major, x = 0 being the LAST query
-// tile of a request (the one that sees the most keys), so taking items in
-// order hands out the heaviest tiles first.
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Wait for this thread's tensor-memory loads, with the 32 destination
+// registers as operands so that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// One work item: query tile x (counted from the LAST tile of the request, the
+// one that sees the most keys) of request b for qo heads hA and hB (hB < 0:
+// block B absent).  Items are numbered request by request (so that the CTAs
+// running at the same time share one request's K/V in L2), inside a request
+// x-major with the (kv head, pair) units innermost, so every request hands
+// out its heaviest tiles first.
 struct PfItem {
-    int b, h, i0, row_base, kvh, shift, qb, kvb, n_tiles;
+    int b, hA, hB, i0, row_base, kvh, shift, qb, kvb, n_tiles;
 };
 
-__device__ __forceinline__ bool pf_item(const PrefillParams &p, int idx, PfItem &it) {
-    const int per_x = p.Hqo * p.B;
-    const int x = idx / per_x, rem = idx - x * per_x;
-    it.h = rem % p.Hqo;
-    it.b = rem / p.Hqo;
+__device__ __forceinline__ void pf_item(const PrefillParams &p, const int4 itm, int bn, PfItem &it) {
+    it.b = itm.x;
+    it.hA = itm.y;
+    it.hB = itm.z;
     it.qb = min(max(p.seq_lens_q[it.b], 0), p.max_q);
     it.kvb = min(max(p.seq_lens_kv[it.b], 0), p.max_kv);
     const int n_qt = (it.qb + kPfRows - 1) / kPfRows;
-    if (x >= n_qt) return false;
-    it.i0 = (n_qt - 1 - x) * kPfRows;
+    it.i0 = (n_qt - 1 - itm.w) * kPfRows;
     it.row_base = p.cu_q[it.b] + it.i0;
-    it.kvh = it.h / p.group;
+    it.kvh = it.hA / p.group;
     it.shift = it.kvb - it.qb;  // query i sits at position shift + i
     int k_hi = p.causal ? min(it.kvb, it.shift + it.i0 + kPfRows) : it.kvb;
     if (k_hi < 0) k_hi = 0;
-    it.n_tiles = (k_hi + kPfBN - 1) / kPfBN;
-    return true;
+    it.n_tiles = (k_hi + bn - 1) / bn;
 }
 
 template <typename T, int DQK, int LAYOUT>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    constexpr int BN = kPfBN;
+    constexpr int BN = PfCfg<DQK>::BN;
     constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
+    constexpr int NC = BN / 32;                  // 32-column chunks of a score row
     constexpr int QA = DQK / 64;                 // 64-column atoms of a Q / K row
-    constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of the Q tile
+    constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of one Q block
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
     constexpr int NI = 2;                        // slots of the work-item ring
-    // TMEM columns: O of group 0 and 1, then the two S buffers; P of a tile
-    // (16-bit pairs, BN/2 columns) overwrites the first half of its S buffer
+    // TMEM columns: S of block X at X * BN (P of chunk i, 16 columns of
+    // 16-bit pairs, overwrites the chunk's first 16 S columns), O of block X
+    // at O_COL + X * 128
     constexpr uint32_t TMEM_COLS = 512;
-    constexpr uint32_t S_COL = 2 * kPfDV;
-    static_assert(S_COL + 2 * BN <= TMEM_COLS, "TMEM budget");
+    constexpr uint32_t O_COL = 2 * BN;
+    static_assert(O_COL + 2 * kPfDV <= TMEM_COLS, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t q_s = smem_u32(smem);
-    const uint32_t k_s = q_s + QB;
+    const uint32_t q_s = smem_u32(smem);  // block A, then block B
+    const uint32_t k_s = q_s + 2 * QB;
     const uint32_t v_s = k_s + SK * KB;
     const uint32_t bar0 = v_s + SV * VB;
-    uint8_t *v_gen = smem + QB + SK * KB;  // generic pointer to the V stages
-    // barriers
+    uint8_t *v_gen = smem + 2 * QB + SK * KB;  // generic pointer to the V stages
     uint32_t nb = 0;
-    const uint32_t b_qfull = bar0 + 8u * nb++;   // Q of the current item landed
-    const uint32_t b_qempty = bar0 + 8u * nb++;  // last QK of an item done: Q buffer free
-    const uint32_t b_ofree = bar0 + 8u * nb++;   // epilogue read O: accumulators free
-    const uint32_t b_xchg = bar0 + 8u * nb++;    // both groups posted (max, sum)
+    const uint32_t b_qfull = bar0 + 8u * nb++;   // Q blocks of the current item landed
+    const uint32_t b_qempty = bar0 + 8u * nb++;  // last QK of an item done: Q buffers free
     const uint32_t b_item_full0 = bar0 + 8u * nb; nb += NI;
     const uint32_t b_item_empty0 = bar0 + 8u * nb; nb += NI;
     const uint32_t b_kfull0 = bar0 + 8u * nb; nb += SK;
     const uint32_t b_kempty0 = bar0 + 8u * nb; nb += SK;
     const uint32_t b_vfull0 = bar0 + 8u * nb; nb += SV;
     const uint32_t b_vempty0 = bar0 + 8u * nb; nb += SV;
-    const uint32_t b_sfull0 = bar0 + 8u * nb; nb += 2;
-    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 4;  // [S buffer][group]
-    const uint32_t b_pvdone0 = bar0 + 8u * nb; nb += 4;  // [S buffer][group]
+    const uint32_t b_sfull0 = bar0 + 8u * nb; nb += 2;  // per block: S tile written
+    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 2;  // per block: P tile written (128 arrivals)
+    const uint32_t b_odone0 = bar0 + 8u * nb; nb += 2;  // per block: last PV of an item done
     auto b_item_full = [&](int i) { return b_item_full0 + 8u * i; };
     auto b_item_empty = [&](int i) { return b_item_empty0 + 8u * i; };
     auto b_kfull = [&](int s) { return b_kfull0 + 8u * s; };
     auto b_kempty = [&](int s) { return b_kempty0 + 8u * s; };
     auto b_vfull = [&](int s) { return b_vfull0 + 8u * s; };
     auto b_vempty = [&](int s) { return b_vempty0 + 8u * s; };
-    auto b_sfull = [&](int i) { return b_sfull0 + 8u * i; };
-    // P of tile t written by group g, and PV of tile t for group g done: one
-    // barrier per S buffer, so that every wait is for the newest phase that
-    // can be pending.  A wait for tile t's phase finds tile t-2's complete
-    // (S_t is written after PV_{t-2}) and tile t+2's impossible (QK_{t+2}
-    // is issued after PV_t, which needs P_t), so parity cannot alias.
-    auto b_pfull = [&](int t, int g) { return b_pfull0 + 8u * (2 * (t & 1) + g); };
-    auto b_pvdone = [&](int t, int g) { return b_pvdone0 + 8u * (2 * (t & 1) + g); };
-    static_assert(SV == 2, "the V tail wait relies on PV_{t-2} having waited for V_{t-2}");
+    auto b_sfull = [&](int x) { return b_sfull0 + 8u * x; };
+    auto b_pfull = [&](int x) { return b_pfull0 + 8u * x; };
+    auto b_odone = [&](int x) { return b_odone0 + 8u * x; };
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
-    __shared__ int item_ring[NI];
-    __shared__ float xchg[2][2][2][kPfRows];  // [item parity][max|sum][group][row]
+    __shared__ int4 item_ring[NI];  // (request, head A, head B, x); request -1: no more work
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int total_items = p.n_qt_max * p.Hqo * p.B;
 
     if (tid == 0) {
         mbar_init(b_qfull, 1);
         mbar_init(b_qempty, 1);
-        mbar_init(b_ofree, 256);
-        mbar_init(b_xchg, 256);
         for (int i = 0; i < NI; ++i) {
             mbar_init(b_item_full(i), 1);
             mbar_init(b_item_empty(i), 2 + 256);  // MMA thread, V producer, 256 softmax threads
@@ -238,12 +248,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(b_vfull(s), 1);
             mbar_init(b_vempty(s), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(b_sfull(i), 1);
-            mbar_init(b_pfull(i, 0), 128);
-            mbar_init(b_pfull(i, 1), 128);
-            mbar_init(b_pvdone(i, 0), 1);
-            mbar_init(b_pvdone(i, 1), 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b_sfull(x), 1);
+            mbar_init(b_pfull(x), 128);
+            mbar_init(b_odone(x), 1);
         }
         abort_s = 0;
         fence_mbar_init();
@@ -261,26 +269,35 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         *abort_flag = 1;
         set_err(p.err, PKV_DEV_ERR_TIMEOUT);
     };
-    // the k-th item published by the K producer (-1: no more work); every
-    // consumer role takes every item, in order, and releases the ring slot
-    auto take_item = [&](int k, bool &ok) -> int {
+    // the k-th item published by the K producer (request -1: no more work);
+    // every consumer role takes every item, in order, and releases the slot
+    auto take_item = [&](int k, bool &ok) -> int4 {
         const int slot = k % NI;
         if (!mbar_wait(b_item_full(slot), (k / NI) & 1, abort_flag)) {
             ok = false;
-            return -1;
+            return make_int4(-1, 0, 0, 0);
         }
-        const int idx = *reinterpret_cast<volatile int *>(&item_ring[slot]);
+        const volatile int *q = reinterpret_cast<const volatile int *>(&item_ring[slot]);
+        const int4 v = make_int4(q[0], q[1], q[2], q[3]);
         mbar_arrive(b_item_empty(slot));
-        return idx;
+        return v;
     };
+
+    // Barrier phases.  Every wait below is for the newest phase that can be
+    // pending, so that a parity can never match an older completed phase:
+    // K/V stage s of tile t: phase t / S{K,V}; sfull/pfull of block X: the
+    // block's tile count; odone of block X: the block's count of items with
+    // tiles; qfull/qempty: the item count.  S_X(t+1) is written by a QK
+    // issued after PV_X(t), which needs P_X(t), so no block can run two
+    // phases ahead of its partner.
 
     if (warp == kTmaWarp || warp == kTmaVWarp) {
         // ------------------------------------------------------------ TMA producers
-        // Warp 8 takes work items from the global counter, publishes them,
-        // and loads Q and the K tiles; warp 10 loads the V tiles.  A K stage
-        // is released by its QK and a V stage by its (later) PV, so the rings
-        // advance independently.  Both warps look up a tile's page ids in one
-        // coalesced load, one tile ahead; lane 0 issues the copies.
+        // Warp 8 takes items from the global counter, publishes them, loads
+        // the Q blocks and the K tiles; warp 10 loads the V tiles.  A K stage
+        // is released by the last QK that reads it and a V stage by the last
+        // PV.  Each warp looks up a tile's page ids in one coalesced load,
+        // one tile ahead; lane 0 issues the copies.
         const bool is_k = warp == kTmaWarp;
         if (lane == 0) {
             if (is_k) {
@@ -295,53 +312,73 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
         const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
         const int NS = is_k ? SK : SV;
+        const int U = p.Hkv * p.pairs;
         bool ok = true;
         int t_base = 0;  // tiles of earlier items (global tile counter)
+        const int total_items = is_k ? p.cu_items[p.B] : 0;
+        int b_scan = 0;  // request of this CTA's previous item: items come in increasing order
         for (int k = 0; ok; ++k) {
-            int idx;
+            int4 itm = make_int4(-1, 0, 0, 0);
             if (is_k) {
-                // fetch the next valid item and publish it
-                idx = -1;
-                if (lane == 0) {
-                    while (true) {
-                        const int c = atomicAdd(p.work_counter, 1);
-                        if (c >= total_items) break;
-                        PfItem tmp;
-                        if (pf_item(p, c, tmp)) {
-                            idx = c;
+                // take the next item from the counter, find its request with a
+                // warp-wide forward scan of cu_items, and publish it
+                int c = 0;
+                if (lane == 0) c = atomicAdd(p.work_counter, 1);
+                c = __shfl_sync(0xffffffffu, c, 0);
+                if (c < total_items) {
+                    while (true) {  // ends: cu_items[B] = total > c
+                        const int bi = b_scan + lane;
+                        const int v = bi <= p.B ? p.cu_items[bi] : 0x7fffffff;
+                        const unsigned m = __ballot_sync(0xffffffffu, v > c);
+                        if (m) {
+                            b_scan += __ffs(m) - 2;  // cu_items[b_scan] <= c always
                             break;
                         }
+                        b_scan += 32;
                     }
+                    const int rem = c - p.cu_items[b_scan];
+                    const int u = rem % U, kvh = u / p.pairs;
+                    const int hA = kvh * p.group + 2 * (u % p.pairs);
+                    const int hB = hA + 1 < (kvh + 1) * p.group ? hA + 1 : -1;
+                    itm = make_int4(b_scan, hA, hB, rem / U);
+                }
+                if (lane == 0) {
                     const int slot = k % NI;
                     if (k >= NI && !mbar_wait(b_item_empty(slot), ((k / NI) - 1) & 1, abort_flag)) {
                         give_up();
                         ok = false;
                     } else {
-                        item_ring[slot] = idx;
+                        item_ring[slot] = itm;
                         mbar_arrive(b_item_full(slot));
                     }
                 }
-                idx = __shfl_sync(0xffffffffu, idx, 0);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
             } else {
-                if (lane == 0) idx = take_item(k, ok);
-                idx = __shfl_sync(0xffffffffu, idx, 0);
+                if (lane == 0) itm = take_item(k, ok);
+                itm.x = __shfl_sync(0xffffffffu, itm.x, 0);
+                itm.y = __shfl_sync(0xffffffffu, itm.y, 0);
+                itm.z = __shfl_sync(0xffffffffu, itm.z, 0);
+                itm.w = __shfl_sync(0xffffffffu, itm.w, 0);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
             }
-            if (!ok || idx < 0) break;
+            if (!ok || itm.x < 0) break;
             PfItem it;
-            pf_item(p, idx, it);
+            pf_item(p, itm, BN, it);
             const int32_t *bt = p.block_tables + static_cast<int64_t>(it.b) * p.bt_stride;
-            // Q of this item, once the previous item's last QK is done; it is
+            // Q blocks of this item, once the previous item's last QK is done;
             // loaded after the item's first K tile so that the two overlap
             auto load_q = [&]() {  // lane 0 of the K producer
                 if (k >= 1 && !mbar_wait(b_qempty, (k - 1) & 1, abort_flag)) {
                     give_up();
                     ok = false;
                 } else {
-                    mbar_expect_tx(b_qfull, QB);
+                    mbar_expect_tx(b_qfull, it.hB >= 0 ? 2 * QB : QB);
                     for (int c = 0; c < QA; ++c)
-                        tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.h, it.row_base);
+                        tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hA, it.row_base);
+                    if (it.hB >= 0)
+                        for (int c = 0; c < QA; ++c)
+                            tma_load_3d(q_s + QB + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hB,
+                                        it.row_base);
                 }
             };
             if (is_k && lane == 0 && it.n_tiles == 0) load_q();
@@ -403,10 +440,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Per item: QK_0, then for every tile j: QK_{j+1}, PV_{j,0}, PV_{j,1}.
-        // QK_{j+1} runs on the tensor core while the softmax works on S_j.
-        // tcgen05 MMAs execute in issue order, so a QK that overwrites an S
-        // buffer cannot disturb the PV still reading P from it.
+        // Per item of n tiles: QK_A(0) QK_B(0), then for every tile t:
+        // PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1).  tcgen05 MMAs execute in issue
+        // order, so QK_X(t+1), which overwrites S_X, cannot disturb PV_X(t)
+        // reading P_X from it, and a completed S_X(t+1) implies that PV_X(t)
+        // is complete (the softmax relies on both).
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
             constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
@@ -414,249 +452,267 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
             const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
             bool ok = true;
-            int t_base = 0;
-            int n_tiled = 0;  // items with at least one key tile so far (o_free phases)
-            auto issue_qk = [&](int t) -> bool {
-                const int sk = t % SK, uk = t / SK;
-                if (!mbar_wait(b_kfull(sk), uk & 1, abort_flag)) return false;
+            int t_base = 0;   // K/V tiles of earlier items
+            int tb_base = 0;  // tiles of block B in earlier items
+            auto wait_k = [&](int t) {
+                if (!mbar_wait(b_kfull(t % SK), (t / SK) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint64_t kd = kdesc0 + ((sk * KB) >> 4);
+                return true;
+            };
+            auto qk = [&](int x, int t) {  // S_X = Q_X K(t)^T
+                const uint64_t kd = kdesc0 + (((t % SK) * KB) >> 4);
+                const uint64_t qd = qdesc0 + ((x * QB) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk)
-                    umma_ss(tmem + S_COL + (t & 1) * BN,
-                            qdesc0 + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
+                    umma_ss(tmem + x * BN, qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
                             kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-                umma_commit(b_sfull(t & 1));
-                umma_commit(b_kempty(sk));
-                return true;
+                umma_commit(b_sfull(x));
             };
-            auto issue_pv = [&](int t, bool first) -> bool {
-                const int sv = t % SV, uv = t / SV;
-                const uint64_t vd = vdesc0 + ((sv * VB) >> 4);
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (!mbar_wait(b_pfull(t, hh), (t >> 1) & 1, abort_flag)) return false;
-                    if (hh == 0 && !mbar_wait(b_vfull(sv), uv & 1, abort_flag)) return false;
-                    tc_fence_after();
+            auto pv = [&](int x, int t, bool first) {  // O_X (+)= P_X V(t)
+                const uint64_t vd = vdesc0 + (((t % SV) * VB) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 32; ++kk)
-                        umma_ts(tmem + hh * kPfDV, tmem + S_COL + (t & 1) * BN + hh * (BN / 2) + kk * 8,
-                                vd + (((hh * (BN / 2) + kk * 16) * 128) >> 4), idesc_pv,
-                                (!first || kk > 0) ? 1u : 0u);
-                    umma_commit(b_pvdone(t, hh));
-                }
-                umma_commit(b_vempty(sv));
-                return true;
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ts(tmem + O_COL + x * kPfDV, tmem + x * BN + 32 * (kk >> 1) + 8 * (kk & 1),
+                            vd + ((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
             };
             for (int k = 0; ok; ++k) {
-                const int idx = take_item(k, ok);
-                if (!ok || idx < 0) break;
+                const int4 itm = take_item(k, ok);
+                if (!ok || itm.x < 0) break;
                 PfItem it;
-                pf_item(p, idx, it);
+                pf_item(p, itm, BN, it);
+                const bool hasB = it.hB >= 0;
+                const int n = it.n_tiles;
                 if (!mbar_wait(b_qfull, k & 1, abort_flag)) { ok = false; break; }
-                if (it.n_tiles > 0) ok = issue_qk(t_base);
-                if (ok && it.n_tiles == 1) umma_commit(b_qempty);
-                for (int j = 0; ok && j < it.n_tiles; ++j) {
-                    if (j + 1 < it.n_tiles) {
-                        if (!issue_qk(t_base + j + 1)) { ok = false; break; }
-                        if (j + 2 == it.n_tiles) umma_commit(b_qempty);  // last QK of the item issued
-                    }
-                    // the epilogue of the previous item with tiles must have
-                    // read O before this item's first PV overwrites it
-                    if (j == 0 && n_tiled >= 1 && !mbar_wait(b_ofree, (n_tiled - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!issue_pv(t_base + j, j == 0)) { ok = false; break; }
+                if (n == 0) {
+                    umma_commit(b_qempty);
+                    continue;
                 }
-                if (ok && it.n_tiles == 0) umma_commit(b_qempty);
-                t_base += it.n_tiles;
-                n_tiled += it.n_tiles > 0;
+                if (!wait_k(t_base)) { ok = false; break; }
+                qk(0, t_base);
+                if (hasB) qk(1, t_base);
+                umma_commit(b_kempty(t_base % SK));
+                if (n == 1) umma_commit(b_qempty);
+                for (int j = 0; j < n; ++j) {
+                    const int t = t_base + j, tb = tb_base + j;
+                    const bool more = j + 1 < n;
+                    // block A: PV_A(t), then QK_A(t+1)
+                    if (!mbar_wait(b_pfull(0), t & 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(b_vfull(t % SV), (t / SV) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    pv(0, t, j == 0);
+                    if (!more) umma_commit(b_odone(0));
+                    if (more) {
+                        if (!wait_k(t + 1)) { ok = false; break; }
+                        qk(0, t + 1);
+                        if (!hasB) {
+                            umma_commit(b_kempty((t + 1) % SK));
+                            if (j + 2 == n) umma_commit(b_qempty);
+                        }
+                    }
+                    // block B: PV_B(t), then QK_B(t+1)
+                    if (hasB) {
+                        if (!mbar_wait(b_pfull(1), tb & 1, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        pv(1, t, j == 0);
+                        if (!more) umma_commit(b_odone(1));
+                        if (more) {
+                            qk(1, t + 1);
+                            umma_commit(b_kempty((t + 1) % SK));
+                            if (j + 2 == n) umma_commit(b_qempty);
+                        }
+                    }
+                    umma_commit(b_vempty(t % SV));
+                }
+                t_base += n;
+                if (hasB) tb_base += n;
             }
             if (!ok) give_up();
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Two groups of four warps split every key tile by columns: group g
-        // owns keys [64g, 64g+64) of each tile and keeps its own running max,
-        // sum and O accumulator (TMEM columns g*128 ..), so the groups never
-        // exchange anything inside the tile loop.  Warp w owns TMEM lanes /
-        // query rows 32*(w%4) .. +31, one thread per (row, group).  The two
-        // partial results of an item are merged in its epilogue.
-        constexpr int HC = BN / 2;  // S columns per thread
-        const int g = warp >> 2;
-        const int r = 32 * (warp & 3) + lane;  // query row of this thread inside the tile
+        // Block X = warp / 4; warp w owns TMEM lanes / query rows
+        // 32*(w%4) .. +31 of the block, one thread per row.  Per tile the
+        // thread walks its row's BN scores in 32-column chunks, loading the
+        // next chunk while it works on this one.  The running max m only
+        // rises when a chunk exceeds it by more than 8 (a factor 2^8): then
+        // the row sum, the P chunks already written for this tile and (once
+        // per tile) O are rescaled -- rare after the first chunk of an item.
+        const int X = warp >> 2;
+        const int r = 32 * (warp & 3) + lane;  // query row inside the tile
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        const uint32_t o_g = g * kPfDV;  // this group's O columns
+        const uint32_t s_col = X * BN, o_col = O_COL + X * kPfDV;
+        const float sc = p.scale_log2;
+        const bool pos_scale = sc > 0.f;        // max on raw scores, one FFMA scales and shifts
+        const float k_mul = pos_scale ? sc : 1.f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
         bool ok = true;
-        int t_base = 0;
+        int t_base = 0;   // K/V tiles of earlier items
+        int tx_base = 0;  // tiles of this block in earlier items
+        int nx_items = 0; // items with tiles processed by this block
         for (int k = 0; ok; ++k) {
-            int idx = take_item(k, ok);
+            const int4 itm = take_item(k, ok);  // every thread reads the same slot
             ok = __all_sync(0xffffffffu, ok);
-            idx = __shfl_sync(0xffffffffu, idx, 0);
-            if (!ok || idx < 0) break;
+            if (!ok || itm.x < 0) break;
             PfItem it;
-            pf_item(p, idx, it);
+            pf_item(p, itm, BN, it);
+            const int n = it.n_tiles;
+            const int h = X == 0 ? it.hA : it.hB;
+            if (h < 0) {  // block B absent in this item
+                t_base += n;
+                continue;
+            }
             const int pos = it.shift + it.i0 + r;
             const int lim = p.causal ? min(pos, it.kvb - 1) : it.kvb - 1;  // last visible key
             float m_used = -INFINITY, l = 0.f;
-            for (int j = 0; j < it.n_tiles; ++j) {
-                const int t = t_base + j;
-                const int j0 = j * BN + g * HC;  // first key of this thread's columns
-                const uint32_t t_s = t_lane + S_COL + (t & 1) * BN + g * HC;
-                // S_t complete; by commit order so is PV_{t-2}, the last reader
-                // of the P columns about to be rewritten
-                if (!wait_warp(b_sfull(t & 1), (t >> 1) & 1)) { ok = false; break; }
+            for (int j = 0; j < n; ++j) {
+                const int t = t_base + j, tx = tx_base + j;
+                const int j0 = j * BN;
+                // S_X(t) complete, and with it PV_X(t-1)
+                if (!wait_warp(b_sfull(X), tx & 1)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t sx[HC];
+                const bool warp_full = __all_sync(0xffffffffu, j0 + BN - 1 <= lim);
+                const uint32_t s_addr = t_lane + s_col;
+                uint32_t ra[32], rb[32];
+                tmem_ld32(s_addr, ra);
+                tmem_wait_ld_regs(ra);
+                float2 l2 = make_float2(0.f, 0.f);
+                float acc_alpha = 1.f;
 #pragma unroll
-                for (int c = 0; c < HC / 32; ++c)
-                    tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sx + c * 32));
-                tmem_wait_ld();
-                const bool full = j0 + HC - 1 <= lim;
-                // row max: on the raw scores when the scale is positive (then
-                // max(scale * s) = scale * max(s) and one FFMA per element
-                // later does both the scaling and the shift), else scaled
-                const float sc = p.scale_log2;
-                const bool pos_scale = sc > 0.f;
-                float m8[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
-                               -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int i = 0; i < NC; ++i) {
+                    uint32_t(&cur)[32] = (i & 1) ? rb : ra;
+                    uint32_t(&nxt)[32] = (i & 1) ? ra : rb;
+                    if (i + 1 < NC) tmem_ld32(s_addr + 32 * (i + 1), nxt);
+                    float v[32];
 #pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    float v = __uint_as_float(sx[c]);
-                    if (!pos_scale) v *= sc;
-                    if (!full && j0 + c > lim) v = -INFINITY;
-                    sx[c] = __float_as_uint(v);
-                    m8[c & 7] = fmaxf(m8[c & 7], v);
-                }
-                float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                if (pos_scale) mx *= sc;
-                const float k_mul = pos_scale ? sc : 1.f;  // x = s * k_mul - base
-                float alpha = 1.f;
-                bool need = false;
-                if (mx != -INFINITY) {
-                    if (m_used == -INFINITY) {
-                        m_used = mx;
-                    } else if (mx > m_used + 8.f) {
-                        alpha = fast_exp2(m_used - mx);
-                        m_used = mx;
-                        l *= alpha;
-                        need = true;
+                    for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(cur[c]);
+                    if (!pos_scale) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) v[c] *= sc;
                     }
-                }
-                const float base = m_used == -INFINITY ? 0.f : m_used;
-                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (!warp_full) {
+                        const int lr = lim - (j0 + 32 * i);  // last visible column of this chunk
 #pragma unroll
-                for (int e = 0; e < HC / 2; ++e) {
-                    const float x0 = fmaf(__uint_as_float(sx[2 * e]), k_mul, -base);
-                    const float x1 = fmaf(__uint_as_float(sx[2 * e + 1]), k_mul, -base);
-                    // pairs e with e % kExpFmaEvery == kExpFmaEvery - 1 on the
-                    // FMA pipe, the rest on the special-function unit
-                    const bool on_fma =
-                        kExpFmaEvery > 0 && (e % (kExpFmaEvery > 0 ? kExpFmaEvery : 1)) == kExpFmaEvery - 1;
-                    const float p0 = on_fma ? exp2_fma(x0) : fast_exp2(x0);
-                    const float p1 = on_fma ? exp2_fma(x1) : fast_exp2(x1);
-                    s4[e & 3] += p0;
-                    s4[(e + 2) & 3] += p1;
-                    sx[e] = pack2<T>(p0, p1);  // P column e = keys 2e, 2e+1 of this half
+                        for (int c = 0; c < 32; ++c)
+                            if (c > lr) v[c] = -INFINITY;
+                    }
+                    float m3[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float a = fmax3(v[8 * q], v[8 * q + 1], v[8 * q + 2]);
+                        const float b = fmax3(v[8 * q + 3], v[8 * q + 4], v[8 * q + 5]);
+                        m3[q] = fmax3(a, b, fmaxf(v[8 * q + 6], v[8 * q + 7]));
+                    }
+                    float mc = fmaxf(fmax3(m3[0], m3[1], m3[2]), m3[3]);
+                    if (pos_scale) mc *= sc;
+                    const bool up = mc > m_used + 8.f;
+                    if (__any_sync(0xffffffffu, up)) {  // rare: raise the running max
+                        const float alpha = up ? fast_exp2(m_used - mc) : 1.f;
+                        if (up) m_used = mc;
+                        l *= alpha;
+                        l2.x *= alpha;
+                        l2.y *= alpha;
+                        acc_alpha *= alpha;
+                        if (i > 0) {  // P chunks of this tile already written
+                            tmem_wait_st();
+#pragma unroll
+                            for (int i2 = 0; i2 < i; ++i2) {
+                                uint32_t pw[16];
+                                tmem_ld16(s_addr + 32 * i2, pw);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    const float2 f = unpack2<T>(pw[e]);
+                                    pw[e] = pack2<T>(f.x * alpha, f.y * alpha);
+                                }
+                                tmem_st16(s_addr + 32 * i2, pw);
+                            }
+                        }
+                    }
+                    const float base = m_used == -INFINITY ? 0.f : m_used;
+                    const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 x = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), kk2, nb2);
+                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                        l2 = __fadd2_rn(l2, make_float2(p0, p1));
+                        pw[e] = pack2<T>(p0, p1);  // P column: keys 2e, 2e+1 of the chunk
+                    }
+                    tmem_st16(s_addr + 32 * i, pw);
+                    if (i + 1 < NC) tmem_wait_ld_regs(nxt);
                 }
-                // P (HC keys, HC/2 columns) over the consumed first half of my S columns
-                tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(sx));
-                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                l += l2.x + l2.y;
                 // rows of V past the sequence end may hold anything (even NaN):
-                // zero the ones this group's PV reads so that P = 0 there
-                // cannot produce 0 * NaN
-                if (j0 + HC > it.kvb) {
+                // block A zeroes them before its PV (block B's PV comes later in
+                // issue order), so that P = 0 there cannot produce 0 * NaN
+                if (X == 0 && j0 + BN > it.kvb) {
                     const int sv = t % SV, uv = t / SV;
                     if (!wait_warp(b_vfull(sv), uv & 1)) { ok = false; break; }
-                    const int zs = max(it.kvb - j * BN, g * HC), ze = (g + 1) * HC;
+                    const int zs = max(it.kvb - j0, 0);
                     uint8_t *vbase = v_gen + sv * VB;
-                    for (int q = r; q < (ze - zs) * 16; q += 128) {
+                    for (int q = r; q < (BN - zs) * 16; q += 128) {
                         const int row = zs + (q >> 4), chunk = q & 15;
                         *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                 }
-                // O_g *= alpha when the running max moved (rare: threshold 2^8);
-                // PV_{t-1} of this group must be complete first
-                if (__any_sync(0xffffffffu, need)) {
-                    if (j >= 1 && !wait_warp(b_pvdone(t - 1, g), ((t - 1) >> 1) & 1)) { ok = false; break; }
-                    tc_fence_after();
+                // O_X *= alpha when the running max moved; PV_X(t-1) is complete
+                // (S_X(t) is), and at the item's first tile O is about to be
+                // overwritten anyway
+                if (j > 0 && __any_sync(0xffffffffu, acc_alpha != 1.f)) {
 #pragma unroll
                     for (int c = 0; c < kPfDV / 32; ++c) {
                         uint32_t ro[32];
-                        tmem_ld32(t_lane + o_g + c * 32, ro);
-                        tmem_wait_ld();
+                        tmem_ld32(t_lane + o_col + c * 32, ro);
+                        tmem_wait_ld_regs(ro);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
-                        tmem_st32(t_lane + o_g + c * 32, ro);
+                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * acc_alpha);
+                        tmem_st32(t_lane + o_col + c * 32, ro);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(b_pfull(t, g));
+                mbar_arrive(b_pfull(X));
             }
             if (!ok) break;
-            // epilogue: wait for this group's last PV of the item (a commit
-            // covers every earlier MMA too), trade (max, sum) with the other
-            // group, merge the two partial O rows; group g writes output
-            // columns [g*64, g*64+64) and group 0 the LSE
-            const int tl = t_base + it.n_tiles - 1;
-            if (it.n_tiles > 0 && !wait_warp(b_pvdone(tl, g), (tl >> 1) & 1)) { ok = false; break; }
-            xchg[k & 1][0][g][r] = m_used;
-            xchg[k & 1][1][g][r] = l;
-            mbar_arrive(b_xchg);
-            if (!wait_warp(b_xchg, k & 1)) { ok = false; break; }
-            const float m0 = xchg[k & 1][0][0][r], m1 = xchg[k & 1][0][1][r];
-            const float M = fmaxf(m0, m1);
-            const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
-            const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
-            const float lt = xchg[k & 1][1][0][r] * w0 + xchg[k & 1][1][1][r] * w1;
-            const bool have = it.n_tiles > 0;
+            // epilogue: after the block's last PV of the item, normalise O and
+            // write it with the LSE
+            const bool have = n > 0;
+            if (have && !wait_warp(b_odone(X), nx_items & 1)) { ok = false; break; }
             tc_fence_after();
             const int qi = it.i0 + r;
             const int64_t grow = static_cast<int64_t>(it.row_base) + r;
             const bool valid = qi < it.qb && grow < p.total_q;
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const uint32_t ocol = g * (kPfDV / 2);
-            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + it.h) * kPfDV + ocol;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV;
 #pragma unroll
-            for (int c = 0; c < kPfDV / 64; ++c) {
-                uint32_t ra[32], rb[32];
+            for (int c = 0; c < kPfDV / 32; ++c) {
+                uint32_t ro[32];
                 if (have) {
-                    tmem_ld32(t_lane + ocol + c * 32, ra);
-                    tmem_ld32(t_lane + kPfDV + ocol + c * 32, rb);
-                    tmem_wait_ld();
-                }
-                float o[32];
+                    tmem_ld32(t_lane + o_col + c * 32, ro);
+                    tmem_wait_ld_regs(ro);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float v = 0.f;
-                    if (have && w0 != 0.f) v += __uint_as_float(ra[e]) * w0;
-                    if (have && w1 != 0.f) v += __uint_as_float(rb[e]) * w1;
-                    o[e] = v * inv;
+                    for (int e = 0; e < 32; ++e) ro[e] = 0u;
                 }
                 if (valid) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint4 w = make_uint4(pack2<T>(o[q * 8 + 0], o[q * 8 + 1]), pack2<T>(o[q * 8 + 2], o[q * 8 + 3]),
-                                             pack2<T>(o[q * 8 + 4], o[q * 8 + 5]), pack2<T>(o[q * 8 + 6], o[q * 8 + 7]));
+                        auto o = [&](int e) { return __uint_as_float(ro[q * 8 + e]) * inv; };
+                        uint4 w = make_uint4(pack2<T>(o(0), o(1)), pack2<T>(o(2), o(3)), pack2<T>(o(4), o(5)),
+                                             pack2<T>(o(6), o(7)));
                         *reinterpret_cast<uint4 *>(orow + c * 32 + q * 8) = w;
                     }
                 }
             }
-            if (valid && g == 0) p.lse[grow * p.Hqo + it.h] = lt > 0.f ? (M + fast_log2(lt)) * kLn2 : -INFINITY;
-            // O has been read: the next item's first PV may overwrite it (items
-            // without key tiles never touch O and are not counted)
-            if (have) {
-                tc_fence_before();
-                mbar_arrive(b_ofree);
-            }
-            t_base += it.n_tiles;
+            if (valid) p.lse[grow * p.Hqo + h] = l > 0.f ? (m_used + fast_log2(l)) * kLn2 : -INFINITY;
+            tc_fence_before();  // O read before the next item's first PV_X overwrites it
+            t_base += n;
+            tx_base += n;
+            nx_items += have;
         }
         if (!ok) give_up();
     }
@@ -671,8 +727,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 template <int DQK>
 static size_t prefill_smem_bytes() {
-    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
-    return 1024 + kPfRows * DQK * 2 + SK * kPfBN * DQK * 2 + SV * kPfBN * kPfDV * 2 + 8 * (20 + 2 * SK + 2 * SV);
+    constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
+    return 1024 + 2 * kPfRows * DQK * 2 + SK * BN * DQK * 2 + SV * BN * kPfDV * 2 + 8 * (12 + 2 * SK + 2 * SV);
 }
 
 template <typename T, int DQK, int LAYOUT>
@@ -726,9 +782,10 @@ static bool cache_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
     return encode_tmap(m, base, dt, 4, dims, strides, box);
 }
 
-// workspace: cu_q[B+1], then the work-item counter of the persistent kernel
+// workspace: cu_q[B+1], cu_items[B+1], then the work-item counter of the
+// persistent kernel
 static size_t prefill_ws_bytes(int B) {
-    return round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256) + 256;
+    return 2 * round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256) + 256;
 }
 
 }  // namespace pkv
@@ -787,7 +844,8 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
 
     const CUtensorMapDataType tdt =
         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const int rows = page_size < kPfBN ? page_size : kPfBN;
+    const int bn = pf_bn(d_qk);
+    const int rows = page_size < bn ? page_size : bn;
     CUtensorMap tq, tk, tv;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),
@@ -804,11 +862,13 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
         return PKV_ERR_CUDA;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t cu_bytes = round_up(static_cast<size_t>(batch_size + 1) * sizeof(int32_t), 256);
     int32_t *cu_q = static_cast<int32_t *>(workspace);
-    int *work_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) +
-                                                round_up(static_cast<size_t>(batch_size + 1) * sizeof(int32_t), 256));
-    prefill_plan_kernel<<<1, 32, 0, st>>>(actual_seq_lens_q, actual_seq_lens_kv, batch_size,
-                                          max_token_per_sequence, max_sequence_kv, cu_q, err_word,
+    int32_t *cu_items = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + cu_bytes);
+    int *work_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) + 2 * cu_bytes);
+    const int pairs = (num_qo_heads / num_kv_heads + 1) / 2;  // head pairs per kv head
+    prefill_plan_kernel<<<1, 32, 0, st>>>(actual_seq_lens_q, actual_seq_lens_kv, batch_size, num_kv_heads * pairs,
+                                          max_token_per_sequence, max_sequence_kv, cu_q, cu_items, err_word,
                                           work_counter);
     PrefillParams p;
     p.max_num_pages = max_num_pages;
@@ -817,6 +877,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     p.seq_lens_q = actual_seq_lens_q;
     p.seq_lens_kv = actual_seq_lens_kv;
     p.cu_q = cu_q;
+    p.cu_items = cu_items;
     p.block_tables = block_tables;
     p.bt_stride = block_table_stride;
     p.B = batch_size;
@@ -824,6 +885,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     p.Hqo = num_qo_heads;
     p.Hkv = num_kv_heads;
     p.group = num_qo_heads / num_kv_heads;
+    p.pairs = pairs;
     p.page_shift = ilog2_exact(page_size);
     p.max_q = max_token_per_sequence;
     p.max_kv = max_sequence_kv;
@@ -832,9 +894,8 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     p.lse = lse;
     p.err = err_word;
     const int n_qt = (max_token_per_sequence + kPfRows - 1) / kPfRows;
-    p.n_qt_max = n_qt;
     int launches = 1;
-    const int64_t items = static_cast<int64_t>(n_qt) * num_qo_heads * batch_size;
+    const int64_t items = static_cast<int64_t>(n_qt) * num_kv_heads * pairs * batch_size;
     if (n_qt > 0) {
         // persistent: one CTA per SM (the shared-memory footprint allows one)
         const int64_t ctas = items < num_sms() ? items : num_sms();
