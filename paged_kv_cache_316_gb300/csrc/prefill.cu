@@ -11,21 +11,24 @@
 // is one 128-row query tile of a request for TWO qo heads of the same kv
 // head (blocks A and B; B is absent when the group size is odd and the
 // heads run out), so every K/V tile brought into shared memory feeds two
-// 128 x BN score tiles.  Warp roles (352 threads):
-//   warps 8, 10  TMA producers: warp 8 takes the items, loads both Q blocks
-//           and the K tiles, warp 10 the V tiles, page by page, through
-//           separate K and V rings of shared-memory stages;
-//   warp 9  allocates tensor memory and issues the tcgen05 MMAs from one
-//           thread in the order QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1)
-//           PV_B(t) QK_B(t+1) | ..., so that while one block's softmax runs
-//           the tensor core works for the other block (ping-pong);
-//   warps 0-3 / 4-7  the softmax of block A / B, one thread per query row:
-//           read the row's S columns from TMEM 32 at a time, mask, online
-//           softmax in base 2 against a running max that is raised only
-//           when a chunk exceeds it by more than 2^8, write P (bf16/fp16)
-//           over the consumed S columns as the A operand of the block's PV
-//           MMA, which accumulates into the block's O in TMEM; at the end of
-//           the item normalise O and write it with the LSE.
+// 128 x BN score tiles.  Warp roles (S = softmax threads per query row, 2
+// for d_qk 128 and 1 for d_qk 192):
+//   warps 0 .. 8S-1  the softmax: block X = (w / 4) % 2, TMEM lane quarter
+//           w % 4, column share w / 8; each thread reads its part of a score
+//           row from TMEM 32 columns at a time, masks, takes the row max
+//           (traded with its partner when S = 2), runs the online softmax in
+//           base 2 against a running max that is raised only when the tile
+//           max exceeds it by more than 2^8, and writes P (bf16/fp16) over
+//           the consumed S columns as the A operand of the block's PV MMA,
+//           which accumulates into the block's O in TMEM; at the end of the
+//           item it normalises its share of O and writes it with the LSE;
+//   warp 8S     TMA producer: takes the items, loads both Q blocks and the K
+//           tiles page by page through a ring of shared-memory stages;
+//   warp 8S+1   allocates tensor memory and issues the tcgen05 MMAs from one
+//           thread in the order QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t)
+//           QK_B(t+1) | ..., so that while one block's softmax runs the
+//           tensor core works for the other block (ping-pong);
+//   warp 8S+2   TMA producer of the V tiles (a second ring).
 // Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
 // other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
@@ -36,22 +39,28 @@
 namespace pkv {
 
 constexpr int kPfRows = 128;     // query rows per block
-constexpr int kPfThreads = 352;  // 8 softmax warps + K-load warp + MMA warp + V-load warp
-constexpr int kTmaWarp = 8, kMmaWarp = 9, kTmaVWarp = 10;
 constexpr int kPfDV = 128;
 
-// Keys per tile (BN) and ring depths.  TMEM holds S of both blocks (BN
-// columns each) and O of both blocks (128 columns each); shared memory holds
-// both Q blocks, SK K stages and SV V stages.
+// Keys per tile (BN), ring depths and softmax threads per query row
+// (SPLIT).  TMEM holds S of both blocks (BN columns each) and O of both
+// blocks (128 columns each); shared memory holds both Q blocks, SK K stages
+// and SV V stages.  Warps 0 .. 8*SPLIT-1 run the softmax, then come the
+// K-load, MMA and V-load warps.
 template <int DQK>
 struct PfCfg;
 template <>
 struct PfCfg<128> {
-    static constexpr int BN = 128, SK = 3, SV = 2;
+    static constexpr int BN = 128, SK = 2, SV = 2, SPLIT = 2;
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int BN = 64, SK = 3, SV = 3;
+    static constexpr int BN = 64, SK = 3, SV = 3, SPLIT = 1;
+};
+template <int DQK>
+struct PfRoles {
+    static constexpr int kSoftmaxWarps = 8 * PfCfg<DQK>::SPLIT;
+    static constexpr int kTmaWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1, kTmaVWarp = kSoftmaxWarps + 2;
+    static constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 };
 static int pf_bn(int d_qk) { return d_qk == 128 ? PfCfg<128>::BN : PfCfg<192>::BN; }
 
@@ -180,12 +189,13 @@ __device__ __forceinline__ void pf_item(const PrefillParams &p, const int4 itm, 
 }
 
 template <typename T, int DQK, int LAYOUT>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     constexpr int BN = PfCfg<DQK>::BN;
-    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
-    constexpr int NC = BN / 32;                  // 32-column chunks of a score row
+    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV, SPLIT = PfCfg<DQK>::SPLIT;
+    constexpr int kTmaWarp = PfRoles<DQK>::kTmaWarp, kMmaWarp = PfRoles<DQK>::kMmaWarp,
+                  kTmaVWarp = PfRoles<DQK>::kTmaVWarp;
     constexpr int QA = DQK / 64;                 // 64-column atoms of a Q / K row
     constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of one Q block
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
@@ -216,8 +226,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t b_vfull0 = bar0 + 8u * nb; nb += SV;
     const uint32_t b_vempty0 = bar0 + 8u * nb; nb += SV;
     const uint32_t b_sfull0 = bar0 + 8u * nb; nb += 2;  // per block: S tile written
-    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 2;  // per block: P tile written (128 arrivals)
+    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 2;  // per block: P tile written (128 * SPLIT arrivals)
     const uint32_t b_odone0 = bar0 + 8u * nb; nb += 2;  // per block: last PV of an item done
+    const uint32_t b_xchg0 = bar0 + 8u * nb; nb += 8;   // per (block, row quarter): partner exchange
     auto b_item_full = [&](int i) { return b_item_full0 + 8u * i; };
     auto b_item_empty = [&](int i) { return b_item_empty0 + 8u * i; };
     auto b_kfull = [&](int s) { return b_kfull0 + 8u * s; };
@@ -227,9 +238,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     auto b_sfull = [&](int x) { return b_sfull0 + 8u * x; };
     auto b_pfull = [&](int x) { return b_pfull0 + 8u * x; };
     auto b_odone = [&](int x) { return b_odone0 + 8u * x; };
+    auto b_xchg = [&](int i) { return b_xchg0 + 8u * i; };
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ int4 item_ring[NI];  // (request, head A, head B, x); request -1: no more work
+    __shared__ float xbuf[2][2][2][kPfRows];  // [exchange parity][block][column half][row]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -238,7 +251,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         mbar_init(b_qempty, 1);
         for (int i = 0; i < NI; ++i) {
             mbar_init(b_item_full(i), 1);
-            mbar_init(b_item_empty(i), 2 + 256);  // MMA thread, V producer, 256 softmax threads
+            mbar_init(b_item_empty(i), 2 + 256 * SPLIT);  // MMA thread, V producer, softmax threads
         }
         for (int s = 0; s < SK; ++s) {
             mbar_init(b_kfull(s), 1);
@@ -250,9 +263,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(b_sfull(x), 1);
-            mbar_init(b_pfull(x), 128);
+            mbar_init(b_pfull(x), 128 * SPLIT);
             mbar_init(b_odone(x), 1);
         }
+        for (int i = 0; i < 8; ++i) mbar_init(b_xchg(i), 64);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -530,27 +544,61 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Block X = warp / 4; warp w owns TMEM lanes / query rows
-        // 32*(w%4) .. +31 of the block, one thread per row.  Per tile the
-        // thread walks its row's BN scores in 32-column chunks, loading the
-        // next chunk while it works on this one.  The running max m only
-        // rises when a chunk exceeds it by more than 8 (a factor 2^8): then
-        // the row sum, the P chunks already written for this tile and (once
-        // per tile) O are rescaled -- rare after the first chunk of an item.
-        const int X = warp >> 2;
-        const int r = 32 * (warp & 3) + lane;  // query row inside the tile
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        const uint32_t s_col = X * BN, o_col = O_COL + X * kPfDV;
+        // Warp w (0..15): block X = (w / 4) % 2, column half hh = w / 8, TMEM
+        // lane quarter w % 4, so each query row of a block is served by two
+        // threads (warps w and w + 8), each owning HC = BN / 2 of the tile's
+        // columns.  Per tile a thread takes the max over its columns, trades
+        // it with its partner (a 64-thread mbarrier per row quarter), and
+        // both continue with the same running max m: it only rises when the
+        // tile max exceeds it by more than 8 (a factor 2^8), and then the
+        // row sum and O (each thread its half of O's columns) are rescaled.
+        // P, 16-bit pairs, overwrites the first half of each consumed 32-column
+        // chunk of S.  The partners' row sums are added at the end of the item.
+        constexpr int HC = BN / SPLIT;  // columns per thread
+        constexpr int NCH = HC / 32; // 32-column chunks per thread
+        const int X = (warp >> 2) & 1;
+        const int hh = warp >> 3;
+        const int qd = warp & 3;
+        const int r = 32 * qd + lane;  // query row inside the tile
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+        const uint32_t s_addr = t_lane + X * BN + hh * HC;
+        const uint32_t o_addr = t_lane + O_COL + X * kPfDV + hh * (kPfDV / SPLIT);
+        const uint32_t b_pair = b_xchg(X * 4 + qd);
         const float sc = p.scale_log2;
-        const bool pos_scale = sc > 0.f;        // max on raw scores, one FFMA scales and shifts
+        const bool pos_scale = sc > 0.f;  // max on raw scores, one FFMA scales and shifts
         const float k_mul = pos_scale ? sc : 1.f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
         };
+        int ex = 0;  // exchanges with the partner thread so far (buffer and phase)
+        auto exchange = [&](float v, float &other) -> bool {
+            xbuf[ex & 1][X][hh][r] = v;
+            mbar_arrive(b_pair);
+            const bool done = wait_warp(b_pair, ex & 1);
+            other = *reinterpret_cast<volatile float *>(&xbuf[ex & 1][X][hh ^ 1][r]);
+            ++ex;
+            return done;
+        };
+        // scores of chunk i of this thread's columns at tile offset j0:
+        // scaled if the scale is not positive, masked past the row's last key
+        auto load_chunk = [&](int i, int j0, bool warp_full, int lim, uint32_t(&ra)[32]) {
+            tmem_ld32(s_addr + 32 * i, ra);
+            tmem_wait_ld_regs(ra);
+            if (!pos_scale) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) ra[c] = __float_as_uint(__uint_as_float(ra[c]) * sc);
+            }
+            if (!warp_full) {
+                const int lr = lim - (j0 + hh * HC + 32 * i);  // last visible column of the chunk
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (c > lr) ra[c] = __float_as_uint(-INFINITY);
+            }
+        };
         bool ok = true;
-        int t_base = 0;   // K/V tiles of earlier items
-        int tx_base = 0;  // tiles of this block in earlier items
-        int nx_items = 0; // items with tiles processed by this block
+        int t_base = 0;    // K/V tiles of earlier items
+        int tx_base = 0;   // tiles of this block in earlier items
+        int nx_items = 0;  // items with tiles processed by this block
         for (int k = 0; ok; ++k) {
             const int4 itm = take_item(k, ok);  // every thread reads the same slot
             ok = __all_sync(0xffffffffu, ok);
@@ -573,77 +621,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (!wait_warp(b_sfull(X), tx & 1)) { ok = false; break; }
                 tc_fence_after();
                 const bool warp_full = __all_sync(0xffffffffu, j0 + BN - 1 <= lim);
-                const uint32_t s_addr = t_lane + s_col;
-                uint32_t ra[32], rb[32];
-                tmem_ld32(s_addr, ra);
-                tmem_wait_ld_regs(ra);
-                float2 l2 = make_float2(0.f, 0.f);
-                float acc_alpha = 1.f;
+                uint32_t ra[32];
+                float mh = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    uint32_t(&cur)[32] = (i & 1) ? rb : ra;
-                    uint32_t(&nxt)[32] = (i & 1) ? ra : rb;
-                    if (i + 1 < NC) tmem_ld32(s_addr + 32 * (i + 1), nxt);
-                    float v[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(cur[c]);
-                    if (!pos_scale) {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) v[c] *= sc;
-                    }
-                    if (!warp_full) {
-                        const int lr = lim - (j0 + 32 * i);  // last visible column of this chunk
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (c > lr) v[c] = -INFINITY;
-                    }
+                for (int i = 0; i < NCH; ++i) {
+                    load_chunk(i, j0, warp_full, lim, ra);
                     float m3[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const float a = fmax3(v[8 * q], v[8 * q + 1], v[8 * q + 2]);
-                        const float b = fmax3(v[8 * q + 3], v[8 * q + 4], v[8 * q + 5]);
-                        m3[q] = fmax3(a, b, fmaxf(v[8 * q + 6], v[8 * q + 7]));
+                        const float a = fmax3(__uint_as_float(ra[8 * q]), __uint_as_float(ra[8 * q + 1]),
+                                              __uint_as_float(ra[8 * q + 2]));
+                        const float b = fmax3(__uint_as_float(ra[8 * q + 3]), __uint_as_float(ra[8 * q + 4]),
+                                              __uint_as_float(ra[8 * q + 5]));
+                        m3[q] = fmax3(a, b, fmaxf(__uint_as_float(ra[8 * q + 6]), __uint_as_float(ra[8 * q + 7])));
                     }
-                    float mc = fmaxf(fmax3(m3[0], m3[1], m3[2]), m3[3]);
-                    if (pos_scale) mc *= sc;
-                    const bool up = mc > m_used + 8.f;
-                    if (__any_sync(0xffffffffu, up)) {  // rare: raise the running max
-                        const float alpha = up ? fast_exp2(m_used - mc) : 1.f;
-                        if (up) m_used = mc;
-                        l *= alpha;
-                        l2.x *= alpha;
-                        l2.y *= alpha;
-                        acc_alpha *= alpha;
-                        if (i > 0) {  // P chunks of this tile already written
-                            tmem_wait_st();
+                    mh = fmax3(mh, fmax3(m3[0], m3[1], m3[2]), m3[3]);
+                }
+                if (pos_scale) mh *= sc;
+                float mo = -INFINITY;
+                if (SPLIT == 2 && !exchange(mh, mo)) { ok = false; break; }
+                const float mt = fmaxf(mh, mo);  // the tile's row max (scaled)
+                float alpha = 1.f;
+                if (mt > m_used + 8.f) {  // raise the running max (first tile: from -inf)
+                    alpha = fast_exp2(m_used - mt);
+                    m_used = mt;
+                    l *= alpha;
+                }
+                const float base = m_used == -INFINITY ? 0.f : m_used;
+                const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
+                float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
-                            for (int i2 = 0; i2 < i; ++i2) {
-                                uint32_t pw[16];
-                                tmem_ld16(s_addr + 32 * i2, pw);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    const float2 f = unpack2<T>(pw[e]);
-                                    pw[e] = pack2<T>(f.x * alpha, f.y * alpha);
-                                }
-                                tmem_st16(s_addr + 32 * i2, pw);
-                            }
-                        }
-                    }
-                    const float base = m_used == -INFINITY ? 0.f : m_used;
-                    const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
+                for (int i = 0; i < NCH; ++i) {
+                    load_chunk(i, j0, warp_full, lim, ra);
                     uint32_t pw[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float2 x = __ffma2_rn(make_float2(v[2 * e], v[2 * e + 1]), kk2, nb2);
+                        const float2 x =
+                            __ffma2_rn(make_float2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), kk2, nb2);
                         const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                        l2 = __fadd2_rn(l2, make_float2(p0, p1));
+                        if (e & 1)
+                            lb = __fadd2_rn(lb, make_float2(p0, p1));
+                        else
+                            la = __fadd2_rn(la, make_float2(p0, p1));
                         pw[e] = pack2<T>(p0, p1);  // P column: keys 2e, 2e+1 of the chunk
                     }
                     tmem_st16(s_addr + 32 * i, pw);
-                    if (i + 1 < NC) tmem_wait_ld_regs(nxt);
                 }
-                l += l2.x + l2.y;
+                l += (la.x + la.y) + (lb.x + lb.y);
                 // rows of V past the sequence end may hold anything (even NaN):
                 // block A zeroes them before its PV (block B's PV comes later in
                 // issue order), so that P = 0 there cannot produce 0 * NaN
@@ -652,25 +676,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!wait_warp(b_vfull(sv), uv & 1)) { ok = false; break; }
                     const int zs = max(it.kvb - j0, 0);
                     uint8_t *vbase = v_gen + sv * VB;
-                    for (int q = r; q < (BN - zs) * 16; q += 128) {
+                    for (int q = hh * 128 + r; q < (BN - zs) * 16; q += 128 * SPLIT) {
                         const int row = zs + (q >> 4), chunk = q & 15;
                         *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                 }
-                // O_X *= alpha when the running max moved; PV_X(t-1) is complete
-                // (S_X(t) is), and at the item's first tile O is about to be
-                // overwritten anyway
-                if (j > 0 && __any_sync(0xffffffffu, acc_alpha != 1.f)) {
+                // O_X *= alpha (this thread's half of the columns) when the
+                // running max moved; PV_X(t-1) is complete (S_X(t) is), and at
+                // the item's first tile O is about to be overwritten anyway
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < kPfDV / 32; ++c) {
+                    for (int c = 0; c < kPfDV / 32 / SPLIT; ++c) {
                         uint32_t ro[32];
-                        tmem_ld32(t_lane + o_col + c * 32, ro);
+                        tmem_ld32(o_addr + c * 32, ro);
                         tmem_wait_ld_regs(ro);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * acc_alpha);
-                        tmem_st32(t_lane + o_col + c * 32, ro);
+                        for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+                        tmem_st32(o_addr + c * 32, ro);
                     }
                 }
                 tmem_wait_st();
@@ -678,21 +702,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 mbar_arrive(b_pfull(X));
             }
             if (!ok) break;
-            // epilogue: after the block's last PV of the item, normalise O and
-            // write it with the LSE
+            // epilogue: after the block's last PV of the item, add the
+            // partners' row sums, normalise this thread's half of O and write
+            // it; the column-half-0 thread writes the LSE
             const bool have = n > 0;
             if (have && !wait_warp(b_odone(X), nx_items & 1)) { ok = false; break; }
+            float lo = 0.f;
+            if (SPLIT == 2 && !exchange(l, lo)) { ok = false; break; }
+            const float lt = l + lo;
             tc_fence_after();
             const int qi = it.i0 + r;
             const int64_t grow = static_cast<int64_t>(it.row_base) + r;
             const bool valid = qi < it.qb && grow < p.total_q;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + hh * (kPfDV / SPLIT);
 #pragma unroll
-            for (int c = 0; c < kPfDV / 32; ++c) {
+            for (int c = 0; c < kPfDV / 32 / SPLIT; ++c) {
                 uint32_t ro[32];
                 if (have) {
-                    tmem_ld32(t_lane + o_col + c * 32, ro);
+                    tmem_ld32(o_addr + c * 32, ro);
                     tmem_wait_ld_regs(ro);
                 } else {
 #pragma unroll
@@ -708,7 +736,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
                 }
             }
-            if (valid) p.lse[grow * p.Hqo + h] = l > 0.f ? (m_used + fast_log2(l)) * kLn2 : -INFINITY;
+            if (valid && hh == 0) p.lse[grow * p.Hqo + h] = lt > 0.f ? (m_used + fast_log2(lt)) * kLn2 : -INFINITY;
             tc_fence_before();  // O read before the next item's first PV_X overwrites it
             t_base += n;
             tx_base += n;
@@ -728,7 +756,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 template <int DQK>
 static size_t prefill_smem_bytes() {
     constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
-    return 1024 + 2 * kPfRows * DQK * 2 + SK * BN * DQK * 2 + SV * BN * kPfDV * 2 + 8 * (12 + 2 * SK + 2 * SV);
+    return 1024 + 2 * kPfRows * DQK * 2 + SK * BN * DQK * 2 + SV * BN * kPfDV * 2 + 8 * (20 + 2 * SK + 2 * SV);
 }
 
 template <typename T, int DQK, int LAYOUT>
@@ -739,7 +767,7 @@ static int launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
-    kern<<<grid, kPfThreads, smem, st>>>(tq, tk, tv, p);
+    kern<<<grid, PfRoles<DQK>::kThreads, smem, st>>>(tq, tk, tv, p);
     return PKV_OK;
 }
 
