@@ -150,15 +150,21 @@ class ClockSampler:
 # ---- distributed plumbing -----------------------------------------------------------------------
 
 def dist_setup(n_gpus: int):
+    """Rank, world size and local rank from the launcher's environment; for
+    more than one rank, a process group (NCCL with GPUs, else gloo) whose
+    collectives fail after PKV_DIST_TIMEOUT_S seconds (default 600) instead of
+    waiting for a rank that died."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
+        import datetime
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         if torch.cuda.is_available():
             torch.cuda.set_device(local)
-        dist.init_process_group(backend)
+        timeout = datetime.timedelta(seconds=float(os.environ.get("PKV_DIST_TIMEOUT_S", "600")))
+        dist.init_process_group(backend, timeout=timeout)
     return ws, rank, local
 
 
@@ -195,11 +201,36 @@ class Part:
         self.ms = []
 
 
+def rank_seed(rank: int) -> int:
+    """Seed offset of a rank's workloads: every rank draws its own requests
+    of the same shape (weak scaling, no shared data)."""
+    return 1000 * rank
+
+
+def aggregate_parts(stats, ws: int, dev, pk_peaks) -> dict:
+    """Whole-job result per part from each rank's (name, mean ms, work,
+    unit): work summed over ranks, divided by the slowest rank's time;
+    roofline_frac is per GPU."""
+    out = {}
+    for name, mean_ms, work, unit in stats:
+        mean_ms = allreduce_max(mean_ms, ws, dev)
+        work = allreduce_sum(float(work), ws, dev)
+        if unit == "GB/s":
+            val = work / (mean_ms * 1e-3) / 1e9
+            peak = pk_peaks["hbm_gbs"]
+        else:
+            val = work / (mean_ms * 1e-3) / 1e12
+            peak = pk_peaks["bf16_tflops"]
+        out[name] = {"value": round(val, 2), "unit": unit, "ms": round(mean_ms, 4),
+                     "work": int(work), "roofline_frac": round(val / peak / ws, 4)}
+    return out
+
+
 def make_parts(rank: int, dev):
     import paged_kv_cache_316_gb300 as pk
     from paged_kv_cache_316_gb300 import workloads as wl
     parts = []
-    seed_off = 1000 * rank
+    seed_off = rank_seed(rank)
 
     # index helpers + append
     ap = wl.append_sweep(4096, seed=1 + seed_off, layout=wl.NHD, device=dev, fill="empty")
@@ -394,18 +425,8 @@ def run_ours(args):
     total_ms = allreduce_max(total_ms, ws, dev)
 
     pk_peaks, peak_src = peaks()
-    out_parts = {}
-    for p in parts:
-        mean_ms = allreduce_max(sum(p.ms) / len(p.ms), ws, dev)
-        work = allreduce_sum(float(p.work), ws, dev)
-        if p.unit == "GB/s":
-            val = work / (mean_ms * 1e-3) / 1e9
-            peak = pk_peaks["hbm_gbs"]
-        else:
-            val = work / (mean_ms * 1e-3) / 1e12
-            peak = pk_peaks["bf16_tflops"]
-        out_parts[p.name] = {"value": round(val, 2), "unit": p.unit, "ms": round(mean_ms, 4),
-                             "work": int(work), "roofline_frac": round(val / peak / ws, 4)}
+    out_parts = aggregate_parts([(p.name, sum(p.ms) / len(p.ms), p.work, p.unit) for p in parts],
+                                ws, dev, pk_peaks)
     step_ms = total_ms / args.steps
     dom = max(parts, key=lambda p: sum(p.ms))
     d = out_parts[dom.name]
