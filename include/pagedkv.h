@@ -126,8 +126,10 @@ int paged_batch_indices_positions(const int32_t *append_indptr,
  *   kv_last_page_len [batch_size]: int32.
  * Device errors: b outside [0, batch_size) -> PKV_DEV_ERR_BATCH; p outside
  * [0, seq_len(b)) -> PKV_DEV_ERR_POS; page outside [0, max_num_pages) ->
- * PKV_DEV_ERR_PAGE; the entry is skipped.  Duplicate (b, p) pairs race.
- * Host errors: head_dim % 8 != 0 or page_size <= 0 -> PKV_ERR_INVALID_ARG.
+ * PKV_DEV_ERR_PAGE; the entry is skipped.  A copy that does not complete
+ * within 1 s -> PKV_DEV_ERR_TIMEOUT.  Duplicate (b, p) pairs race.
+ * Host errors: head_dim % 8 != 0 or page_size <= 0 -> PKV_ERR_INVALID_ARG;
+ * head_dim > 4096 -> PKV_ERR_UNSUPPORTED.
  */
 int paged_append(const void *append_key, const void *append_value, int64_t nnz,
                  const int32_t *batch_indices, const int32_t *positions,

@@ -6,6 +6,7 @@
 // (get_seq_lens, get_batch_indices_positions) and its note that the page
 // table already covers the appended tokens.
 #include "pkv_common.cuh"
+#include "sm103_ptx.cuh"
 
 namespace pkv {
 
@@ -44,8 +45,8 @@ __global__ void batch_pos_kernel(const int32_t *__restrict__ indptr,
 }
 
 struct AppendParams {
-    const uint4 *key;    // [nnz, H, D] 16-bit elements, viewed as 16-byte chunks
-    const uint4 *value;
+    const uint8_t *key;    // [nnz, H, D] 16-bit elements
+    const uint8_t *value;
     int64_t nnz;
     const int32_t *batch_indices;
     const int32_t *positions;
@@ -57,72 +58,162 @@ struct AppendParams {
     const int32_t *kv_indptr;
     const int32_t *kv_last_page_len;
     int B, H, D, page_size;
-    int chunks_per_row;  // H * D / 8 (16-byte chunks in one token's K row)
-    int tokens_per_cta;
+    int heads_per_piece;   // whole heads per copied piece (piece <= kApSlotBytes)
+    int pieces_per_row;    // ceil(H / heads_per_piece)
+    int64_t tokens_per_cta;
     int32_t *err;
 };
 
-constexpr int kAppendThreads = 256;
-constexpr int kAppendUnroll = 4;
+constexpr int kApSlots = 6;            // shared-memory ring of one CTA
+constexpr int kApSlotBytes = 8192;     // largest piece of a token row
+constexpr int kApCtasPerSm = 4;
 
-// Each CTA copies `tokens_per_cta` whole tokens (K row then V row, H*D
-// elements each) as 16-byte chunks: every thread first issues up to
-// kAppendUnroll streaming loads, then the matching stores, so a warp keeps
-// 2 KB in flight per round.  Source reads are contiguous; destination rows
-// are contiguous H*D runs (NHD) or D-element runs page_size*D apart (HND).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
+// Destination of one token: element offset of head 0 of its K (and V) row in
+// the pool, or -1 when its request, position or page is out of range (the
+// matching bit goes to the error word and the token is skipped).
 template <int LAYOUT>
-__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendParams p) {
-    const int two_ch = 2 * p.chunks_per_row;
-    const int per_cta = p.tokens_per_cta * two_ch;
-    const int dchunks = p.D >> 3;
-    const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * p.tokens_per_cta;
-    for (int base = 0; base < per_cta; base += kAppendThreads * kAppendUnroll) {
-        uint4 val[kAppendUnroll];
-        uint4 *dst[kAppendUnroll];
-#pragma unroll
-        for (int u = 0; u < kAppendUnroll; ++u) {
-            dst[u] = nullptr;
-            int li = base + u * kAppendThreads + threadIdx.x;
-            if (li >= per_cta) continue;
-            int tl = li / two_ch;
-            int rem = li - tl * two_ch;
-            int64_t tok = tok0 + tl;
-            if (tok >= p.nnz) continue;
-            bool is_v = rem >= p.chunks_per_row;
-            int c = is_v ? rem - p.chunks_per_row : rem;
-            bool leader = rem == 0;
-            int b = p.batch_indices[tok];
-            if (b < 0 || b >= p.B) {
-                if (leader) set_err(p.err, PKV_DEV_ERR_BATCH);
-                continue;
-            }
-            int first = p.kv_indptr[b];
-            int pages = p.kv_indptr[b + 1] - first;
-            int len = pages > 0 ? (pages - 1) * p.page_size + p.kv_last_page_len[b] : 0;
-            int pos = p.positions[tok];
-            if (pos < 0 || pos >= len) {
-                if (leader) set_err(p.err, PKV_DEV_ERR_POS);
-                continue;
-            }
-            int64_t page = p.kv_indices[first + pos / p.page_size];
-            if (page < 0 || page >= p.max_num_pages) {
-                if (leader) set_err(p.err, PKV_DEV_ERR_PAGE);
-                continue;
-            }
-            int slot = pos % p.page_size;
-            int h = c / dchunks;
-            int dc = c - h * dchunks;
-            const uint4 *src = (is_v ? p.value : p.key) + tok * p.chunks_per_row + c;
-            val[u] = __ldcs(src);
-            uint16_t *cache = is_v ? p.v_cache : p.k_cache;
-            int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, h, slot, p.H, p.page_size, p.D) +
-                          static_cast<int64_t>(dc) * 8;
-            dst[u] = reinterpret_cast<uint4 *>(cache + off);
-        }
-#pragma unroll
-        for (int u = 0; u < kAppendUnroll; ++u)
-            if (dst[u]) __stcs(dst[u], val[u]);
+__device__ __forceinline__ int64_t append_dst(const AppendParams &p, int64_t tok) {
+    if (tok >= p.nnz) return -1;
+    const int b = p.batch_indices[tok];
+    if (b < 0 || b >= p.B) {
+        set_err(p.err, PKV_DEV_ERR_BATCH);
+        return -1;
     }
+    const int first = p.kv_indptr[b];
+    const int pages = p.kv_indptr[b + 1] - first;
+    const int len = pages > 0 ? (pages - 1) * p.page_size + p.kv_last_page_len[b] : 0;
+    const int pos = p.positions[tok];
+    if (pos < 0 || pos >= len) {
+        set_err(p.err, PKV_DEV_ERR_POS);
+        return -1;
+    }
+    const int64_t page = p.kv_indices[first + pos / p.page_size];
+    if (page < 0 || page >= p.max_num_pages) {
+        set_err(p.err, PKV_DEV_ERR_PAGE);
+        return -1;
+    }
+    return kv_row_offset<LAYOUT>(page, p.page_stride, 0, pos % p.page_size, p.H, p.page_size, p.D);
+}
+
+// One warp per CTA copies a contiguous run of tokens with the bulk-copy
+// engine: every token row (K, then V; H*D 16-bit elements) is cut into
+// pieces of whole heads of at most kApSlotBytes, each loaded from the new
+// tokens into a slot of a shared-memory ring and stored from there into its
+// page (one store for NHD, where a token's heads are contiguous; one per
+// head for HND).  Loads run kApSlots-1 pieces ahead of the stores; a slot is
+// reloaded once the store that read it has finished reading.  The lanes
+// resolve the destinations of 32 tokens at a time (lane i: token i), two
+// groups ahead of need; lane 0 issues every copy.
+template <int LAYOUT>
+__global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t full[kApSlots];
+    const int lane = threadIdx.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * p.tokens_per_cta;
+    const int64_t t1 = min(p.nnz, t0 + p.tokens_per_cta);
+    if (t0 >= t1) return;
+    if (lane == 0) {
+        for (int s = 0; s < kApSlots; ++s) mbar_init(smem_u32(&full[s]), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint32_t ring_s = smem_u32(ring);
+    const int npr = p.pieces_per_row;
+    const int64_t per_tok = 2 * npr;
+    const int64_t total = (t1 - t0) * per_tok;
+    const int64_t row_elems = static_cast<int64_t>(p.H) * p.D;
+    // destinations of tokens gA .. gA+31 (lane i: gA + i) and of the next 32
+    int64_t gA = t0;
+    int64_t dA = append_dst<LAYOUT>(p, gA + lane);
+    int64_t dB = append_dst<LAYOUT>(p, gA + 32 + lane);
+    auto dst_of = [&](int64_t tok) -> int64_t {  // warp-uniform tok
+        const int64_t i = tok - gA;
+        const int64_t a = __shfl_sync(0xffffffffu, dA, static_cast<int>(i & 31));
+        const int64_t b = __shfl_sync(0xffffffffu, dB, static_cast<int>(i & 31));
+        return i < 32 ? a : b;
+    };
+    // piece j: token, row (0 = K, 1 = V), first head and head count
+    auto piece = [&](int64_t j, int64_t &tok, int &row, int &h0, int &nh) {
+        tok = t0 + j / per_tok;
+        const int r = static_cast<int>(j % per_tok);
+        row = r / npr;
+        h0 = (r % npr) * p.heads_per_piece;
+        nh = min(p.heads_per_piece, p.H - h0);
+    };
+    auto issue_load = [&](int64_t j) {
+        int64_t tok;
+        int row, h0, nh;
+        piece(j, tok, row, h0, nh);
+        const int64_t dst = dst_of(tok);
+        const int s = static_cast<int>(j % kApSlots);
+        const uint32_t bar = smem_u32(&full[s]);
+        if (lane == 0) {
+            if (dst >= 0) {
+                const uint32_t bytes = static_cast<uint32_t>(nh) * p.D * 2;
+                mbar_expect_tx(bar, bytes);
+                const uint8_t *src = (row ? p.value : p.key) + (tok * row_elems + static_cast<int64_t>(h0) * p.D) * 2;
+                bulk_load(ring_s + s * kApSlotBytes, src, bytes, bar);
+            } else {
+                mbar_arrive(bar);  // nothing to copy: complete the phase
+            }
+        }
+    };
+    bool ok = true;
+    volatile int no_abort = 0;
+    int64_t jl = 0;
+    for (; jl < total && jl < kApSlots - 1; ++jl) issue_load(jl);
+    for (int64_t js = 0; js < total; ++js) {
+        int64_t tok;
+        int row, h0, nh;
+        piece(js, tok, row, h0, nh);
+        if (tok - gA >= 32) {  // the store side left group A: shift, resolve the next group
+            gA += 32;
+            dA = dB;
+            dB = append_dst<LAYOUT>(p, gA + 32 + lane);
+        }
+        const int64_t dst = dst_of(tok);
+        const int s = static_cast<int>(js % kApSlots);
+        if (lane == 0) {
+            if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((js / kApSlots) & 1), &no_abort)) {
+                set_err(p.err, PKV_DEV_ERR_TIMEOUT);
+                ok = false;
+            } else if (dst >= 0) {
+                uint16_t *cache = row ? p.v_cache : p.k_cache;
+                const uint32_t src = ring_s + s * kApSlotBytes;
+                const uint32_t hb = static_cast<uint32_t>(p.D) * 2;
+                if (LAYOUT == PKV_NHD) {
+                    bulk_store(cache + dst + static_cast<int64_t>(h0) * p.D, src, nh * hb);
+                } else {
+                    for (int h = 0; h < nh; ++h)
+                        bulk_store(cache + dst + static_cast<int64_t>(h0 + h) * p.page_size * p.D, src + h * hb, hb);
+                }
+            }
+            bulk_commit();
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (jl < total) {
+            if (lane == 0) bulk_wait_read1();  // the store that last read slot jl % kApSlots is done reading
+            issue_load(jl);
+            ++jl;
+        }
+    }
+    if (lane == 0) bulk_wait_all();
 }
 
 }  // namespace pkv
@@ -173,6 +264,7 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
         max_num_pages < 0 || page_stride <= 0)
         return PKV_ERR_INVALID_ARG;
     if (head_dim % 8) return PKV_ERR_INVALID_ARG;
+    if (head_dim * 2 > kApSlotBytes) return PKV_ERR_UNSUPPORTED;  // one head must fit a ring slot
     if (page_stride < static_cast<int64_t>(num_kv_heads) * page_size * head_dim)
         return PKV_ERR_INVALID_ARG;
     if (nnz == 0) return PKV_OK;
@@ -184,8 +276,8 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
         return PKV_ERR_INVALID_ARG;
 
     AppendParams p;
-    p.key = static_cast<const uint4 *>(append_key);
-    p.value = static_cast<const uint4 *>(append_value);
+    p.key = static_cast<const uint8_t *>(append_key);
+    p.value = static_cast<const uint8_t *>(append_value);
     p.nnz = nnz;
     p.batch_indices = batch_indices;
     p.positions = positions;
@@ -200,17 +292,20 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
     p.H = num_kv_heads;
     p.D = head_dim;
     p.page_size = page_size;
-    p.chunks_per_row = num_kv_heads * head_dim / 8;
+    p.heads_per_piece = head_dim * 2 >= kApSlotBytes ? 1 : min(num_kv_heads, kApSlotBytes / (head_dim * 2));
+    p.pieces_per_row = (num_kv_heads + p.heads_per_piece - 1) / p.heads_per_piece;
     p.err = err_word;
-    int target = kAppendThreads * kAppendUnroll;
-    p.tokens_per_cta = 2 * p.chunks_per_row >= target ? 1 : target / (2 * p.chunks_per_row);
-    int64_t blocks = (nnz + p.tokens_per_cta - 1) / p.tokens_per_cta;
-    if (blocks > 0x7fffffff) return PKV_ERR_INVALID_ARG;
+    const int64_t ctas_max = static_cast<int64_t>(num_sms()) * kApCtasPerSm;
+    p.tokens_per_cta = (nnz + ctas_max - 1) / ctas_max;
+    const int64_t blocks = (nnz + p.tokens_per_cta - 1) / p.tokens_per_cta;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (layout == PKV_HND)
-        append_kernel<PKV_HND><<<static_cast<unsigned>(blocks), kAppendThreads, 0, st>>>(p);
-    else
-        append_kernel<PKV_NHD><<<static_cast<unsigned>(blocks), kAppendThreads, 0, st>>>(p);
+    const size_t smem = static_cast<size_t>(kApSlots) * kApSlotBytes;
+    // the ring plus the static barriers exceed the default 48 KB per block
+    auto kern = layout == PKV_HND ? append_kernel<PKV_HND> : append_kernel<PKV_NHD>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
+    kern<<<static_cast<unsigned>(blocks), 32, smem, st>>>(p);
     note_launches(1);
     return launch_status();
 }
