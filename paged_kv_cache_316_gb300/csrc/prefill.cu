@@ -54,7 +54,7 @@ struct PfCfg<128> {
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int BN = 64, SK = 3, SV = 3, SPLIT = 1;
+    static constexpr int BN = 96, SK = 2, SV = 2, SPLIT = 2;
 };
 template <int DQK>
 struct PfRoles {
@@ -63,6 +63,12 @@ struct PfRoles {
     static constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 };
 static int pf_bn(int d_qk) { return d_qk == 128 ? PfCfg<128>::BN : PfCfg<192>::BN; }
+// Rows per TMA box: pages, or parts of pages of the largest power of two
+// dividing BN, so that no box crosses a page and the boxes tile a key tile.
+__host__ __device__ __forceinline__ int pf_box_rows(int page_size, int bn) {
+    const int p2 = bn & -bn;
+    return page_size < p2 ? page_size : p2;
+}
 
 struct PrefillParams {
     int64_t max_num_pages;
@@ -162,6 +168,15 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_wait_ld_regs16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // One work item: query tile x (counted from the LAST tile of the request, the
 // one that sees the most keys) of request b for qo heads hA and hB (hB < 0:
 // block B absent).  Items are numbered request by request (so that the CTAs
@@ -201,11 +216,13 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
     constexpr int NI = 2;                        // slots of the work-item ring
-    // TMEM columns: S of block X at X * BN (P of chunk i, 16 columns of
-    // 16-bit pairs, overwrites the chunk's first 16 S columns), O of block X
-    // at O_COL + X * 128
+    // TMEM columns (every region starts at a multiple of 128): S of block X
+    // at X * S_STRIDE (BN columns; P of a chunk, 16-bit pairs,
+    // overwrites the chunk's first columns), O of block X at O_COL + X * 128
     constexpr uint32_t TMEM_COLS = 512;
-    constexpr uint32_t O_COL = 2 * BN;
+    constexpr uint32_t S_STRIDE = 128;
+    constexpr uint32_t O_COL = 2 * S_STRIDE;
+    static_assert(BN <= S_STRIDE, "score tile wider than its TMEM region");
     static_assert(O_COL + 2 * kPfDV <= TMEM_COLS, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
@@ -322,7 +339,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             }
         }
         const int S = 1 << p.page_shift;
-        const int RB = S < BN ? S : BN;  // rows per TMA box
+        const int RB = pf_box_rows(S, BN);  // rows per TMA box
         const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
         const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
         const int NS = is_k ? SK : SV;
@@ -478,16 +495,24 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 const uint64_t qd = qdesc0 + ((x * QB) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk)
-                    umma_ss(tmem + x * BN, qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
+                    umma_ss(tmem + x * S_STRIDE, qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
                             kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
                 umma_commit(b_sfull(x));
+            };
+            // P column of keys 16kk .. 16kk+15: each softmax thread owns HC
+            // columns, and writes chunk i (32 keys, or a final 16) as 16-bit
+            // pairs at the chunk's first column
+            constexpr int HC = BN / SPLIT;
+            auto pcol = [](int kk) {
+                const int k0 = 16 * kk, c = k0 % HC;
+                return (k0 / HC) * HC + 32 * (c / 32) + (c % 32) / 2;
             };
             auto pv = [&](int x, int t, bool first) {  // O_X (+)= P_X V(t)
                 const uint64_t vd = vdesc0 + (((t % SV) * VB) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(tmem + O_COL + x * kPfDV, tmem + x * BN + 32 * (kk >> 1) + 8 * (kk & 1),
-                            vd + ((kk * 16 * 128) >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                    umma_ts(tmem + O_COL + x * kPfDV, tmem + x * S_STRIDE + pcol(kk), vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                            (!first || kk > 0) ? 1u : 0u);
             };
             for (int k = 0; ok; ++k) {
                 const int4 itm = take_item(k, ok);
@@ -555,13 +580,15 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         // P, 16-bit pairs, overwrites the first half of each consumed 32-column
         // chunk of S.  The partners' row sums are added at the end of the item.
         constexpr int HC = BN / SPLIT;  // columns per thread
-        constexpr int NCH = HC / 32; // 32-column chunks per thread
+        constexpr int NCH = HC / 32;         // full 32-column chunks per thread
+        constexpr bool TAIL = HC % 32 != 0;  // and a final 16-column chunk
+        static_assert(HC % 16 == 0, "columns per thread");
         const int X = (warp >> 2) & 1;
         const int hh = warp >> 3;
         const int qd = warp & 3;
         const int r = 32 * qd + lane;  // query row inside the tile
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-        const uint32_t s_addr = t_lane + X * BN + hh * HC;
+        const uint32_t s_addr = t_lane + X * S_STRIDE + hh * HC;
         const uint32_t o_addr = t_lane + O_COL + X * kPfDV + hh * (kPfDV / SPLIT);
         const uint32_t b_pair = b_xchg(X * 4 + qd);
         const float sc = p.scale_log2;
@@ -593,6 +620,21 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
                     if (c > lr) ra[c] = __float_as_uint(-INFINITY);
+            }
+        };
+        // the same for the final 16-column chunk (columns 32*NCH .. HC-1)
+        auto load_tail = [&](int j0, bool warp_full, int lim, uint32_t(&rt)[16]) {
+            tmem_ld16(s_addr + 32 * NCH, rt);
+            tmem_wait_ld_regs16(rt);
+            if (!pos_scale) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) rt[c] = __float_as_uint(__uint_as_float(rt[c]) * sc);
+            }
+            if (!warp_full) {
+                const int lr = lim - (j0 + hh * HC + 32 * NCH);
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    if (c > lr) rt[c] = __float_as_uint(-INFINITY);
             }
         };
         bool ok = true;
@@ -637,6 +679,20 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     }
                     mh = fmax3(mh, fmax3(m3[0], m3[1], m3[2]), m3[3]);
                 }
+                if constexpr (TAIL) {
+                    uint32_t rt[16];
+                    load_tail(j0, warp_full, lim, rt);
+                    float m2[2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const float a = fmax3(__uint_as_float(rt[8 * q]), __uint_as_float(rt[8 * q + 1]),
+                                              __uint_as_float(rt[8 * q + 2]));
+                        const float b = fmax3(__uint_as_float(rt[8 * q + 3]), __uint_as_float(rt[8 * q + 4]),
+                                              __uint_as_float(rt[8 * q + 5]));
+                        m2[q] = fmax3(a, b, fmaxf(__uint_as_float(rt[8 * q + 6]), __uint_as_float(rt[8 * q + 7])));
+                    }
+                    mh = fmax3(mh, m2[0], m2[1]);
+                }
                 if (pos_scale) mh *= sc;
                 float mo = -INFINITY;
                 if (SPLIT == 2 && !exchange(mh, mo)) { ok = false; break; }
@@ -666,6 +722,23 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         pw[e] = pack2<T>(p0, p1);  // P column: keys 2e, 2e+1 of the chunk
                     }
                     tmem_st16(s_addr + 32 * i, pw);
+                }
+                if constexpr (TAIL) {
+                    uint32_t rt[16];
+                    load_tail(j0, warp_full, lim, rt);
+                    uint32_t pw[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 x =
+                            __ffma2_rn(make_float2(__uint_as_float(rt[2 * e]), __uint_as_float(rt[2 * e + 1])), kk2, nb2);
+                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                        if (e & 1)
+                            lb = __fadd2_rn(lb, make_float2(p0, p1));
+                        else
+                            la = __fadd2_rn(la, make_float2(p0, p1));
+                        pw[e] = pack2<T>(p0, p1);
+                    }
+                    tmem_st8(s_addr + 32 * NCH, pw);
                 }
                 l += (la.x + la.y) + (lb.x + lb.y);
                 // rows of V past the sequence end may hold anything (even NaN):
@@ -873,7 +946,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     const CUtensorMapDataType tdt =
         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int bn = pf_bn(d_qk);
-    const int rows = page_size < bn ? page_size : bn;
+    const int rows = pf_box_rows(page_size, bn);
     CUtensorMap tq, tk, tv;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),

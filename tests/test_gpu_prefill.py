@@ -32,6 +32,9 @@ CASES = [
     ([300, 50], [300, 333], 16, 8, 8, 128, False, wl.F16, wl.NHD, 3),
     ([64, 200], [500, 200], 64, 16, 2, 192, False, wl.BF16, wl.NHD, 4),
     ([513], [1100], 8, 4, 1, 128, True, wl.F16, wl.HND, 5),
+    ([77, 300], [500, 300], 16, 16, 4, 192, True, wl.BF16, wl.HND, 6),    # 96-key tiles, 16-slot pages
+    ([130, 45], [900, 45], 256, 8, 2, 192, True, wl.F16, wl.NHD, 7),     # tiles inside 256-slot pages
+    ([200], [333], 8, 6, 2, 192, False, wl.BF16, wl.HND, 8),             # odd group: block B absent
 ]
 
 
