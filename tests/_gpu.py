@@ -34,14 +34,16 @@ def assert_lse_close(got, ref, what="lse"):
     assert err.size == 0 or err.max() <= LSE_TOL, f"{what}: max err {err.max():.3e}"
 
 
-def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None):
+def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None, ws=None):
     pool = c.pool
     kv = pool.storage[0].to(DEV) if len(pool.storage) == 1 else tuple(t.to(DEV) for t in pool.storage)
     B = c.seq_lens.shape[0]
     ws_bytes = pk.paged_decode_workspace_size(B, c.q_len_per_req, c.num_qo_heads, c.num_kv_heads,
                                               c.head_dim, c.max_seq_len, pool.page_size,
                                               c.window_left)
-    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=DEV)
+    if ws is None:
+        ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=DEV)
+    assert ws.numel() >= ws_bytes
     lse = torch.empty((B * c.q_len_per_req, c.num_qo_heads), dtype=torch.float32,
                       device=DEV) if with_lse else None
     out = pk.paged_decode(c.query.to(DEV), kv, ws, c.block_tables.to(DEV), c.seq_lens.to(DEV),

@@ -115,6 +115,24 @@ def test_bad_page_flagged_and_treated_as_absent():
     assert_lse_close(lse, rl)
 
 
+def test_workspace_reused_across_sizes():
+    # one workspace serves calls of different sizes in turn, the split
+    # partials of a larger call staying behind
+    big = wl.decode_case([3000, 2500, 4100, 900, 5000, 1800], 16, 32, 8, 128, wl.HND, seed=11,
+                         window_left=-1, slack=0.2)
+    small = wl.decode_case([2100, 4000], 32, 64, 8, 128, wl.HND, seed=12, q_len_per_req=2,
+                           with_sinks=True, slack=0.2)
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    for c in (big, small, big, small):
+        _check(c, ws=ws)
+
+
+def test_hundreds_of_splits():
+    # one long request on one kv head: the keys are cut into ~780 splits
+    c = wl.decode_case([200000], 256, 64, 1, 128, wl.HND, seed=13, with_sinks=True)
+    _check(c)
+
+
 def test_without_lse_output():
     c = wl.decode_case([500, 20], 16, 32, 8, 128, wl.NHD, seed=10)
     out, _ = decode_on_gpu(c, with_lse=False)
