@@ -534,14 +534,19 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 for (int j = 0; j < n; ++j) {
                     const int t = t_base + j, tb = tb_base + j;
                     const bool more = j + 1 < n;
-                    // block A: PV_A(t), then QK_A(t+1)
-                    if (!mbar_wait(b_pfull(0), t & 1, abort_flag)) { ok = false; break; }
+                    // block A: PV_A(t), then QK_A(t+1).  V(t) and K(t+1) arrive
+                    // long before P_A(t): wait for them first, so that once P_A
+                    // is there the MMAs go out back to back
                     if (!mbar_wait(b_vfull(t % SV), (t / SV) & 1, abort_flag)) { ok = false; break; }
+                    if (more && !mbar_wait(b_kfull((t + 1) % SK), ((t + 1) / SK) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(b_pfull(0), t & 1, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     pv(0, t, j == 0);
                     if (!more) umma_commit(b_odone(0));
                     if (more) {
-                        if (!wait_k(t + 1)) { ok = false; break; }
                         qk(0, t + 1);
                         if (!hasB) {
                             umma_commit(b_kempty((t + 1) % SK));
@@ -601,7 +606,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         auto exchange = [&](float v, float &other) -> bool {
             xbuf[ex & 1][X][hh][r] = v;
             mbar_arrive(b_pair);
-            const bool done = wait_warp(b_pair, ex & 1);
+            // the partner arrives within a few hundred cycles: spin, no sleep
+            const bool done = __all_sync(0xffffffffu, mbar_wait_spin(b_pair, ex & 1, abort_flag));
             other = *reinterpret_cast<volatile float *>(&xbuf[ex & 1][X][hh ^ 1][r]);
             ++ex;
             return done;
