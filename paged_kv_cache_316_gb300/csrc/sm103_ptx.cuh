@@ -51,7 +51,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 // up (returns false) after about one second, or as soon as *abort is set by
 // another thread of the CTA that gave up first.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity);
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (mbar_test_wait(bar, parity)) return true;  // already complete: no potentially blocking poll
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
