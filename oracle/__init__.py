@@ -127,8 +127,10 @@ def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
            block_tables, seq_lens_, max_seq_len: int, bmm1_scale: float,
            bmm2_scale: float, window_left: int, sinks, q_len_per_req: int,
            num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
-           layout: int, dtype: int, threads: int | None = None):
-    """Returns (out [B*Q, Hqo, D] float64, lse [B*Q, Hqo] float64, err)."""
+           layout: int, dtype: int, threads: int | None = None, cum_seq_lens_q=None):
+    """Returns (out [rows, Hqo, D] float64, lse [rows, Hqo] float64, err) with
+    rows = B*Q, or cum_seq_lens_q[B] for variable-length queries (request b
+    then has rows cum[b] .. cum[b+1]-1 and q_len_per_req is unused)."""
     q = _u16(query)
     kc, vc = k_cache, v_cache
     _check_pool(kc, page_stride, max_num_pages)
@@ -136,7 +138,10 @@ def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
     bt = _i32(block_tables)
     sl = np.ascontiguousarray(np.asarray(seq_lens_), dtype=np.uint32)
     B = sl.shape[0]
-    rows = B * q_len_per_req
+    cq = None if cum_seq_lens_q is None else _i32(cum_seq_lens_q)
+    if cq is not None:
+        assert cq.shape == (B + 1,) and cq[0] == 0 and np.all(np.diff(cq) >= 0)
+    rows = B * q_len_per_req if cq is None else int(cq[-1])
     out = np.zeros((rows, num_qo_heads, head_dim), np.float64)
     lse = np.zeros((rows, num_qo_heads), np.float64)
     sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float32)
@@ -149,7 +154,7 @@ def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
         ctypes.c_int64(page_stride), ctypes.c_int64(max_num_pages), _p(bt),
         ctypes.c_int(bt.shape[1]), _p(sl), ctypes.c_int(B), ctypes.c_int(max_seq_len),
         ctypes.c_double(bmm1_scale), ctypes.c_double(bmm2_scale),
-        ctypes.c_int(window_left), _p(sk), ctypes.c_int(q_len_per_req),
+        ctypes.c_int(window_left), _p(sk), ctypes.c_int(q_len_per_req), _p(cq),
         ctypes.c_int(num_qo_heads), ctypes.c_int(num_kv_heads),
         ctypes.c_int(head_dim), ctypes.c_int(page_size), ctypes.c_int(layout),
         ctypes.c_int(dtype), _p(out), _p(lse), _p(scratch), ctypes.c_int(nthr),

@@ -238,12 +238,16 @@ static int orc_attend_row(const uint16_t *q, int dtype, const uint16_t *k_cache,
 /* For request b, query token t < Q and qo head h (query row b*Q + t):
  *   kv head    = h / (num_qo_heads / num_kv_heads)
  *   position   p = seq_lens[b] - Q + t   (the Q tokens are the last ones)
+ * With cum_seq_lens_q (the decode page's variable-length queries) request b
+ * has Q = cum_seq_lens_q[b+1] - cum_seq_lens_q[b] tokens at rows
+ * cum_seq_lens_q[b] + t, and q_len_per_req is unused.
  *   keys       max(0, p - window_left) <= j <= p  (window_left = -1: j >= 0)
  *   logits     s_j = bmm1_scale * <q, k_j>
  *   out        bmm2_scale * softmax-weighted sum of v_j, where the softmax
  *              denominator also holds e^{sinks[h]} when sinks != NULL
  *   lse        log of that denominator.
- * out: [B*Q, num_qo_heads, head_dim], lse: [B*Q, num_qo_heads] (may be NULL).
+ * out: [rows, num_qo_heads, head_dim], lse: [rows, num_qo_heads] (may be
+ * NULL), rows = B*Q or cum_seq_lens_q[B].
  * scratch: caller buffer of at least max_seq_len doubles per thread slot
  * (threads * max_seq_len when OpenMP is used; pass n_scratch_threads). */
 int orc_decode(const uint16_t *query, const uint16_t *k_cache,
@@ -252,14 +256,15 @@ int orc_decode(const uint16_t *query, const uint16_t *k_cache,
                int block_table_stride, const uint32_t *seq_lens, int B,
                int max_seq_len, double bmm1_scale, double bmm2_scale,
                int window_left, const float *sinks, int q_len_per_req,
-               int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
-               int layout, int dtype, double *out, double *lse, double *scratch,
+               const int32_t *cum_seq_lens_q, int num_qo_heads,
+               int num_kv_heads, int head_dim, int page_size, int layout,
+               int dtype, double *out, double *lse, double *scratch,
                int n_scratch_threads, int num_threads)
 {
     int err = 0;
-    int Q = q_len_per_req;
     int group = num_qo_heads / num_kv_heads;
-    int64_t rows = (int64_t)B * Q * num_qo_heads;
+    int64_t tokens = cum_seq_lens_q ? cum_seq_lens_q[B] : (int64_t)B * q_len_per_req;
+    int64_t rows = tokens * num_qo_heads;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err) num_threads(num_threads)
 #endif
@@ -272,8 +277,26 @@ int orc_decode(const uint16_t *query, const uint16_t *k_cache,
             tid = 0; /* never happens when the caller sizes scratch */
         double *s = scratch + (int64_t)tid * (max_seq_len + 1);
         int h = (int)(r % num_qo_heads);
-        int64_t row = r / num_qo_heads; /* b * Q + t */
-        int b = (int)(row / Q), t = (int)(row % Q);
+        int64_t row = r / num_qo_heads; /* query row */
+        int b, t, Q;
+        if (cum_seq_lens_q) {
+            /* the request whose rows [cum[b], cum[b+1]) hold this row */
+            int lo_b = 0, hi_b = B - 1;
+            while (lo_b < hi_b) {
+                int mid = (lo_b + hi_b + 1) / 2;
+                if (cum_seq_lens_q[mid] <= row)
+                    lo_b = mid;
+                else
+                    hi_b = mid - 1;
+            }
+            b = lo_b;
+            Q = cum_seq_lens_q[b + 1] - cum_seq_lens_q[b];
+            t = (int)(row - cum_seq_lens_q[b]);
+        } else {
+            Q = q_len_per_req;
+            b = (int)(row / Q);
+            t = (int)(row % Q);
+        }
         int64_t L = seq_lens[b];
         int64_t p = L - Q + t;
         int64_t lo = 0, hi = p;

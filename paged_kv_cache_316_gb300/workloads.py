@@ -15,6 +15,7 @@ them (see ``CONFIGS``).
 """
 from __future__ import annotations
 
+import itertools
 import math
 from dataclasses import dataclass, field
 
@@ -202,7 +203,7 @@ def read_tokens(pool: Pool, pt: PageTable, b: int, n: int | None = None):
 
 @dataclass
 class DecodeCase:
-    query: torch.Tensor          # [B*Q, Hqo, D]
+    query: torch.Tensor          # [B*Q, Hqo, D] (or [sum q_lens, Hqo, D])
     pool: Pool
     pt: PageTable
     block_tables: torch.Tensor   # [B, width] int32 (poison padded)
@@ -217,6 +218,9 @@ class DecodeCase:
     num_kv_heads: int
     head_dim: int
     dtype: int
+    # variable-length queries: request b owns query rows cum[b] .. cum[b+1]-1
+    # and q_len_per_req holds the largest length (max_q_len)
+    cum_seq_lens_q: torch.Tensor | None = None
 
 
 def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
@@ -225,7 +229,9 @@ def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
                 bmm1_scale: float | None = None, bmm2_scale: float = 1.0,
                 pool_pages: int | None = None, slack: float = 0.0, form: str = "5d",
                 device="cpu", bt_width: int | None = None, fill: str = "randn",
-                shuffle: bool = True) -> DecodeCase:
+                shuffle: bool = True, q_lens=None) -> DecodeCase:
+    """Decode problem over freshly reserved pages.  q_lens (one entry per
+    request) gives variable query lengths instead of q_len_per_req."""
     g = generator(seed)
     gd = g if str(device) == "cpu" else generator(seed + 7919, device)
     pt = reserve_pages(lengths, page_size, g if shuffle else None, slack=slack,
@@ -234,7 +240,13 @@ def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
     tdt = torch_dtype(dtype)
     pool = make_pool(pt.num_pages, num_kv_heads, page_size, head_dim, head_dim,
                      layout, tdt, gd, form=form, device=device, fill=fill)
-    query = randn((B * q_len_per_req, num_qo_heads, head_dim), tdt, gd, device)
+    cum = None
+    if q_lens is not None:
+        assert len(q_lens) == B
+        cum = torch.tensor([0] + list(itertools.accumulate(q_lens)), dtype=torch.int32)
+        q_len_per_req = max(q_lens) if B else 1
+    rows = B * q_len_per_req if cum is None else int(cum[-1])
+    query = randn((rows, num_qo_heads, head_dim), tdt, gd, device)
     sinks = randn((num_qo_heads,), torch.float32, g) if with_sinks else None
     if bmm1_scale is None:
         bmm1_scale = 1.0 / math.sqrt(head_dim)
@@ -243,7 +255,7 @@ def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
                       torch.tensor(pt.lengths, dtype=torch.int32),
                       max(pt.lengths) if B else 0, bmm1_scale, bmm2_scale,
                       window_left, sinks, q_len_per_req, num_qo_heads,
-                      num_kv_heads, head_dim, dtype)
+                      num_kv_heads, head_dim, dtype, cum)
 
 
 @dataclass

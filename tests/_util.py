@@ -23,7 +23,8 @@ def oracle_decode(c: wl.DecodeCase, threads=None):
         c.max_seq_len, c.bmm1_scale, c.bmm2_scale, c.window_left,
         None if c.sinks is None else c.sinks.numpy(), c.q_len_per_req,
         c.num_qo_heads, c.num_kv_heads, c.head_dim, p.page_size, p.layout,
-        c.dtype, threads=threads)
+        c.dtype, threads=threads,
+        cum_seq_lens_q=None if c.cum_seq_lens_q is None else c.cum_seq_lens_q.numpy())
 
 
 def oracle_prefill(c: wl.PrefillCase, threads=None):

@@ -22,6 +22,9 @@ MUTANTS = {
                                       "double den = 0.0;"),
     "window_not_inclusive": ("lo = p - window_left;", "lo = p - window_left + 1;"),
     "decode_tokens_not_causal": ("int64_t p = L - Q + t;", "int64_t p = L - 1;"),
+    "varlen_rows_from_request_start": ("t = (int)(row - cum_seq_lens_q[b]);", "t = 0;"),
+    "varlen_uniform_length": ("Q = cum_seq_lens_q[b + 1] - cum_seq_lens_q[b];", "Q = q_len_per_req;"),
+    "varlen_request_search_strict": ("if (cum_seq_lens_q[mid] <= row)", "if (cum_seq_lens_q[mid] < row)"),
     "prefill_top_left_causal": ("int64_t pos = kvb - qb + i;", "int64_t pos = i;"),
     "hnd_addressed_as_nhd": ("within = ((int64_t)head * page_size + slot) * head_dim + d;",
                              "within = ((int64_t)slot * num_kv_heads + head) * head_dim + d;"),

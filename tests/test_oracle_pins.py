@@ -294,6 +294,50 @@ def test_decode_multi_token_matches_prefill_and_single_tokens():
             np.testing.assert_array_equal(sl[0], lse[b * Q + t])
 
 
+def test_decode_varlen_with_equal_lengths_is_uniform():
+    # cum_seq_lens_q with every request at Q tokens is the uniform layout
+    fixed = _small_decode([9, 14, 6], q_len_per_req=2)
+    var = _replace(fixed, cum_seq_lens_q=torch.tensor([0, 2, 4, 6], dtype=torch.int32))
+    a, b = oracle_decode(fixed), oracle_decode(var)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_decode_varlen_rows_follow_their_request():
+    # request b's rows are its Q_b last tokens, exactly as a lone request
+    # with q_len_per_req = Q_b would give them; an empty request has no rows
+    q_lens, lengths = [3, 0, 1, 2], [9, 5, 14, 7]
+    c = _small_decode(lengths, q_lens=q_lens, window_left=4, with_sinks=True)
+    out, lse, err = oracle_decode(c)
+    assert err == 0 and out.shape[0] == sum(q_lens)
+    cum = c.cum_seq_lens_q.tolist()
+    for b, (Q, L) in enumerate(zip(q_lens, lengths)):
+        if Q == 0:
+            continue
+        s = _replace(c, query=c.query[cum[b]:cum[b + 1]], q_len_per_req=Q, cum_seq_lens_q=None,
+                     seq_lens=torch.tensor([L], dtype=torch.int32),
+                     block_tables=c.block_tables[b:b + 1])
+        so, sl, _ = oracle_decode(s)
+        np.testing.assert_array_equal(so, out[cum[b]:cum[b + 1]])
+        np.testing.assert_array_equal(sl, lse[cum[b]:cum[b + 1]])
+
+
+def test_decode_varlen_matches_prefill():
+    # without window and sinks, variable-length decode is causal prefill
+    # with q_b = Q_b over the same pages
+    q_lens, lengths = [2, 4, 1], [9, 14, 5]
+    c = _small_decode(lengths, q_lens=q_lens)
+    out, lse, err = oracle_decode(c)
+    assert err == 0
+    p = wl.PrefillCase(c.query, c.pool, c.pt, c.block_tables,
+                       torch.tensor(q_lens, dtype=torch.int32), c.seq_lens,
+                       max(q_lens), max(lengths), c.bmm1_scale, True, c.num_qo_heads,
+                       c.num_kv_heads, c.head_dim, c.head_dim, c.dtype)
+    po, pl, _ = oracle_prefill(p)
+    np.testing.assert_allclose(out, po, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, pl, rtol=0, atol=1e-14)
+
+
 def test_decode_split_merge_recombines():
     L = 24  # 6 pages of 4
     c = _small_decode([L])
