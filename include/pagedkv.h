@@ -195,6 +195,34 @@ int paged_decode(const void *query, const void *k_cache, const void *v_cache,
                  int32_t *err_word, void *stream);
 
 /*
+ * paged_decode_varlen -- [decode] with variable-length queries: the page's
+ * cum_seq_lens_q ([batch_size + 1] int32, device) and max_q_len.  Request b
+ * has Q_b = cum_seq_lens_q[b+1] - cum_seq_lens_q[b] query tokens, at rows
+ * cum_seq_lens_q[b] + t (t < Q_b) of query/out/lse; they are the last Q_b
+ * positions of its kv sequence (p = L - Q_b + t), causal among themselves,
+ * with everything else as in paged_decode.  num_tokens is the number of
+ * rows query/out hold (the page's num_tokens); max_q_len bounds every Q_b
+ * and sizes the workspace (paged_decode_workspace_size with q_len_per_req =
+ * max_q_len).  The uniform case is cum_seq_lens_q[b] = b * q_len_per_req.
+ * Device errors: an entry with cum[b] < 0, Q_b < 0, Q_b > max_q_len or
+ * cum[b+1] > num_tokens -> PKV_DEV_ERR_QLEN and the request is skipped.
+ * Host errors: cum_seq_lens_q NULL -> PKV_ERR_NULL; num_tokens < 0 ->
+ * PKV_ERR_INVALID_ARG; others as paged_decode (max_q_len in the role of
+ * q_len_per_req).
+ */
+int paged_decode_varlen(const void *query, int64_t num_tokens, const void *k_cache,
+                        const void *v_cache, int64_t page_stride, int64_t max_num_pages,
+                        void *workspace, size_t workspace_bytes,
+                        const int32_t *block_tables, int32_t block_table_stride,
+                        const uint32_t *seq_lens, int32_t batch_size, int32_t max_seq_len,
+                        float bmm1_scale, float bmm2_scale, int32_t window_left,
+                        const float *sinks, int32_t max_q_len,
+                        const int32_t *cum_seq_lens_q, int32_t num_qo_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                        int32_t layout, int32_t dtype, void *out, float *lse,
+                        int32_t *err_word, void *stream);
+
+/*
  * paged_decode_noalloc -- paged_decode without a caller workspace.  The API
  * pages have no counterpart: this entry point exists for callers that cannot
  * allocate device memory where they call decode (a plugin inside another

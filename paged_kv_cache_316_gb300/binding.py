@@ -39,6 +39,9 @@ _SIGNATURES = {
     "paged_decode": ([_c_p, _c_p, _c_p, _i64, _i64, _c_p, _sz, _c_p, _i32, _c_p,
                       _i32, _i32, _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32,
                       _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
+    "paged_decode_varlen": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _c_p, _sz, _c_p, _i32, _c_p,
+                             _i32, _i32, _f32, _f32, _i32, _c_p, _i32, _c_p, _i32, _i32, _i32,
+                             _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
     "paged_decode_noalloc": ([_c_p, _c_p, _c_p, _i64, _i64, _c_p, _i32, _c_p, _i32, _i32,
                               _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
                               _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
@@ -200,8 +203,11 @@ def paged_decode_workspace_size(batch_size, q_len_per_req, num_qo_heads, num_kv_
 def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len: int,
                  bmm1_scale: float = 1.0, bmm2_scale: float = 1.0, window_left: int = -1,
                  sinks=None, kv_layout="HND", q_len_per_req: int = 1, out=None,
-                 lse=None, err_word=None, stream=None):
-    """seq_lens: int32 (or uint32) tensor holding the unsigned kv lengths."""
+                 lse=None, err_word=None, stream=None, max_q_len=None, cum_seq_lens_q=None):
+    """seq_lens: int32 (or uint32) tensor holding the unsigned kv lengths.
+    With cum_seq_lens_q ([B+1] int32 on the device) and max_q_len, request b
+    has the query rows cum[b] .. cum[b+1]-1 (variable-length queries) and
+    q_len_per_req is ignored."""
     layout = _layout_code(kv_layout)
     kp, vp, stride, P, Hkv, S, D, _ = split_cache(kv_cache, layout)
     rows, Hqo, Dq = query.shape
@@ -210,6 +216,17 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
     B = seq_lens.shape[0]
     if out is None:
         out = torch.empty_like(query)
+    if (cum_seq_lens_q is None) != (max_q_len is None):
+        raise PagedKVError("cum_seq_lens_q and max_q_len go together")
+    if cum_seq_lens_q is not None:
+        _check(load_library().paged_decode_varlen(
+            _ptr(query), rows, kp, vp, stride, P, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(block_tables),
+            block_tables.stride(0), _ptr(seq_lens), B, max_seq_len, bmm1_scale,
+            bmm2_scale, window_left, _ptr(sinks), int(max_q_len), _ptr(cum_seq_lens_q), Hqo,
+            Hkv, D, S, layout, _dtype_code(query), _ptr(out), _ptr(lse), _ptr(err_word),
+            _stream(stream)))
+        return out
     _check(load_library().paged_decode(
         _ptr(query), kp, vp, stride, P, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(block_tables),

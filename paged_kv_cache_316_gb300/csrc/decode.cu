@@ -50,7 +50,9 @@ struct DecodeParams {
     float bmm2;
     int window_left;
     const float *sinks;
-    int Q, Hqo, Hkv, group, R;
+    int Q, Hqo, Hkv, group, R;  // Q: query tokens per request (the largest, with cu_q)
+    const int32_t *cu_q;        // [B+1] variable-length query rows, or NULL (rows b*Q + t)
+    int64_t num_tokens;         // query / out rows the caller holds
     int page_shift;
     int chunk;        // keys per split
     int n_split_max;  // split slots per (request, kv head) in the workspace
@@ -110,7 +112,22 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
     const int L = L_in > static_cast<uint32_t>(p.max_seq_len) ? p.max_seq_len : static_cast<int>(L_in);
     if (L_in > static_cast<uint32_t>(p.max_seq_len) && s == 0 && kvh == 0 && threadIdx.x == 0)
         set_err(p.err, PKV_DEV_ERR_LEN);
-    const int Q = p.Q;
+    // this request's query tokens: Q at rows b*Q + t, or Q_b at rows
+    // cu_q[b] + t (an inconsistent entry -- decreasing, longer than the
+    // planned maximum, or past the caller's rows -- is flagged and skipped)
+    int Q = p.Q;
+    int64_t qrow0 = static_cast<int64_t>(b) * p.Q;
+    if (p.cu_q) {
+        const int c0 = p.cu_q[b], c1 = p.cu_q[b + 1];
+        Q = c1 - c0;
+        qrow0 = c0;
+        if (c0 < 0 || Q < 0 || Q > p.Q || c1 > p.num_tokens) {
+            if (s == 0 && kvh == 0 && threadIdx.x == 0) set_err(p.err, PKV_DEV_ERR_QLEN);
+            Q = 0;
+        }
+        if (Q == 0) return;  // uniform over the CTA: before any barrier
+    }
+    const int R = p.group * Q;  // query rows of this (request, kv head)
     int lo, first, n_split;
     decode_split_geometry(L, Q, p.window_left, p.chunk, lo, first, n_split);
     if (s >= n_split) return;
@@ -175,11 +192,11 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
     const T *qp = static_cast<const T *>(p.q);
     for (int idx = tid; idx < ROWS * 16; idx += kDecThreads) {
         int r = idx >> 4, c = idx & 15;
-        bool ok = r < p.R;
+        bool ok = r < R;
         const T *src = qp;
         if (ok) {
             int t = r / p.group, i = r - t * p.group;
-            src = qp + (static_cast<int64_t>(b * Q + t) * p.Hqo + kvh * p.group + i) * kDecD + c * 8;
+            src = qp + ((qrow0 + t) * p.Hqo + kvh * p.group + i) * kDecD + c * 8;
         }
         cp_async_16(smem_u32(q_s) + swz(r, c, kDecRowBytes), src, ok);
     }
@@ -331,7 +348,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
     }
     __syncthreads();
 
-    for (int idx = tid; idx < p.R * 32; idx += kDecThreads) {
+    for (int idx = tid; idx < R * 32; idx += kDecThreads) {
         const int r = idx >> 5, d = (idx & 31) * 4;
         float M = -INFINITY;
 #pragma unroll
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
                 sc_o = 0.f;
                 lse_v = -INFINITY;
             }
-            const int64_t orow = static_cast<int64_t>(b * Q + t) * p.Hqo + h;
+            const int64_t orow = (qrow0 + t) * p.Hqo + h;
             store4(static_cast<T *>(p.out) + orow * kDecD + d, a0 * sc_o, a1 * sc_o, a2 * sc_o, a3 * sc_o);
             if (p.lse && d == 0) p.lse[orow] = lse_v;
         } else {
@@ -389,10 +406,19 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     const int h = static_cast<int>(row % p.Hqo);
     const int64_t bq = row / p.Hqo;
     const int t = static_cast<int>(bq % p.Q), b = static_cast<int>(bq / p.Q);
+    int Q = p.Q;
+    int64_t qrow0 = static_cast<int64_t>(b) * p.Q;
+    if (p.cu_q) {  // the split kernel flagged inconsistent entries; skip them the same way
+        const int c0 = p.cu_q[b], c1 = p.cu_q[b + 1];
+        Q = c1 - c0;
+        qrow0 = c0;
+        if (c0 < 0 || Q < 0 || Q > p.Q || c1 > p.num_tokens) Q = 0;
+    }
+    if (t >= Q) return;
     const uint32_t L_in = p.seq_lens[b];
     const int L = L_in > static_cast<uint32_t>(p.max_seq_len) ? p.max_seq_len : static_cast<int>(L_in);
     int lo, first, n_split;
-    decode_split_geometry(L, p.Q, p.window_left, p.chunk, lo, first, n_split);
+    decode_split_geometry(L, Q, p.window_left, p.chunk, lo, first, n_split);
     if (n_split <= 1) return;  // the split kernel wrote this row itself
     const int kvh = h / p.group;
     const int r = t * p.group + (h - kvh * p.group);
@@ -416,8 +442,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
         if (p.sinks) den += fast_exp2(p.sinks[h] * kLog2e - M);
     }
     const float sc = den > 0.f ? p.bmm2 / den : 0.f;
-    store4(static_cast<T *>(p.out) + row * kDecD + d, acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
-    if (p.lse && lane == 0) p.lse[row] = den > 0.f ? (M + fast_log2(den)) * kLn2 : -INFINITY;
+    const int64_t orow = (qrow0 + t) * p.Hqo + h;
+    store4(static_cast<T *>(p.out) + orow * kDecD + d, acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+    if (p.lse && lane == 0) p.lse[orow] = den > 0.f ? (M + fast_log2(den)) * kLn2 : -INFINITY;
 }
 
 struct DecodePlan {
@@ -519,13 +546,14 @@ extern "C" size_t paged_decode_workspace_size(int32_t batch_size, int32_t q_len_
     return pl.ws_bytes;
 }
 
-extern "C" int paged_decode(const void *query, const void *k_cache, const void *v_cache,
+static int decode_impl(const void *query, const void *k_cache, const void *v_cache,
                             int64_t page_stride, int64_t max_num_pages, void *workspace,
                             size_t workspace_bytes, const int32_t *block_tables,
                             int32_t block_table_stride, const uint32_t *seq_lens,
                             int32_t batch_size, int32_t max_seq_len, float bmm1_scale,
                             float bmm2_scale, int32_t window_left, const float *sinks,
-                            int32_t q_len_per_req, int32_t num_qo_heads, int32_t num_kv_heads,
+                            int32_t q_len_per_req, const int32_t *cum_seq_lens_q, int64_t num_tokens,
+                            int32_t num_qo_heads, int32_t num_kv_heads,
                             int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
                             void *out, float *lse, int32_t *err_word, void *stream) {
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
@@ -563,6 +591,8 @@ extern "C" int paged_decode(const void *query, const void *k_cache, const void *
     p.window_left = window_left;
     p.sinks = sinks;
     p.Q = q_len_per_req;
+    p.cu_q = cum_seq_lens_q;
+    p.num_tokens = num_tokens;
     p.Hqo = num_qo_heads;
     p.Hkv = num_kv_heads;
     p.group = num_qo_heads / num_kv_heads;
@@ -579,6 +609,40 @@ extern "C" int paged_decode(const void *query, const void *k_cache, const void *
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return dtype == PKV_BF16 ? run_decode<__nv_bfloat16>(p, pl, layout, st)
                              : run_decode<__half>(p, pl, layout, st);
+}
+
+extern "C" int paged_decode(const void *query, const void *k_cache, const void *v_cache,
+                            int64_t page_stride, int64_t max_num_pages, void *workspace,
+                            size_t workspace_bytes, const int32_t *block_tables,
+                            int32_t block_table_stride, const uint32_t *seq_lens,
+                            int32_t batch_size, int32_t max_seq_len, float bmm1_scale,
+                            float bmm2_scale, int32_t window_left, const float *sinks,
+                            int32_t q_len_per_req, int32_t num_qo_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
+                            void *out, float *lse, int32_t *err_word, void *stream) {
+    return decode_impl(query, k_cache, v_cache, page_stride, max_num_pages, workspace, workspace_bytes,
+                       block_tables, block_table_stride, seq_lens, batch_size, max_seq_len, bmm1_scale,
+                       bmm2_scale, window_left, sinks, q_len_per_req, nullptr,
+                       static_cast<int64_t>(batch_size) * q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
+                       page_size, layout, dtype, out, lse, err_word, stream);
+}
+
+extern "C" int paged_decode_varlen(const void *query, int64_t num_tokens, const void *k_cache,
+                                   const void *v_cache, int64_t page_stride, int64_t max_num_pages,
+                                   void *workspace, size_t workspace_bytes, const int32_t *block_tables,
+                                   int32_t block_table_stride, const uint32_t *seq_lens, int32_t batch_size,
+                                   int32_t max_seq_len, float bmm1_scale, float bmm2_scale,
+                                   int32_t window_left, const float *sinks, int32_t max_q_len,
+                                   const int32_t *cum_seq_lens_q, int32_t num_qo_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
+                                   void *out, float *lse, int32_t *err_word, void *stream) {
+    if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (batch_size > 0 && num_tokens > 0 && !cum_seq_lens_q) return PKV_ERR_NULL;
+    if (num_tokens == 0) return PKV_OK;
+    return decode_impl(query, k_cache, v_cache, page_stride, max_num_pages, workspace, workspace_bytes,
+                       block_tables, block_table_stride, seq_lens, batch_size, max_seq_len, bmm1_scale,
+                       bmm2_scale, window_left, sinks, max_q_len, cum_seq_lens_q, num_tokens, num_qo_heads,
+                       num_kv_heads, head_dim, page_size, layout, dtype, out, lse, err_word, stream);
 }
 
 // ---- decode with a library-owned scratch array ------------------------------

@@ -44,14 +44,16 @@ def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None, w
     if ws is None:
         ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=DEV)
     assert ws.numel() >= ws_bytes
-    lse = torch.empty((B * c.q_len_per_req, c.num_qo_heads), dtype=torch.float32,
+    lse = torch.empty((c.query.shape[0], c.num_qo_heads), dtype=torch.float32,
                       device=DEV) if with_lse else None
     out = pk.paged_decode(c.query.to(DEV), kv, ws, c.block_tables.to(DEV), c.seq_lens.to(DEV),
                           c.max_seq_len, bmm1_scale=c.bmm1_scale, bmm2_scale=c.bmm2_scale,
                           window_left=c.window_left,
                           sinks=None if c.sinks is None else c.sinks.to(DEV),
                           kv_layout=pool.layout if layout is None else layout,
-                          q_len_per_req=c.q_len_per_req, lse=lse, err_word=err_word)
+                          q_len_per_req=c.q_len_per_req, lse=lse, err_word=err_word,
+                          **({} if c.cum_seq_lens_q is None else
+                             dict(cum_seq_lens_q=c.cum_seq_lens_q.to(DEV), max_q_len=c.q_len_per_req)))
     torch.cuda.synchronize()
     return out, lse
 

@@ -95,6 +95,23 @@ def test_decode_rejects_bad_arguments(lib):
     assert call(B=0) == 0
 
 
+def test_decode_varlen_rejects_bad_arguments(lib):
+    good = 0x1000
+
+    def call(**over):
+        a = dict(query=good, ntok=10, k=good, v=good, stride=2 * 8 * 16 * 128, pages=64, ws=good,
+                 ws_bytes=1 << 30, bt=good, bt_stride=10000, seq=good, B=4, max_len=100, s1=0.1,
+                 s2=1.0, win=-1, sinks=None, maxq=4, cum=good, hqo=32, hkv=8, D=128, S=16,
+                 layout=1, dtype=1, out=good, lse=None, err=None, stream=None)
+        a.update(over)
+        return lib.paged_decode_varlen(*a.values())
+
+    assert call(cum=None) == 1          # cum_seq_lens_q required
+    assert call(ntok=-1) == 2
+    assert call(maxq=9, hqo=64) == 3    # group 8 x 9 tokens > 64 rows
+    assert call(ntok=0) == 0            # no query rows: nothing to do
+
+
 def test_decode_workspace_size_grows_with_length(lib):
     f = lib.paged_decode_workspace_size
     small = f(64, 1, 32, 8, 128, 512, 16, -1)

@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from paged_kv_cache_316_gb300 import workloads as wl
+import paged_kv_cache_316_gb300 as pk
 from _gpu import (DEV, assert_attn_close, assert_lse_close, compact_request, decode_on_gpu,
                   err_word)
 from _util import oracle_decode
@@ -131,6 +132,47 @@ def test_hundreds_of_splits():
     # one long request on one kv head: the keys are cut into ~780 splits
     c = wl.decode_case([200000], 256, 64, 1, 128, wl.HND, seed=13, with_sinks=True)
     _check(c)
+
+
+VARLEN = [
+    # lengths, q_lens, page, Hqo, Hkv, window, sinks, layout, seed
+    ([700, 40, 1500, 3, 2100], [3, 0, 1, 2, 4], 16, 64, 8, 300, True, wl.HND, 21),   # 32 rows
+    ([900, 4000, 77], [4, 1, 2], 32, 16, 4, -1, False, wl.NHD, 22),                  # 16 rows
+    ([1200, 650], [8, 5], 64, 64, 8, 511, True, wl.HND, 23),                          # 64 rows
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[f"v{i}" for i in range(len(VARLEN))])
+def test_variable_length_queries(case):
+    L, ql, S, hq, hk, w, sk, lay, seed = case
+    c = wl.decode_case(L, S, hq, hk, 128, lay, q_lens=ql, window_left=w, with_sinks=sk,
+                       seed=seed, slack=0.2, bmm2_scale=1.3)
+    err = err_word()
+    out, lse = decode_on_gpu(c, err_word=err)
+    ro, rl, oerr = oracle_decode(c)
+    assert int(err.item()) == oerr == 0
+    assert_attn_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_variable_length_bad_entry_flagged_and_skipped():
+    # request 1 claims more tokens than max_q_len: flagged, its rows untouched;
+    # the others are computed as usual
+    c = wl.decode_case([500, 800, 300], 16, 32, 8, 128, wl.HND, q_lens=[2, 3, 1], seed=24)
+    B = 3
+    ws = torch.zeros(max(1, pk.paged_decode_workspace_size(B, 2, 32, 8, 128, c.max_seq_len, 16)),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.full((6, 32, 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    err = err_word()
+    pk.paged_decode(c.query.to(DEV), c.pool.storage[0].to(DEV), ws, c.block_tables.to(DEV),
+                    c.seq_lens.to(DEV), c.max_seq_len, bmm1_scale=c.bmm1_scale,
+                    cum_seq_lens_q=c.cum_seq_lens_q.to(DEV), max_q_len=2, out=out, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & oracle.E_QLEN
+    ro, _, _ = oracle_decode(c)
+    rows_ok = [0, 1, 5]  # requests 0 and 2
+    assert_attn_close(out[rows_ok], ro[rows_ok])
+    assert torch.all(out[2:5].float() == 7.0)
 
 
 def test_without_lse_output():
