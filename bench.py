@@ -67,10 +67,12 @@ def peaks():
 def decode_bytes(c) -> int:
     """K and V rows each visible query row set needs (read once per kv head),
     query, output, the block-table entries used and the lengths."""
-    Q, S = c.q_len_per_req, c.pool.page_size
+    S = c.pool.page_size
+    cum = None if c.cum_seq_lens_q is None else c.cum_seq_lens_q.tolist()
     kv_tok = 0
     pages = 0
-    for L in c.pt.lengths:
+    for b, L in enumerate(c.pt.lengths):
+        Q = c.q_len_per_req if cum is None else cum[b + 1] - cum[b]
         lo = max(0, L - Q - c.window_left) if c.window_left >= 0 else 0
         kv_tok += L - lo
         pages += (L + S - 1) // S - lo // S
@@ -293,6 +295,28 @@ def make_parts(rank: int, dev):
     return parts
 
 
+def make_next_parts(rank: int, dev):
+    """Rows beyond the hot path's configurations, measured the same way but
+    outside the step: variable-length multi-token decode."""
+    import paged_kv_cache_316_gb300 as pk
+    from paged_kv_cache_316_gb300 import workloads as wl
+    c = wl.long_decode_varlen(seed=rank_seed(rank), device=dev)
+    B = len(c.pt.lengths)
+    ws = torch.zeros(max(1, pk.paged_decode_workspace_size(
+        B, c.q_len_per_req, c.num_qo_heads, c.num_kv_heads, c.head_dim, c.max_seq_len,
+        c.pool.page_size, c.window_left)), dtype=torch.uint8, device=dev)
+    bt, sl, cum = c.block_tables.to(dev), c.seq_lens.to(dev), c.cum_seq_lens_q.to(dev)
+    sinks = c.sinks.to(dev)
+    kv = c.pool.storage[0]
+    out = torch.empty_like(c.query)
+
+    def run():
+        pk.paged_decode(c.query, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=c.bmm1_scale,
+                        window_left=c.window_left, sinks=sinks, kv_layout=c.pool.layout,
+                        cum_seq_lens_q=cum, max_q_len=c.q_len_per_req, out=out)
+    return [Part("decode_varlen", run, decode_bytes(c), "GB/s", "hbm", "decode.cu")]
+
+
 def traffic_for(kernel_file: str, part: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the kernel source as it is now."""
@@ -438,6 +462,24 @@ def run_ours(args):
                 "peak_source": f"{peak_src} ({'hbm_gbs' if dom.unit == 'GB/s' else 'bf16_tflops'})",
                 "traffic": traffic_for(dom.kernel, dom.name)}
 
+    # rows beyond the step's configurations: timed the same way, after the step
+    nxt = make_next_parts(rank, dev)
+    for _ in range(args.warmup):
+        for p in nxt:
+            p.fn()
+    torch.cuda.synchronize()
+    for p in nxt:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, z in evs:
+            a.record(st)
+            p.fn()
+            z.record(st)
+        torch.cuda.synchronize()
+        p.ms = [a.elapsed_time(z) for a, z in evs]
+    next_rows = aggregate_parts([(p.name, sum(p.ms) / len(p.ms), p.work, p.unit) for p in nxt],
+                                ws, dev, pk_peaks)
+
     llama = next(p for p in parts if p.name == "decode_llama")
     e2e_ms, h2d, d2h = e2e_decode(llama, max(10, args.steps // 4), dev)
     e2e_ms = allreduce_max(e2e_ms, ws, dev)
@@ -450,6 +492,9 @@ def run_ours(args):
                    "l2": "no flush: every part's inputs exceed the 129 MB L2",
                    "headline_part": "decode_llama"},
         "parts": out_parts, "roofline": roofline,
+        "next_rows": dict(next_rows, note="outside the step and its ms_per_step: variable-length "
+                                          "multi-token decode on the long-context shape (1..4 query "
+                                          "tokens per request)"),
         "e2e": {"value": round(allreduce_sum(float(llama.work), ws, dev) / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),

@@ -1,7 +1,7 @@
 """Run one operation of the library on its named synthetic workload.
 
     python -m paged_kv_cache_316_gb300.run_case --op prefill [--d-qk 128] [--iters 3]
-    python -m paged_kv_cache_316_gb300.run_case --op decode_llama | decode_long | append
+    python -m paged_kv_cache_316_gb300.run_case --op decode_llama | decode_long | decode_varlen | append
                                                 [--batch N] [--iters 3]
 
 Used to drive profilers (ncu) on one kernel at a size that keeps a capture
@@ -22,7 +22,7 @@ from . import workloads as wl
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", required=True,
-                    choices=["prefill", "decode_llama", "decode_long", "append"])
+                    choices=["prefill", "decode_llama", "decode_long", "decode_varlen", "append"])
     ap.add_argument("--d-qk", type=int, default=128)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--iters", type=int, default=3)
@@ -41,8 +41,10 @@ def main():
         def run():
             pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv,
                              bt, causal=True, kv_layout="HND")
-    elif a.op in ("decode_llama", "decode_long"):
-        if not a.batch:
+    elif a.op in ("decode_llama", "decode_long", "decode_varlen"):
+        if a.op == "decode_varlen":
+            c = wl.long_decode_varlen(device=dev)
+        elif not a.batch:
             c = wl.llama_decode(device=dev) if a.op == "decode_llama" else wl.long_decode(device=dev)
         elif a.op == "decode_llama":  # the first `batch` requests of the same length draw
             L = wl.uniform_lengths(wl.generator(0), 64, 512, 8192)[:a.batch]
@@ -59,10 +61,13 @@ def main():
         sinks = None if c.sinks is None else c.sinks.to(dev)
         kv = c.pool.storage[0]
 
+        cum = None if c.cum_seq_lens_q is None else c.cum_seq_lens_q.to(dev)
+        vl = {} if cum is None else dict(cum_seq_lens_q=cum, max_q_len=c.q_len_per_req)
+
         def run():
             pk.paged_decode(c.query, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=c.bmm1_scale,
                             window_left=c.window_left, sinks=sinks, kv_layout=c.pool.layout,
-                            q_len_per_req=c.q_len_per_req)
+                            q_len_per_req=c.q_len_per_req, **vl)
     else:
         c = wl.append_sweep(a.batch or 4096, seed=1, layout=wl.NHD, device=dev, fill="empty")
         kvi, kvp, last = (x.to(dev) for x in (c.kv_indices, c.kv_indptr, c.kv_last_page_len))

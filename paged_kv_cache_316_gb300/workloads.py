@@ -376,6 +376,15 @@ def long_decode(seed: int = 0, layout: int = HND, device="cpu", **kw) -> DecodeC
                        device=device, bt_width=32768 // 64, **kw)
 
 
+def long_decode_varlen(seed: int = 0, layout: int = HND, device="cpu", **kw) -> DecodeCase:
+    """The long-context decode with variable-length queries: each of the 256
+    requests has 1 to 4 query tokens (uniform), max_q_len 4."""
+    L = lognormal_lengths(generator(seed), 256, 4096.0, 1.0, 4, 32768)
+    ql = uniform_lengths(generator(seed + 101), 256, 1, 4)
+    return decode_case(L, 64, 64, 8, 128, layout, BF16, q_lens=ql, window_left=4095,
+                       with_sinks=True, seed=seed, device=device, bt_width=32768 // 64, **kw)
+
+
 def ragged_prefill(seed: int = 0, d_qk: int = 128, device="cpu", **kw) -> PrefillCase:
     """Causal ragged prefill: 16 requests, q lengths uniform in [128, 2048],
     kv = q + prefix with prefix uniform in [0, 2048], page_size 32, 32/8
@@ -426,6 +435,8 @@ CONFIGS = {
     "llama_decode": "bf16 decode, batch 64, kv U[512,8192], page 16, 32/8 heads, d 128, HND",
     "long_decode": "bf16 decode, batch 256, lognormal kv (median 4096, cap 32768), page 64, "
                    "64/8 heads, window 4095, sinks, q_len_per_req 4",
+    "long_decode_varlen": "the long-context decode with 1..4 query tokens per request "
+                          "(cum_seq_lens_q, max_q_len 4)",
     "ragged_prefill": "bf16 causal ragged prefill, batch 16, q U[128,2048], prefix "
                       "U[0,2048], page 32, 32/8 heads, d 128 (and 192/128)",
 }

@@ -210,3 +210,20 @@ def test_long_context_config_full_size_sampled():
     lengths = np.array(c.pt.lengths)
     pick = sorted({int(lengths.argmin()), int(lengths.argmax()), 1, 100, 255})
     _sampled_full_size(c, pick)
+
+
+def test_long_context_varlen_full_size_sampled():
+    c = wl.long_decode_varlen(device=DEV)
+    out, lse = decode_on_gpu(c)
+    cum = c.cum_seq_lens_q.tolist()
+    lengths = np.array(c.pt.lengths)
+    for b in sorted({int(lengths.argmin()), int(lengths.argmax()), 3, 130, 255}):
+        pool, pt = compact_request(c.pool, c.pt, b)
+        Q = cum[b + 1] - cum[b]
+        sub = dataclasses.replace(
+            c, query=c.query[cum[b]:cum[b + 1]].cpu(), pool=pool, pt=pt,
+            block_tables=pt.block_tables(), seq_lens=torch.tensor([pt.lengths[0]], dtype=torch.int32),
+            max_seq_len=pt.lengths[0], sinks=c.sinks.cpu(), q_len_per_req=Q, cum_seq_lens_q=None)
+        ro, rl, _ = oracle_decode(sub)
+        assert_attn_close(out[cum[b]:cum[b + 1]], ro, f"request {b}")
+        assert_lse_close(lse[cum[b]:cum[b + 1]], rl, f"request {b} lse")
