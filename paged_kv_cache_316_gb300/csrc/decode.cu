@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
     }
     cp_async_wait<0>();
     __syncthreads();
+    pdl_launch_dependents();  // the merge kernel may get ready; it waits for this grid
 
     // combine the key groups of this CTA through shared memory
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
 // 2^lse_s, adds the sink to the denominator, applies bmm2_scale.
 template <typename T>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+    pdl_wait();  // the split kernel's partials
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
     if (row >= static_cast<int64_t>(p.B) * p.Q * p.Hqo) return;
@@ -524,7 +526,9 @@ static int run_decode(const DecodeParams &p, const DecodePlan &pl, int layout, c
     int launches = 1;
     if (pl.n_split_max > 1) {
         int64_t rows = static_cast<int64_t>(p.B) * p.Q * p.Hqo;
-        decode_merge_kernel<T><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(p);
+        if (launch_dependent(decode_merge_kernel<T>, dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128), 0,
+                             st, p) != cudaSuccess)
+            return PKV_ERR_CUDA;
         ++launches;
     }
     note_launches(launches);

@@ -15,6 +15,31 @@ namespace pkv {
 // Count `n` kernel launches (diagnostics; see pkv_kernel_launches).
 void note_launches(int n);
 
+// Programmatic dependent launch between the kernels of one call: the second
+// kernel is launched with programmatic stream serialisation, may start while
+// the first finishes, and waits (griddepcontrol.wait) for the first grid's
+// completion and memory before it reads what that grid wrote.  Both
+// instructions are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+template <typename... Params, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // PKV_OK if the launches just made succeeded, PKV_ERR_CUDA otherwise.
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

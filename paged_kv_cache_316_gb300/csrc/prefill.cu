@@ -96,6 +96,7 @@ __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_
                                     int B, int U, int max_q, int max_kv, int32_t *__restrict__ cu_q,
                                     int32_t *__restrict__ cu_items, int32_t *err, int *work_counter) {
     const int lane = threadIdx.x;
+    pdl_launch_dependents();  // the main kernel may start its prologue meanwhile
     int carry = 0, carry_t = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         int b = b0 + lane;
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();  // the plan kernel's prefix sums and zeroed work counter
     const uint32_t tmem = tmem_base_s;
     volatile int *abort_flag = &abort_s;
     auto give_up = [&]() {
@@ -846,7 +848,10 @@ static int launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
-    kern<<<grid, PfRoles<DQK>::kThreads, smem, st>>>(tq, tk, tv, p);
+    // launched as the plan kernel's dependent: the prologue (barriers, tensor
+    // memory, descriptor prefetch) overlaps the plan kernel
+    if (launch_dependent(kern, grid, dim3(PfRoles<DQK>::kThreads), smem, st, tq, tk, tv, p) != cudaSuccess)
+        return PKV_ERR_CUDA;
     return PKV_OK;
 }
 

@@ -1,0 +1,87 @@
+"""The hot path under CUDA-graph capture: every call is asynchronous on the
+caller's stream and allocates nothing, so append, decode (uniform and
+variable-length) and prefill can be captured into one graph -- including the
+programmatic-dependent launches inside decode and prefill -- and every
+replay reproduces the eager results bit for bit."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import paged_kv_cache_316_gb300 as pk
+from paged_kv_cache_316_gb300 import workloads as wl
+from _gpu import DEV
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype in (torch.bfloat16, torch.float16) else t
+
+
+def test_graph_replay_matches_eager():
+    # append into its own pool
+    ap = wl.append_sweep(16, seed=3, layout=wl.NHD, device=DEV, fill="empty")
+    kvi, kvp, last = (x.to(DEV) for x in (ap.kv_indices, ap.kv_indptr, ap.kv_last_page_len))
+    seq = pk.paged_seq_lens(kvp, last, 16)
+    nnz = ap.append_key.shape[0]
+    bi, pos = pk.paged_batch_indices_positions(ap.append_indptr.to(DEV), seq, nnz)
+    pool = ap.pool.storage[0]
+    # decode, uniform and variable-length
+    dc = wl.decode_case([900, 2500, 64, 4100], 16, 32, 8, 128, wl.HND, q_len_per_req=2,
+                        window_left=1000, with_sinks=True, seed=31, device=DEV)
+    vc = wl.decode_case([1300, 70, 3000], 32, 64, 8, 128, wl.HND, q_lens=[1, 4, 2],
+                        with_sinks=True, seed=32, device=DEV)
+    ws_d = torch.zeros(max(1, pk.paged_decode_workspace_size(4, 2, 32, 8, 128, dc.max_seq_len, 16, 1000)),
+                       dtype=torch.uint8, device=DEV)
+    ws_v = torch.zeros(max(1, pk.paged_decode_workspace_size(3, 4, 64, 8, 128, vc.max_seq_len, 32, -1)),
+                       dtype=torch.uint8, device=DEV)
+    d_args = [t.to(DEV) for t in (dc.block_tables, dc.seq_lens, dc.sinks)]
+    v_args = [t.to(DEV) for t in (vc.block_tables, vc.seq_lens, vc.sinks, vc.cum_seq_lens_q)]
+    d_out, d_lse = torch.empty_like(dc.query), torch.empty(dc.query.shape[:2], device=DEV)
+    v_out, v_lse = torch.empty_like(vc.query), torch.empty(vc.query.shape[:2], device=DEV)
+    # prefill
+    pc = wl.prefill_case([130, 64, 300], [200, 64, 900], 32, 32, 8, 128, 128, wl.HND, wl.BF16,
+                         seed=33, device=DEV)
+    ws_p = torch.zeros(pk.paged_prefill_workspace_size(3, 32, pc.max_q, pc.max_kv), dtype=torch.uint8,
+                       device=DEV)
+    p_args = [t.to(DEV) for t in (pc.seq_lens_q, pc.seq_lens_kv, pc.block_tables)]
+    p_out = torch.empty((pc.q.shape[0], 32, 128), dtype=pc.q.dtype, device=DEV)
+    p_lse = torch.empty((pc.q.shape[0], 32), dtype=torch.float32, device=DEV)
+
+    def step():
+        pk.paged_append(ap.append_key, ap.append_value, bi, pos, pool, kvi, kvp, last,
+                        kv_layout="NHD")
+        pk.paged_decode(dc.query, dc.pool.storage[0], ws_d, d_args[0], d_args[1], dc.max_seq_len,
+                        bmm1_scale=dc.bmm1_scale, window_left=1000, sinks=d_args[2],
+                        q_len_per_req=2, out=d_out, lse=d_lse)
+        pk.paged_decode(vc.query, vc.pool.storage[0], ws_v, v_args[0], v_args[1], vc.max_seq_len,
+                        bmm1_scale=vc.bmm1_scale, sinks=v_args[2], cum_seq_lens_q=v_args[3],
+                        max_q_len=4, out=v_out, lse=v_lse)
+        pk.paged_prefill(pc.q, pc.pool.k, pc.pool.v, pc.scale, ws_p, pc.max_q, pc.max_kv,
+                         p_args[0], p_args[1], p_args[2], causal=True, out=p_out, lse=p_lse,
+                         kv_layout="HND")
+
+    outs = (pool, d_out, d_lse, v_out, v_lse, p_out, p_lse)
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in outs]
+    for t in outs[1:]:
+        t.fill_(0)
+    pool.zero_()
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        for t in outs[1:]:
+            t.fill_(0)
+        pool.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for e, t in zip(eager, outs):
+            assert torch.equal(_bits(e), _bits(t))
