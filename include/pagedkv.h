@@ -296,6 +296,12 @@ size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_qo_heads,
  * gave up (the affected rows are then zero).
  * Device errors: bad page id -> PKV_DEV_ERR_PAGE; kv_b < q_b ->
  * PKV_DEV_ERR_QLEN (rows that see no key get out = 0, lse = -inf).
+ * block_tables = NULL (the page's non-paged case): k_cache / v_cache are
+ * contiguous [max_num_pages rows, num_kv_heads, d] tensors (token-major, so
+ * layout must be PKV_NHD), k_page_stride / v_page_stride are their row
+ * strides in elements, request b's keys are rows cu_kv[b] + j (cu_kv the
+ * exclusive prefix sum of the kv lengths), and page_size /
+ * block_table_stride are ignored.
  */
 int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
                   const void *v_cache,
@@ -308,6 +314,32 @@ int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
                   int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
                   int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
                   void *out, float *lse, int32_t *err_word, void *stream);
+
+/*
+ * paged_prefill_ex -- paged_prefill with the prefill page's batch offsets
+ * (batch_offsets_q, batch_offsets_o, batch_offsets_k, batch_offsets_v:
+ * [batch_size] int32 on the device, each optional).  The page gives no unit;
+ * they are read as token rows: request b's queries are rows
+ * batch_offsets_q[b] + i of q, its outputs and LSEs rows
+ * batch_offsets_o[b] + i of out / lse, and (contiguous K/V only) its keys /
+ * values rows batch_offsets_k[b] + j / batch_offsets_v[b] + j.  A NULL array
+ * keeps the packed placement of paged_prefill.  Output rows outside
+ * [0, total_q) are not written.  Host errors: K/V offsets together with a
+ * block table -> PKV_ERR_INVALID_ARG; the rest as paged_prefill.
+ */
+int paged_prefill_ex(const void *q, int64_t total_q, const void *k_cache,
+                     const void *v_cache,
+                     int64_t k_page_stride, int64_t v_page_stride,
+                     int64_t max_num_pages, float scale, void *workspace,
+                     size_t workspace_bytes, int32_t max_token_per_sequence,
+                     int32_t max_sequence_kv, const int32_t *actual_seq_lens_q,
+                     const int32_t *actual_seq_lens_kv, const int32_t *block_tables,
+                     int32_t block_table_stride, int32_t batch_size, int32_t causal,
+                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                     int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
+                     void *out, float *lse, const int32_t *batch_offsets_q,
+                     const int32_t *batch_offsets_o, const int32_t *batch_offsets_k,
+                     const int32_t *batch_offsets_v, int32_t *err_word, void *stream);
 
 #ifdef __cplusplus
 }

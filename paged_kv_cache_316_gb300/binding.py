@@ -49,6 +49,10 @@ _SIGNATURES = {
     "paged_prefill": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _sz, _i32,
                        _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
                        _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
+    "paged_prefill_ex": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _sz, _i32,
+                          _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
+                          _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                          _c_p], ctypes.c_int),
 }
 
 
@@ -274,10 +278,20 @@ def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
                   max_token_per_sequence: int, max_sequence_kv: int,
                   actual_seq_lens_q, actual_seq_lens_kv, block_tables,
                   causal: bool = True, out=None, lse=None, kv_layout="HND",
-                  err_word=None, stream=None):
+                  err_word=None, stream=None, batch_offsets_q=None, batch_offsets_o=None,
+                  batch_offsets_k=None, batch_offsets_v=None):
+    """block_tables=None: k_cache / v_cache are contiguous [rows, Hkv, d]
+    tensors (the page's non-paged case; kv_layout is then NHD).  The
+    batch_offsets_* tensors ([B] int32 on the device, token rows) place each
+    request's queries, outputs / LSEs and (contiguous K/V) keys / values."""
+    if block_tables is None:
+        kv_layout = "NHD"
     layout = _layout_code(kv_layout)
     total_q, Hqo, d_qk = q.shape
-    if layout == HND:
+    if block_tables is None:
+        P, Hkv, dk = k_cache.shape
+        S, dv = 1, v_cache.shape[2]
+    elif layout == HND:
         P, Hkv, S, dk = k_cache.shape
         dv = v_cache.shape[3]
     else:
@@ -290,11 +304,22 @@ def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
     if lse is None:
         lse = torch.empty((total_q, Hqo), dtype=torch.float32, device=q.device)
     B = actual_seq_lens_q.shape[0]
-    _check(load_library().paged_prefill(
-        _ptr(q), total_q, _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
-        P, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
-        max_token_per_sequence, max_sequence_kv, _ptr(actual_seq_lens_q),
-        _ptr(actual_seq_lens_kv), _ptr(block_tables), block_tables.stride(0), B,
-        int(causal), Hqo, Hkv, d_qk, dv, S, layout, _dtype_code(q), _ptr(out),
-        _ptr(lse), _ptr(err_word), _stream(stream)))
+    bt_stride = 0 if block_tables is None else block_tables.stride(0)
+    offsets = (batch_offsets_q, batch_offsets_o, batch_offsets_k, batch_offsets_v)
+    if all(o is None for o in offsets):
+        _check(load_library().paged_prefill(
+            _ptr(q), total_q, _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
+            P, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            max_token_per_sequence, max_sequence_kv, _ptr(actual_seq_lens_q),
+            _ptr(actual_seq_lens_kv), _ptr(block_tables), bt_stride, B,
+            int(causal), Hqo, Hkv, d_qk, dv, S, layout, _dtype_code(q), _ptr(out),
+            _ptr(lse), _ptr(err_word), _stream(stream)))
+    else:
+        _check(load_library().paged_prefill_ex(
+            _ptr(q), total_q, _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
+            P, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            max_token_per_sequence, max_sequence_kv, _ptr(actual_seq_lens_q),
+            _ptr(actual_seq_lens_kv), _ptr(block_tables), bt_stride, B,
+            int(causal), Hqo, Hkv, d_qk, dv, S, layout, _dtype_code(q), _ptr(out),
+            _ptr(lse), *(_ptr(o) for o in offsets), _ptr(err_word), _stream(stream)))
     return out, lse

@@ -82,22 +82,30 @@ struct PrefillParams {
     const int32_t *cu_items;  // [B+1] in the workspace: U x prefix sum of query tiles
     int B, causal, Hqo, Hkv, group, page_shift, max_q, max_kv;
     int pairs;  // head pairs per kv head: (group + 1) / 2; U = Hkv * pairs items per query tile
+    // contiguous K/V (no block table): [rows, Hkv, d] tensors, request b's keys
+    // from row off_k[b] (K) / off_v[b] (V), by default the prefix sum cu_kv[b]
+    int contiguous;
+    const int32_t *cu_kv;   // [B+1] in the workspace
+    // optional placement (token rows) of each request's queries, outputs and
+    // keys/values; NULL = packed by the prefix sums
+    const int32_t *off_q, *off_o, *off_k, *off_v;
     int *work_counter;  // in the workspace, zeroed by the plan kernel
     void *out;
     float *lse;
     int32_t *err;
 };
 
-// cu_q = exclusive prefix sum of the query lengths and cu_items = U x the
-// exclusive prefix sum of the 128-row query tiles (one warp, 32 requests at
-// a time); flags lengths above their maxima and requests with fewer keys
+// cu_q / cu_kv = exclusive prefix sums of the query / kv lengths and
+// cu_items = U x the exclusive prefix sum of the 128-row query tiles (one
+// warp, 32 requests at a time); flags lengths above their maxima and requests with fewer keys
 // than queries; zeroes the work-item counter.
 __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_t *__restrict__ lkv,
                                     int B, int U, int max_q, int max_kv, int32_t *__restrict__ cu_q,
-                                    int32_t *__restrict__ cu_items, int32_t *err, int *work_counter) {
+                                    int32_t *__restrict__ cu_items, int32_t *__restrict__ cu_kv,
+                                    int32_t *err, int *work_counter) {
     const int lane = threadIdx.x;
     pdl_launch_dependents();  // the main kernel may start its prologue meanwhile
-    int carry = 0, carry_t = 0;
+    int carry = 0, carry_t = 0, carry_k = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         int b = b0 + lane;
         int v = b < B ? lq[b] : 0;
@@ -105,26 +113,32 @@ __global__ void prefill_plan_kernel(const int32_t *__restrict__ lq, const int32_
         v = min(max(v, 0), max_q);
         if (b < B && min(lkv[b], max_kv) < v) set_err(err, PKV_DEV_ERR_QLEN);
         const int nt = (v + kPfRows - 1) / kPfRows;
-        int x = v, xt = nt;
+        const int vk = b < B ? min(max(lkv[b], 0), max_kv) : 0;
+        int x = v, xt = nt, xk = vk;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int y = __shfl_up_sync(0xffffffffu, x, o);
             int yt = __shfl_up_sync(0xffffffffu, xt, o);
+            int yk = __shfl_up_sync(0xffffffffu, xk, o);
             if (lane >= o) {
                 x += y;
                 xt += yt;
+                xk += yk;
             }
         }
         if (b < B) {
             cu_q[b] = carry + x - v;
             cu_items[b] = (carry_t + xt - nt) * U;
+            cu_kv[b] = carry_k + xk - vk;
         }
         carry += __shfl_sync(0xffffffffu, x, 31);
         carry_t += __shfl_sync(0xffffffffu, xt, 31);
+        carry_k += __shfl_sync(0xffffffffu, xk, 31);
     }
     if (lane == 0) {
         cu_q[B] = carry;
         cu_items[B] = carry_t * U;
+        cu_kv[B] = carry_k;
         *work_counter = 0;
     }
 }
@@ -185,7 +199,8 @@ __device__ __forceinline__ void tmem_wait_ld_regs16(uint32_t (&r)[16]) {
 // x-major with the (kv head, pair) units innermost, so every request hands
 // out its heaviest tiles first.
 struct PfItem {
-    int b, hA, hB, i0, row_base, kvh, shift, qb, kvb, n_tiles;
+    int b, hA, hB, i0, row_base, orow_base, kvh, shift, qb, kvb, n_tiles;
+    int kv_k, kv_v;  // first K / V row of the request (contiguous K/V)
 };
 
 __device__ __forceinline__ void pf_item(const PrefillParams &p, const int4 itm, int bn, PfItem &it) {
@@ -196,7 +211,12 @@ __device__ __forceinline__ void pf_item(const PrefillParams &p, const int4 itm, 
     it.kvb = min(max(p.seq_lens_kv[it.b], 0), p.max_kv);
     const int n_qt = (it.qb + kPfRows - 1) / kPfRows;
     it.i0 = (n_qt - 1 - itm.w) * kPfRows;
-    it.row_base = p.cu_q[it.b] + it.i0;
+    it.row_base = (p.off_q ? p.off_q[it.b] : p.cu_q[it.b]) + it.i0;
+    it.orow_base = (p.off_o ? p.off_o[it.b] : p.cu_q[it.b]) + it.i0;
+    if (p.contiguous) {
+        it.kv_k = p.off_k ? p.off_k[it.b] : p.cu_kv[it.b];
+        it.kv_v = p.off_v ? p.off_v[it.b] : p.cu_kv[it.b];
+    }
     it.kvh = it.hA / p.group;
     it.shift = it.kvb - it.qb;  // query i sits at position shift + i
     int k_hi = p.causal ? min(it.kvb, it.shift + it.i0 + kPfRows) : it.kvb;
@@ -341,7 +361,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             }
         }
         const int S = 1 << p.page_shift;
-        const int RB = pf_box_rows(S, BN);  // rows per TMA box
+        // rows per TMA box: a page or part of one; a whole tile for contiguous K/V
+        const int RB = p.contiguous ? BN : pf_box_rows(S, BN);
         const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
         const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
         const int NS = is_k ? SK : SV;
@@ -420,6 +441,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
                 const int key = j * BN + lane * RB;
                 int page = oob;
+                if (p.contiguous) return 0;  // one page: the whole tensor
                 if (lane < nbox && key < it.kvb) {
                     page = bt[key >> p.page_shift];
                     if (page < 0 || page >= p.max_num_pages) {
@@ -450,7 +472,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         for (int i = 0; i < 16; ++i) {
                             if (i >= nbox) break;
                             const int r0 = i * RB;
-                            const int slot0 = (j0 + r0) & (S - 1);
+                            const int slot0 = p.contiguous ? (is_k ? it.kv_k : it.kv_v) + j0 + r0
+                                                           : (j0 + r0) & (S - 1);
                             const int ca = LAYOUT == PKV_HND ? slot0 : it.kvh;
                             const int cb = LAYOUT == PKV_HND ? it.kvh : slot0;
                             if (is_k) {
@@ -793,8 +816,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             const float lt = l + lo;
             tc_fence_after();
             const int qi = it.i0 + r;
-            const int64_t grow = static_cast<int64_t>(it.row_base) + r;
-            const bool valid = qi < it.qb && grow < p.total_q;
+            const int64_t grow = static_cast<int64_t>(it.orow_base) + r;
+            const bool valid = qi < it.qb && grow >= 0 && grow < p.total_q;
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + hh * (kPfDV / SPLIT);
 #pragma unroll
@@ -894,10 +917,23 @@ static bool cache_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
     return encode_tmap(m, base, dt, 4, dims, strides, box);
 }
 
-// workspace: cu_q[B+1], cu_items[B+1], then the work-item counter of the
-// persistent kernel
+// Contiguous K or V ([rows, num_kv_heads, d], row stride in elements) as the
+// NHD map of a single page holding every row; a box is one 64-element d-atom
+// of `box_rows` consecutive rows of one kv head.
+static bool contiguous_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int d, int num_kv_heads,
+                            int64_t row_stride, int64_t rows, int box_rows) {
+    uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(num_kv_heads),
+                        static_cast<uint64_t>(rows > 0 ? rows : 1), 1};
+    uint64_t strides[3] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(row_stride) * 2,
+                           static_cast<uint64_t>(row_stride) * 2 * (rows > 0 ? rows : 1)};
+    uint32_t box[4] = {64, 1, static_cast<uint32_t>(box_rows), 1};
+    return encode_tmap(m, base, dt, 4, dims, strides, box);
+}
+
+// workspace: cu_q[B+1], cu_items[B+1], cu_kv[B+1], then the work-item
+// counter of the persistent kernel
 static size_t prefill_ws_bytes(int B) {
-    return 2 * round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256) + 256;
+    return 3 * round_up(static_cast<size_t>(B + 1) * sizeof(int32_t), 256) + 256;
 }
 
 }  // namespace pkv
@@ -912,7 +948,7 @@ extern "C" size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_q
     return prefill_ws_bytes(batch_size);
 }
 
-extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
+static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
                              const void *v_cache, int64_t k_page_stride, int64_t v_page_stride,
                              int64_t max_num_pages, float scale, void *workspace,
                              size_t workspace_bytes, int32_t max_token_per_sequence,
@@ -921,7 +957,16 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
                              int32_t block_table_stride, int32_t batch_size, int32_t causal,
                              int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
                              int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
-                             void *out, float *lse, int32_t *err_word, void *stream) {
+                             void *out, float *lse, int32_t *err_word, void *stream,
+                             const int32_t *off_q, const int32_t *off_o, const int32_t *off_k,
+                             const int32_t *off_v) {
+    // no block table: contiguous K/V of max_num_pages rows, page strides are row strides
+    const bool contiguous = block_tables == nullptr;
+    if (contiguous) {
+        if (layout != PKV_NHD) return PKV_ERR_INVALID_ARG;  // [rows, heads, d] is token-major
+        page_size = 1;
+        block_table_stride = max_sequence_kv;
+    }
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
     if (batch_size < 0 || num_qo_heads < 1 || num_kv_heads < 1 || max_token_per_sequence < 0 ||
@@ -929,7 +974,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
         return PKV_ERR_INVALID_ARG;
     if (num_qo_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
     if ((d_qk != 128 && d_qk != 192) || d_vo != 128) return PKV_ERR_UNSUPPORTED;
-    if (ilog2_exact(page_size) < 3 || page_size > 256) return PKV_ERR_UNSUPPORTED;
+    if (!contiguous && (ilog2_exact(page_size) < 3 || page_size > 256)) return PKV_ERR_UNSUPPORTED;
     if (batch_size > 65535 || num_qo_heads > 65535 || max_num_pages > 0x7fffffff ||
         total_q > 0x7fffffff)
         return PKV_ERR_UNSUPPORTED;
@@ -943,8 +988,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     if (static_cast<int64_t>((max_token_per_sequence + kPfRows - 1) / kPfRows) * num_qo_heads * batch_size >
         0x7fffffff - 65536)
         return PKV_ERR_UNSUPPORTED;
-    if (!q || !k_cache || !v_cache || !actual_seq_lens_q || !actual_seq_lens_kv || !block_tables ||
-        !out || !lse)
+    if (!q || !k_cache || !v_cache || !actual_seq_lens_q || !actual_seq_lens_kv || !out || !lse)
         return PKV_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (k_page_stride % 8) || (v_page_stride % 8))
@@ -967,20 +1011,26 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
         uint32_t box[3] = {64, 1, static_cast<uint32_t>(kPfRows)};
         if (!encode_tmap(&tq, q, tdt, 3, dims, strides, box)) return PKV_ERR_CUDA;
     }
-    if (!cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride,
-                    max_num_pages, rows) ||
-        !cache_tmap(&tv, v_cache, tdt, layout, d_vo, page_size, num_kv_heads, v_page_stride,
-                    max_num_pages, rows))
+    if (contiguous) {
+        if (!contiguous_tmap(&tk, k_cache, tdt, d_qk, num_kv_heads, k_page_stride, max_num_pages, bn) ||
+            !contiguous_tmap(&tv, v_cache, tdt, d_vo, num_kv_heads, v_page_stride, max_num_pages, bn))
+            return PKV_ERR_CUDA;
+    } else if (!cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride,
+                           max_num_pages, rows) ||
+               !cache_tmap(&tv, v_cache, tdt, layout, d_vo, page_size, num_kv_heads, v_page_stride,
+                           max_num_pages, rows)) {
         return PKV_ERR_CUDA;
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t cu_bytes = round_up(static_cast<size_t>(batch_size + 1) * sizeof(int32_t), 256);
     int32_t *cu_q = static_cast<int32_t *>(workspace);
     int32_t *cu_items = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + cu_bytes);
-    int *work_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) + 2 * cu_bytes);
+    int32_t *cu_kv = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + 2 * cu_bytes);
+    int *work_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) + 3 * cu_bytes);
     const int pairs = (num_qo_heads / num_kv_heads + 1) / 2;  // head pairs per kv head
     prefill_plan_kernel<<<1, 32, 0, st>>>(actual_seq_lens_q, actual_seq_lens_kv, batch_size, num_kv_heads * pairs,
-                                          max_token_per_sequence, max_sequence_kv, cu_q, cu_items, err_word,
+                                          max_token_per_sequence, max_sequence_kv, cu_q, cu_items, cu_kv, err_word,
                                           work_counter);
     PrefillParams p;
     p.max_num_pages = max_num_pages;
@@ -998,6 +1048,12 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     p.Hkv = num_kv_heads;
     p.group = num_qo_heads / num_kv_heads;
     p.pairs = pairs;
+    p.contiguous = contiguous ? 1 : 0;
+    p.cu_kv = cu_kv;
+    p.off_q = off_q;
+    p.off_o = off_o;
+    p.off_k = off_k;
+    p.off_v = off_v;
     p.page_shift = ilog2_exact(page_size);
     p.max_q = max_token_per_sequence;
     p.max_kv = max_sequence_kv;
@@ -1019,4 +1075,41 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
     }
     note_launches(launches);
     return launch_status();
+}
+
+extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
+                             const void *v_cache, int64_t k_page_stride, int64_t v_page_stride,
+                             int64_t max_num_pages, float scale, void *workspace,
+                             size_t workspace_bytes, int32_t max_token_per_sequence,
+                             int32_t max_sequence_kv, const int32_t *actual_seq_lens_q,
+                             const int32_t *actual_seq_lens_kv, const int32_t *block_tables,
+                             int32_t block_table_stride, int32_t batch_size, int32_t causal,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                             int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
+                             void *out, float *lse, int32_t *err_word, void *stream) {
+    return prefill_impl(q, total_q, k_cache, v_cache, k_page_stride, v_page_stride, max_num_pages, scale,
+                        workspace, workspace_bytes, max_token_per_sequence, max_sequence_kv, actual_seq_lens_q,
+                        actual_seq_lens_kv, block_tables, block_table_stride, batch_size, causal, num_qo_heads,
+                        num_kv_heads, d_qk, d_vo, page_size, layout, dtype, out, lse, err_word, stream, nullptr,
+                        nullptr, nullptr, nullptr);
+}
+
+extern "C" int paged_prefill_ex(const void *q, int64_t total_q, const void *k_cache,
+                                const void *v_cache, int64_t k_page_stride, int64_t v_page_stride,
+                                int64_t max_num_pages, float scale, void *workspace,
+                                size_t workspace_bytes, int32_t max_token_per_sequence,
+                                int32_t max_sequence_kv, const int32_t *actual_seq_lens_q,
+                                const int32_t *actual_seq_lens_kv, const int32_t *block_tables,
+                                int32_t block_table_stride, int32_t batch_size, int32_t causal,
+                                int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                                int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
+                                void *out, float *lse, const int32_t *batch_offsets_q,
+                                const int32_t *batch_offsets_o, const int32_t *batch_offsets_k,
+                                const int32_t *batch_offsets_v, int32_t *err_word, void *stream) {
+    if (block_tables && (batch_offsets_k || batch_offsets_v)) return PKV_ERR_INVALID_ARG;  // pages place K/V
+    return prefill_impl(q, total_q, k_cache, v_cache, k_page_stride, v_page_stride, max_num_pages, scale,
+                        workspace, workspace_bytes, max_token_per_sequence, max_sequence_kv, actual_seq_lens_q,
+                        actual_seq_lens_kv, block_tables, block_table_stride, batch_size, causal, num_qo_heads,
+                        num_kv_heads, d_qk, d_vo, page_size, layout, dtype, out, lse, err_word, stream,
+                        batch_offsets_q, batch_offsets_o, batch_offsets_k, batch_offsets_v);
 }

@@ -140,5 +140,6 @@ def test_prefill_rejects_bad_arguments(lib):
     assert call(ws_bytes=8) == 4
     assert call(bt_stride=3) == 2     # 3 pages of 32 < max_sequence_kv 200
     assert call(S=4) == 3             # TMA boxes need pages of >= 8 slots
+    assert call(bt=None, layout=1) == 2  # contiguous K/V is token-major: NHD only
     assert call(total_q=0) == 0       # no query rows: nothing to do
     assert call(B=0) == 0

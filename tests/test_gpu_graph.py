@@ -63,6 +63,7 @@ def test_graph_replay_matches_eager():
                          kv_layout="HND")
 
     outs = (pool, d_out, d_lse, v_out, v_lse, p_out, p_lse)
+    pool.zero_()  # the pool is allocated uninitialised: only appended slots are written
     step()
     torch.cuda.synchronize()
     eager = [t.clone() for t in outs]
@@ -83,5 +84,7 @@ def test_graph_replay_matches_eager():
         pool.zero_()
         g.replay()
         torch.cuda.synchronize()
-        for e, t in zip(eager, outs):
-            assert torch.equal(_bits(e), _bits(t))
+        names = ("append pool", "decode out", "decode lse", "varlen out", "varlen lse", "prefill out",
+                 "prefill lse")
+        bad = [n for n, e, t in zip(names, eager, outs) if not torch.equal(_bits(e), _bits(t))]
+        assert not bad, f"replay differs from eager: {bad}"

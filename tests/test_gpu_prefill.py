@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+import paged_kv_cache_316_gb300 as pk
 from paged_kv_cache_316_gb300 import workloads as wl
 from _gpu import (DEV, assert_attn_close, assert_lse_close, compact_request, err_word,
                   prefill_on_gpu)
@@ -100,3 +101,79 @@ def test_ragged_config_full_size_sampled(d_qk):
         ro, rl, _ = oracle_prefill(sub)
         assert_attn_close(out[cu[b]:cu[b + 1]], ro, f"request {b}")
         assert_lse_close(lse[cu[b]:cu[b + 1]], rl, f"request {b} lse")
+
+
+def _contiguous_kv(c):
+    """The case's keys and values packed request after request: [sum kv, Hkv, d]."""
+    ks, vs = [], []
+    for b in range(len(c.pt.lengths)):
+        k, v = wl.read_tokens(c.pool, c.pt, b)
+        ks.append(k)
+        vs.append(v)
+    return torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+
+
+@pytest.mark.parametrize("dqk", [128, 192])
+def test_contiguous_kv_matches_paged(dqk):
+    # block_tables = None: the same logical keys and values, packed
+    c = wl.prefill_case([130, 7, 300, 64], [400, 7, 300, 900], 32, 32, 8, dqk, 128, wl.HND, wl.BF16,
+                        seed=41, slack=0.2)
+    k, v = _contiguous_kv(c)
+    B = len(c.pt.lengths)
+    ws = torch.zeros(pk.paged_prefill_workspace_size(B, 32, c.max_q, c.max_kv), dtype=torch.uint8, device=DEV)
+    out, lse = pk.paged_prefill(c.q.to(DEV), k.to(DEV), v.to(DEV), c.scale, ws, c.max_q, c.max_kv,
+                                c.seq_lens_q.to(DEV), c.seq_lens_kv.to(DEV), None, causal=True)
+    torch.cuda.synchronize()
+    ro, rl, _ = oracle_prefill(c)
+    assert_attn_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_batch_offsets_place_rows():
+    # every request's queries, outputs, keys and values at shuffled row
+    # offsets with gaps between them (contiguous K/V)
+    ql, kvl = [130, 7, 300], [400, 7, 900]
+    c = wl.prefill_case(ql, kvl, 32, 16, 4, 128, 128, wl.HND, wl.BF16, seed=42, slack=0.2, causal=True)
+    k, v = _contiguous_kv(c)
+    g = torch.Generator().manual_seed(5)
+    B, H, Hk = 3, 16, 4
+
+    def scatter(lens, gap):
+        order = torch.randperm(B, generator=g).tolist()
+        offs, at = [0] * B, gap
+        for b in order:
+            offs[b] = at
+            at += lens[b] + gap
+        return offs, at
+
+    oq, nq = scatter(ql, 5)
+    oo, no = scatter(ql, 3)
+    ok_, nk = scatter(kvl, 17)
+    ov, nv = scatter(kvl, 2)
+    n_rows = max(nq, no)
+    cu_q = [0] + list(np.cumsum(ql))
+    cu_kv = [0] + list(np.cumsum(kvl))
+    qx = torch.zeros((n_rows, H, 128), dtype=c.q.dtype)
+    kx = torch.full((nk, Hk, 128), float("nan"), dtype=k.dtype)
+    vx = torch.full((nv, Hk, 128), float("nan"), dtype=v.dtype)
+    for b in range(B):
+        qx[oq[b]:oq[b] + ql[b]] = c.q[cu_q[b]:cu_q[b + 1]]
+        kx[ok_[b]:ok_[b] + kvl[b]] = k[cu_kv[b]:cu_kv[b + 1]]
+        vx[ov[b]:ov[b] + kvl[b]] = v[cu_kv[b]:cu_kv[b + 1]]
+    ws = torch.zeros(pk.paged_prefill_workspace_size(B, H, c.max_q, c.max_kv), dtype=torch.uint8, device=DEV)
+    out = torch.full((n_rows, H, 128), 3.0, dtype=c.q.dtype, device=DEV)
+    lse = torch.full((n_rows, H), 3.0, dtype=torch.float32, device=DEV)
+    offs = [torch.tensor(o, dtype=torch.int32, device=DEV) for o in (oq, oo, ok_, ov)]
+    pk.paged_prefill(qx.to(DEV), kx.to(DEV), vx.to(DEV), c.scale, ws, c.max_q, c.max_kv,
+                     c.seq_lens_q.to(DEV), c.seq_lens_kv.to(DEV), None, causal=True, out=out, lse=lse,
+                     batch_offsets_q=offs[0], batch_offsets_o=offs[1], batch_offsets_k=offs[2],
+                     batch_offsets_v=offs[3])
+    torch.cuda.synchronize()
+    ro, rl, _ = oracle_prefill(c)
+    written = torch.zeros(n_rows, dtype=torch.bool)
+    for b in range(B):
+        rows = slice(oo[b], oo[b] + ql[b])
+        assert_attn_close(out[rows], ro[cu_q[b]:cu_q[b + 1]], f"request {b}")
+        assert_lse_close(lse[rows], rl[cu_q[b]:cu_q[b + 1]], f"request {b} lse")
+        written[rows] = True
+    assert torch.all(out[~written.to(DEV)].float() == 3.0) and torch.all(lse[~written.to(DEV)] == 3.0)
