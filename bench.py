@@ -297,7 +297,7 @@ def make_parts(rank: int, dev):
 
 def make_next_parts(rank: int, dev):
     """Rows beyond the hot path's configurations, measured the same way but
-    outside the step: variable-length multi-token decode."""
+    outside the step: variable-length multi-token decode and non-paged prefill."""
     import paged_kv_cache_316_gb300 as pk
     from paged_kv_cache_316_gb300 import workloads as wl
     c = wl.long_decode_varlen(seed=rank_seed(rank), device=dev)
@@ -314,7 +314,28 @@ def make_next_parts(rank: int, dev):
         pk.paged_decode(c.query, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=c.bmm1_scale,
                         window_left=c.window_left, sinks=sinks, kv_layout=c.pool.layout,
                         cum_seq_lens_q=cum, max_q_len=c.q_len_per_req, out=out)
-    return [Part("decode_varlen", run, decode_bytes(c), "GB/s", "hbm", "decode.cu")]
+    parts = [Part("decode_varlen", run, decode_bytes(c), "GB/s", "hbm", "decode.cu")]
+
+    # the ragged prefill with contiguous (non-paged) K/V, d_qk 128
+    pc = wl.ragged_prefill(seed=rank_seed(rank), d_qk=128, device=dev)
+    ks, vs = [], []
+    for b in range(len(pc.pt.lengths)):
+        k, v = wl.read_tokens(pc.pool, pc.pt, b)
+        ks.append(k)
+        vs.append(v)
+    kc, vc = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+    pws = torch.zeros(pk.paged_prefill_workspace_size(16, 32, pc.max_q, pc.max_kv), dtype=torch.uint8,
+                      device=dev)
+    lq, lkv = pc.seq_lens_q.to(dev), pc.seq_lens_kv.to(dev)
+    pout = torch.empty((pc.q.shape[0], 32, 128), dtype=pc.q.dtype, device=dev)
+    plse = torch.empty((pc.q.shape[0], 32), dtype=torch.float32, device=dev)
+
+    def run_prefill():
+        pk.paged_prefill(pc.q, kc, vc, pc.scale, pws, pc.max_q, pc.max_kv, lq, lkv, None,
+                         causal=True, out=pout, lse=plse)
+    parts.append(Part("prefill_d128_contiguous", run_prefill, prefill_flops(pc), "TFLOP/s", "tensor",
+                      "prefill.cu"))
+    return parts
 
 
 def traffic_for(kernel_file: str, part: str):
@@ -494,7 +515,8 @@ def run_ours(args):
         "parts": out_parts, "roofline": roofline,
         "next_rows": dict(next_rows, note="outside the step and its ms_per_step: variable-length "
                                           "multi-token decode on the long-context shape (1..4 query "
-                                          "tokens per request)"),
+                                          "tokens per request); the ragged prefill (d_qk 128) with "
+                                          "contiguous, non-paged K/V"),
         "e2e": {"value": round(allreduce_sum(float(llama.work), ws, dev) / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
