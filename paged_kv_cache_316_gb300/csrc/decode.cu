@@ -474,7 +474,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     // Larger row groups write larger partials: scale the chunk with R so the
     // partial traffic stays a few percent of the K/V bytes; then shrink it
     // while the grid would leave SMs idle.
-    int chunk = 64 * pl.R;
+    int chunk = 128 * pl.R;
     chunk = chunk < 1024 ? 1024 : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
     chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
     const int64_t want = 2LL * num_sms();
