@@ -26,7 +26,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 NHD, HND = 0, 1
-FP16, BF16 = 0, 1
+FP16, BF16, E4M3 = 0, 1, 2  # E4M3: 8-bit cache elements (OCP FP8)
 E_PAGE, E_POS, E_BATCH, E_QLEN = 1, 2, 4, 8
 
 
@@ -73,9 +73,9 @@ def _i32(a) -> np.ndarray:
 def _check_pool(arr, page_stride: int, num_pages: int):
     """The C code addresses page p at p * page_stride elements from the
     array's first element: refuse views whose layout says otherwise."""
-    assert arr.dtype == np.uint16, "pass uint16 views of the pool"
+    assert arr.dtype in (np.uint16, np.uint8), "pass uint16 (or, for e4m3, uint8) views of the pool"
     assert arr.ndim >= 2 and arr.shape[0] >= num_pages, (arr.shape, num_pages)
-    assert arr.strides[0] == 2 * page_stride, (arr.strides, page_stride)
+    assert arr.strides[0] == arr.dtype.itemsize * page_stride, (arr.strides, page_stride)
     assert arr[0].size <= page_stride and arr[0].flags.c_contiguous, "pages must be contiguous"
 
 
@@ -108,9 +108,14 @@ def append(append_key, append_value, batch_indices, positions, k_cache, v_cache,
            kv_last_page_len, num_kv_heads: int, head_dim: int, page_size: int,
            layout: int) -> int:
     """Scatter in place into ``k_cache``/``v_cache`` (uint16 views of the
-    pool; for the 5-D pool these are two views into one buffer).  Returns the
-    error mask."""
-    ak, av = _u16(append_key), _u16(append_value)
+    pool, or uint8 for 8-bit elements; for the 5-D pool these are two views
+    into one buffer).  Returns the error mask."""
+    eb = k_cache.dtype.itemsize
+    if eb == 1:
+        ak = np.ascontiguousarray(append_key).view(np.uint8)
+        av = np.ascontiguousarray(append_value).view(np.uint8)
+    else:
+        ak, av = _u16(append_key), _u16(append_value)
     bi, pos = _i32(batch_indices), _i32(positions)
     ind, ptr, last = _i32(kv_indices), _i32(kv_indptr), _i32(kv_last_page_len)
     for c in (k_cache, v_cache):
@@ -120,14 +125,16 @@ def append(append_key, append_value, batch_indices, positions, k_cache, v_cache,
         ctypes.c_void_p(k_cache.ctypes.data), ctypes.c_void_p(v_cache.ctypes.data),
         ctypes.c_int64(page_stride), ctypes.c_int64(max_num_pages), _p(ind),
         _p(ptr), _p(last), ctypes.c_int(last.shape[0]), ctypes.c_int(num_kv_heads),
-        ctypes.c_int(head_dim), ctypes.c_int(page_size), ctypes.c_int(layout)))
+        ctypes.c_int(head_dim), ctypes.c_int(page_size), ctypes.c_int(layout),
+        ctypes.c_int(eb)))
 
 
 def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
            block_tables, seq_lens_, max_seq_len: int, bmm1_scale: float,
            bmm2_scale: float, window_left: int, sinks, q_len_per_req: int,
            num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
-           layout: int, dtype: int, threads: int | None = None, cum_seq_lens_q=None):
+           layout: int, dtype: int, threads: int | None = None, cum_seq_lens_q=None,
+           kv_dtype: int | None = None):
     """Returns (out [rows, Hqo, D] float64, lse [rows, Hqo] float64, err) with
     rows = B*Q, or cum_seq_lens_q[B] for variable-length queries (request b
     then has rows cum[b] .. cum[b+1]-1 and q_len_per_req is unused)."""
@@ -142,6 +149,7 @@ def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
     if cq is not None:
         assert cq.shape == (B + 1,) and cq[0] == 0 and np.all(np.diff(cq) >= 0)
     rows = B * q_len_per_req if cq is None else int(cq[-1])
+    kvd = dtype if kv_dtype is None else kv_dtype  # E4M3: uint8 views of the caches
     out = np.zeros((rows, num_qo_heads, head_dim), np.float64)
     lse = np.zeros((rows, num_qo_heads), np.float64)
     sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float32)
@@ -157,7 +165,7 @@ def decode(query, k_cache, v_cache, page_stride: int, max_num_pages: int,
         ctypes.c_int(window_left), _p(sk), ctypes.c_int(q_len_per_req), _p(cq),
         ctypes.c_int(num_qo_heads), ctypes.c_int(num_kv_heads),
         ctypes.c_int(head_dim), ctypes.c_int(page_size), ctypes.c_int(layout),
-        ctypes.c_int(dtype), _p(out), _p(lse), _p(scratch), ctypes.c_int(nthr),
+        ctypes.c_int(dtype), ctypes.c_int(kvd), _p(out), _p(lse), _p(scratch), ctypes.c_int(nthr),
         ctypes.c_int(nthr))
     return out, lse, int(err)
 
@@ -194,8 +202,9 @@ def prefill(q, k_cache, v_cache, k_page_stride: int, v_page_stride: int,
 
 
 def widen16(bits, dtype: int) -> np.ndarray:
-    """Exact float64 value of each 16-bit pattern (fp16 or bf16)."""
-    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    """Exact float64 value of each 16-bit pattern (fp16 or bf16), or of each
+    8-bit pattern for E4M3."""
+    b = np.ascontiguousarray(bits, dtype=np.uint8 if dtype == E4M3 else np.uint16)
     out = np.zeros(b.shape, np.float64)
     _load().orc_widen16(_p(b), ctypes.c_int64(b.size), ctypes.c_int(dtype), _p(out))
     return out

@@ -31,6 +31,7 @@
 
 #define ORC_FP16 0
 #define ORC_BF16 1
+#define ORC_E4M3 2 /* 8-bit float cache elements (OCP FP8 E4M3) */
 
 #define ORC_E_PAGE 1  /* physical page id outside [0, max_num_pages)       */
 #define ORC_E_POS 2   /* position / page slot outside the request's pages  */
@@ -64,9 +65,31 @@ static double orc_from_fp16(uint16_t bits)
     return sign ? -v : v;
 }
 
-static double orc_elem(const uint16_t *p, int64_t i, int dtype)
+static double orc_from_e4m3(uint8_t bits)
 {
-    return dtype == ORC_BF16 ? orc_from_bf16(p[i]) : orc_from_fp16(p[i]);
+    /* OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no
+     * infinities, exponent 15 with mantissa 7 is NaN, the largest normal is
+     * 1.75 * 2^8 = 448 */
+    int sign = (bits >> 7) & 1;
+    int expo = (bits >> 3) & 0xf;
+    int mant = bits & 0x7;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)mant, -9); /* subnormal: mant/8 * 2^-6 */
+    else if (expo == 15 && mant == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + mant), expo - 10); /* (1.m) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* element i of an array of 16-bit (fp16 / bf16) or 8-bit (e4m3) floats */
+static double orc_elem(const void *p, int64_t i, int dtype)
+{
+    if (dtype == ORC_E4M3)
+        return orc_from_e4m3(((const uint8_t *)p)[i]);
+    const uint16_t *h = (const uint16_t *)p;
+    return dtype == ORC_BF16 ? orc_from_bf16(h[i]) : orc_from_fp16(h[i]);
 }
 
 /* Element offset of (page, kv head, slot, d) inside one cache tensor
@@ -128,13 +151,13 @@ int orc_batch_indices_positions(const int32_t *append_indptr,
 /* Copy the bits of append_key[i] / append_value[i] into the page slot that
  * (batch_indices[i], positions[i]) addresses through kv_indptr/kv_indices.
  * Entries whose addressing is out of range are skipped and flagged. */
-int orc_append(const uint16_t *append_key, const uint16_t *append_value,
+int orc_append(const void *append_key, const void *append_value,
                int64_t nnz, const int32_t *batch_indices,
-               const int32_t *positions, uint16_t *k_cache, uint16_t *v_cache,
+               const int32_t *positions, void *k_cache, void *v_cache,
                int64_t page_stride, int64_t max_num_pages,
                const int32_t *kv_indices, const int32_t *kv_indptr,
                const int32_t *kv_last_page_len, int B, int num_kv_heads,
-               int head_dim, int page_size, int layout)
+               int head_dim, int page_size, int layout, int elem_bytes)
 {
     int err = 0;
     for (int64_t i = 0; i < nnz; ++i) {
@@ -161,8 +184,10 @@ int orc_append(const uint16_t *append_key, const uint16_t *append_value,
                 int64_t dst = orc_kv_offset(layout, page, page_stride, h, slot, d,
                                             num_kv_heads, page_size, head_dim);
                 int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim + d;
-                k_cache[dst] = append_key[src];
-                v_cache[dst] = append_value[src];
+                memcpy((char *)k_cache + dst * elem_bytes,
+                       (const char *)append_key + src * elem_bytes, elem_bytes);
+                memcpy((char *)v_cache + dst * elem_bytes,
+                       (const char *)append_value + src * elem_bytes, elem_bytes);
             }
     }
     return err;
@@ -175,8 +200,8 @@ int orc_append(const uint16_t *append_key, const uint16_t *append_value,
  * (+ e^{sink - M} when has_sink), M the largest term.  Keys are read through
  * the block table row `bt` of one request.  An empty key set without a sink
  * gives o = 0 and lse = -inf. */
-static int orc_attend_row(const uint16_t *q, int dtype, const uint16_t *k_cache,
-                          const uint16_t *v_cache, int64_t k_page_stride,
+static int orc_attend_row(const uint16_t *q, int dtype, const void *k_cache,
+                          const void *v_cache, int kv_dtype, int64_t k_page_stride,
                           int64_t v_page_stride, int64_t max_num_pages,
                           const int32_t *bt, int kvh, int num_kv_heads,
                           int page_size, int d_qk, int d_vo, int layout,
@@ -200,7 +225,7 @@ static int orc_attend_row(const uint16_t *q, int dtype, const uint16_t *k_cache,
         for (int d = 0; d < d_qk; ++d) {
             int64_t off = orc_kv_offset(layout, page, k_page_stride, kvh, slot, d,
                                         num_kv_heads, page_size, d_qk);
-            dot += orc_elem(q, d, dtype) * orc_elem(k_cache, off, dtype);
+            dot += orc_elem(q, d, dtype) * orc_elem(k_cache, off, kv_dtype);
         }
         s[jj] = scale * dot;
         if (s[jj] > m)
@@ -224,7 +249,7 @@ static int orc_attend_row(const uint16_t *q, int dtype, const uint16_t *k_cache,
         for (int d = 0; d < d_vo; ++d) {
             int64_t off = orc_kv_offset(layout, page, v_page_stride, kvh, slot, d,
                                         num_kv_heads, page_size, d_vo);
-            o[d] += w * orc_elem(v_cache, off, dtype);
+            o[d] += w * orc_elem(v_cache, off, kv_dtype);
         }
     }
     for (int d = 0; d < d_vo; ++d)
@@ -250,15 +275,15 @@ static int orc_attend_row(const uint16_t *q, int dtype, const uint16_t *k_cache,
  * NULL), rows = B*Q or cum_seq_lens_q[B].
  * scratch: caller buffer of at least max_seq_len doubles per thread slot
  * (threads * max_seq_len when OpenMP is used; pass n_scratch_threads). */
-int orc_decode(const uint16_t *query, const uint16_t *k_cache,
-               const uint16_t *v_cache, int64_t page_stride,
+int orc_decode(const uint16_t *query, const void *k_cache,
+               const void *v_cache, int64_t page_stride,
                int64_t max_num_pages, const int32_t *block_tables,
                int block_table_stride, const uint32_t *seq_lens, int B,
                int max_seq_len, double bmm1_scale, double bmm2_scale,
                int window_left, const float *sinks, int q_len_per_req,
                const int32_t *cum_seq_lens_q, int num_qo_heads,
                int num_kv_heads, int head_dim, int page_size, int layout,
-               int dtype, double *out, double *lse, double *scratch,
+               int dtype, int kv_dtype, double *out, double *lse, double *scratch,
                int n_scratch_threads, int num_threads)
 {
     int err = 0;
@@ -305,7 +330,7 @@ int orc_decode(const uint16_t *query, const uint16_t *k_cache,
         if (window_left >= 0 && p - window_left > 0)
             lo = p - window_left;
         double lse_r;
-        err |= orc_attend_row(query + r * head_dim, dtype, k_cache, v_cache,
+        err |= orc_attend_row(query + r * head_dim, dtype, k_cache, v_cache, kv_dtype,
                               page_stride, page_stride, max_num_pages,
                               block_tables + (int64_t)b * block_table_stride,
                               h / group, num_kv_heads, page_size, head_dim,
@@ -370,7 +395,7 @@ int orc_prefill(const uint16_t *q, const uint16_t *k_cache,
         int64_t pos = kvb - qb + i;
         int64_t hi = causal ? (pos < kvb - 1 ? pos : kvb - 1) : kvb - 1;
         double lse_r;
-        err |= orc_attend_row(q + r * d_qk, dtype, k_cache, v_cache,
+        err |= orc_attend_row(q + r * d_qk, dtype, k_cache, v_cache, dtype,
                               k_page_stride, v_page_stride, max_num_pages,
                               block_tables + (int64_t)b * block_table_stride,
                               h / group, num_kv_heads, page_size, d_qk, d_vo,
@@ -412,7 +437,7 @@ int orc_merge(const double *o_parts, const double *lse_parts, int n_parts,
 }
 
 /* Widen n 16-bit values (exposes the decoders above to the tests). */
-int orc_widen16(const uint16_t *src, int64_t n, int dtype, double *dst)
+int orc_widen16(const void *src, int64_t n, int dtype, double *dst)
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = orc_elem(src, i, dtype);

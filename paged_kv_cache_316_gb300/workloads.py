@@ -22,10 +22,10 @@ from dataclasses import dataclass, field
 import torch
 
 NHD, HND = 0, 1
-F16, BF16 = 0, 1
+F16, BF16, E4M3 = 0, 1, 2  # E4M3: 8-bit float cache elements
 POISON = 0x7FFFFFFF  # block-table padding that must never be read
 
-_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn}
 
 
 def torch_dtype(code: int) -> torch.dtype:
@@ -221,6 +221,7 @@ class DecodeCase:
     # variable-length queries: request b owns query rows cum[b] .. cum[b+1]-1
     # and q_len_per_req holds the largest length (max_q_len)
     cum_seq_lens_q: torch.Tensor | None = None
+    kv_dtype: int | None = None  # cache element type when it differs from dtype (E4M3)
 
 
 def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
@@ -229,7 +230,7 @@ def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
                 bmm1_scale: float | None = None, bmm2_scale: float = 1.0,
                 pool_pages: int | None = None, slack: float = 0.0, form: str = "5d",
                 device="cpu", bt_width: int | None = None, fill: str = "randn",
-                shuffle: bool = True, q_lens=None) -> DecodeCase:
+                shuffle: bool = True, q_lens=None, kv_dtype: int | None = None) -> DecodeCase:
     """Decode problem over freshly reserved pages.  q_lens (one entry per
     request) gives variable query lengths instead of q_len_per_req."""
     g = generator(seed)
@@ -238,8 +239,9 @@ def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
                        pool_pages=pool_pages)
     B = len(lengths)
     tdt = torch_dtype(dtype)
+    kdt = torch_dtype(dtype if kv_dtype is None else kv_dtype)
     pool = make_pool(pt.num_pages, num_kv_heads, page_size, head_dim, head_dim,
-                     layout, tdt, gd, form=form, device=device, fill=fill)
+                     layout, kdt, gd, form=form, device=device, fill=fill)
     cum = None
     if q_lens is not None:
         assert len(q_lens) == B
@@ -255,7 +257,7 @@ def decode_case(lengths, page_size: int, num_qo_heads: int, num_kv_heads: int,
                       torch.tensor(pt.lengths, dtype=torch.int32),
                       max(pt.lengths) if B else 0, bmm1_scale, bmm2_scale,
                       window_left, sinks, q_len_per_req, num_qo_heads,
-                      num_kv_heads, head_dim, dtype, cum)
+                      num_kv_heads, head_dim, dtype, cum, kv_dtype)
 
 
 @dataclass

@@ -10,8 +10,12 @@ from paged_kv_cache_316_gb300 import workloads as wl
 
 
 def u16(t: torch.Tensor) -> np.ndarray:
-    """uint16 numpy view of a 16-bit torch tensor on the CPU (shares memory)."""
-    assert t.element_size() == 2 and t.device.type == "cpu"
+    """uint16 numpy view of a 16-bit torch tensor on the CPU (shares memory);
+    uint8 for an 8-bit (e4m3) tensor."""
+    assert t.device.type == "cpu"
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy()
+    assert t.element_size() == 2
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
@@ -24,7 +28,8 @@ def oracle_decode(c: wl.DecodeCase, threads=None):
         None if c.sinks is None else c.sinks.numpy(), c.q_len_per_req,
         c.num_qo_heads, c.num_kv_heads, c.head_dim, p.page_size, p.layout,
         c.dtype, threads=threads,
-        cum_seq_lens_q=None if c.cum_seq_lens_q is None else c.cum_seq_lens_q.numpy())
+        cum_seq_lens_q=None if c.cum_seq_lens_q is None else c.cum_seq_lens_q.numpy(),
+        kv_dtype=c.kv_dtype)
 
 
 def oracle_prefill(c: wl.PrefillCase, threads=None):

@@ -43,8 +43,13 @@ MUTANTS = {
     "merge_weights_unnormalised": ("double w = exp(lse_parts[i] - total);",
                                    "double w = exp(lse_parts[i] - m);"),
     "append_slot_shifted": ("int slot = p % page_size;", "int slot = (p + 1) % page_size;"),
-    "value_row_from_key_cache": ("o[d] += w * orc_elem(v_cache, off, dtype);",
-                                 "o[d] += w * orc_elem(k_cache, off, dtype);"),
+    "e4m3_exponent_bias": ("v = ldexp((double)(8 + mant), expo - 10);",
+                           "v = ldexp((double)(8 + mant), expo - 9);"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)mant, -9);", "v = ldexp((double)mant, -10);"),
+    "append_copies_half_the_bytes": ("(const char *)append_key + src * elem_bytes, elem_bytes);",
+                                     "(const char *)append_key + src * elem_bytes, 1);"),
+    "value_row_from_key_cache": ("o[d] += w * orc_elem(v_cache, off, kv_dtype);",
+                                 "o[d] += w * orc_elem(k_cache, off, kv_dtype);"),
 }
 
 

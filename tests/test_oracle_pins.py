@@ -4,6 +4,7 @@ library attention routine (torch SDPA in float64) on special cases, and brute
 force on tiny shapes.  CPU only."""
 from __future__ import annotations
 
+import dataclasses
 import json
 import math
 import os
@@ -336,6 +337,46 @@ def test_decode_varlen_matches_prefill():
     po, pl, _ = oracle_prefill(p)
     np.testing.assert_allclose(out, po, rtol=0, atol=1e-15)
     np.testing.assert_allclose(lse, pl, rtol=0, atol=1e-14)
+
+
+def test_e4m3_codes_match_torch():
+    # every 8-bit pattern decodes to torch's float8_e4m3fn value (NaN codes too)
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.widen16(codes, oracle.E4M3)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert got[0x7e] == 448.0 and got[0x01] == 2.0 ** -9  # largest normal, smallest subnormal
+
+
+def test_decode_fp8_cache_equals_widened_cache():
+    # every e4m3 value is a bf16 value: decode over an e4m3 cache equals decode
+    # over the same values stored as bf16 (fp64 math on identical numbers)
+    c8 = _small_decode([9, 14, 5], kv_dtype=wl.E4M3, with_sinks=True, window_left=6)
+    wide = tuple(t.to(torch.bfloat16) for t in c8.pool.storage)
+    p16 = dataclasses.replace(c8.pool, storage=wide, k=wide[0][:, 0], v=wide[0][:, 1])
+    c16 = _replace(c8, pool=p16, kv_dtype=None)
+    a, b = oracle_decode(c8), oracle_decode(c16)
+    assert a[2] == 0
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_append_fp8_places_bytes():
+    # 8-bit elements: every appended byte lands at its page slot, nothing else moves
+    c = wl.append_case([3, 5], [2, 7], 4, 2, 16, wl.NHD, wl.E4M3, seed=7, slack=0.5)
+    before = c.pool.storage[0].clone()
+    sl = oracle.seq_lens(c.kv_indptr.numpy(), c.kv_last_page_len.numpy(), 4)
+    bi, pos = oracle.batch_indices_positions(c.append_indptr.numpy(), sl, c.append_key.shape[0])
+    assert oracle_append(c, bi, pos) == 0
+    for i in range(len(bi)):
+        b, p = int(bi[i]), int(pos[i])
+        page = int(c.kv_indices[int(c.kv_indptr[b]) + p // 4])
+        assert torch.equal(c.pool.k[page, p % 4].view(torch.uint8), c.append_key[i].view(torch.uint8))
+        assert torch.equal(c.pool.v[page, p % 4].view(torch.uint8), c.append_value[i].view(torch.uint8))
+    changed = (c.pool.storage[0].view(torch.uint8) != before.view(torch.uint8)).any(-1).any(-1)
+    assert int(changed.sum()) <= 2 * len(bi)
 
 
 def test_decode_split_merge_recombines():
