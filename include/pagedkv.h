@@ -28,7 +28,10 @@
  *    caller clears it.
  *  - 16-bit elements: dtype PKV_F16 (IEEE half) or PKV_BF16.  Attention
  *    accumulates in fp32 and rounds the output to nearest-even in the input
- *    dtype; LSE is fp32, natural log.
+ *    dtype; LSE is fp32, natural log.  An 8-bit (OCP FP8 E4M3) K/V cache:
+ *    PKV_E4M3 for paged_append, PKV_F16_E4M3 / PKV_BF16_E4M3 for decode (the
+ *    query and output stay 16-bit; the caller folds the K and V scales into
+ *    bmm1_scale / bmm2_scale, as the decode page's fused scales do).
  *  - Layouts (both pages list the same two):
  *      PKV_HND: a page is [num_kv_heads][page_size][head_dim];
  *      PKV_NHD: a page is [page_size][num_kv_heads][head_dim].
@@ -64,7 +67,13 @@ typedef enum pkv_status {
 } pkv_status;
 
 enum { PKV_NHD = 0, PKV_HND = 1 };
-enum { PKV_F16 = 0, PKV_BF16 = 1 };
+enum {
+    PKV_F16 = 0,
+    PKV_BF16 = 1,
+    PKV_E4M3 = 2,      /* 8-bit float (OCP FP8 E4M3) cache elements: paged_append   */
+    PKV_F16_E4M3 = 3,  /* decode: fp16 query/out over an E4M3 K/V cache            */
+    PKV_BF16_E4M3 = 4  /* decode: bf16 query/out over an E4M3 K/V cache            */
+};
 
 /* bits of the device error word */
 #define PKV_DEV_ERR_PAGE 1    /* physical page id outside [0, max_num_pages)        */
@@ -128,8 +137,10 @@ int paged_batch_indices_positions(const int32_t *append_indptr,
  * [0, seq_len(b)) -> PKV_DEV_ERR_POS; page outside [0, max_num_pages) ->
  * PKV_DEV_ERR_PAGE; the entry is skipped.  A copy that does not complete
  * within 1 s -> PKV_DEV_ERR_TIMEOUT.  Duplicate (b, p) pairs race.
- * Host errors: head_dim % 8 != 0 or page_size <= 0 -> PKV_ERR_INVALID_ARG;
- * head_dim > 4096 -> PKV_ERR_UNSUPPORTED.
+ * dtype: PKV_F16 / PKV_BF16 (2-byte elements) or PKV_E4M3 (1-byte).
+ * Host errors: a head row (head_dim elements) not a multiple of 16 bytes or
+ * page_size <= 0 -> PKV_ERR_INVALID_ARG; a head row above 8 KB ->
+ * PKV_ERR_UNSUPPORTED.
  */
 int paged_append(const void *append_key, const void *append_value, int64_t nnz,
                  const int32_t *batch_indices, const int32_t *positions,

@@ -14,7 +14,7 @@ import os
 import torch
 
 NHD, HND = 0, 1
-F16, BF16 = 0, 1
+F16, BF16, E4M3, F16_E4M3, BF16_E4M3 = 0, 1, 2, 3, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libpagedkv.so"
@@ -111,7 +111,22 @@ def _dtype_code(t: torch.Tensor) -> int:
         return F16
     if t.dtype == torch.bfloat16:
         return BF16
+    if t.dtype == torch.float8_e4m3fn:
+        return E4M3
     raise PagedKVError(f"unsupported element type {t.dtype}")
+
+
+def _decode_dtype(query: torch.Tensor, cache: torch.Tensor) -> int:
+    """Decode's dtype code: the query/output type, with an E4M3 cache when
+    the cache holds 8-bit floats."""
+    q = _dtype_code(query)
+    if q not in (F16, BF16):
+        raise PagedKVError(f"query must be fp16 or bf16, not {query.dtype}")
+    if cache.dtype == torch.float8_e4m3fn:
+        return F16_E4M3 if q == F16 else BF16_E4M3
+    if cache.dtype != query.dtype:
+        raise PagedKVError("the cache holds the query's type or e4m3")
+    return q
 
 
 def _layout_code(kv_layout) -> int:
@@ -213,7 +228,7 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
     has the query rows cum[b] .. cum[b+1]-1 (variable-length queries) and
     q_len_per_req is ignored."""
     layout = _layout_code(kv_layout)
-    kp, vp, stride, P, Hkv, S, D, _ = split_cache(kv_cache, layout)
+    kp, vp, stride, P, Hkv, S, D, base = split_cache(kv_cache, layout)
     rows, Hqo, Dq = query.shape
     if Dq != D:
         raise PagedKVError("query head_dim differs from the cache's")
@@ -228,7 +243,7 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
             workspace.numel() * workspace.element_size(), _ptr(block_tables),
             block_tables.stride(0), _ptr(seq_lens), B, max_seq_len, bmm1_scale,
             bmm2_scale, window_left, _ptr(sinks), int(max_q_len), _ptr(cum_seq_lens_q), Hqo,
-            Hkv, D, S, layout, _dtype_code(query), _ptr(out), _ptr(lse), _ptr(err_word),
+            Hkv, D, S, layout, _decode_dtype(query, base), _ptr(out), _ptr(lse), _ptr(err_word),
             _stream(stream)))
         return out
     _check(load_library().paged_decode(
@@ -236,7 +251,7 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
         workspace.numel() * workspace.element_size(), _ptr(block_tables),
         block_tables.stride(0), _ptr(seq_lens), B, max_seq_len, bmm1_scale,
         bmm2_scale, window_left, _ptr(sinks), q_len_per_req, Hqo, Hkv, D, S,
-        layout, _dtype_code(query), _ptr(out), _ptr(lse), _ptr(err_word),
+        layout, _decode_dtype(query, base), _ptr(out), _ptr(lse), _ptr(err_word),
         _stream(stream)))
     return out
 
@@ -251,7 +266,7 @@ def paged_decode_noalloc(query, kv_cache, block_tables, seq_lens, max_seq_len: i
     (PKV_NOALLOC_SCRATCH_BYTES) instead of a workspace tensor.  Calls that
     overlap on the GPU share that array and race."""
     layout = _layout_code(kv_layout)
-    kp, vp, stride, P, Hkv, S, D, _ = split_cache(kv_cache, layout)
+    kp, vp, stride, P, Hkv, S, D, base = split_cache(kv_cache, layout)
     rows, Hqo, Dq = query.shape
     if Dq != D:
         raise PagedKVError("query head_dim differs from the cache's")
@@ -261,7 +276,7 @@ def paged_decode_noalloc(query, kv_cache, block_tables, seq_lens, max_seq_len: i
     _check(load_library().paged_decode_noalloc(
         _ptr(query), kp, vp, stride, P, _ptr(block_tables), block_tables.stride(0),
         _ptr(seq_lens), B, max_seq_len, bmm1_scale, bmm2_scale, window_left, _ptr(sinks),
-        q_len_per_req, Hqo, Hkv, D, S, layout, _dtype_code(query), _ptr(out), _ptr(lse),
+        q_len_per_req, Hqo, Hkv, D, S, layout, _decode_dtype(query, base), _ptr(out), _ptr(lse),
         _ptr(err_word), _stream(stream)))
     return out
 

@@ -50,8 +50,9 @@ struct AppendParams {
     int64_t nnz;
     const int32_t *batch_indices;
     const int32_t *positions;
-    uint16_t *k_cache;
-    uint16_t *v_cache;
+    uint8_t *k_cache;
+    uint8_t *v_cache;
+    int esize;  // bytes per element: 2 (fp16 / bf16) or 1 (e4m3)
     int64_t page_stride;  // elements
     int64_t max_num_pages;
     const int32_t *kv_indices;
@@ -165,9 +166,9 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
         const uint32_t bar = smem_u32(&full[s]);
         if (lane == 0) {
             if (dst >= 0) {
-                const uint32_t bytes = static_cast<uint32_t>(nh) * p.D * 2;
+                const uint32_t bytes = static_cast<uint32_t>(nh) * p.D * p.esize;
                 mbar_expect_tx(bar, bytes);
-                const uint8_t *src = (row ? p.value : p.key) + (tok * row_elems + static_cast<int64_t>(h0) * p.D) * 2;
+                const uint8_t *src = (row ? p.value : p.key) + (tok * row_elems + static_cast<int64_t>(h0) * p.D) * p.esize;
                 bulk_load(ring_s + s * kApSlotBytes, src, bytes, bar);
             } else {
                 mbar_arrive(bar);  // nothing to copy: complete the phase
@@ -194,14 +195,15 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
                 set_err(p.err, PKV_DEV_ERR_TIMEOUT);
                 ok = false;
             } else if (dst >= 0) {
-                uint16_t *cache = row ? p.v_cache : p.k_cache;
+                uint8_t *cache = row ? p.v_cache : p.k_cache;
                 const uint32_t src = ring_s + s * kApSlotBytes;
-                const uint32_t hb = static_cast<uint32_t>(p.D) * 2;
+                const uint32_t hb = static_cast<uint32_t>(p.D) * p.esize;
                 if (LAYOUT == PKV_NHD) {
-                    bulk_store(cache + dst + static_cast<int64_t>(h0) * p.D, src, nh * hb);
+                    bulk_store(cache + (dst + static_cast<int64_t>(h0) * p.D) * p.esize, src, nh * hb);
                 } else {
                     for (int h = 0; h < nh; ++h)
-                        bulk_store(cache + dst + static_cast<int64_t>(h0 + h) * p.page_size * p.D, src + h * hb, hb);
+                        bulk_store(cache + (dst + static_cast<int64_t>(h0 + h) * p.page_size * p.D) * p.esize,
+                                   src + h * hb, hb);
                 }
             }
             bulk_commit();
@@ -259,12 +261,13 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
                             int32_t page_size, int32_t layout, int32_t dtype,
                             int32_t *err_word, void *stream) {
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
-    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_E4M3) return PKV_ERR_INVALID_ARG;
+    const int esize = dtype == PKV_E4M3 ? 1 : 2;  // bytes per element; bits are copied unchanged
     if (nnz < 0 || batch_size < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
         max_num_pages < 0 || page_stride <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (head_dim % 8) return PKV_ERR_INVALID_ARG;
-    if (head_dim * 2 > kApSlotBytes) return PKV_ERR_UNSUPPORTED;  // one head must fit a ring slot
+    if ((head_dim * esize) % 16) return PKV_ERR_INVALID_ARG;  // 16-byte head rows
+    if (head_dim * esize > kApSlotBytes) return PKV_ERR_UNSUPPORTED;  // one head must fit a ring slot
     if (page_stride < static_cast<int64_t>(num_kv_heads) * page_size * head_dim)
         return PKV_ERR_INVALID_ARG;
     if (nnz == 0) return PKV_OK;
@@ -272,7 +275,7 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
         !kv_indices || !kv_indptr || !kv_last_page_len)
         return PKV_ERR_NULL;
     if (!aligned16(append_key) || !aligned16(append_value) || !aligned16(k_cache) ||
-        !aligned16(v_cache) || (page_stride % 8))
+        !aligned16(v_cache) || ((page_stride * esize) % 16))
         return PKV_ERR_INVALID_ARG;
 
     AppendParams p;
@@ -281,8 +284,9 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
     p.nnz = nnz;
     p.batch_indices = batch_indices;
     p.positions = positions;
-    p.k_cache = static_cast<uint16_t *>(k_cache);
-    p.v_cache = static_cast<uint16_t *>(v_cache);
+    p.k_cache = static_cast<uint8_t *>(k_cache);
+    p.v_cache = static_cast<uint8_t *>(v_cache);
+    p.esize = esize;
     p.page_stride = page_stride;
     p.max_num_pages = max_num_pages;
     p.kv_indices = kv_indices;
@@ -292,7 +296,7 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
     p.H = num_kv_heads;
     p.D = head_dim;
     p.page_size = page_size;
-    p.heads_per_piece = head_dim * 2 >= kApSlotBytes ? 1 : min(num_kv_heads, kApSlotBytes / (head_dim * 2));
+    p.heads_per_piece = head_dim * esize >= kApSlotBytes ? 1 : min(num_kv_heads, kApSlotBytes / (head_dim * esize));
     p.pieces_per_row = (num_kv_heads + p.heads_per_piece - 1) / p.heads_per_piece;
     p.err = err_word;
     const int64_t ctas_max = static_cast<int64_t>(num_sms()) * kApCtasPerSm;

@@ -31,6 +31,32 @@ constexpr int kDecThreads = 128;
 constexpr int kDecRowBytes = kDecD * 2;           // one K or V row
 constexpr int kDecTileBytes = kDecTile * kDecRowBytes;
 constexpr int kDecStageBytes = 2 * kDecTileBytes; // K tile then V tile
+// An E4M3 cache is staged as 128-byte rows (K then V, 8 KB each per tile) and
+// widened once per tile into one 16-bit tile pair laid out as above.
+constexpr int kDec8RowBytes = kDecD;
+constexpr int kDec8TileBytes = kDecTile * kDec8RowBytes;
+template <bool KV8>
+struct DecSmem {
+    static constexpr int STAGE = KV8 ? 2 * kDec8TileBytes : kDecStageBytes;  // one ring stage
+    static constexpr int CONV = KV8 ? kDecStageBytes : 0;                    // the widened tile pair
+};
+
+// Two E4M3 values (low byte first) widened exactly to two 16-bit values.
+template <typename T>
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two);
+template <>
+__device__ __forceinline__ uint32_t widen_e4m3x2<__half>(uint32_t two) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h) : "h"(static_cast<unsigned short>(two)));
+    return h;
+}
+template <>
+__device__ __forceinline__ uint32_t widen_e4m3x2<__nv_bfloat16>(uint32_t two) {
+    // every E4M3 value is an fp16 and a bf16 value: through fp16 and fp32, exactly
+    const uint32_t h = widen_e4m3x2<__half>(two);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack2<__nv_bfloat16>(f.x, f.y);
+}
 constexpr int kDecMinPage = 8;                    // smallest supported page size
 constexpr int kDecMaxChunk = 4096;                // largest split (keys)
 constexpr int kDecMaxPages = kDecMaxChunk / kDecMinPage + 2;  // page ids one split can touch
@@ -90,15 +116,17 @@ __device__ __forceinline__ void store4(T *dst, float a, float b, float c, float 
     *reinterpret_cast<uint2 *>(dst) = v;
 }
 
-template <typename T, int MT, int LAYOUT>
+template <typename T, int MT, int LAYOUT, bool KV8>
 __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_kernel(const DecodeParams p) {
     constexpr int kDecStages = DecCfg<MT>::STAGES;
+    constexpr int STAGE_BYTES = DecSmem<KV8>::STAGE;
     constexpr int NKG = 4 / MT;          // warps that split the keys of a tile
     constexpr int KPW = kDecTile / NKG;  // keys per warp per tile
     constexpr int NT = KPW / 8;          // 8-key score tiles per warp
     constexpr int ROWS = 16 * MT;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *q_s = smem + kDecStages * kDecStageBytes;
+    uint8_t *conv = smem + kDecStages * STAGE_BYTES;  // widened E4M3 tile pair (KV8)
+    uint8_t *q_s = conv + DecSmem<KV8>::CONV;
     uint8_t *kvalid = q_s + ROWS * kDecRowBytes;
     float *comb_m = reinterpret_cast<float *>(kvalid + kDecStages * kDecTile);
     float *comb_l = comb_m + NKG * ROWS;
@@ -138,6 +166,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
 
     const T *kc = static_cast<const T *>(p.k);
     const T *vc = static_cast<const T *>(p.v);
+    const uint8_t *kc8 = static_cast<const uint8_t *>(p.k);  // E4M3 cache (KV8)
+    const uint8_t *vc8 = static_cast<const uint8_t *>(p.v);
     const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
     const int S = 1 << p.page_shift;
     if (tid == 0) any_bad = 0;
@@ -161,7 +191,33 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
     // end or on an out-of-range page are zero-filled and never read from
     // global memory; kvalid records which rows hold a key.
     auto load_tile = [&](int stage, int j0) {
-        const uint32_t dst = smem_u32(smem + stage * kDecStageBytes);
+        const uint32_t dst = smem_u32(smem + stage * STAGE_BYTES);
+        if constexpr (KV8) {
+            // 128-byte E4M3 rows: 8 consecutive lanes copy one row, unswizzled
+#pragma unroll
+            for (int k = 0; k < kDecTile * 8 / kDecThreads; ++k) {
+                const int idx = k * kDecThreads + tid;
+                const int r = idx >> 3, c = idx & 7;
+                const int j = j0 + r;
+                bool ok = j < k_end;
+                const uint8_t *ks = kc8, *vs = vc8;
+                if (ok) {
+                    const int page = pages_s[(j >> p.page_shift) - first_page];
+                    if (page < 0) {
+                        ok = false;
+                        any_bad = 1;
+                    } else {
+                        const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
+                                                                  S, kDecD) + c * 16;
+                        ks = kc8 + off;
+                        vs = vc8 + off;
+                    }
+                }
+                if (c == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
+                cp_async_16(dst + r * kDec8RowBytes + c * 16, ks, ok);
+                cp_async_16(dst + kDec8TileBytes + r * kDec8RowBytes + c * 16, vs, ok);
+            }
+        } else {
 #pragma unroll
         for (int k = 0; k < kDecTile * 16 / kDecThreads; ++k) {
             const int idx = k * kDecThreads + tid;
@@ -185,6 +241,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
             const uint32_t o = swz(r, c, kDecRowBytes);
             cp_async_16(dst + o, ks, ok);
             cp_async_16(dst + kDecTileBytes + o, vs, ok);
+        }
         }
     };
 
@@ -239,7 +296,32 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
         }
         const int stage = it % kDecStages;
         const int j0 = k_begin + it * kDecTile;
-        const uint32_t kb = smem_u32(smem + stage * kDecStageBytes);
+        uint32_t kb = smem_u32(smem + stage * STAGE_BYTES);
+        if constexpr (KV8) {
+            // widen the landed E4M3 tile pair into the 16-bit, swizzled layout
+            // the fragments are read from (the barrier above also ended every
+            // warp's reads of the previous widened tile)
+            const uint8_t *st8 = smem + stage * STAGE_BYTES;
+#pragma unroll
+            for (int k = 0; k < 2 * kDecTile * 8 / kDecThreads; ++k) {
+                const int idx = k * kDecThreads + tid;
+                const int kv = idx / (kDecTile * 8), rem = idx % (kDecTile * 8);
+                const int r = rem >> 3, c = rem & 7;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(st8 + kv * kDec8TileBytes + r * kDec8RowBytes + c * 16);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t h[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    h[2 * i] = widen_e4m3x2<T>(w[i] & 0xffffu);
+                    h[2 * i + 1] = widen_e4m3x2<T>(w[i] >> 16);
+                }
+                uint8_t *dt = conv + kv * kDecTileBytes;
+                *reinterpret_cast<uint4 *>(dt + swz(r, 2 * c, kDecRowBytes)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(dt + swz(r, 2 * c + 1, kDecRowBytes)) = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            __syncthreads();
+            kb = smem_u32(conv);
+        }
         const uint32_t vb = kb + kDecTileBytes;
 
         float sc[NT][4];
@@ -496,13 +578,13 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     return PKV_OK;
 }
 
-template <typename T, int MT, int LAYOUT>
+template <typename T, int MT, int LAYOUT, bool KV8>
 static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
     constexpr int kDecStages = DecCfg<MT>::STAGES;
-    const size_t smem = kDecStages * kDecStageBytes + ROWS * kDecRowBytes + kDecStages * kDecTile +
-                        2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
-    auto kern = decode_split_kernel<T, MT, LAYOUT>;
+    const size_t smem = kDecStages * DecSmem<KV8>::STAGE + DecSmem<KV8>::CONV + ROWS * kDecRowBytes +
+                        kDecStages * kDecTile + 2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
+    auto kern = decode_split_kernel<T, MT, LAYOUT, KV8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -510,18 +592,20 @@ static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
     return PKV_OK;
 }
 
-template <typename T, int LAYOUT>
+template <typename T, int LAYOUT, bool KV8>
 static int launch_split_mt(int MT, const DecodeParams &p, dim3 grid, cudaStream_t st) {
-    if (MT == 1) return launch_split<T, 1, LAYOUT>(p, grid, st);
-    if (MT == 2) return launch_split<T, 2, LAYOUT>(p, grid, st);
-    return launch_split<T, 4, LAYOUT>(p, grid, st);
+    if (MT == 1) return launch_split<T, 1, LAYOUT, KV8>(p, grid, st);
+    if (MT == 2) return launch_split<T, 2, LAYOUT, KV8>(p, grid, st);
+    return launch_split<T, 4, LAYOUT, KV8>(p, grid, st);
 }
 
 template <typename T>
-static int run_decode(const DecodeParams &p, const DecodePlan &pl, int layout, cudaStream_t st) {
+static int run_decode(const DecodeParams &p, const DecodePlan &pl, int layout, bool kv8, cudaStream_t st) {
     dim3 grid(pl.n_split_max, p.Hkv, p.B);
-    int rc = layout == PKV_HND ? launch_split_mt<T, PKV_HND>(pl.MT, p, grid, st)
-                               : launch_split_mt<T, PKV_NHD>(pl.MT, p, grid, st);
+    int rc = kv8 ? (layout == PKV_HND ? launch_split_mt<T, PKV_HND, true>(pl.MT, p, grid, st)
+                                      : launch_split_mt<T, PKV_NHD, true>(pl.MT, p, grid, st))
+                 : (layout == PKV_HND ? launch_split_mt<T, PKV_HND, false>(pl.MT, p, grid, st)
+                                      : launch_split_mt<T, PKV_NHD, false>(pl.MT, p, grid, st));
     if (rc != PKV_OK) return rc;
     int launches = 1;
     if (pl.n_split_max > 1) {
@@ -561,7 +645,10 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
                             int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
                             void *out, float *lse, int32_t *err_word, void *stream) {
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
-    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_F16_E4M3 && dtype != PKV_BF16_E4M3)
+        return PKV_ERR_INVALID_ARG;
+    const bool kv8 = dtype == PKV_F16_E4M3 || dtype == PKV_BF16_E4M3;  // 8-bit cache, 16-bit query/out
+    const bool bf16 = dtype == PKV_BF16 || dtype == PKV_BF16_E4M3;
     DecodePlan pl;
     int rc = plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
                          max_seq_len, page_size, window_left, pl);
@@ -572,7 +659,7 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
     if (batch_size == 0) return PKV_OK;
     if (!query || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_NULL;
     if (!aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-        (page_stride % 8))
+        (page_stride % (kv8 ? 16 : 8)))  // 16-byte page starts
         return PKV_ERR_INVALID_ARG;
     if (pl.ws_bytes > 0) {
         if (!workspace) return PKV_ERR_NULL;
@@ -611,8 +698,7 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
                            : nullptr;
     p.err = err_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return dtype == PKV_BF16 ? run_decode<__nv_bfloat16>(p, pl, layout, st)
-                             : run_decode<__half>(p, pl, layout, st);
+    return bf16 ? run_decode<__nv_bfloat16>(p, pl, layout, kv8, st) : run_decode<__half>(p, pl, layout, kv8, st);
 }
 
 extern "C" int paged_decode(const void *query, const void *k_cache, const void *v_cache,

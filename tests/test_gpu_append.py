@@ -143,3 +143,18 @@ def test_full_size_sweep_properties():
     expect = torch.zeros_like(changed)
     expect[page, :, slot] = True
     assert torch.equal(changed, expect)
+
+
+@pytest.mark.parametrize("layout", [wl.NHD, wl.HND])
+def test_fp8_append_bit_exact(layout):
+    # 8-bit (E4M3) cache elements are copied byte for byte
+    c = wl.append_sweep(64, seed=8, layout=layout)
+    c8 = wl.append_case([int(x) for x in (c.append_indptr[1:] - c.append_indptr[:-1])],
+                        [0] * 64, 16, 32, 128, layout, wl.E4M3, seed=8, slack=0.1)
+    seq, bi, pos = _gpu_helpers(c8)
+    got = _run_append(c8, bi, pos)
+    sl = oracle.seq_lens(c8.kv_indptr.numpy(), c8.kv_last_page_len.numpy(), 16)
+    obi, opos = oracle.batch_indices_positions(c8.append_indptr.numpy(), sl, c8.append_key.shape[0])
+    assert oracle_append(c8, obi, opos) == 0
+    for g, r in zip(got, c8.pool.storage):
+        assert torch.equal(g.view(torch.uint8), r.view(torch.uint8))

@@ -227,3 +227,30 @@ def test_long_context_varlen_full_size_sampled():
         ro, rl, _ = oracle_decode(sub)
         assert_attn_close(out[cum[b]:cum[b + 1]], ro, f"request {b}")
         assert_lse_close(lse[cum[b]:cum[b + 1]], rl, f"request {b} lse")
+
+
+FP8 = [
+    # lengths, page, Hqo, Hkv, Q, window, sinks, query dtype, layout, seed
+    ([700, 45, 1500], 16, 32, 8, 1, -1, False, wl.BF16, wl.HND, 51),     # 4 rows
+    ([2100, 777, 40], 64, 64, 8, 4, 300, True, wl.BF16, wl.NHD, 52),     # 32 rows
+    ([900, 130], 32, 16, 16, 1, -1, True, wl.F16, wl.HND, 53),           # MHA, fp16 query
+    ([1025, 64], 16, 32, 4, 8, 100, False, wl.BF16, wl.HND, 54),         # 64 rows
+]
+
+
+@pytest.mark.parametrize("case", FP8, ids=[f"f{i}" for i in range(len(FP8))])
+def test_fp8_cache(case):
+    # E4M3 K/V cache with 16-bit query and output; bmm scales fold the cache scales
+    L, S, hq, hk, Q, w, sk, dt, lay, seed = case
+    c = wl.decode_case(L, S, hq, hk, 128, lay, dt, q_len_per_req=Q, window_left=w, with_sinks=sk,
+                       seed=seed, kv_dtype=wl.E4M3, bmm1_scale=0.07, bmm2_scale=0.6, slack=0.2)
+    err = err_word()
+    _check(c, err_word=err)
+    assert int(err.item()) == 0
+
+
+def test_fp8_cache_full_size_sampled():
+    # the Llama-shaped decode over an E4M3 cache
+    c = wl.llama_decode(device=DEV, kv_dtype=wl.E4M3)
+    lengths = np.array(c.pt.lengths)
+    _sampled_full_size(c, sorted({int(lengths.argmin()), int(lengths.argmax()), 9, 40}))
