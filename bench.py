@@ -76,14 +76,14 @@ def decode_bytes(c) -> int:
         lo = max(0, L - Q - c.window_left) if c.window_left >= 0 else 0
         kv_tok += L - lo
         pages += (L + S - 1) // S - lo // S
-    row = c.num_kv_heads * c.head_dim * 2
+    row = c.num_kv_heads * c.head_dim * c.pool.k.element_size()  # 1 byte per E4M3 element
     qo = 2 * c.query.numel() * 2
     return kv_tok * row * 2 + qo + pages * 4 + len(c.pt.lengths) * 4
 
 
 def append_bytes(c) -> int:
     nnz, H, D = c.append_key.shape
-    return nnz * (2 * 2 * H * D * 2 + 8)
+    return nnz * (2 * 2 * H * D * c.append_key.element_size() + 8)
 
 
 def prefill_flops(c) -> int:
@@ -335,6 +335,30 @@ def make_next_parts(rank: int, dev):
                          causal=True, out=pout, lse=plse)
     parts.append(Part("prefill_d128_contiguous", run_prefill, prefill_flops(pc), "TFLOP/s", "tensor",
                       "prefill.cu"))
+
+    # the Llama-shaped decode over an E4M3 (FP8) cache
+    c8 = wl.llama_decode(seed=rank_seed(rank), device=dev, kv_dtype=wl.E4M3)
+    ws8 = torch.zeros(max(1, pk.paged_decode_workspace_size(
+        64, 1, 32, 8, 128, c8.max_seq_len, 16, -1)), dtype=torch.uint8, device=dev)
+    bt8, sl8 = c8.block_tables.to(dev), c8.seq_lens.to(dev)
+    out8 = torch.empty_like(c8.query)
+
+    def run_fp8():
+        pk.paged_decode(c8.query, c8.pool.storage[0], ws8, bt8, sl8, c8.max_seq_len,
+                        bmm1_scale=c8.bmm1_scale, kv_layout=c8.pool.layout, out=out8)
+    parts.append(Part("decode_llama_e4m3", run_fp8, decode_bytes(c8), "GB/s", "hbm", "decode.cu"))
+
+    # the append sweep point in E4M3
+    a8 = wl.append_sweep(4096, seed=1 + rank_seed(rank), layout=wl.NHD, device=dev, fill="empty",
+                         dtype=wl.E4M3)
+    kvi8, kvp8, last8 = (x.to(dev) for x in (a8.kv_indices, a8.kv_indptr, a8.kv_last_page_len))
+    seq8 = pk.paged_seq_lens(kvp8, last8, 16)
+    bi8, pos8 = pk.paged_batch_indices_positions(a8.append_indptr.to(dev), seq8, a8.append_key.shape[0])
+    pool8 = a8.pool.storage[0]
+
+    def run_append8():
+        pk.paged_append(a8.append_key, a8.append_value, bi8, pos8, pool8, kvi8, kvp8, last8, kv_layout="NHD")
+    parts.append(Part("append_e4m3", run_append8, append_bytes(a8), "GB/s", "hbm", "append.cu"))
     return parts
 
 
@@ -516,7 +540,8 @@ def run_ours(args):
         "next_rows": dict(next_rows, note="outside the step and its ms_per_step: variable-length "
                                           "multi-token decode on the long-context shape (1..4 query "
                                           "tokens per request); the ragged prefill (d_qk 128) with "
-                                          "contiguous, non-paged K/V"),
+                                          "contiguous, non-paged K/V; the Llama-shaped decode and the "
+                                          "4096-request append over an E4M3 (FP8) cache"),
         "e2e": {"value": round(allreduce_sum(float(llama.work), ws, dev) / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),

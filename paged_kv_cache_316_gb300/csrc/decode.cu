@@ -14,15 +14,19 @@
 // from HBM feeds every query row that needs it.
 #include <math.h>
 
+#include <type_traits>
+
 #include "pkv_common.cuh"
 
 namespace pkv {
 
 constexpr int kDecD = 128;                        // head_dim
 constexpr int kDecTile = 64;                      // keys per pipeline stage
-// One row tile (up to 16 packed query rows): 3 CTAs per SM with a 2-stage
-// ring; more row tiles need more registers: 2 CTAs per SM, 3 stages.
-template <int MT>
+// Ring depth and CTAs per SM.  One row tile (up to 16 packed query rows): 3
+// CTAs per SM with a 2-stage ring; more row tiles need more registers: 2
+// CTAs per SM, 3 stages (the same for an E4M3 cache: a deeper ring with
+// fewer CTAs measured slower there).
+template <int MT, bool KV8 = false>
 struct DecCfg {
     static constexpr int STAGES = MT == 1 ? 2 : 3;
     static constexpr int CTAS = MT == 1 ? 3 : 2;
@@ -41,7 +45,8 @@ struct DecSmem {
     static constexpr int CONV = KV8 ? kDecStageBytes : 0;                    // the widened tile pair
 };
 
-// Two E4M3 values (low byte first) widened exactly to two 16-bit values.
+// Two E4M3 values (low byte first) widened exactly to fp16 (every E4M3
+// value is an fp16 value).
 template <typename T>
 __device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two);
 template <>
@@ -50,12 +55,8 @@ __device__ __forceinline__ uint32_t widen_e4m3x2<__half>(uint32_t two) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h) : "h"(static_cast<unsigned short>(two)));
     return h;
 }
-template <>
-__device__ __forceinline__ uint32_t widen_e4m3x2<__nv_bfloat16>(uint32_t two) {
-    // every E4M3 value is an fp16 and a bf16 value: through fp16 and fp32, exactly
-    const uint32_t h = widen_e4m3x2<__half>(two);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    return pack2<__nv_bfloat16>(f.x, f.y);
+__device__ __forceinline__ float2 unpack2_bf16(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
 }
 constexpr int kDecMinPage = 8;                    // smallest supported page size
 constexpr int kDecMaxChunk = 4096;                // largest split (keys)
@@ -117,9 +118,13 @@ __device__ __forceinline__ void store4(T *dst, float a, float b, float c, float 
 }
 
 template <typename T, int MT, int LAYOUT, bool KV8>
-__global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_kernel(const DecodeParams p) {
-    constexpr int kDecStages = DecCfg<MT>::STAGES;
+__global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_split_kernel(const DecodeParams p) {
+    constexpr int kDecStages = DecCfg<MT, KV8>::STAGES;
     constexpr int STAGE_BYTES = DecSmem<KV8>::STAGE;
+    // the MMA element type: over an E4M3 cache always fp16 (E4M3 widens to
+    // fp16 in one instruction; a bf16 query is brought to fp16 exactly, see
+    // below)
+    using TM = typename std::conditional<KV8, __half, T>::type;
     constexpr int NKG = 4 / MT;          // warps that split the keys of a tile
     constexpr int KPW = kDecTile / NKG;  // keys per warp per tile
     constexpr int NT = KPW / 8;          // 8-key score tiles per warp
@@ -266,6 +271,53 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
     cp_async_wait<kDecStages - 1>();
     __syncthreads();
 
+    float scale_log2 = p.scale_log2;
+    if constexpr (KV8 && !std::is_same<T, __half>::value) {
+        // bf16 query -> fp16 for the fp16 MMAs: scaled by 2^e so that the
+        // largest |q| of the CTA lies in [2^14, 2^15) -- every bf16 value of
+        // the rows then converts exactly unless it falls below fp16's normal
+        // range, 2^29 under that largest element -- with 2^-e moved into the
+        // logit scale (powers of two, exact)
+        __shared__ float qmax_s[kDecThreads / 32];
+        float mx = 0.f;
+        for (int idx = tid; idx < ROWS * 16; idx += kDecThreads) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(q_s + swz(idx >> 4, idx & 15, kDecRowBytes));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = unpack2_bf16(w[i]);
+                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) qmax_s[warp] = mx;
+        __syncthreads();
+        mx = fmaxf(fmaxf(qmax_s[0], qmax_s[1]), fmaxf(qmax_s[2], qmax_s[3]));
+        int e = 0;
+        if (mx > 0.f && isfinite(mx)) {
+            int ex;
+            frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
+            e = min(max(15 - ex, -100), 100);  // (beyond that the row is all but zero)
+        }
+        const float up = ldexpf(1.f, e);
+        scale_log2 = ldexpf(scale_log2, -e);
+        __syncthreads();  // every warp has its max before the tile is rewritten
+        for (int idx = tid; idx < ROWS * 16; idx += kDecThreads) {
+            uint4 *a = reinterpret_cast<uint4 *>(q_s + swz(idx >> 4, idx & 15, kDecRowBytes));
+            const uint4 v = *a;
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = unpack2_bf16(w[i]);
+                h[i] = pack2<__half>(f.x * up, f.y * up);
+            }
+            *a = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        __syncthreads();
+    }
+
     uint32_t qa[8][4];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
@@ -312,8 +364,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
                 uint32_t h[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    h[2 * i] = widen_e4m3x2<T>(w[i] & 0xffffu);
-                    h[2 * i + 1] = widen_e4m3x2<T>(w[i] >> 16);
+                    h[2 * i] = widen_e4m3x2<TM>(w[i] & 0xffffu);
+                    h[2 * i + 1] = widen_e4m3x2<TM>(w[i] >> 16);
                 }
                 uint8_t *dt = conv + kv * kDecTileBytes;
                 *reinterpret_cast<uint4 *>(dt + swz(r, 2 * c, kDecRowBytes)) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -334,8 +386,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
                 uint32_t bf[4];
                 int key = kw0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
                 ldsm_x4(bf, kb + swz(key, 2 * kk + ((lane >> 3) & 1), kDecRowBytes));
-                mma16816<T>(sc[2 * np], qa[kk], bf[0], bf[1]);
-                mma16816<T>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
+                mma16816<TM>(sc[2 * np], qa[kk], bf[0], bf[1]);
+                mma16816<TM>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
             }
         }
 
@@ -344,7 +396,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float x = sc[nt][e] * p.scale_log2;
+                float x = sc[nt][e] * scale_log2;
                 if (!interior) {
                     int jj = kw0 + nt * 8 + 2 * (lane & 3) + (e & 1);
                     int j = j0 + jj;
@@ -393,17 +445,17 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT>::CTAS) decode_split_ke
 #pragma unroll
         for (int ks = 0; ks < NT / 2; ++ks) {
             uint32_t a[4];
-            a[0] = pack2<T>(sc[2 * ks][0], sc[2 * ks][1]);
-            a[1] = pack2<T>(sc[2 * ks][2], sc[2 * ks][3]);
-            a[2] = pack2<T>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-            a[3] = pack2<T>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+            a[0] = pack2<TM>(sc[2 * ks][0], sc[2 * ks][1]);
+            a[1] = pack2<TM>(sc[2 * ks][2], sc[2 * ks][3]);
+            a[2] = pack2<TM>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+            a[3] = pack2<TM>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
             const int key = kw0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
             for (int dp = 0; dp < 8; ++dp) {
                 uint32_t vf[4];
                 ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), kDecRowBytes));
-                mma16816<T>(o[2 * dp], a, vf[0], vf[1]);
-                mma16816<T>(o[2 * dp + 1], a, vf[2], vf[3]);
+                mma16816<TM>(o[2 * dp], a, vf[0], vf[1]);
+                mma16816<TM>(o[2 * dp + 1], a, vf[2], vf[3]);
             }
         }
     }
@@ -581,7 +633,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
 template <typename T, int MT, int LAYOUT, bool KV8>
 static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
-    constexpr int kDecStages = DecCfg<MT>::STAGES;
+    constexpr int kDecStages = DecCfg<MT, KV8>::STAGES;
     const size_t smem = kDecStages * DecSmem<KV8>::STAGE + DecSmem<KV8>::CONV + ROWS * kDecRowBytes +
                         kDecStages * kDecTile + 2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
     auto kern = decode_split_kernel<T, MT, LAYOUT, KV8>;

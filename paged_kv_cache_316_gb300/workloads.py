@@ -416,14 +416,14 @@ def append_example(layout: int = NHD, form: str = "5d", seed: int = 0,
 
 
 def append_sweep(batch: int, seed: int = 1, layout: int = NHD, one_token: bool = False,
-                 device="cpu", **kw) -> AppendCase:
+                 device="cpu", dtype: int = F16, **kw) -> AppendCase:
     """Seeded append sweep point: ``batch`` requests with a cached prefix
     uniform in [0, 256] appending uniform [1, 128] tokens (or exactly one),
     32 kv heads, head_dim 128, page_size 16, fp16, pool = pages + 10%."""
     g = generator(seed)
     prefix = uniform_lengths(g, batch, 0, 256)
     app = [1] * batch if one_token else uniform_lengths(g, batch, 1, 128)
-    return append_case(app, prefix, 16, 32, 128, layout, F16, seed=seed,
+    return append_case(app, prefix, 16, 32, 128, layout, dtype, seed=seed,
                        slack=0.1, device=device, **kw)
 
 
