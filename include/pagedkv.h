@@ -234,6 +234,37 @@ int paged_decode_varlen(const void *query, int64_t num_tokens, const void *k_cac
                         int32_t *err_word, void *stream);
 
 /*
+ * paged_decode_ex -- [decode] with the two remaining options of the page's
+ * decode call: bmm1_scale / bmm2_scale given as float32 device tensors, and
+ * enable_pdl.
+ *  - bmm1_scale_dev / bmm2_scale_dev: NULL, or a device pointer to one fp32
+ *    value that replaces the host bmm1_scale / bmm2_scale.  The kernels read
+ *    it when they run (not when the call is made), so a CUDA graph captured
+ *    once follows later writes to that value; the caller keeps it alive until
+ *    the call's kernels finish.
+ *  - enable_pdl != 0: the first kernel of the call is launched as a
+ *    programmatic dependent of the stream's previous kernel (the page's
+ *    programmatic dependent launch); it starts its prologue early and waits
+ *    for that kernel's memory before touching any input.  0: an ordinary
+ *    launch.  Results are identical either way.
+ *  - cum_seq_lens_q NULL: uniform queries, max_q_len tokens per request
+ *    (paged_decode with q_len_per_req = max_q_len; num_tokens must be at
+ *    least batch_size * max_q_len).  Otherwise as paged_decode_varlen.
+ * Everything else, including errors, is as paged_decode_varlen.
+ */
+int paged_decode_ex(const void *query, int64_t num_tokens, const void *k_cache,
+                    const void *v_cache, int64_t page_stride, int64_t max_num_pages,
+                    void *workspace, size_t workspace_bytes,
+                    const int32_t *block_tables, int32_t block_table_stride,
+                    const uint32_t *seq_lens, int32_t batch_size, int32_t max_seq_len,
+                    float bmm1_scale, float bmm2_scale, const float *bmm1_scale_dev,
+                    const float *bmm2_scale_dev, int32_t window_left, const float *sinks,
+                    int32_t max_q_len, const int32_t *cum_seq_lens_q,
+                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, int32_t layout, int32_t dtype, int32_t enable_pdl,
+                    void *out, float *lse, int32_t *err_word, void *stream);
+
+/*
  * paged_decode_noalloc -- paged_decode without a caller workspace.  The API
  * pages have no counterpart: this entry point exists for callers that cannot
  * allocate device memory where they call decode (a plugin inside another

@@ -42,6 +42,9 @@ _SIGNATURES = {
     "paged_decode_varlen": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _c_p, _sz, _c_p, _i32, _c_p,
                              _i32, _i32, _f32, _f32, _i32, _c_p, _i32, _c_p, _i32, _i32, _i32,
                              _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
+    "paged_decode_ex": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _c_p, _sz, _c_p, _i32, _c_p,
+                         _i32, _i32, _f32, _f32, _c_p, _c_p, _i32, _c_p, _i32, _c_p, _i32, _i32,
+                         _i32, _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
     "paged_decode_noalloc": ([_c_p, _c_p, _c_p, _i64, _i64, _c_p, _i32, _c_p, _i32, _i32,
                               _f32, _f32, _i32, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
                               _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
@@ -212,6 +215,16 @@ def paged_append(append_key, append_value, batch_indices, positions, paged_kv_ca
 
 # ---- decode -------------------------------------------------------------------------------
 
+def _scale_arg(scale, device):
+    """A host float -> (value, NULL); a one-element float32 tensor on the
+    query's device -> (1.0, its address)."""
+    if isinstance(scale, torch.Tensor):
+        if scale.dtype != torch.float32 or scale.numel() != 1 or scale.device != device:
+            raise PagedKVError("a tensor scale is one float32 value on the query's device")
+        return 1.0, _ptr(scale)
+    return float(scale), None
+
+
 def paged_decode_workspace_size(batch_size, q_len_per_req, num_qo_heads, num_kv_heads,
                                 head_dim, max_seq_len, page_size, window_left=-1) -> int:
     return int(load_library().paged_decode_workspace_size(
@@ -222,11 +235,15 @@ def paged_decode_workspace_size(batch_size, q_len_per_req, num_qo_heads, num_kv_
 def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len: int,
                  bmm1_scale: float = 1.0, bmm2_scale: float = 1.0, window_left: int = -1,
                  sinks=None, kv_layout="HND", q_len_per_req: int = 1, out=None,
-                 lse=None, err_word=None, stream=None, max_q_len=None, cum_seq_lens_q=None):
+                 lse=None, err_word=None, stream=None, max_q_len=None, cum_seq_lens_q=None,
+                 enable_pdl=None):
     """seq_lens: int32 (or uint32) tensor holding the unsigned kv lengths.
     With cum_seq_lens_q ([B+1] int32 on the device) and max_q_len, request b
     has the query rows cum[b] .. cum[b+1]-1 (variable-length queries) and
-    q_len_per_req is ignored."""
+    q_len_per_req is ignored.  bmm1_scale / bmm2_scale may be one-element
+    float32 device tensors, read when the kernels run; enable_pdl launches
+    the call's first kernel as a programmatic dependent of the stream's
+    previous kernel (None / False: an ordinary launch)."""
     layout = _layout_code(kv_layout)
     kp, vp, stride, P, Hkv, S, D, base = split_cache(kv_cache, layout)
     rows, Hqo, Dq = query.shape
@@ -237,6 +254,18 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
         out = torch.empty_like(query)
     if (cum_seq_lens_q is None) != (max_q_len is None):
         raise PagedKVError("cum_seq_lens_q and max_q_len go together")
+    s1, s1_dev = _scale_arg(bmm1_scale, query.device)
+    s2, s2_dev = _scale_arg(bmm2_scale, query.device)
+    if s1_dev or s2_dev or enable_pdl:
+        mq = int(max_q_len) if cum_seq_lens_q is not None else q_len_per_req
+        _check(load_library().paged_decode_ex(
+            _ptr(query), rows, kp, vp, stride, P, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(block_tables),
+            block_tables.stride(0), _ptr(seq_lens), B, max_seq_len, s1, s2, s1_dev, s2_dev,
+            window_left, _ptr(sinks), mq, _ptr(cum_seq_lens_q), Hqo, Hkv, D, S, layout,
+            _decode_dtype(query, base), 1 if enable_pdl else 0, _ptr(out), _ptr(lse),
+            _ptr(err_word), _stream(stream)))
+        return out
     if cum_seq_lens_q is not None:
         _check(load_library().paged_decode_varlen(
             _ptr(query), rows, kp, vp, stride, P, _ptr(workspace),

@@ -74,6 +74,9 @@ struct DecodeParams {
     int B;
     int max_seq_len;
     float scale_log2;  // bmm1_scale * log2(e): logits in base-2 units
+    // device-resident fp32 bmm1 / bmm2 scales (NULL: the host values), read
+    // when the kernels run, so a captured graph follows their current value
+    const float *bmm1_dev, *bmm2_dev;
     float bmm2;
     int window_left;
     const float *sinks;
@@ -138,6 +141,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     int *pages_s = reinterpret_cast<int *>(comb_l + NKG * ROWS);  // the split's page ids
     __shared__ int any_bad;
 
+    // launched as a dependent of the stream's previous kernel (enable_pdl):
+    // wait for it before reading anything it may have written
+    pdl_wait();
     const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = warp % MT, kg = warp / MT;
@@ -271,7 +277,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     cp_async_wait<kDecStages - 1>();
     __syncthreads();
 
-    float scale_log2 = p.scale_log2;
+    float scale_log2 = p.bmm1_dev ? __ldg(p.bmm1_dev) * kLog2e : p.scale_log2;
+    const float bmm2 = p.bmm2_dev ? __ldg(p.bmm2_dev) : p.bmm2;
     if constexpr (KV8 && !std::is_same<T, __half>::value) {
         // bf16 query -> fp16 for the fp16 MMAs: scaled by 2^e so that the
         // largest |q| of the CTA lies in [2^14, 2^15) -- every bf16 value of
@@ -508,10 +515,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                 const float Mf = fmaxf(M, sk);
                 const float wk = fast_exp2(M - Mf);
                 const float den = lsum * wk + fast_exp2(sk - Mf);
-                sc_o = p.bmm2 * wk / den;
+                sc_o = bmm2 * wk / den;
                 lse_v = (Mf + fast_log2(den)) * kLn2;
             } else if (lsum > 0.f) {
-                sc_o = p.bmm2 / lsum;
+                sc_o = bmm2 / lsum;
                 lse_v = (M + fast_log2(lsum)) * kLn2;
             } else {
                 sc_o = 0.f;
@@ -577,7 +584,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
         }
         if (p.sinks) den += fast_exp2(p.sinks[h] * kLog2e - M);
     }
-    const float sc = den > 0.f ? p.bmm2 / den : 0.f;
+    const float bmm2 = p.bmm2_dev ? __ldg(p.bmm2_dev) : p.bmm2;
+    const float sc = den > 0.f ? bmm2 / den : 0.f;
     const int64_t orow = (qrow0 + t) * p.Hqo + h;
     store4(static_cast<T *>(p.out) + orow * kDecD + d, acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
     if (p.lse && lane == 0) p.lse[orow] = den > 0.f ? (M + fast_log2(den)) * kLn2 : -INFINITY;
@@ -631,7 +639,7 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
 }
 
 template <typename T, int MT, int LAYOUT, bool KV8>
-static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
+static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
     constexpr int kDecStages = DecCfg<MT, KV8>::STAGES;
     const size_t smem = kDecStages * DecSmem<KV8>::STAGE + DecSmem<KV8>::CONV + ROWS * kDecRowBytes +
@@ -640,24 +648,26 @@ static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
+    if (pdl) return launch_dependent(kern, grid, dim3(kDecThreads), smem, st, p) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
     kern<<<grid, kDecThreads, smem, st>>>(p);
     return PKV_OK;
 }
 
 template <typename T, int LAYOUT, bool KV8>
-static int launch_split_mt(int MT, const DecodeParams &p, dim3 grid, cudaStream_t st) {
-    if (MT == 1) return launch_split<T, 1, LAYOUT, KV8>(p, grid, st);
-    if (MT == 2) return launch_split<T, 2, LAYOUT, KV8>(p, grid, st);
-    return launch_split<T, 4, LAYOUT, KV8>(p, grid, st);
+static int launch_split_mt(int MT, const DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
+    if (MT == 1) return launch_split<T, 1, LAYOUT, KV8>(p, grid, st, pdl);
+    if (MT == 2) return launch_split<T, 2, LAYOUT, KV8>(p, grid, st, pdl);
+    return launch_split<T, 4, LAYOUT, KV8>(p, grid, st, pdl);
 }
 
 template <typename T>
-static int run_decode(const DecodeParams &p, const DecodePlan &pl, int layout, bool kv8, cudaStream_t st) {
+static int run_decode(const DecodeParams &p, const DecodePlan &pl, int layout, bool kv8, bool pdl,
+                      cudaStream_t st) {
     dim3 grid(pl.n_split_max, p.Hkv, p.B);
-    int rc = kv8 ? (layout == PKV_HND ? launch_split_mt<T, PKV_HND, true>(pl.MT, p, grid, st)
-                                      : launch_split_mt<T, PKV_NHD, true>(pl.MT, p, grid, st))
-                 : (layout == PKV_HND ? launch_split_mt<T, PKV_HND, false>(pl.MT, p, grid, st)
-                                      : launch_split_mt<T, PKV_NHD, false>(pl.MT, p, grid, st));
+    int rc = kv8 ? (layout == PKV_HND ? launch_split_mt<T, PKV_HND, true>(pl.MT, p, grid, st, pdl)
+                                      : launch_split_mt<T, PKV_NHD, true>(pl.MT, p, grid, st, pdl))
+                 : (layout == PKV_HND ? launch_split_mt<T, PKV_HND, false>(pl.MT, p, grid, st, pdl)
+                                      : launch_split_mt<T, PKV_NHD, false>(pl.MT, p, grid, st, pdl));
     if (rc != PKV_OK) return rc;
     int launches = 1;
     if (pl.n_split_max > 1) {
@@ -695,7 +705,9 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
                             int32_t q_len_per_req, const int32_t *cum_seq_lens_q, int64_t num_tokens,
                             int32_t num_qo_heads, int32_t num_kv_heads,
                             int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
-                            void *out, float *lse, int32_t *err_word, void *stream) {
+                            void *out, float *lse, int32_t *err_word, void *stream,
+                            const float *bmm1_dev = nullptr, const float *bmm2_dev = nullptr,
+                            bool enable_pdl = false) {
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_F16_E4M3 && dtype != PKV_BF16_E4M3)
         return PKV_ERR_INVALID_ARG;
@@ -731,6 +743,8 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
     p.max_seq_len = max_seq_len;
     p.scale_log2 = bmm1_scale * kLog2e;
     p.bmm2 = bmm2_scale;
+    p.bmm1_dev = bmm1_dev;
+    p.bmm2_dev = bmm2_dev;
     p.window_left = window_left;
     p.sinks = sinks;
     p.Q = q_len_per_req;
@@ -750,7 +764,8 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
                            : nullptr;
     p.err = err_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return bf16 ? run_decode<__nv_bfloat16>(p, pl, layout, kv8, st) : run_decode<__half>(p, pl, layout, kv8, st);
+    return bf16 ? run_decode<__nv_bfloat16>(p, pl, layout, kv8, enable_pdl, st)
+                : run_decode<__half>(p, pl, layout, kv8, enable_pdl, st);
 }
 
 extern "C" int paged_decode(const void *query, const void *k_cache, const void *v_cache,
@@ -785,6 +800,27 @@ extern "C" int paged_decode_varlen(const void *query, int64_t num_tokens, const 
                        block_tables, block_table_stride, seq_lens, batch_size, max_seq_len, bmm1_scale,
                        bmm2_scale, window_left, sinks, max_q_len, cum_seq_lens_q, num_tokens, num_qo_heads,
                        num_kv_heads, head_dim, page_size, layout, dtype, out, lse, err_word, stream);
+}
+
+extern "C" int paged_decode_ex(const void *query, int64_t num_tokens, const void *k_cache,
+                               const void *v_cache, int64_t page_stride, int64_t max_num_pages,
+                               void *workspace, size_t workspace_bytes, const int32_t *block_tables,
+                               int32_t block_table_stride, const uint32_t *seq_lens, int32_t batch_size,
+                               int32_t max_seq_len, float bmm1_scale, float bmm2_scale,
+                               const float *bmm1_scale_dev, const float *bmm2_scale_dev, int32_t window_left,
+                               const float *sinks, int32_t max_q_len, const int32_t *cum_seq_lens_q,
+                               int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               int32_t layout, int32_t dtype, int32_t enable_pdl, void *out, float *lse,
+                               int32_t *err_word, void *stream) {
+    if (num_tokens < 0 || max_q_len < 1) return PKV_ERR_INVALID_ARG;
+    if (!cum_seq_lens_q && num_tokens < static_cast<int64_t>(batch_size) * max_q_len) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    return decode_impl(query, k_cache, v_cache, page_stride, max_num_pages, workspace, workspace_bytes,
+                       block_tables, block_table_stride, seq_lens, batch_size, max_seq_len, bmm1_scale,
+                       bmm2_scale, window_left, sinks, max_q_len, cum_seq_lens_q,
+                       cum_seq_lens_q ? num_tokens : static_cast<int64_t>(batch_size) * max_q_len, num_qo_heads,
+                       num_kv_heads, head_dim, page_size, layout, dtype, out, lse, err_word, stream,
+                       bmm1_scale_dev, bmm2_scale_dev, enable_pdl != 0);
 }
 
 // ---- decode with a library-owned scratch array ------------------------------

@@ -34,7 +34,12 @@ def assert_lse_close(got, ref, what="lse"):
     assert err.size == 0 or err.max() <= LSE_TOL, f"{what}: max err {err.max():.3e}"
 
 
-def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None, ws=None):
+def _scale(v, as_tensor):
+    return torch.tensor([v], dtype=torch.float32, device=DEV) if as_tensor else v
+
+
+def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None, ws=None,
+                  tensor_scales=False, enable_pdl=None):
     pool = c.pool
     kv = pool.storage[0].to(DEV) if len(pool.storage) == 1 else tuple(t.to(DEV) for t in pool.storage)
     B = c.seq_lens.shape[0]
@@ -47,8 +52,9 @@ def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None, w
     lse = torch.empty((c.query.shape[0], c.num_qo_heads), dtype=torch.float32,
                       device=DEV) if with_lse else None
     out = pk.paged_decode(c.query.to(DEV), kv, ws, c.block_tables.to(DEV), c.seq_lens.to(DEV),
-                          c.max_seq_len, bmm1_scale=c.bmm1_scale, bmm2_scale=c.bmm2_scale,
-                          window_left=c.window_left,
+                          c.max_seq_len, bmm1_scale=_scale(c.bmm1_scale, tensor_scales),
+                          bmm2_scale=_scale(c.bmm2_scale, tensor_scales), window_left=c.window_left,
+                          enable_pdl=enable_pdl,
                           sinks=None if c.sinks is None else c.sinks.to(DEV),
                           kv_layout=pool.layout if layout is None else layout,
                           q_len_per_req=c.q_len_per_req, lse=lse, err_word=err_word,

@@ -59,6 +59,39 @@ def test_bmm_scales_and_window_zero():
     _check(c)
 
 
+SCALE_CASES = [
+    # uniform queries, split and single-split requests, sinks, window
+    dict(L=[1500, 3, 1029, 5000], Q=2, w=700, sinks=True, q_lens=None),
+    # variable-length queries
+    dict(L=[1300, 70, 3000], Q=4, w=-1, sinks=False, q_lens=[1, 4, 2]),
+]
+
+
+@pytest.mark.parametrize("k", SCALE_CASES, ids=["uniform", "varlen"])
+def test_device_scales_and_pdl_bit_identical(k):
+    # bmm1/bmm2 given as device tensors, and the programmatic dependent
+    # launch, give bit for bit what the host scalars and a plain launch give
+    c = wl.decode_case(k["L"], 16, 32, 8, 128, wl.HND, q_len_per_req=k["Q"],
+                       q_lens=k["q_lens"], window_left=k["w"], with_sinks=k["sinks"], seed=40,
+                       bmm1_scale=0.07, bmm2_scale=1.7)
+    ref_o, ref_l = _check(c)
+    for ts, pdl in ((True, None), (False, True), (True, True)):
+        o, l = decode_on_gpu(c, tensor_scales=ts, enable_pdl=pdl)
+        assert torch.equal(o.view(torch.int16), ref_o.view(torch.int16)), (ts, pdl)
+        assert torch.equal(l, ref_l), (ts, pdl)
+
+
+def test_tensor_scale_must_be_one_float32_on_device():
+    c = wl.decode_case([100], 16, 32, 8, 128, wl.HND, seed=41)
+    for bad in (torch.tensor([0.1], dtype=torch.float64, device=DEV),
+                torch.tensor([0.1, 0.2], device=DEV), torch.tensor([0.1])):
+        with pytest.raises(pk.PagedKVError):
+            pk.paged_decode(c.query.to(DEV), c.pool.storage[0].to(DEV),
+                            torch.zeros(1 << 20, dtype=torch.uint8, device=DEV),
+                            c.block_tables.to(DEV), c.seq_lens.to(DEV), c.max_seq_len,
+                            bmm1_scale=bad)
+
+
 def test_page_permutation_bit_identical():
     a = wl.decode_case([700, 1300], 16, 32, 8, 128, wl.HND, seed=3, pool_pages=200)
     b = wl.decode_case([700, 1300], 16, 32, 8, 128, wl.HND, seed=4, pool_pages=200)

@@ -88,3 +88,46 @@ def test_graph_replay_matches_eager():
                  "prefill lse")
         bad = [n for n, e, t in zip(names, eager, outs) if not torch.equal(_bits(e), _bits(t))]
         assert not bad, f"replay differs from eager: {bad}"
+
+
+def test_graph_follows_device_scale_tensors():
+    # a decode captured once with device-tensor scales (and the programmatic
+    # dependent launch) picks up new scale values written between replays
+    c = wl.decode_case([2100, 90, 4000], 16, 32, 8, 128, wl.HND, q_len_per_req=2,
+                       with_sinks=True, seed=42)
+    kv, bt, sl, sk = (t.to(DEV) for t in (c.pool.storage[0], c.block_tables, c.seq_lens, c.sinks))
+    q = c.query.to(DEV)
+    ws = torch.zeros(max(1, pk.paged_decode_workspace_size(3, 2, 32, 8, 128, c.max_seq_len, 16)),
+                     dtype=torch.uint8, device=DEV)
+    s1 = torch.tensor([0.09], device=DEV)
+    s2 = torch.tensor([1.0], device=DEV)
+    out, lse = torch.empty_like(q), torch.empty(q.shape[:2], device=DEV)
+
+    def step():
+        pk.paged_decode(q, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=s1, bmm2_scale=s2,
+                        sinks=sk, q_len_per_req=2, out=out, lse=lse, enable_pdl=True)
+
+    def eager(a, b):
+        o = pk.paged_decode(q, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=a, bmm2_scale=b,
+                            sinks=sk, q_len_per_req=2, lse=(l := torch.empty_like(lse)))
+        torch.cuda.synchronize()
+        return o, l
+
+    step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    for a, b in ((0.09, 1.0), (0.03, 0.5), (0.12, 2.0)):
+        s1.fill_(a)
+        s2.fill_(b)
+        out.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        ro, rl = eager(a, b)
+        assert torch.equal(_bits(out), _bits(ro)), (a, b)
+        assert torch.equal(lse, rl), (a, b)
