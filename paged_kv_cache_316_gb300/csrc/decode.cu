@@ -24,26 +24,27 @@ constexpr int kDecD = 128;                        // head_dim
 constexpr int kDecTile = 64;                      // keys per pipeline stage
 // Ring depth and CTAs per SM.  One row tile (up to 16 packed query rows): 3
 // CTAs per SM with a 2-stage ring; more row tiles need more registers: 2
-// CTAs per SM, 3 stages (the same for an E4M3 cache: a deeper ring with
-// fewer CTAs measured slower there).
+// CTAs per SM, 3 stages.  An E4M3 stage is half as large, so its ring is 4
+// stages deep at the same CTA counts.
 template <int MT, bool KV8 = false>
 struct DecCfg {
-    static constexpr int STAGES = MT == 1 ? 2 : 3;
+    static constexpr int STAGES = KV8 ? 4 : (MT == 1 ? 2 : 3);
     static constexpr int CTAS = MT == 1 ? 3 : 2;
 };
 constexpr int kDecThreads = 128;
 constexpr int kDecRowBytes = kDecD * 2;           // one K or V row
 constexpr int kDecTileBytes = kDecTile * kDecRowBytes;
 constexpr int kDecStageBytes = 2 * kDecTileBytes; // K tile then V tile
-// An E4M3 cache is staged as 128-byte rows (K then V, 8 KB each per tile) and
-// widened once per tile into one 16-bit tile pair laid out as above.
+// An E4M3 cache is staged as 128-byte rows (K then V, 8 KB each per tile),
+// 16-byte chunk c of row r at chunk c ^ (r & 7), and the MMA fragments are
+// widened straight from those bytes (no 16-bit copy of the tile).
 constexpr int kDec8RowBytes = kDecD;
 constexpr int kDec8TileBytes = kDecTile * kDec8RowBytes;
 template <bool KV8>
 struct DecSmem {
     static constexpr int STAGE = KV8 ? 2 * kDec8TileBytes : kDecStageBytes;  // one ring stage
-    static constexpr int CONV = KV8 ? kDecStageBytes : 0;                    // the widened tile pair
 };
+__device__ __forceinline__ int swz8(int r, int c) { return r * kDec8RowBytes + ((c ^ (r & 7)) << 4); }
 
 // Two E4M3 values (low byte first) widened exactly to fp16 (every E4M3
 // value is an fp16 value).
@@ -112,6 +113,20 @@ __host__ __device__ inline void decode_split_geometry(int L, int Q, int window_l
     n_split = (L + chunk - 1) / chunk - first;
 }
 
+// Barrier over the MT warps that share a slice of keys (warps kg*MT ..
+// kg*MT + MT - 1): a warp sync for one, __syncthreads for all four, else the
+// named barrier 1 + kg.
+template <int MT>
+__device__ __forceinline__ void key_group_sync(int kg) {
+    if constexpr (MT == 1) {
+        __syncwarp();
+    } else if constexpr (MT * 32 == kDecThreads) {
+        __syncthreads();
+    } else {
+        asm volatile("bar.sync %0, %1;\n" ::"r"(1 + kg), "n"(MT * 32) : "memory");
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ void store4(T *dst, float a, float b, float c, float d) {
     uint2 v;
@@ -133,13 +148,12 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     constexpr int NT = KPW / 8;          // 8-key score tiles per warp
     constexpr int ROWS = 16 * MT;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *conv = smem + kDecStages * STAGE_BYTES;  // widened E4M3 tile pair (KV8)
-    uint8_t *q_s = conv + DecSmem<KV8>::CONV;
+    uint8_t *q_s = smem + kDecStages * STAGE_BYTES;
     uint8_t *kvalid = q_s + ROWS * kDecRowBytes;
     float *comb_m = reinterpret_cast<float *>(kvalid + kDecStages * kDecTile);
     float *comb_l = comb_m + NKG * ROWS;
     int *pages_s = reinterpret_cast<int *>(comb_l + NKG * ROWS);  // the split's page ids
-    __shared__ int any_bad;
+    __shared__ int any_bad[4];  // per key group: a row of its slice was on a bad page
 
     // launched as a dependent of the stream's previous kernel (enable_pdl):
     // wait for it before reading anything it may have written
@@ -147,6 +161,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = warp % MT, kg = warp / MT;
+    const int gtid = tid - kg * MT * 32;  // thread index within the key group
+    const int kw0 = kg * KPW;             // the group's key slice of every tile
     const uint32_t L_in = p.seq_lens[b];
     const int L = L_in > static_cast<uint32_t>(p.max_seq_len) ? p.max_seq_len : static_cast<int>(L_in);
     if (L_in > static_cast<uint32_t>(p.max_seq_len) && s == 0 && kvh == 0 && threadIdx.x == 0)
@@ -181,7 +197,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     const uint8_t *vc8 = static_cast<const uint8_t *>(p.v);
     const int32_t *bt = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
     const int S = 1 << p.page_shift;
-    if (tid == 0) any_bad = 0;
+    if (tid < 4) any_bad[tid] = 0;
     // page ids of the split, fetched once (coalesced) so that the per-tile
     // address computation does not wait on global memory; -1 marks an id
     // outside the pool
@@ -197,18 +213,20 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     }
     __syncthreads();
 
-    // K and V rows of a tile: 16 consecutive lanes copy one 256-byte row,
-    // so every warp instruction moves two whole rows.  Rows past the split
-    // end or on an out-of-range page are zero-filled and never read from
-    // global memory; kvalid records which rows hold a key.
+    // K and V rows of a tile.  Every key group loads (and later widens) only
+    // the KPW rows of its own key slice, the only rows its warps read, so a
+    // tile needs no barrier wider than the group.  16 consecutive lanes copy
+    // one 256-byte row: every warp instruction moves two whole rows.  Rows
+    // past the split end or on an out-of-range page are zero-filled and never
+    // read from global memory; kvalid records which rows hold a key.
     auto load_tile = [&](int stage, int j0) {
         const uint32_t dst = smem_u32(smem + stage * STAGE_BYTES);
         if constexpr (KV8) {
-            // 128-byte E4M3 rows: 8 consecutive lanes copy one row, unswizzled
+            // 128-byte E4M3 rows: 8 consecutive lanes copy one row
 #pragma unroll
-            for (int k = 0; k < kDecTile * 8 / kDecThreads; ++k) {
-                const int idx = k * kDecThreads + tid;
-                const int r = idx >> 3, c = idx & 7;
+            for (int k = 0; k < KPW * 8 / (MT * 32); ++k) {
+                const int idx = k * MT * 32 + gtid;
+                const int r = kw0 + (idx >> 3), c = idx & 7;
                 const int j = j0 + r;
                 bool ok = j < k_end;
                 const uint8_t *ks = kc8, *vs = vc8;
@@ -216,7 +234,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                     const int page = pages_s[(j >> p.page_shift) - first_page];
                     if (page < 0) {
                         ok = false;
-                        any_bad = 1;
+                        any_bad[kg] = 1;
                     } else {
                         const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
                                                                   S, kDecD) + c * 16;
@@ -225,14 +243,14 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                     }
                 }
                 if (c == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
-                cp_async_16(dst + r * kDec8RowBytes + c * 16, ks, ok);
-                cp_async_16(dst + kDec8TileBytes + r * kDec8RowBytes + c * 16, vs, ok);
+                cp_async_16(dst + swz8(r, c), ks, ok);
+                cp_async_16(dst + kDec8TileBytes + swz8(r, c), vs, ok);
             }
         } else {
 #pragma unroll
-        for (int k = 0; k < kDecTile * 16 / kDecThreads; ++k) {
-            const int idx = k * kDecThreads + tid;
-            const int r = idx >> 4, c = idx & 15;
+        for (int k = 0; k < KPW * 16 / (MT * 32); ++k) {
+            const int idx = k * MT * 32 + gtid;
+            const int r = kw0 + (idx >> 4), c = idx & 15;
             const int j = j0 + r;
             bool ok = j < k_end;
             const T *ks = kc, *vs = vc;
@@ -240,7 +258,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                 const int page = pages_s[(j >> p.page_shift) - first_page];
                 if (page < 0) {
                     ok = false;
-                    any_bad = 1;
+                    any_bad[kg] = 1;
                 } else {
                     const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
                                                               S, kDecD) + c * 8;
@@ -326,9 +344,30 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     }
 
     uint32_t qa[8][4];
+    if constexpr (KV8) {
+        // Over an E4M3 cache the head dimension is taken in a permuted order,
+        // the same for Q and K (a dot product does not depend on it): the k
+        // pairs {2c, 2c+1} and {2c+8, 2c+9} of k-step kk are the dims
+        // 32c + 4kk + {0,1} and {2,3}, so that one 32-bit word of a K row
+        // holds both halves of a B fragment.
+        const int gq = lane >> 2, cq = lane & 3;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        ldsm_x4(qa[kk], smem_u32(q_s) + swz(16 * mt + (lane & 15), 2 * kk + (lane >> 4), kDecRowBytes));
+        for (int kk = 0; kk < 8; ++kk) {
+            const int dim = cq * 32 + kk * 4;
+            const uint2 lo = *reinterpret_cast<const uint2 *>(q_s + swz(16 * mt + gq, dim >> 3, kDecRowBytes) +
+                                                              (dim & 7) * 2);
+            const uint2 hi = *reinterpret_cast<const uint2 *>(q_s + swz(16 * mt + gq + 8, dim >> 3, kDecRowBytes) +
+                                                              (dim & 7) * 2);
+            qa[kk][0] = lo.x;
+            qa[kk][1] = hi.x;
+            qa[kk][2] = lo.y;
+            qa[kk][3] = hi.y;
+        }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            ldsm_x4(qa[kk], smem_u32(q_s) + swz(16 * mt + (lane & 15), 2 * kk + (lane >> 4), kDecRowBytes));
+    }
 
     // the two rows this lane holds in every accumulator fragment
     const int r0 = 16 * mt + (lane >> 2), r1 = r0 + 8;
@@ -343,11 +382,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const int kw0 = kg * KPW;
 
     for (int it = 0; it < n_tiles; ++it) {
         cp_async_wait<kDecStages - 2>();
-        __syncthreads();
+        key_group_sync<MT>(kg);  // the slice landed; the group is done with the stage reloaded next
         {
             int nxt = it + kDecStages - 1;
             if (nxt < n_tiles) load_tile(nxt % kDecStages, k_begin + nxt * kDecTile);
@@ -355,37 +393,29 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         }
         const int stage = it % kDecStages;
         const int j0 = k_begin + it * kDecTile;
-        uint32_t kb = smem_u32(smem + stage * STAGE_BYTES);
-        if constexpr (KV8) {
-            // widen the landed E4M3 tile pair into the 16-bit, swizzled layout
-            // the fragments are read from (the barrier above also ended every
-            // warp's reads of the previous widened tile)
-            const uint8_t *st8 = smem + stage * STAGE_BYTES;
-#pragma unroll
-            for (int k = 0; k < 2 * kDecTile * 8 / kDecThreads; ++k) {
-                const int idx = k * kDecThreads + tid;
-                const int kv = idx / (kDecTile * 8), rem = idx % (kDecTile * 8);
-                const int r = rem >> 3, c = rem & 7;
-                const uint4 raw = *reinterpret_cast<const uint4 *>(st8 + kv * kDec8TileBytes + r * kDec8RowBytes + c * 16);
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t h[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    h[2 * i] = widen_e4m3x2<TM>(w[i] & 0xffffu);
-                    h[2 * i + 1] = widen_e4m3x2<TM>(w[i] >> 16);
-                }
-                uint8_t *dt = conv + kv * kDecTileBytes;
-                *reinterpret_cast<uint4 *>(dt + swz(r, 2 * c, kDecRowBytes)) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(dt + swz(r, 2 * c + 1, kDecRowBytes)) = make_uint4(h[4], h[5], h[6], h[7]);
-            }
-            __syncthreads();
-            kb = smem_u32(conv);
-        }
+        const uint32_t kb = smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t vb = kb + kDecTileBytes;
+        const uint8_t *k8 = smem + stage * STAGE_BYTES;  // E4M3 K rows (KV8)
+        const uint8_t *v8 = k8 + kDec8TileBytes;         // E4M3 V rows (KV8)
 
         float sc[NT][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+        if constexpr (KV8) {
+            // key kw0 + 8nt + g: its 32 bytes at dims 32c .. 32c + 31 hold the
+            // B fragments of all eight k-steps (see the Q fragments)
+            const int g8 = lane >> 2, c8 = lane & 3;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int row = kw0 + nt * 8 + g8;
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(k8 + swz8(row, 2 * c8));
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(k8 + swz8(row, 2 * c8 + 1));
+                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma16816<TM>(sc[nt], qa[kk], widen_e4m3x2<TM>(w[kk] & 0xffffu), widen_e4m3x2<TM>(w[kk] >> 16));
+            }
+        } else {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
@@ -397,8 +427,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                 mma16816<TM>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
             }
         }
+        }
 
-        const bool interior = !any_bad && j0 >= lo_max && j0 + kDecTile - 1 <= hi_min;
+        const bool interior = !any_bad[kg] && j0 >= lo_max && j0 + kDecTile - 1 <= hi_min;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -456,13 +487,36 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
             a[1] = pack2<TM>(sc[2 * ks][2], sc[2 * ks][3]);
             a[2] = pack2<TM>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
             a[3] = pack2<TM>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
-            const int key = kw0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            if constexpr (KV8) {
+                // The output dims are permuted too: column g of n-tile nt is
+                // dim 16g + nt, so the lane's 16 bytes of the keys 2c, 2c+1,
+                // 2c+8, 2c+9 feed all 16 n-tiles, the two keys of a B
+                // register interleaved byte by byte.
+                const int g8 = lane >> 2, rb = kw0 + ks * 16 + 2 * (lane & 3);
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb, g8));
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 1, g8));
+                const uint4 y0 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 8, g8));
+                const uint4 y1 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 9, g8));
+                const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
+                const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {
-                uint32_t vf[4];
-                ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), kDecRowBytes));
-                mma16816<TM>(o[2 * dp], a, vf[0], vf[1]);
-                mma16816<TM>(o[2 * dp + 1], a, vf[2], vf[3]);
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t p01 = __byte_perm(X0[i], X1[i], 0x5140), p23 = __byte_perm(X0[i], X1[i], 0x7362);
+                    const uint32_t q01 = __byte_perm(Y0[i], Y1[i], 0x5140), q23 = __byte_perm(Y0[i], Y1[i], 0x7362);
+                    mma16816<TM>(o[4 * i], a, widen_e4m3x2<TM>(p01 & 0xffffu), widen_e4m3x2<TM>(q01 & 0xffffu));
+                    mma16816<TM>(o[4 * i + 1], a, widen_e4m3x2<TM>(p01 >> 16), widen_e4m3x2<TM>(q01 >> 16));
+                    mma16816<TM>(o[4 * i + 2], a, widen_e4m3x2<TM>(p23 & 0xffffu), widen_e4m3x2<TM>(q23 & 0xffffu));
+                    mma16816<TM>(o[4 * i + 3], a, widen_e4m3x2<TM>(p23 >> 16), widen_e4m3x2<TM>(q23 >> 16));
+                }
+            } else {
+                const int key = kw0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+                for (int dp = 0; dp < 8; ++dp) {
+                    uint32_t vf[4];
+                    ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), kDecRowBytes));
+                    mma16816<TM>(o[2 * dp], a, vf[0], vf[1]);
+                    mma16816<TM>(o[2 * dp + 1], a, vf[2], vf[3]);
+                }
             }
         }
     }
@@ -476,11 +530,25 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     float *comb_o = reinterpret_cast<float *>(smem);  // [NKG][ROWS][128]
+    if constexpr (KV8) {
+        // undo the output permutation: o[nt][e] is dim 16 (2c + (e & 1)) + nt
+        const int d0 = 32 * (lane & 3);
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-        int d = nd * 8 + 2 * (lane & 3);
-        *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r0) * kDecD + d]) = make_float2(o[nd][0], o[nd][1]);
-        *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r1) * kDecD + d]) = make_float2(o[nd][2], o[nd][3]);
+        for (int i = 0; i < 4; ++i) {
+            float *w0 = &comb_o[(kg * ROWS + r0) * kDecD + d0 + 4 * i];
+            float *w1 = &comb_o[(kg * ROWS + r1) * kDecD + d0 + 4 * i];
+            *reinterpret_cast<float4 *>(w0) = make_float4(o[4 * i][0], o[4 * i + 1][0], o[4 * i + 2][0], o[4 * i + 3][0]);
+            *reinterpret_cast<float4 *>(w0 + 16) = make_float4(o[4 * i][1], o[4 * i + 1][1], o[4 * i + 2][1], o[4 * i + 3][1]);
+            *reinterpret_cast<float4 *>(w1) = make_float4(o[4 * i][2], o[4 * i + 1][2], o[4 * i + 2][2], o[4 * i + 3][2]);
+            *reinterpret_cast<float4 *>(w1 + 16) = make_float4(o[4 * i][3], o[4 * i + 1][3], o[4 * i + 2][3], o[4 * i + 3][3]);
+        }
+    } else {
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) {
+            int d = nd * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r0) * kDecD + d]) = make_float2(o[nd][0], o[nd][1]);
+            *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r1) * kDecD + d]) = make_float2(o[nd][2], o[nd][3]);
+        }
     }
     if ((lane & 3) == 0) {
         comb_m[kg * ROWS + r0] = m0;
@@ -642,7 +710,7 @@ template <typename T, int MT, int LAYOUT, bool KV8>
 static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
     constexpr int kDecStages = DecCfg<MT, KV8>::STAGES;
-    const size_t smem = kDecStages * DecSmem<KV8>::STAGE + DecSmem<KV8>::CONV + ROWS * kDecRowBytes +
+    const size_t smem = kDecStages * DecSmem<KV8>::STAGE + ROWS * kDecRowBytes +
                         kDecStages * kDecTile + 2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
     auto kern = decode_split_kernel<T, MT, LAYOUT, KV8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
