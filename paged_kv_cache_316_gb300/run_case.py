@@ -2,7 +2,7 @@
 
     python -m paged_kv_cache_316_gb300.run_case --op prefill [--d-qk 128] [--iters 3]
     python -m paged_kv_cache_316_gb300.run_case --op decode_llama | decode_long | decode_varlen | append
-                                                [--batch N] [--iters 3]
+                                                [--batch N] [--iters 3] [--kv-dtype e4m3]
 
 Used to drive profilers (ncu) on one kernel at a size that keeps a capture
 short; it prints the mean CUDA-event time per call, which is informational
@@ -26,6 +26,8 @@ def main():
     ap.add_argument("--d-qk", type=int, default=128)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--kv-dtype", choices=["same", "e4m3"], default="same",
+                    help="decode: the cache in the query's dtype, or E4M3 (FP8)")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     from . import build
@@ -42,17 +44,19 @@ def main():
             pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv,
                              bt, causal=True, kv_layout="HND")
     elif a.op in ("decode_llama", "decode_long", "decode_varlen"):
+        kvd = dict(kv_dtype=wl.E4M3) if a.kv_dtype == "e4m3" else {}
         if a.op == "decode_varlen":
-            c = wl.long_decode_varlen(device=dev)
+            c = wl.long_decode_varlen(device=dev, **kvd)
         elif not a.batch:
-            c = wl.llama_decode(device=dev) if a.op == "decode_llama" else wl.long_decode(device=dev)
+            c = (wl.llama_decode(device=dev, **kvd) if a.op == "decode_llama"
+                 else wl.long_decode(device=dev, **kvd))
         elif a.op == "decode_llama":  # the first `batch` requests of the same length draw
             L = wl.uniform_lengths(wl.generator(0), 64, 512, 8192)[:a.batch]
-            c = wl.decode_case(L, 16, 32, 8, 128, wl.HND, wl.BF16, device=dev, bt_width=512)
+            c = wl.decode_case(L, 16, 32, 8, 128, wl.HND, wl.BF16, device=dev, bt_width=512, **kvd)
         else:
             L = wl.lognormal_lengths(wl.generator(0), 256, 4096.0, 1.0, 4, 32768)[:a.batch]
             c = wl.decode_case(L, 64, 64, 8, 128, wl.HND, wl.BF16, q_len_per_req=4,
-                               window_left=4095, with_sinks=True, device=dev, bt_width=512)
+                               window_left=4095, with_sinks=True, device=dev, bt_width=512, **kvd)
         B = len(c.pt.lengths)
         ws = torch.zeros(max(1, pk.paged_decode_workspace_size(
             B, c.q_len_per_req, c.num_qo_heads, c.num_kv_heads, c.head_dim, c.max_seq_len,
