@@ -219,8 +219,39 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     // one 256-byte row: every warp instruction moves two whole rows.  Rows
     // past the split end or on an out-of-range page are zero-filled and never
     // read from global memory; kvalid records which rows hold a key.
+    // A thread's rows of a tile are RSTEP apart; when they all lie before the
+    // split end on one page (the common case), the page is looked up once
+    // and the row address advances by a fixed step.
+    constexpr int LPR = KV8 ? 8 : 16;                 // lanes per row
+    constexpr int RSTEP = MT * 32 / LPR;              // rows between a thread's rows
+    constexpr int NLOAD = KPW * LPR / (MT * 32);      // rows per thread per tile
+    const int64_t row_step = (LAYOUT == PKV_HND ? kDecD : static_cast<int64_t>(p.Hkv) * kDecD) * RSTEP;
     auto load_tile = [&](int stage, int j0) {
         const uint32_t dst = smem_u32(smem + stage * STAGE_BYTES);
+        {
+            const int r0 = kw0 + gtid / LPR, c = gtid % LPR;
+            const int jA = j0 + r0, jZ = jA + (NLOAD - 1) * RSTEP;
+            const int page = jZ < k_end && (jA >> p.page_shift) == (jZ >> p.page_shift)
+                                 ? pages_s[(jA >> p.page_shift) - first_page]
+                                 : -1;
+            if (__all_sync(0xffffffffu, page >= 0)) {
+                const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, jA & (S - 1), p.Hkv, S, kDecD);
+#pragma unroll
+                for (int k = 0; k < NLOAD; ++k) {
+                    const int r = r0 + k * RSTEP;
+                    if (c == 0) kvalid[stage * kDecTile + r] = 1;
+                    if constexpr (KV8) {
+                        cp_async_16(dst + swz8(r, c), kc8 + off + k * row_step + c * 16, true);
+                        cp_async_16(dst + kDec8TileBytes + swz8(r, c), vc8 + off + k * row_step + c * 16, true);
+                    } else {
+                        const uint32_t o = swz(r, c, kDecRowBytes);
+                        cp_async_16(dst + o, kc + off + k * row_step + c * 8, true);
+                        cp_async_16(dst + kDecTileBytes + o, vc + off + k * row_step + c * 8, true);
+                    }
+                }
+                return;
+            }
+        }
         if constexpr (KV8) {
             // 128-byte E4M3 rows: 8 consecutive lanes copy one row
 #pragma unroll
