@@ -174,9 +174,15 @@ def prefill(q, k_cache, v_cache, k_page_stride: int, v_page_stride: int,
             max_num_pages: int, scale: float, seq_lens_q, seq_lens_kv,
             block_tables, causal: bool, num_qo_heads: int, num_kv_heads: int,
             d_qk: int, d_vo: int, page_size: int, layout: int, dtype: int,
-            threads: int | None = None):
-    """Returns (out [total_q, Hqo, d_vo], lse [total_q, Hqo], err), float64."""
-    qq = _u16(q)
+            threads: int | None = None, q_dtype: int | None = None,
+            kv_dtype: int | None = None, q_scale: float = 1.0, k_scale: float = 1.0,
+            v_scale: float = 1.0):
+    """Returns (out [total_q, Hqo, d_vo], lse [total_q, Hqo], err), float64.
+    q_dtype / kv_dtype (default `dtype`) may be E4M3, with uint8 arrays;
+    q_scale, k_scale, v_scale dequantise the stored elements."""
+    qd = dtype if q_dtype is None else q_dtype
+    kvd = dtype if kv_dtype is None else kv_dtype
+    qq = np.ascontiguousarray(q).view(np.uint8) if qd == E4M3 else _u16(q)
     lq, lkv = _i32(seq_lens_q), _i32(seq_lens_kv)
     _check_pool(k_cache, k_page_stride, max_num_pages)
     _check_pool(v_cache, v_page_stride, max_num_pages)
@@ -195,7 +201,8 @@ def prefill(q, k_cache, v_cache, k_page_stride: int, v_page_stride: int,
         ctypes.c_double(scale), _p(lq), _p(lkv), _p(bt), ctypes.c_int(bt.shape[1]),
         ctypes.c_int(B), ctypes.c_int(int(causal)), ctypes.c_int(num_qo_heads),
         ctypes.c_int(num_kv_heads), ctypes.c_int(d_qk), ctypes.c_int(d_vo),
-        ctypes.c_int(page_size), ctypes.c_int(layout), ctypes.c_int(dtype),
+        ctypes.c_int(page_size), ctypes.c_int(layout), ctypes.c_int(qd), ctypes.c_int(kvd),
+        ctypes.c_double(q_scale), ctypes.c_double(k_scale), ctypes.c_double(v_scale),
         _p(out), _p(lse), _p(scratch), ctypes.c_int(slen), ctypes.c_int(nthr),
         ctypes.c_int(nthr))
     return out, lse, int(err)

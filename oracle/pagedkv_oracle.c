@@ -197,10 +197,13 @@ int orc_append(const void *append_key, const void *append_value,
 
 /* o[0:d_vo] = out_scale * sum_{j in [lo, hi]} e^{s_j - M} v_j / den and
  * lse = M + log den, with s_j = scale * <q, k_j>, den = sum e^{s_j - M}
- * (+ e^{sink - M} when has_sink), M the largest term.  Keys are read through
- * the block table row `bt` of one request.  An empty key set without a sink
- * gives o = 0 and lse = -inf. */
-static int orc_attend_row(const uint16_t *q, int dtype, const void *k_cache,
+ * (+ e^{sink - M} when has_sink), M the largest term.  Every stored element
+ * is dequantised by its tensor's factor first (q_mul * q, k_mul * k,
+ * v_mul * v; 1 for 16-bit tensors).  The query row is elements q_off ..
+ * q_off + d_qk - 1 of q.  Keys are read through the block table row `bt` of
+ * one request.  An empty key set without a sink gives o = 0 and lse = -inf. */
+static int orc_attend_row(const void *q, int64_t q_off, int dtype, double q_mul,
+                          double k_mul, double v_mul, const void *k_cache,
                           const void *v_cache, int kv_dtype, int64_t k_page_stride,
                           int64_t v_page_stride, int64_t max_num_pages,
                           const int32_t *bt, int kvh, int num_kv_heads,
@@ -225,7 +228,7 @@ static int orc_attend_row(const uint16_t *q, int dtype, const void *k_cache,
         for (int d = 0; d < d_qk; ++d) {
             int64_t off = orc_kv_offset(layout, page, k_page_stride, kvh, slot, d,
                                         num_kv_heads, page_size, d_qk);
-            dot += orc_elem(q, d, dtype) * orc_elem(k_cache, off, kv_dtype);
+            dot += (q_mul * orc_elem(q, q_off + d, dtype)) * (k_mul * orc_elem(k_cache, off, kv_dtype));
         }
         s[jj] = scale * dot;
         if (s[jj] > m)
@@ -249,7 +252,7 @@ static int orc_attend_row(const uint16_t *q, int dtype, const void *k_cache,
         for (int d = 0; d < d_vo; ++d) {
             int64_t off = orc_kv_offset(layout, page, v_page_stride, kvh, slot, d,
                                         num_kv_heads, page_size, d_vo);
-            o[d] += w * orc_elem(v_cache, off, kv_dtype);
+            o[d] += w * (v_mul * orc_elem(v_cache, off, kv_dtype));
         }
     }
     for (int d = 0; d < d_vo; ++d)
@@ -330,7 +333,7 @@ int orc_decode(const uint16_t *query, const void *k_cache,
         if (window_left >= 0 && p - window_left > 0)
             lo = p - window_left;
         double lse_r;
-        err |= orc_attend_row(query + r * head_dim, dtype, k_cache, v_cache, kv_dtype,
+        err |= orc_attend_row(query, r * head_dim, dtype, 1.0, 1.0, 1.0, k_cache, v_cache, kv_dtype,
                               page_stride, page_stride, max_num_pages,
                               block_tables + (int64_t)b * block_table_stride,
                               h / group, num_kv_heads, page_size, head_dim,
@@ -351,14 +354,18 @@ int orc_decode(const uint16_t *query, const void *k_cache,
  * kv_b - q_b + i; with causal it attends keys j <= that position, otherwise
  * every j < kv_b.  out = softmax(scale * q k^T) v over those keys and
  * lse = log sum_j e^{scale * <q, k_j>} (natural log).  out: [total_q,
- * num_qo_heads, d_vo], lse: [total_q, num_qo_heads]. */
-int orc_prefill(const uint16_t *q, const uint16_t *k_cache,
-                const uint16_t *v_cache, int64_t k_page_stride,
+ * num_qo_heads, d_vo], lse: [total_q, num_qo_heads].
+ * q is stored as q_dtype, the caches as kv_dtype (16-bit, or E4M3 with one
+ * byte per element); q, k and v above are the stored values times the
+ * page's q_scale, k_scale and v_scale (1 for 16-bit tensors). */
+int orc_prefill(const void *q, const void *k_cache,
+                const void *v_cache, int64_t k_page_stride,
                 int64_t v_page_stride, int64_t max_num_pages, double scale,
                 const int32_t *seq_lens_q, const int32_t *seq_lens_kv,
                 const int32_t *block_tables, int block_table_stride, int B,
                 int causal, int num_qo_heads, int num_kv_heads, int d_qk,
-                int d_vo, int page_size, int layout, int dtype, double *out,
+                int d_vo, int page_size, int layout, int q_dtype, int kv_dtype,
+                double q_scale, double k_scale, double v_scale, double *out,
                 double *lse, double *scratch, int scratch_len,
                 int n_scratch_threads, int num_threads)
 {
@@ -395,7 +402,7 @@ int orc_prefill(const uint16_t *q, const uint16_t *k_cache,
         int64_t pos = kvb - qb + i;
         int64_t hi = causal ? (pos < kvb - 1 ? pos : kvb - 1) : kvb - 1;
         double lse_r;
-        err |= orc_attend_row(q + r * d_qk, dtype, k_cache, v_cache, dtype,
+        err |= orc_attend_row(q, r * d_qk, q_dtype, q_scale, k_scale, v_scale, k_cache, v_cache, kv_dtype,
                               k_page_stride, v_page_stride, max_num_pages,
                               block_tables + (int64_t)b * block_table_stride,
                               h / group, num_kv_heads, page_size, d_qk, d_vo,

@@ -277,6 +277,13 @@ class PrefillCase:
     d_qk: int
     d_vo: int
     dtype: int
+    # E4M3 (FP8) storage: the query and/or the caches hold 1-byte elements
+    # whose values are the stored ones times q_scale / k_scale / v_scale
+    q_dtype: int | None = None
+    kv_dtype: int | None = None
+    q_scale: float = 1.0
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
 
 def prefill_case(q_lens, kv_lens, page_size: int, num_qo_heads: int,
@@ -284,15 +291,21 @@ def prefill_case(q_lens, kv_lens, page_size: int, num_qo_heads: int,
                  dtype: int = BF16, causal: bool = True, seed: int = 0,
                  scale: float | None = None, slack: float = 0.0, device="cpu",
                  bt_width: int | None = None, fill: str = "randn",
-                 shuffle: bool = True) -> PrefillCase:
+                 shuffle: bool = True, q_dtype: int | None = None,
+                 kv_dtype: int | None = None, q_scale: float = 1.0, k_scale: float = 1.0,
+                 v_scale: float = 1.0) -> PrefillCase:
+    """q_dtype / kv_dtype = E4M3 store the query / caches as FP8 (N(0,1)
+    draws rounded to E4M3); the scales dequantise them."""
     g = generator(seed)
     gd = g if str(device) == "cpu" else generator(seed + 7919, device)
     pt = reserve_pages(kv_lens, page_size, g if shuffle else None, slack=slack)
     tdt = torch_dtype(dtype)
     pool = make_pool(pt.num_pages, num_kv_heads, page_size, d_qk, d_vo, layout,
-                     tdt, gd, form="tuple", device=device, fill=fill)
+                     torch_dtype(dtype if kv_dtype is None else kv_dtype), gd, form="tuple",
+                     device=device, fill=fill)
     total_q = int(sum(q_lens))
-    q = randn((total_q, num_qo_heads, d_qk), tdt, gd, device)
+    q = randn((total_q, num_qo_heads, d_qk), torch_dtype(dtype if q_dtype is None else q_dtype),
+              gd, device)
     if scale is None:
         scale = 1.0 / math.sqrt(d_qk)
     width = bt_width or max(1, pt.max_pages())
@@ -301,7 +314,8 @@ def prefill_case(q_lens, kv_lens, page_size: int, num_qo_heads: int,
                        torch.tensor([int(x) for x in kv_lens], dtype=torch.int32),
                        max(q_lens) if len(q_lens) else 0,
                        max(kv_lens) if len(kv_lens) else 0, scale, causal,
-                       num_qo_heads, num_kv_heads, d_qk, d_vo, dtype)
+                       num_qo_heads, num_kv_heads, d_qk, d_vo, dtype, q_dtype, kv_dtype,
+                       q_scale, k_scale, v_scale)
 
 
 @dataclass

@@ -38,7 +38,9 @@ def oracle_prefill(c: wl.PrefillCase, threads=None):
         u16(c.q), u16(p.k), u16(p.v), p.k_page_stride, p.v_page_stride,
         p.num_pages, c.scale, c.seq_lens_q.numpy(), c.seq_lens_kv.numpy(),
         c.block_tables.numpy(), c.causal, c.num_qo_heads, c.num_kv_heads,
-        c.d_qk, c.d_vo, p.page_size, p.layout, c.dtype, threads=threads)
+        c.d_qk, c.d_vo, p.page_size, p.layout, c.dtype, threads=threads,
+        q_dtype=c.q_dtype, kv_dtype=c.kv_dtype, q_scale=c.q_scale, k_scale=c.k_scale,
+        v_scale=c.v_scale)
 
 
 def oracle_append(c: wl.AppendCase, batch_indices, positions, layout=None):

@@ -48,8 +48,15 @@ MUTANTS = {
     "e4m3_subnormal_scale": ("v = ldexp((double)mant, -9);", "v = ldexp((double)mant, -10);"),
     "append_copies_half_the_bytes": ("(const char *)append_key + src * elem_bytes, elem_bytes);",
                                      "(const char *)append_key + src * elem_bytes, 1);"),
-    "value_row_from_key_cache": ("o[d] += w * orc_elem(v_cache, off, kv_dtype);",
-                                 "o[d] += w * orc_elem(k_cache, off, kv_dtype);"),
+    "value_row_from_key_cache": ("o[d] += w * (v_mul * orc_elem(v_cache, off, kv_dtype));",
+                                 "o[d] += w * (v_mul * orc_elem(k_cache, off, kv_dtype));"),
+    "v_scale_not_applied": ("o[d] += w * (v_mul * orc_elem(v_cache, off, kv_dtype));",
+                            "o[d] += w * orc_elem(v_cache, off, kv_dtype);"),
+    "k_scale_used_for_q": ("dot += (q_mul * orc_elem(q, q_off + d, dtype)) * (k_mul * orc_elem(k_cache, off, kv_dtype));",
+                           "dot += (k_mul * orc_elem(q, q_off + d, dtype)) * (k_mul * orc_elem(k_cache, off, kv_dtype));"),
+    "prefill_query_read_as_cache_type": (
+        "err |= orc_attend_row(q, r * d_qk, q_dtype, q_scale, k_scale, v_scale, k_cache, v_cache, kv_dtype,",
+        "err |= orc_attend_row(q, r * d_qk, kv_dtype, q_scale, k_scale, v_scale, k_cache, v_cache, kv_dtype,"),
 }
 
 

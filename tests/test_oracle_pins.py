@@ -500,6 +500,62 @@ def test_prefill_noncausal_matches_library():
         off += n
 
 
+FP8_PREFILL = [
+    # (q stored as, caches stored as)
+    (wl.E4M3, wl.E4M3),
+    (None, wl.E4M3),
+    (wl.E4M3, None),
+]
+
+
+@pytest.mark.parametrize("qd,kvd", FP8_PREFILL, ids=["q8_kv8", "q16_kv8", "q8_kv16"])
+def test_prefill_fp8_equals_rescaled_16bit(qd, kvd):
+    # Powers of two keep (stored value x scale) an exact bf16 value, so the
+    # FP8 prefill must equal the 16-bit prefill over the rescaled tensors,
+    # decoded by torch's float8 type (not the oracle's decoder)
+    qs, ks, vs = 2.0, 0.25, 0.5
+    c8 = _small_prefill([7, 3], [9, 3], q_dtype=qd, kv_dtype=kvd, q_scale=qs if qd else 1.0,
+                        k_scale=ks if kvd else 1.0, v_scale=vs if kvd else 1.0)
+
+    def rescale(t, f):
+        return (t.to(torch.float64) * f).to(torch.bfloat16)
+
+    q16 = rescale(c8.q, c8.q_scale)
+    k16, v16 = rescale(c8.pool.k, c8.k_scale), rescale(c8.pool.v, c8.v_scale)
+    assert torch.equal(q16.double(), c8.q.double() * c8.q_scale)  # exact
+    p16 = dataclasses.replace(c8.pool, storage=(k16, v16), k=k16, v=v16)
+    c16 = dataclasses.replace(c8, q=q16, pool=p16, q_dtype=None, kv_dtype=None, q_scale=1.0,
+                              k_scale=1.0, v_scale=1.0)
+    a, b = oracle_prefill(c8), oracle_prefill(c16)
+    assert a[2] == b[2] == 0
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12, atol=1e-14)
+
+
+def test_prefill_fp8_scales_match_library():
+    # arbitrary scales: q_scale and k_scale multiply the logits, v_scale the
+    # output; against library attention on torch-dequantised tensors
+    q_lens, kv_lens = [5, 4], [8, 4]
+    c = _small_prefill(q_lens, kv_lens, q_dtype=wl.E4M3, kv_dtype=wl.E4M3, q_scale=0.37,
+                       k_scale=1.9, v_scale=0.61)
+    out, lse, err = oracle_prefill(c)
+    assert err == 0
+    off = 0
+    for b, (nq, nk) in enumerate(zip(q_lens, kv_lens)):
+        k, v = wl.read_tokens(c.pool, c.pt, b)
+        g = c.num_qo_heads // c.num_kv_heads
+        q = c.q[off:off + nq].double() * c.q_scale
+        k = expand_heads(k.double() * c.k_scale, g)
+        v = expand_heads(v.double() * c.v_scale, g)
+        for i in range(nq):
+            vis = nk - nq + i + 1
+            ref = sdpa64(q[i:i + 1], k[:vis], v[:vis], c.scale)
+            np.testing.assert_allclose(out[off + i], ref[0].numpy(), rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(lse[off + i], logsumexp64(q[i:i + 1], k[:vis], c.scale)[0].numpy(),
+                                       rtol=1e-12, atol=1e-13)
+        off += nq
+
+
 def test_prefill_causal_ignores_later_keys():
     c = _small_prefill([6], [6])
     out, lse, _ = oracle_prefill(c)
