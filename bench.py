@@ -359,6 +359,25 @@ def make_next_parts(rank: int, dev):
     def run_append8():
         pk.paged_append(a8.append_key, a8.append_value, bi8, pos8, pool8, kvi8, kvp8, last8, kv_layout="NHD")
     parts.append(Part("append_e4m3", run_append8, append_bytes(a8), "GB/s", "hbm", "append.cu"))
+
+    # the ragged prefill (d_qk 128) over an E4M3 query and E4M3 caches, with
+    # device scales: the call widens them, then attends (both timed)
+    pf = wl.ragged_prefill(seed=rank_seed(rank), d_qk=128, device=dev, q_dtype=wl.E4M3,
+                           kv_dtype=wl.E4M3)
+    fws = torch.zeros(pk.paged_prefill_fp8_workspace_size(
+        16, 32, 8, pf.max_q, pf.max_kv, pf.q.shape[0], 128, 128, pf.q.dtype, pf.pool.k.dtype),
+        dtype=torch.uint8, device=dev)
+    flq, flkv, fbt = pf.seq_lens_q.to(dev), pf.seq_lens_kv.to(dev), pf.block_tables.to(dev)
+    fout = torch.empty((pf.q.shape[0], 32, 128), dtype=torch.bfloat16, device=dev)
+    flse = torch.empty((pf.q.shape[0], 32), dtype=torch.float32, device=dev)
+    qs, kscale, vscale = (torch.ones(1, device=dev) for _ in range(3))
+
+    def run_prefill8():
+        pk.paged_prefill(pf.q, pf.pool.k, pf.pool.v, pf.scale, fws, pf.max_q, pf.max_kv, flq, flkv,
+                         fbt, causal=True, out=fout, lse=flse, kv_layout="HND", q_scale=qs,
+                         k_scale=kscale, v_scale=vscale)
+    parts.append(Part("prefill_d128_e4m3", run_prefill8, prefill_flops(pf), "TFLOP/s", "tensor",
+                      "prefill.cu"))
     return parts
 
 
@@ -541,7 +560,9 @@ def run_ours(args):
                                           "multi-token decode on the long-context shape (1..4 query "
                                           "tokens per request); the ragged prefill (d_qk 128) with "
                                           "contiguous, non-paged K/V; the Llama-shaped decode and the "
-                                          "4096-request append over an E4M3 (FP8) cache"),
+                                          "4096-request append over an E4M3 (FP8) cache; the ragged "
+                                          "prefill (d_qk 128) over an E4M3 query and E4M3 caches "
+                                          "(the call's widening pass included)"),
         "e2e": {"value": round(allreduce_sum(float(llama.work), ws, dev) / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),

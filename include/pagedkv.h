@@ -383,6 +383,50 @@ int paged_prefill_ex(const void *q, int64_t total_q, const void *k_cache,
                      const int32_t *batch_offsets_o, const int32_t *batch_offsets_k,
                      const int32_t *batch_offsets_v, int32_t *err_word, void *stream);
 
+/*
+ * paged_prefill_fp8 -- [prefill] with the page's q_scale, k_scale and
+ * v_scale: the query and/or the paged caches hold E4M3 (OCP FP8, one byte
+ * per element) values, dequantised as q_scale * q, k_scale * k and
+ * v_scale * v.  The output is out_dtype (PKV_F16 or PKV_BF16, the page's
+ * o_data_type); lse is the log-sum-exp of the dequantised logits.
+ *  - q_dtype: PKV_E4M3 or out_dtype; kv_dtype: PKV_E4M3 or out_dtype.
+ *  - q_scale, k_scale, v_scale: NULL (1) or a device pointer to one fp32
+ *    value, read when the kernels run (a captured graph follows later
+ *    writes).
+ *  - Page strides are in elements (bytes for E4M3); E4M3 caches need
+ *    16-byte aligned bases and page strides that are multiples of 16.
+ *  - Paged caches only (block_tables non-NULL); packed rows (no batch
+ *    offsets).
+ *  - workspace: >= paged_prefill_fp8_workspace_size(...) bytes, 256-byte
+ *    aligned.  E4M3 inputs are widened (exactly: every E4M3 value is an fp16
+ *    and a bf16 value) into it before the attention kernel: the query rows,
+ *    and the caches packed request by request, for which it reserves
+ *    batch_size * max_sequence_kv keys.
+ * Device errors as paged_prefill (a page id outside the pool flags
+ * PKV_DEV_ERR_PAGE and its keys read as zeros).  Host errors: a dtype other
+ * than those above or no block table -> PKV_ERR_INVALID_ARG; misaligned
+ * E4M3 caches -> PKV_ERR_INVALID_ARG; the rest as paged_prefill.
+ */
+size_t paged_prefill_fp8_workspace_size(int32_t batch_size, int32_t num_qo_heads,
+                                        int32_t num_kv_heads,
+                                        int32_t max_token_per_sequence,
+                                        int32_t max_sequence_kv, int64_t total_q,
+                                        int32_t d_qk, int32_t d_vo, int32_t q_dtype,
+                                        int32_t kv_dtype);
+int paged_prefill_fp8(const void *q, int64_t total_q, const void *k_cache,
+                      const void *v_cache, int64_t k_page_stride,
+                      int64_t v_page_stride, int64_t max_num_pages, float scale,
+                      const float *q_scale, const float *k_scale, const float *v_scale,
+                      void *workspace, size_t workspace_bytes,
+                      int32_t max_token_per_sequence, int32_t max_sequence_kv,
+                      const int32_t *actual_seq_lens_q,
+                      const int32_t *actual_seq_lens_kv, const int32_t *block_tables,
+                      int32_t block_table_stride, int32_t batch_size, int32_t causal,
+                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                      int32_t d_vo, int32_t page_size, int32_t layout, int32_t q_dtype,
+                      int32_t kv_dtype, int32_t out_dtype, void *out, float *lse,
+                      int32_t *err_word, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

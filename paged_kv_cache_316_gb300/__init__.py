@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     paged_decode,
     paged_decode_noalloc,
     paged_prefill_workspace_size,
+    paged_prefill_fp8_workspace_size,
     paged_prefill,
     kernel_launches,
 )

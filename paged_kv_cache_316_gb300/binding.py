@@ -56,6 +56,10 @@ _SIGNATURES = {
                           _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
                           _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                           _c_p], ctypes.c_int),
+    "paged_prefill_fp8_workspace_size": ([_i32] * 5 + [_i64] + [_i32] * 4, _sz),
+    "paged_prefill_fp8": ([_c_p, _i64, _c_p, _c_p, _i64, _i64, _i64, _f32, _c_p, _c_p, _c_p, _c_p,
+                           _sz, _i32, _i32, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32,
+                           _i32, _i32, _i32, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p], ctypes.c_int),
 }
 
 
@@ -318,16 +322,40 @@ def paged_prefill_workspace_size(batch_size, num_qo_heads, max_token_per_sequenc
         batch_size, num_qo_heads, max_token_per_sequence, max_sequence_kv))
 
 
+def paged_prefill_fp8_workspace_size(batch_size, num_qo_heads, num_kv_heads,
+                                     max_token_per_sequence, max_sequence_kv, total_q, d_qk, d_vo,
+                                     q_dtype, kv_dtype) -> int:
+    """Workspace of paged_prefill with an E4M3 query and/or caches (dtypes
+    as torch dtypes)."""
+    return int(load_library().paged_prefill_fp8_workspace_size(
+        batch_size, num_qo_heads, num_kv_heads, max_token_per_sequence, max_sequence_kv, total_q,
+        d_qk, d_vo, E4M3 if q_dtype == torch.float8_e4m3fn else BF16,
+        E4M3 if kv_dtype == torch.float8_e4m3fn else BF16))
+
+
+def _scale_ptr(t, device):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() != 1 or t.device != device:
+        raise PagedKVError("q_scale / k_scale / v_scale: one float32 value on the query's device")
+    return _ptr(t)
+
+
 def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
                   max_token_per_sequence: int, max_sequence_kv: int,
                   actual_seq_lens_q, actual_seq_lens_kv, block_tables,
                   causal: bool = True, out=None, lse=None, kv_layout="HND",
                   err_word=None, stream=None, batch_offsets_q=None, batch_offsets_o=None,
-                  batch_offsets_k=None, batch_offsets_v=None):
+                  batch_offsets_k=None, batch_offsets_v=None, q_scale=None, k_scale=None,
+                  v_scale=None, o_data_type=None):
     """block_tables=None: k_cache / v_cache are contiguous [rows, Hkv, d]
     tensors (the page's non-paged case; kv_layout is then NHD).  The
     batch_offsets_* tensors ([B] int32 on the device, token rows) place each
-    request's queries, outputs / LSEs and (contiguous K/V) keys / values."""
+    request's queries, outputs / LSEs and (contiguous K/V) keys / values.
+    q and/or the (paged) caches may be float8_e4m3fn: q_scale, k_scale and
+    v_scale (one float32 each on the device, or None for 1) dequantise them,
+    and the output is o_data_type (bf16 when q is E4M3 and none is given);
+    the workspace then needs paged_prefill_fp8_workspace_size bytes."""
     if block_tables is None:
         kv_layout = "NHD"
     layout = _layout_code(kv_layout)
@@ -343,14 +371,30 @@ def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
         dv = v_cache.shape[3]
     if dk != d_qk:
         raise PagedKVError("q head_dim differs from the key cache's")
+    e4 = torch.float8_e4m3fn
+    fp8 = q.dtype == e4 or k_cache.dtype == e4 or any(x is not None for x in (q_scale, k_scale, v_scale))
+    odt = o_data_type or (torch.bfloat16 if q.dtype == e4 else q.dtype)
     if out is None:
-        out = torch.empty((total_q, Hqo, dv), dtype=q.dtype, device=q.device)
+        out = torch.empty((total_q, Hqo, dv), dtype=odt, device=q.device)
     if lse is None:
         lse = torch.empty((total_q, Hqo), dtype=torch.float32, device=q.device)
     B = actual_seq_lens_q.shape[0]
     bt_stride = 0 if block_tables is None else block_tables.stride(0)
     offsets = (batch_offsets_q, batch_offsets_o, batch_offsets_k, batch_offsets_v)
-    if all(o is None for o in offsets):
+    if fp8:
+        if block_tables is None or any(o is not None for o in offsets):
+            raise PagedKVError("the E4M3 prefill takes paged caches and packed rows")
+        if v_cache.dtype != k_cache.dtype:
+            raise PagedKVError("k_cache and v_cache hold the same element type")
+        _check(load_library().paged_prefill_fp8(
+            _ptr(q), total_q, _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
+            P, scale, _scale_ptr(q_scale, q.device), _scale_ptr(k_scale, q.device),
+            _scale_ptr(v_scale, q.device), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            max_token_per_sequence, max_sequence_kv, _ptr(actual_seq_lens_q),
+            _ptr(actual_seq_lens_kv), _ptr(block_tables), bt_stride, B, int(causal), Hqo, Hkv, d_qk,
+            dv, S, layout, _dtype_code(q), _dtype_code(k_cache), _dtype_code(out), _ptr(out),
+            _ptr(lse), _ptr(err_word), _stream(stream)))
+    elif all(o is None for o in offsets):
         _check(load_library().paged_prefill(
             _ptr(q), total_q, _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), v_cache.stride(0),
             P, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),

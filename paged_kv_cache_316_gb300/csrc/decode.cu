@@ -46,16 +46,6 @@ struct DecSmem {
 };
 __device__ __forceinline__ int swz8(int r, int c) { return r * kDec8RowBytes + ((c ^ (r & 7)) << 4); }
 
-// Two E4M3 values (low byte first) widened exactly to fp16 (every E4M3
-// value is an fp16 value).
-template <typename T>
-__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two);
-template <>
-__device__ __forceinline__ uint32_t widen_e4m3x2<__half>(uint32_t two) {
-    uint32_t h;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h) : "h"(static_cast<unsigned short>(two)));
-    return h;
-}
 __device__ __forceinline__ float2 unpack2_bf16(uint32_t w) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
 }

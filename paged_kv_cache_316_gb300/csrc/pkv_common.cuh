@@ -137,6 +137,24 @@ __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Two E4M3 values (low byte first) widened exactly to a 16-bit pair: every
+// E4M3 value is an fp16 and a bf16 value.  To bf16 through fp16 and fp32,
+// each step exact.
+template <typename T>
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two);
+template <>
+__device__ __forceinline__ uint32_t widen_e4m3x2<__half>(uint32_t two) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h) : "h"(static_cast<unsigned short>(two)));
+    return h;
+}
+template <>
+__device__ __forceinline__ uint32_t widen_e4m3x2<__nv_bfloat16>(uint32_t two) {
+    const uint32_t h = widen_e4m3x2<__half>(two);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack2<__nv_bfloat16>(f.x, f.y);
+}
+
 // 2^x on the special-function unit (PTX ex2.approx; -inf -> 0).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

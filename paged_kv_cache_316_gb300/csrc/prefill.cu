@@ -90,6 +90,9 @@ struct PrefillParams {
     // keys/values; NULL = packed by the prefix sums
     const int32_t *off_q, *off_o, *off_k, *off_v;
     int *work_counter;  // in the workspace, zeroed by the plan kernel
+    // device-resident dequantisation factors of E4M3 inputs (NULL: 1):
+    // q_scale * k_scale multiplies the logits, v_scale the output
+    const float *q_scale, *k_scale, *v_scale;
     void *out;
     float *lse;
     int32_t *err;
@@ -621,7 +624,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         const uint32_t s_addr = t_lane + X * S_STRIDE + hh * HC;
         const uint32_t o_addr = t_lane + O_COL + X * kPfDV + hh * (kPfDV / SPLIT);
         const uint32_t b_pair = b_xchg(X * 4 + qd);
-        const float sc = p.scale_log2;
+        const float sc = p.scale_log2 * (p.q_scale ? __ldg(p.q_scale) : 1.f) * (p.k_scale ? __ldg(p.k_scale) : 1.f);
+        const float v_mul = p.v_scale ? __ldg(p.v_scale) : 1.f;
         const bool pos_scale = sc > 0.f;  // max on raw scores, one FFMA scales and shifts
         const float k_mul = pos_scale ? sc : 1.f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
@@ -818,7 +822,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             const int qi = it.i0 + r;
             const int64_t grow = static_cast<int64_t>(it.orow_base) + r;
             const bool valid = qi < it.qb && grow >= 0 && grow < p.total_q;
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float inv = lt > 0.f ? v_mul / lt : 0.f;
             T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + hh * (kPfDV / SPLIT);
 #pragma unroll
             for (int c = 0; c < kPfDV / 32 / SPLIT; ++c) {
@@ -877,6 +881,98 @@ static int launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
         return PKV_ERR_CUDA;
     return PKV_OK;
 }
+
+// ---- E4M3 (FP8) inputs --------------------------------------------------------
+// The tensor-core path multiplies 16-bit operands.  E4M3 query rows and cache
+// rows are widened into the workspace first -- exactly: every E4M3 value is a
+// bf16 and an fp16 value -- the caches packed request by request as
+// contiguous [rows, Hkv, d] tensors (request b at rows cu_kv[b] ..); the
+// scale tensors are applied inside the main kernel.
+struct WidenKvParams {
+    const uint8_t *src[2];  // K, V caches, one byte per element
+    int64_t page_stride[2];
+    int d[2];
+    void *dst[2];           // widened K, V: [rows, Hkv, d] of the 16-bit type
+    int64_t max_num_pages;
+    const int32_t *block_tables;
+    int64_t bt_stride;
+    const int32_t *seq_lens_kv;
+    const int32_t *cu_kv;   // from the plan kernel
+    int max_kv, Hkv, page_shift;
+    int32_t *err;
+};
+constexpr int kWidenTok = 32;  // keys per CTA of the cache widening
+
+// CTA (key block, request, K or V): every 16-byte source chunk of its keys
+// becomes 32 bytes of the packed 16-bit tensor.  A page id outside the pool
+// flags PKV_DEV_ERR_PAGE and its rows widen to zeros, as the 16-bit path's
+// zero-filled rows.
+template <typename T, int LAYOUT>
+__global__ void __launch_bounds__(256) prefill_widen_kv_kernel(const WidenKvParams w) {
+    pdl_wait();  // cu_kv
+    pdl_launch_dependents();
+    const int b = blockIdx.y, z = blockIdx.z;
+    const int kvb = min(max(w.seq_lens_kv[b], 0), w.max_kv);
+    const int j0 = blockIdx.x * kWidenTok;
+    if (j0 >= kvb) return;
+    const int d = w.d[z], CH = d / 16;
+    const int S = 1 << w.page_shift;
+    const int64_t row0 = w.cu_kv[b];
+    const int n = min(kWidenTok, kvb - j0) * w.Hkv * CH;
+    const int32_t *bt = w.block_tables + b * w.bt_stride;
+    T *dst = static_cast<T *>(w.dst[z]);
+    for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
+        const int c = idx % CH, rest = idx / CH;
+        const int h = rest % w.Hkv, j = j0 + rest / w.Hkv;
+        const int page = bt[j >> w.page_shift];
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (page < 0 || page >= w.max_num_pages) {
+            if (z == 0 && h == 0 && c == 0) set_err(w.err, PKV_DEV_ERR_PAGE);
+        } else {
+            raw = *reinterpret_cast<const uint4 *>(
+                w.src[z] + kv_row_offset<LAYOUT>(page, w.page_stride[z], h, j & (S - 1), w.Hkv, S, d) + c * 16);
+        }
+        const uint32_t x[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[2 * i] = widen_e4m3x2<T>(x[i] & 0xffffu);
+            o[2 * i + 1] = widen_e4m3x2<T>(x[i] >> 16);
+        }
+        uint4 *out = reinterpret_cast<uint4 *>(dst + ((row0 + j) * w.Hkv + h) * d + c * 16);
+        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// n16 chunks of 16 E4M3 values (the query rows) -> 16-bit, in order.
+template <typename T>
+__global__ void __launch_bounds__(256) widen_rows_kernel(const uint8_t *__restrict__ src, T *__restrict__ dst,
+                                                         int64_t n16) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 raw = reinterpret_cast<const uint4 *>(src)[i];
+        const uint32_t x[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            o[2 * k] = widen_e4m3x2<T>(x[k] & 0xffffu);
+            o[2 * k + 1] = widen_e4m3x2<T>(x[k] >> 16);
+        }
+        uint4 *out = reinterpret_cast<uint4 *>(dst) + 2 * i;
+        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// What an E4M3 call adds to the 16-bit path.
+struct PrefillFp8 {
+    const float *q_scale = nullptr, *k_scale = nullptr, *v_scale = nullptr;
+    const uint8_t *q_src = nullptr;  // E4M3 query rows, widened into the call's `q` first
+    bool kv8 = false;                // widen the paged caches after the plan kernel
+    WidenKvParams widen{};           // (cu_kv and err filled in by prefill_impl)
+    int layout = PKV_HND;            // of the E4M3 caches
+};
 
 template <typename T>
 static int dispatch_prefill(int d_qk, int layout, const CUtensorMap &tq, const CUtensorMap &tk,
@@ -959,7 +1055,7 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
                              int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
                              void *out, float *lse, int32_t *err_word, void *stream,
                              const int32_t *off_q, const int32_t *off_o, const int32_t *off_k,
-                             const int32_t *off_v) {
+                             const int32_t *off_v, PrefillFp8 *f8 = nullptr) {
     // no block table: contiguous K/V of max_num_pages rows, page strides are row strides
     const bool contiguous = block_tables == nullptr;
     if (contiguous) {
@@ -1023,6 +1119,19 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    if (f8 && f8->q_src) {  // E4M3 query rows -> the 16-bit rows `q` points at
+        const int64_t n16 = total_q * num_qo_heads * d_qk / 16;
+        const int64_t cap = 8LL * num_sms();
+        const unsigned blocks = static_cast<unsigned>((n16 + 255) / 256 < cap ? (n16 + 255) / 256 : cap);
+        if (dtype == PKV_BF16)
+            widen_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+                f8->q_src, static_cast<__nv_bfloat16 *>(const_cast<void *>(q)), n16);
+        else
+            widen_rows_kernel<__half><<<blocks, 256, 0, st>>>(f8->q_src, static_cast<__half *>(const_cast<void *>(q)),
+                                                              n16);
+        ++launches;
+    }
     const size_t cu_bytes = round_up(static_cast<size_t>(batch_size + 1) * sizeof(int32_t), 256);
     int32_t *cu_q = static_cast<int32_t *>(workspace);
     int32_t *cu_items = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + cu_bytes);
@@ -1032,6 +1141,24 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     prefill_plan_kernel<<<1, 32, 0, st>>>(actual_seq_lens_q, actual_seq_lens_kv, batch_size, num_kv_heads * pairs,
                                           max_token_per_sequence, max_sequence_kv, cu_q, cu_items, cu_kv, err_word,
                                           work_counter);
+    ++launches;
+    if (f8 && f8->kv8) {
+        // widen the E4M3 caches (needs cu_kv); the main kernel then reads them
+        // as contiguous K/V
+        f8->widen.cu_kv = cu_kv;
+        f8->widen.err = err_word;
+        const dim3 wgrid(static_cast<unsigned>((max_sequence_kv + kWidenTok - 1) / kWidenTok),
+                         static_cast<unsigned>(batch_size), 2);
+        if (max_sequence_kv > 0) {
+            auto wk = dtype == PKV_BF16
+                          ? (f8->layout == PKV_HND ? prefill_widen_kv_kernel<__nv_bfloat16, PKV_HND>
+                                                   : prefill_widen_kv_kernel<__nv_bfloat16, PKV_NHD>)
+                          : (f8->layout == PKV_HND ? prefill_widen_kv_kernel<__half, PKV_HND>
+                                                   : prefill_widen_kv_kernel<__half, PKV_NHD>);
+            if (launch_dependent(wk, wgrid, dim3(256), 0, st, f8->widen) != cudaSuccess) return PKV_ERR_CUDA;
+            ++launches;
+        }
+    }
     PrefillParams p;
     p.max_num_pages = max_num_pages;
     p.total_q = total_q;
@@ -1058,11 +1185,13 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     p.max_q = max_token_per_sequence;
     p.max_kv = max_sequence_kv;
     p.work_counter = work_counter;
+    p.q_scale = f8 ? f8->q_scale : nullptr;
+    p.k_scale = f8 ? f8->k_scale : nullptr;
+    p.v_scale = f8 ? f8->v_scale : nullptr;
     p.out = out;
     p.lse = lse;
     p.err = err_word;
     const int n_qt = (max_token_per_sequence + kPfRows - 1) / kPfRows;
-    int launches = 1;
     const int64_t items = static_cast<int64_t>(n_qt) * num_kv_heads * pairs * batch_size;
     if (n_qt > 0) {
         // persistent: one CTA per SM (the shared-memory footprint allows one)
@@ -1112,4 +1241,116 @@ extern "C" int paged_prefill_ex(const void *q, int64_t total_q, const void *k_ca
                         actual_seq_lens_kv, block_tables, block_table_stride, batch_size, causal, num_qo_heads,
                         num_kv_heads, d_qk, d_vo, page_size, layout, dtype, out, lse, err_word, stream,
                         batch_offsets_q, batch_offsets_o, batch_offsets_k, batch_offsets_v);
+}
+
+// ---- E4M3 (FP8) query and/or caches ----------------------------------------------
+
+// Workspace of paged_prefill_fp8: the 16-bit path's, then the widened query
+// rows (E4M3 query) and the widened, packed K and V (E4M3 caches; room for
+// batch_size * max_sequence_kv keys, the most the lengths allow).
+static size_t prefill_fp8_ws_bytes(int B, int Hqo, int Hkv, int max_kv, int64_t total_q, int d_qk, int d_vo,
+                                   bool q8, bool kv8, size_t *q_off, size_t *k_off, size_t *v_off) {
+    size_t off = prefill_ws_bytes(B);
+    *q_off = off;
+    if (q8) off += round_up(static_cast<size_t>(total_q) * Hqo * d_qk * 2, 256);
+    *k_off = off;
+    const size_t rows = static_cast<size_t>(B) * max_kv;
+    if (kv8) off += round_up(rows * Hkv * d_qk * 2, 256);
+    *v_off = off;
+    if (kv8) off += round_up(rows * Hkv * d_vo * 2, 256);
+    return off;
+}
+
+extern "C" size_t paged_prefill_fp8_workspace_size(int32_t batch_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                                                   int32_t max_token_per_sequence, int32_t max_sequence_kv,
+                                                   int64_t total_q, int32_t d_qk, int32_t d_vo, int32_t q_dtype,
+                                                   int32_t kv_dtype) {
+    if (batch_size < 0 || num_qo_heads < 1 || num_kv_heads < 1 || max_token_per_sequence < 0 ||
+        max_sequence_kv < 0 || total_q < 0 || d_qk < 1 || d_vo < 1)
+        return 0;
+    size_t a, b, c;
+    return prefill_fp8_ws_bytes(batch_size, num_qo_heads, num_kv_heads, max_sequence_kv, total_q, d_qk, d_vo,
+                                q_dtype == PKV_E4M3, kv_dtype == PKV_E4M3, &a, &b, &c);
+}
+
+extern "C" int paged_prefill_fp8(const void *q, int64_t total_q, const void *k_cache, const void *v_cache,
+                                 int64_t k_page_stride, int64_t v_page_stride, int64_t max_num_pages, float scale,
+                                 const float *q_scale, const float *k_scale, const float *v_scale, void *workspace,
+                                 size_t workspace_bytes, int32_t max_token_per_sequence, int32_t max_sequence_kv,
+                                 const int32_t *actual_seq_lens_q, const int32_t *actual_seq_lens_kv,
+                                 const int32_t *block_tables, int32_t block_table_stride, int32_t batch_size,
+                                 int32_t causal, int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
+                                 int32_t d_vo, int32_t page_size, int32_t layout, int32_t q_dtype,
+                                 int32_t kv_dtype, int32_t out_dtype, void *out, float *lse, int32_t *err_word,
+                                 void *stream) {
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    const bool q8 = q_dtype == PKV_E4M3, kv8 = kv_dtype == PKV_E4M3;
+    if ((!q8 && q_dtype != out_dtype) || (!kv8 && kv_dtype != out_dtype)) return PKV_ERR_INVALID_ARG;
+    if (!block_tables) return PKV_ERR_INVALID_ARG;  // paged caches
+    if (batch_size < 0 || num_qo_heads < 1 || num_kv_heads < 1 || max_token_per_sequence < 0 ||
+        max_sequence_kv < 0 || max_num_pages < 0 || block_table_stride < 0 || total_q < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
+    if (num_qo_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if ((d_qk != 128 && d_qk != 192) || d_vo != 128) return PKV_ERR_UNSUPPORTED;
+    if (ilog2_exact(page_size) < 3 || page_size > 256) return PKV_ERR_UNSUPPORTED;
+    if (batch_size > 65535 || static_cast<int64_t>(batch_size) * max_sequence_kv > 0x7fffffff)
+        return PKV_ERR_UNSUPPORTED;
+    if (k_page_stride < static_cast<int64_t>(num_kv_heads) * page_size * d_qk ||
+        v_page_stride < static_cast<int64_t>(num_kv_heads) * page_size * d_vo ||
+        static_cast<int64_t>(block_table_stride) * page_size < max_sequence_kv)
+        return PKV_ERR_INVALID_ARG;
+    if (batch_size == 0 || total_q == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !actual_seq_lens_q || !actual_seq_lens_kv || !out || !lse)
+        return PKV_ERR_NULL;
+    // 16-byte page starts and rows (an E4M3 element is one byte)
+    if (kv8 && (!aligned16(k_cache) || !aligned16(v_cache) || (k_page_stride % 16) || (v_page_stride % 16)))
+        return PKV_ERR_INVALID_ARG;
+    if (q8 && !aligned16(q)) return PKV_ERR_INVALID_ARG;
+    size_t q_off, k_off, v_off;
+    const size_t need = prefill_fp8_ws_bytes(batch_size, num_qo_heads, num_kv_heads, max_sequence_kv, total_q,
+                                             d_qk, d_vo, q8, kv8, &q_off, &k_off, &v_off);
+    if (!workspace) return PKV_ERR_NULL;
+    if (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255)) return PKV_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    PrefillFp8 f8;
+    f8.q_scale = q_scale;
+    f8.k_scale = k_scale;
+    f8.v_scale = v_scale;
+    const void *qq = q;
+    if (q8) {
+        f8.q_src = static_cast<const uint8_t *>(q);
+        qq = ws + q_off;
+    }
+    if (!kv8)
+        return prefill_impl(qq, total_q, k_cache, v_cache, k_page_stride, v_page_stride, max_num_pages, scale,
+                            workspace, workspace_bytes, max_token_per_sequence, max_sequence_kv,
+                            actual_seq_lens_q, actual_seq_lens_kv, block_tables, block_table_stride, batch_size,
+                            causal, num_qo_heads, num_kv_heads, d_qk, d_vo, page_size, layout, out_dtype, out, lse,
+                            err_word, stream, nullptr, nullptr, nullptr, nullptr, &f8);
+    f8.kv8 = true;
+    f8.layout = layout;
+    WidenKvParams &w = f8.widen;
+    w.src[0] = static_cast<const uint8_t *>(k_cache);
+    w.src[1] = static_cast<const uint8_t *>(v_cache);
+    w.page_stride[0] = k_page_stride;
+    w.page_stride[1] = v_page_stride;
+    w.d[0] = d_qk;
+    w.d[1] = d_vo;
+    w.dst[0] = ws + k_off;
+    w.dst[1] = ws + v_off;
+    w.max_num_pages = max_num_pages;
+    w.block_tables = block_tables;
+    w.bt_stride = block_table_stride;
+    w.seq_lens_kv = actual_seq_lens_kv;
+    w.max_kv = max_sequence_kv;
+    w.Hkv = num_kv_heads;
+    w.page_shift = ilog2_exact(page_size);
+    // the main kernel reads the widened caches as contiguous K/V: [rows, Hkv, d]
+    const int64_t rows = static_cast<int64_t>(batch_size) * max_sequence_kv;
+    return prefill_impl(qq, total_q, ws + k_off, ws + v_off, static_cast<int64_t>(num_kv_heads) * d_qk,
+                        static_cast<int64_t>(num_kv_heads) * d_vo, rows, scale, workspace, workspace_bytes,
+                        max_token_per_sequence, max_sequence_kv, actual_seq_lens_q, actual_seq_lens_kv, nullptr, 0,
+                        batch_size, causal, num_qo_heads, num_kv_heads, d_qk, d_vo, 1, PKV_NHD, out_dtype, out, lse,
+                        err_word, stream, nullptr, nullptr, nullptr, nullptr, &f8);
 }

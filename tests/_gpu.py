@@ -66,12 +66,24 @@ def decode_on_gpu(c: wl.DecodeCase, with_lse=True, err_word=None, layout=None, w
 
 def prefill_on_gpu(c: wl.PrefillCase, err_word=None):
     B = c.seq_lens_q.shape[0]
-    ws = torch.zeros(pk.paged_prefill_workspace_size(B, c.num_qo_heads, c.max_q, c.max_kv),
-                     dtype=torch.uint8, device=DEV)
+    fp8 = c.q_dtype == wl.E4M3 or c.kv_dtype == wl.E4M3
+    if fp8:
+        nbytes = pk.paged_prefill_fp8_workspace_size(
+            B, c.num_qo_heads, c.num_kv_heads, c.max_q, c.max_kv, c.q.shape[0], c.d_qk, c.d_vo,
+            c.q.dtype, c.pool.k.dtype)
+    else:
+        nbytes = pk.paged_prefill_workspace_size(B, c.num_qo_heads, c.max_q, c.max_kv)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    kw = {}
+    if fp8:
+        def dev_scale(x):
+            return torch.tensor([x], dtype=torch.float32, device=DEV)
+        kw = dict(q_scale=dev_scale(c.q_scale), k_scale=dev_scale(c.k_scale),
+                  v_scale=dev_scale(c.v_scale), o_data_type=wl.torch_dtype(c.dtype))
     out, lse = pk.paged_prefill(c.q.to(DEV), c.pool.k.to(DEV), c.pool.v.to(DEV), c.scale, ws,
                                 c.max_q, c.max_kv, c.seq_lens_q.to(DEV), c.seq_lens_kv.to(DEV),
                                 c.block_tables.to(DEV), causal=c.causal,
-                                kv_layout=c.pool.layout, err_word=err_word)
+                                kv_layout=c.pool.layout, err_word=err_word, **kw)
     torch.cuda.synchronize()
     return out, lse
 
@@ -85,8 +97,12 @@ def compact_request(pool: wl.Pool, pt: wl.PageTable, b: int, kv_len: int | None 
     table row -- for checking sampled requests of a full-size case."""
     pages = pt.pages[b]
     idx = torch.tensor(pages, dtype=torch.long, device=pool.k.device)
-    k = pool.k.index_select(0, idx).cpu().contiguous()
-    v = pool.v.index_select(0, idx).cpu().contiguous()
+
+    def pick(t):  # (through a byte view for 8-bit floats)
+        if t.element_size() == 1:
+            return t.view(torch.uint8).index_select(0, idx).cpu().contiguous().view(t.dtype)
+        return t.index_select(0, idx).cpu().contiguous()
+    k, v = pick(pool.k), pick(pool.v)
     sub = wl.Pool((k, v), k, v, pool.layout, len(pages), pool.num_heads, pool.page_size,
                   pool.d_k, pool.d_v, k[0].numel(), v[0].numel())
     L = pt.lengths[b] if kv_len is None else kv_len

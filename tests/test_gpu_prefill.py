@@ -177,3 +177,64 @@ def test_batch_offsets_place_rows():
         assert_lse_close(lse[rows], rl[cu_q[b]:cu_q[b + 1]], f"request {b} lse")
         written[rows] = True
     assert torch.all(out[~written.to(DEV)].float() == 3.0) and torch.all(lse[~written.to(DEV)] == 3.0)
+
+
+FP8_CASES = [
+    # q lens, kv lens, page, Hqo, Hkv, d_qk, causal, out dtype, layout, E4M3 query, E4M3 caches, seed
+    ([130, 7, 64], [200, 7, 300], 32, 32, 8, 128, True, wl.BF16, wl.HND, True, True, 11),
+    ([1, 255, 129], [1, 255, 700], 32, 32, 8, 192, True, wl.BF16, wl.HND, False, True, 12),
+    ([300, 50], [300, 333], 16, 8, 8, 128, False, wl.F16, wl.NHD, True, False, 13),
+    ([64, 200], [500, 200], 64, 16, 2, 192, False, wl.BF16, wl.NHD, True, True, 14),
+    ([77, 300], [500, 300], 16, 16, 4, 192, True, wl.F16, wl.HND, True, True, 15),
+    ([200], [333], 8, 6, 2, 128, True, wl.BF16, wl.HND, False, True, 16),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[f"f{i}" for i in range(len(FP8_CASES))])
+def test_fp8_small_shapes(case):
+    lq, lkv, S, hq, hk, dqk, causal, dt, lay, q8, kv8, seed = case
+    c = wl.prefill_case(lq, lkv, S, hq, hk, dqk, 128, lay, dt, causal=causal, seed=seed, slack=0.2,
+                        q_dtype=wl.E4M3 if q8 else None, kv_dtype=wl.E4M3 if kv8 else None,
+                        q_scale=0.37 if q8 else 1.0, k_scale=1.9 if kv8 else 1.0,
+                        v_scale=0.61 if kv8 else 1.0)
+    _check(c)
+
+
+def test_fp8_with_unit_scales_equals_16bit_on_widened_values():
+    # every E4M3 value is a bf16 value: the E4M3 prefill with unit scales
+    # gives bit for bit the 16-bit prefill over the same values
+    c8 = wl.prefill_case([130, 7, 300], [400, 7, 300], 32, 32, 8, 128, 128, wl.HND, wl.BF16, seed=17,
+                         slack=0.2, q_dtype=wl.E4M3, kv_dtype=wl.E4M3)
+    o8, l8 = prefill_on_gpu(c8)
+    k16, v16 = c8.pool.k.to(torch.bfloat16), c8.pool.v.to(torch.bfloat16)
+    c16 = dataclasses.replace(c8, q=c8.q.to(torch.bfloat16), q_dtype=None, kv_dtype=None,
+                              pool=dataclasses.replace(c8.pool, storage=(k16, v16), k=k16, v=v16))
+    o16, l16 = prefill_on_gpu(c16)
+    assert torch.equal(o8.view(torch.int16), o16.view(torch.int16))
+    assert torch.equal(l8, l16)
+
+
+def test_fp8_bad_page_flagged():
+    c = wl.prefill_case([40], [100], 16, 8, 2, 128, 128, wl.HND, wl.BF16, seed=18, slack=0.5,
+                        q_dtype=wl.E4M3, kv_dtype=wl.E4M3)
+    c.block_tables[0, 2] = c.pool.num_pages + 5
+    err = err_word()
+    prefill_on_gpu(c, err_word=err)
+    assert int(err.item()) & oracle.E_PAGE
+
+
+def test_fp8_ragged_config_full_size_sampled():
+    c = wl.ragged_prefill(d_qk=128, device=DEV, q_dtype=wl.E4M3, kv_dtype=wl.E4M3, q_scale=0.5,
+                          k_scale=1.25, v_scale=0.8)
+    out, lse = prefill_on_gpu(c)
+    lq = c.seq_lens_q.tolist()
+    cu = np.concatenate([[0], np.cumsum(lq)])
+    for b in sorted({0, int(np.argmax(lq)), len(lq) - 1}):
+        pool, pt = compact_request(c.pool, c.pt, b)
+        sub = dataclasses.replace(
+            c, q=c.q[cu[b]:cu[b + 1]].cpu(), pool=pool, pt=pt, block_tables=pt.block_tables(),
+            seq_lens_q=c.seq_lens_q[b:b + 1], seq_lens_kv=c.seq_lens_kv[b:b + 1])
+        ro, rl, _ = oracle_prefill(sub)
+        assert_attn_close(out[cu[b]:cu[b + 1]], ro, f"request {b}")
+        assert_lse_close(lse[cu[b]:cu[b + 1]], rl, f"request {b} lse")
+
