@@ -179,7 +179,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     if (L < Q && s == 0 && kvh == 0 && tid == 0) set_err(p.err, PKV_DEV_ERR_QLEN);
     const int k_begin = max(lo, (first + s) * p.chunk);
     const int k_end = min(L, (first + s + 1) * p.chunk);
-    const int n_tiles = k_end > k_begin ? (k_end - k_begin + kDecTile - 1) / kDecTile : 0;
+    // tiles start on 64-key boundaries (a window's first key need not): the
+    // rows before k_begin are zero-filled and masked like rows past the end
+    const int k_tile0 = k_begin & ~(kDecTile - 1);
+    const int n_tiles = k_end > k_begin ? (k_end - k_tile0 + kDecTile - 1) / kDecTile : 0;
 
     const T *kc = static_cast<const T *>(p.k);
     const T *vc = static_cast<const T *>(p.v);
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         {
             const int r0 = kw0 + gtid / LPR, c = gtid % LPR;
             const int jA = j0 + r0, jZ = jA + (NLOAD - 1) * RSTEP;
-            const int page = jZ < k_end && (jA >> p.page_shift) == (jZ >> p.page_shift)
+            const int page = jA >= k_begin && jZ < k_end && (jA >> p.page_shift) == (jZ >> p.page_shift)
                                  ? pages_s[(jA >> p.page_shift) - first_page]
                                  : -1;
             if (__all_sync(0xffffffffu, page >= 0)) {
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                 const int idx = k * MT * 32 + gtid;
                 const int r = kw0 + (idx >> 3), c = idx & 7;
                 const int j = j0 + r;
-                bool ok = j < k_end;
+                bool ok = j >= k_begin && j < k_end;
                 const uint8_t *ks = kc8, *vs = vc8;
                 if (ok) {
                     const int page = pages_s[(j >> p.page_shift) - first_page];
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
             const int idx = k * MT * 32 + gtid;
             const int r = kw0 + (idx >> 4), c = idx & 15;
             const int j = j0 + r;
-            bool ok = j < k_end;
+            bool ok = j >= k_begin && j < k_end;
             const T *ks = kc, *vs = vc;
             if (ok) {
                 const int page = pages_s[(j >> p.page_shift) - first_page];
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     cp_async_commit();
 #pragma unroll
     for (int st = 0; st < kDecStages - 1; ++st) {
-        if (st < n_tiles) load_tile(st, k_begin + st * kDecTile);
+        if (st < n_tiles) load_tile(st, k_tile0 + st * kDecTile);
         cp_async_commit();
     }
     cp_async_wait<kDecStages - 1>();
@@ -409,11 +412,11 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         key_group_sync<MT>(kg);  // the slice landed; the group is done with the stage reloaded next
         {
             int nxt = it + kDecStages - 1;
-            if (nxt < n_tiles) load_tile(nxt % kDecStages, k_begin + nxt * kDecTile);
+            if (nxt < n_tiles) load_tile(nxt % kDecStages, k_tile0 + nxt * kDecTile);
             cp_async_commit();
         }
         const int stage = it % kDecStages;
-        const int j0 = k_begin + it * kDecTile;
+        const int j0 = k_tile0 + it * kDecTile;
         const uint32_t kb = smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t vb = kb + kDecTileBytes;
         const uint8_t *k8 = smem + stage * STAGE_BYTES;  // E4M3 K rows (KV8)
