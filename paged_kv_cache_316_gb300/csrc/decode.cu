@@ -50,7 +50,7 @@ __device__ __forceinline__ float2 unpack2_bf16(uint32_t w) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
 }
 constexpr int kDecMinPage = 8;                    // smallest supported page size
-constexpr int kDecMaxChunk = 4096;                // largest split (keys)
+constexpr int kDecMaxChunk = 5120;                // largest split (keys)
 constexpr int kDecMaxPages = kDecMaxChunk / kDecMinPage + 2;  // page ids one split can touch
 
 struct DecodeParams {
@@ -85,8 +85,9 @@ struct DecodeParams {
 };
 
 // Lowest visible key `lo` of a request and how its range [lo, L) is cut into
-// splits: split s covers keys [max(lo, (first + s) * chunk), min(L, (first +
-// s + 1) * chunk)).  An empty request keeps one split so its rows are written.
+// splits: from `first` = lo rounded down to a 64-key tile, split s covers
+// keys [max(lo, first + s * chunk), min(L, first + (s + 1) * chunk)).  An
+// empty request keeps one split so its rows are written.
 __host__ __device__ inline void decode_split_geometry(int L, int Q, int window_left, int chunk,
                                                       int &lo, int &first, int &n_split) {
     lo = 0;
@@ -94,13 +95,8 @@ __host__ __device__ inline void decode_split_geometry(int L, int Q, int window_l
         lo = L - Q - window_left;
         if (lo < 0) lo = 0;
     }
-    if (L <= lo) {
-        first = 0;
-        n_split = 1;
-        return;
-    }
-    first = lo / chunk;
-    n_split = (L + chunk - 1) / chunk - first;
+    first = lo & ~(kDecTile - 1);
+    n_split = L <= lo ? 1 : (L - first + chunk - 1) / chunk;
 }
 
 // Barrier over the MT warps that share a slice of keys (warps kg*MT ..
@@ -177,8 +173,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     decode_split_geometry(L, Q, p.window_left, p.chunk, lo, first, n_split);
     if (s >= n_split) return;
     if (L < Q && s == 0 && kvh == 0 && tid == 0) set_err(p.err, PKV_DEV_ERR_QLEN);
-    const int k_begin = max(lo, (first + s) * p.chunk);
-    const int k_end = min(L, (first + s + 1) * p.chunk);
+    const int k_begin = max(lo, first + s * p.chunk);
+    const int k_end = min(L, first + (s + 1) * p.chunk);
     // tiles start on 64-key boundaries (a window's first key need not): the
     // rows before k_begin are zero-filled and masked like rows past the end
     const int k_tile0 = k_begin & ~(kDecTile - 1);
@@ -709,15 +705,20 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     // partial traffic stays a few percent of the K/V bytes; then shrink it
     // while the grid would leave SMs idle.
     int chunk = 128 * pl.R;
-    chunk = chunk < 1024 ? 1024 : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
+    chunk = chunk < 1024 ? 1024 : (chunk > 4096 ? 4096 : chunk);
     chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+    // a window a little longer than the chunk (its first key need not sit on
+    // a tile edge: up to 63 keys more) takes one split rather than a second,
+    // nearly empty one
+    const int64_t span_t = window_left >= 0 ? span + kDecTile - 1 : span;
+    if (window_left >= 0 && span_t > chunk && span_t <= chunk + chunk / 4 && span_t <= kDecMaxChunk)
+        chunk = static_cast<int>((span_t + kDecTile - 1) / kDecTile * kDecTile);
     const int64_t want = 2LL * num_sms();
     while (chunk > 4 * kDecTile &&
            static_cast<int64_t>(B) * Hkv * ((span + chunk - 1) / chunk) < want)
-        chunk /= 2;
+        chunk = (chunk / 2 + kDecTile - 1) / kDecTile * kDecTile;  // (tile multiples)
     pl.chunk = chunk;
-    int64_t ns = span > 0 ? (span + chunk - 1) / chunk : 1;
-    if (window_left >= 0 && span > 0) ns += 1;  // a window start need not sit on a chunk edge
+    int64_t ns = span > 0 ? (span_t + chunk - 1) / chunk : 1;
     if (ns > 65535) return PKV_ERR_UNSUPPORTED;
     pl.n_split_max = static_cast<int>(ns);
     if (pl.n_split_max > 1) {
