@@ -625,7 +625,6 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         const uint32_t o_addr = t_lane + O_COL + X * kPfDV + hh * (kPfDV / SPLIT);
         const uint32_t b_pair = b_xchg(X * 4 + qd);
         const float sc = p.scale_log2 * (p.q_scale ? __ldg(p.q_scale) : 1.f) * (p.k_scale ? __ldg(p.k_scale) : 1.f);
-        const float v_mul = p.v_scale ? __ldg(p.v_scale) : 1.f;
         const bool pos_scale = sc > 0.f;  // max on raw scores, one FFMA scales and shifts
         const float k_mul = pos_scale ? sc : 1.f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
@@ -822,7 +821,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             const int qi = it.i0 + r;
             const int64_t grow = static_cast<int64_t>(it.orow_base) + r;
             const bool valid = qi < it.qb && grow >= 0 && grow < p.total_q;
-            const float inv = lt > 0.f ? v_mul / lt : 0.f;
+            const float inv = lt > 0.f ? (p.v_scale ? __ldg(p.v_scale) : 1.f) / lt : 0.f;
             T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + hh * (kPfDV / SPLIT);
 #pragma unroll
             for (int c = 0; c < kPfDV / 32 / SPLIT; ++c) {
