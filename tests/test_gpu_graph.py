@@ -131,3 +131,42 @@ def test_graph_follows_device_scale_tensors():
         ro, rl = eager(a, b)
         assert torch.equal(_bits(out), _bits(ro)), (a, b)
         assert torch.equal(lse, rl), (a, b)
+
+
+def test_graph_follows_fp8_prefill_scales():
+    # an E4M3 prefill captured once reads q/k/v scales written between replays
+    c = wl.prefill_case([130, 64, 300], [200, 64, 900], 32, 32, 8, 128, 128, wl.HND, wl.BF16, seed=43,
+                        q_dtype=wl.E4M3, kv_dtype=wl.E4M3, device=DEV)
+    B = 3
+    ws = torch.zeros(pk.paged_prefill_fp8_workspace_size(B, 32, 8, c.max_q, c.max_kv, c.q.shape[0], 128, 128,
+                                                         c.q.dtype, c.pool.k.dtype),
+                     dtype=torch.uint8, device=DEV)
+    lq, lkv, bt = (t.to(DEV) for t in (c.seq_lens_q, c.seq_lens_kv, c.block_tables))
+    sc = [torch.ones(1, device=DEV) for _ in range(3)]
+    out = torch.empty((c.q.shape[0], 32, 128), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((c.q.shape[0], 32), dtype=torch.float32, device=DEV)
+
+    def call(o, l, scales):
+        pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv, bt, causal=True,
+                         out=o, lse=l, kv_layout="HND", q_scale=scales[0], k_scale=scales[1], v_scale=scales[2])
+
+    call(out, lse, sc)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            call(out, lse, sc)
+    torch.cuda.current_stream().wait_stream(side)
+    for vals in ((1.0, 1.0, 1.0), (0.5, 1.5, 0.25), (2.0, 0.75, 3.0)):
+        for t, v in zip(sc, vals):
+            t.fill_(v)
+        out.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        ro, rl = torch.empty_like(out), torch.empty_like(lse)
+        call(ro, rl, [torch.tensor([v], device=DEV) for v in vals])
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(out), _bits(ro)), vals
+        assert torch.equal(lse, rl), vals

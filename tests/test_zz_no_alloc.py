@@ -55,14 +55,15 @@ def test_noalloc_matches_workspace_decode_on_consecutive_calls():
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
-    # the long-context decode sizes need more partial storage than the fixed
-    # array holds: refused on the host, before any launch (pointers unused)
-    need = pk.paged_decode_workspace_size(256, 4, 64, 8, 128, 32768, 64, 4095)
+    # the long-context decode shape without its window (8 splits of 4096 keys
+    # per request) needs more partial storage than the fixed array holds:
+    # refused on the host, before any launch (pointers unused)
+    need = pk.paged_decode_workspace_size(256, 4, 64, 8, 128, 32768, 64, -1)
     limit = 32 << 20
     assert need > limit
     lib = pk.load_library()
     fake = ctypes.c_void_p(0x1000)
     rc = lib.paged_decode_noalloc(fake, fake, fake, 2 * 8 * 64 * 128, 100000, fake, 512, fake,
-                                  256, 32768, 0.088, 1.0, 4095, None, 4, 64, 8, 128, 64, 1, 1,
+                                  256, 32768, 0.088, 1.0, -1, None, 4, 64, 8, 128, 64, 1, 1,
                                   fake, None, None, None)
     assert rc == 4  # PKV_ERR_WORKSPACE
