@@ -105,7 +105,10 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples (the JSON line carries their summary); PKV_BENCH_OUT
+        # picks the directory
+        out_dir = os.environ.get("PKV_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out_dir, f"clocks_gpu{index}.csv")
 
     def __enter__(self):
         try:
