@@ -475,7 +475,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        // the running max rises only when a tile's exceeds it by more than 8
+        // (a factor 2^8; from -inf at the first key): P stays below 2^8 and
+        // O is rarely rescaled
+        const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
         const float base0 = mn0 == -INFINITY ? 0.f : mn0;
         const float base1 = mn1 == -INFINITY ? 0.f : mn1;
         const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
@@ -493,12 +496,14 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         l1 = l1 * al1 + rs1;
         m0 = mn0;
         m1 = mn1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            o[i][0] *= al0;
-            o[i][1] *= al0;
-            o[i][2] *= al1;
-            o[i][3] *= al1;
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= al0;
+                o[i][1] *= al0;
+                o[i][2] *= al1;
+                o[i][3] *= al1;
+            }
         }
 #pragma unroll
         for (int ks = 0; ks < NT / 2; ++ks) {
