@@ -54,7 +54,7 @@ struct PfCfg<128> {
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int BN = 96, SK = 2, SV = 2, SPLIT = 2;
+    static constexpr int BN = 96, SK = 2, SV = 2, SPLIT = 1;
 };
 template <int DQK>
 struct PfRoles {
@@ -642,6 +642,30 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         };
         // scores of chunk i of this thread's columns at tile offset j0:
         // scaled if the scale is not positive, masked past the row's last key
+        auto scale_mask = [&](int i, int j0, bool warp_full, int lim, uint32_t(&ra)[32]) {
+            if (!pos_scale) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) ra[c] = __float_as_uint(__uint_as_float(ra[c]) * sc);
+            }
+            if (!warp_full) {
+                const int lr = lim - (j0 + hh * HC + 32 * i);  // last visible column of the chunk
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (c > lr) ra[c] = __float_as_uint(-INFINITY);
+            }
+        };
+        auto chunk_max = [&](const uint32_t(&ra)[32]) {
+            float m3[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = fmax3(__uint_as_float(ra[8 * q]), __uint_as_float(ra[8 * q + 1]),
+                                      __uint_as_float(ra[8 * q + 2]));
+                const float b = fmax3(__uint_as_float(ra[8 * q + 3]), __uint_as_float(ra[8 * q + 4]),
+                                      __uint_as_float(ra[8 * q + 5]));
+                m3[q] = fmax3(a, b, fmaxf(__uint_as_float(ra[8 * q + 6]), __uint_as_float(ra[8 * q + 7])));
+            }
+            return fmax3(fmaxf(m3[0], m3[1]), m3[2], m3[3]);
+        };
         auto load_chunk = [&](int i, int j0, bool warp_full, int lim, uint32_t(&ra)[32]) {
             tmem_ld32(s_addr + 32 * i, ra);
             tmem_wait_ld_regs(ra);
@@ -697,52 +721,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 if (!wait_warp(b_sfull(X), tx & 1)) { ok = false; break; }
                 tc_fence_after();
                 const bool warp_full = __all_sync(0xffffffffu, j0 + BN - 1 <= lim);
-                uint32_t ra[32];
-                float mh = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < NCH; ++i) {
-                    load_chunk(i, j0, warp_full, lim, ra);
-                    float m3[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float a = fmax3(__uint_as_float(ra[8 * q]), __uint_as_float(ra[8 * q + 1]),
-                                              __uint_as_float(ra[8 * q + 2]));
-                        const float b = fmax3(__uint_as_float(ra[8 * q + 3]), __uint_as_float(ra[8 * q + 4]),
-                                              __uint_as_float(ra[8 * q + 5]));
-                        m3[q] = fmax3(a, b, fmaxf(__uint_as_float(ra[8 * q + 6]), __uint_as_float(ra[8 * q + 7])));
-                    }
-                    mh = fmax3(mh, fmax3(m3[0], m3[1], m3[2]), m3[3]);
-                }
-                if constexpr (TAIL) {
-                    uint32_t rt[16];
-                    load_tail(j0, warp_full, lim, rt);
-                    float m2[2];
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const float a = fmax3(__uint_as_float(rt[8 * q]), __uint_as_float(rt[8 * q + 1]),
-                                              __uint_as_float(rt[8 * q + 2]));
-                        const float b = fmax3(__uint_as_float(rt[8 * q + 3]), __uint_as_float(rt[8 * q + 4]),
-                                              __uint_as_float(rt[8 * q + 5]));
-                        m2[q] = fmax3(a, b, fmaxf(__uint_as_float(rt[8 * q + 6]), __uint_as_float(rt[8 * q + 7])));
-                    }
-                    mh = fmax3(mh, m2[0], m2[1]);
-                }
-                if (pos_scale) mh *= sc;
-                float mo = -INFINITY;
-                if (SPLIT == 2 && !exchange(mh, mo)) { ok = false; break; }
-                const float mt = fmaxf(mh, mo);  // the tile's row max (scaled)
-                float alpha = 1.f;
-                if (mt > m_used + 8.f) {  // raise the running max (first tile: from -inf)
-                    alpha = fast_exp2(m_used - mt);
-                    m_used = mt;
-                    l *= alpha;
-                }
-                const float base = m_used == -INFINITY ? 0.f : m_used;
-                const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
                 float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < NCH; ++i) {
-                    load_chunk(i, j0, warp_full, lim, ra);
+                float alpha = 1.f;
+                // P of chunk i from its scores, relative to the running max
+                auto exp_chunk = [&](int i, const uint32_t(&ra)[32], float2 kk2, float2 nb2) {
                     uint32_t pw[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -756,23 +738,93 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         pw[e] = pack2<T>(p0, p1);  // P column: keys 2e, 2e+1 of the chunk
                     }
                     tmem_st16(s_addr + 32 * i, pw);
-                }
-                if constexpr (TAIL) {
-                    uint32_t rt[16];
-                    load_tail(j0, warp_full, lim, rt);
-                    uint32_t pw[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 x =
-                            __ffma2_rn(make_float2(__uint_as_float(rt[2 * e]), __uint_as_float(rt[2 * e + 1])), kk2, nb2);
-                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                        if (e & 1)
-                            lb = __fadd2_rn(lb, make_float2(p0, p1));
-                        else
-                            la = __fadd2_rn(la, make_float2(p0, p1));
-                        pw[e] = pack2<T>(p0, p1);
+                };
+                auto raise_max = [&](float mt) {  // (first tile: from -inf)
+                    if (mt > m_used + 8.f) {
+                        alpha = fast_exp2(m_used - mt);
+                        m_used = mt;
+                        l *= alpha;
                     }
-                    tmem_st8(s_addr + 32 * NCH, pw);
+                };
+                if constexpr (SPLIT == 1) {
+                    // one thread per row: the whole row of scores in registers,
+                    // one pass over TMEM, no partner
+                    uint32_t rs[NCH][32];
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) tmem_ld32(s_addr + 32 * i, rs[i]);
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) tmem_wait_ld_regs(rs[i]);  // (the first waits for all)
+                    float mh = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) {
+                        scale_mask(i, j0, warp_full, lim, rs[i]);
+                        mh = fmaxf(mh, chunk_max(rs[i]));
+                    }
+                    raise_max(pos_scale ? mh * sc : mh);
+                    const float base = m_used == -INFINITY ? 0.f : m_used;
+                    const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) exp_chunk(i, rs[i], kk2, nb2);
+                } else {
+                    uint32_t ra[32];
+                    float mh = -INFINITY;
+    #pragma unroll
+                    for (int i = 0; i < NCH; ++i) {
+                        load_chunk(i, j0, warp_full, lim, ra);
+                        float m3[4];
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float a = fmax3(__uint_as_float(ra[8 * q]), __uint_as_float(ra[8 * q + 1]),
+                                                  __uint_as_float(ra[8 * q + 2]));
+                            const float b = fmax3(__uint_as_float(ra[8 * q + 3]), __uint_as_float(ra[8 * q + 4]),
+                                                  __uint_as_float(ra[8 * q + 5]));
+                            m3[q] = fmax3(a, b, fmaxf(__uint_as_float(ra[8 * q + 6]), __uint_as_float(ra[8 * q + 7])));
+                        }
+                        mh = fmax3(mh, fmax3(m3[0], m3[1], m3[2]), m3[3]);
+                    }
+                    if constexpr (TAIL) {
+                        uint32_t rt[16];
+                        load_tail(j0, warp_full, lim, rt);
+                        float m2[2];
+    #pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const float a = fmax3(__uint_as_float(rt[8 * q]), __uint_as_float(rt[8 * q + 1]),
+                                                  __uint_as_float(rt[8 * q + 2]));
+                            const float b = fmax3(__uint_as_float(rt[8 * q + 3]), __uint_as_float(rt[8 * q + 4]),
+                                                  __uint_as_float(rt[8 * q + 5]));
+                            m2[q] = fmax3(a, b, fmaxf(__uint_as_float(rt[8 * q + 6]), __uint_as_float(rt[8 * q + 7])));
+                        }
+                        mh = fmax3(mh, m2[0], m2[1]);
+                    }
+                    if (pos_scale) mh *= sc;
+                    float mo = -INFINITY;
+                    if (SPLIT == 2 && !exchange(mh, mo)) { ok = false; break; }
+                    const float mt = fmaxf(mh, mo);  // the tile's row max (scaled)
+                    raise_max(mt);
+                    const float base = m_used == -INFINITY ? 0.f : m_used;
+                    const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
+    #pragma unroll
+                    for (int i = 0; i < NCH; ++i) {
+                        load_chunk(i, j0, warp_full, lim, ra);
+                        exp_chunk(i, ra, kk2, nb2);
+                    }
+                    if constexpr (TAIL) {
+                        uint32_t rt[16];
+                        load_tail(j0, warp_full, lim, rt);
+                        uint32_t pw[8];
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float2 x =
+                                __ffma2_rn(make_float2(__uint_as_float(rt[2 * e]), __uint_as_float(rt[2 * e + 1])), kk2, nb2);
+                            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                            if (e & 1)
+                                lb = __fadd2_rn(lb, make_float2(p0, p1));
+                            else
+                                la = __fadd2_rn(la, make_float2(p0, p1));
+                            pw[e] = pack2<T>(p0, p1);
+                        }
+                        tmem_st8(s_addr + 32 * NCH, pw);
+                    }
                 }
                 l += (la.x + la.y) + (lb.x + lb.y);
                 // rows of V past the sequence end may hold anything (even NaN):
