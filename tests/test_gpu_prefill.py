@@ -238,3 +238,20 @@ def test_fp8_ragged_config_full_size_sampled():
         assert_attn_close(out[cu[b]:cu[b + 1]], ro, f"request {b}")
         assert_lse_close(lse[cu[b]:cu[b + 1]], rl, f"request {b} lse")
 
+
+
+@pytest.mark.parametrize("d_qk", [128, 192])
+def test_max_jumps_within_a_tile(d_qk):
+    # keys 64..127 of every 128 (and 48..95 of every 96) score ~8x higher:
+    # the running max jumps by far more than 2^8 inside a tile, which
+    # exercises the late raise of the max (and the rescale of P already
+    # written for the tile's first columns)
+    c = wl.prefill_case([200, 130], [450, 300], 32, 8, 2, d_qk, 128, wl.HND, wl.BF16, seed=19, slack=0.1)
+    for b in range(2):
+        k, v = wl.read_tokens(c.pool, c.pt, b)
+        j = torch.arange(k.shape[0])
+        tile = 128 if d_qk == 128 else 96
+        f = torch.where((j % tile) >= tile // 2, 8.0, 1.0).to(torch.float32)
+        k2 = (k.float() * f[:, None, None]).to(k.dtype)
+        wl.write_tokens(c.pool, c.pt, b, k2, v)
+    _check(c)
