@@ -186,15 +186,6 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld_regs16(uint32_t (&r)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                   "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-
 // One work item: query tile x (counted from the LAST tile of the request, the
 // one that sees the most keys) of request b for qo heads hA and hB (hB < 0:
 // block B absent).  Items are numbered request by request (so that the CTAs
@@ -613,9 +604,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         // P, 16-bit pairs, overwrites the first half of each consumed 32-column
         // chunk of S.  The partners' row sums are added at the end of the item.
         constexpr int HC = BN / SPLIT;  // columns per thread
-        constexpr int NCH = HC / 32;         // full 32-column chunks per thread
-        constexpr bool TAIL = HC % 32 != 0;  // and a final 16-column chunk
-        static_assert(HC % 16 == 0, "columns per thread");
+        constexpr int NCH = HC / 32;    // 32-column chunks per thread
+        static_assert(HC % 32 == 0, "columns per thread");
         const int X = (warp >> 2) & 1;
         const int hh = warp >> 3;
         const int qd = warp & 3;
@@ -678,21 +668,6 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
                     if (c > lr) ra[c] = __float_as_uint(-INFINITY);
-            }
-        };
-        // the same for the final 16-column chunk (columns 32*NCH .. HC-1)
-        auto load_tail = [&](int j0, bool warp_full, int lim, uint32_t(&rt)[16]) {
-            tmem_ld16(s_addr + 32 * NCH, rt);
-            tmem_wait_ld_regs16(rt);
-            if (!pos_scale) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c) rt[c] = __float_as_uint(__uint_as_float(rt[c]) * sc);
-            }
-            if (!warp_full) {
-                const int lr = lim - (j0 + hh * HC + 32 * NCH);
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    if (c > lr) rt[c] = __float_as_uint(-INFINITY);
             }
         };
         bool ok = true;
@@ -768,33 +743,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 } else {
                     uint32_t ra[32];
                     float mh = -INFINITY;
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < NCH; ++i) {
                         load_chunk(i, j0, warp_full, lim, ra);
-                        float m3[4];
-    #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float a = fmax3(__uint_as_float(ra[8 * q]), __uint_as_float(ra[8 * q + 1]),
-                                                  __uint_as_float(ra[8 * q + 2]));
-                            const float b = fmax3(__uint_as_float(ra[8 * q + 3]), __uint_as_float(ra[8 * q + 4]),
-                                                  __uint_as_float(ra[8 * q + 5]));
-                            m3[q] = fmax3(a, b, fmaxf(__uint_as_float(ra[8 * q + 6]), __uint_as_float(ra[8 * q + 7])));
-                        }
-                        mh = fmax3(mh, fmax3(m3[0], m3[1], m3[2]), m3[3]);
-                    }
-                    if constexpr (TAIL) {
-                        uint32_t rt[16];
-                        load_tail(j0, warp_full, lim, rt);
-                        float m2[2];
-    #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const float a = fmax3(__uint_as_float(rt[8 * q]), __uint_as_float(rt[8 * q + 1]),
-                                                  __uint_as_float(rt[8 * q + 2]));
-                            const float b = fmax3(__uint_as_float(rt[8 * q + 3]), __uint_as_float(rt[8 * q + 4]),
-                                                  __uint_as_float(rt[8 * q + 5]));
-                            m2[q] = fmax3(a, b, fmaxf(__uint_as_float(rt[8 * q + 6]), __uint_as_float(rt[8 * q + 7])));
-                        }
-                        mh = fmax3(mh, m2[0], m2[1]);
+                        mh = fmaxf(mh, chunk_max(ra));
                     }
                     if (pos_scale) mh *= sc;
                     float mo = -INFINITY;
@@ -803,27 +755,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     raise_max(mt);
                     const float base = m_used == -INFINITY ? 0.f : m_used;
                     const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < NCH; ++i) {
                         load_chunk(i, j0, warp_full, lim, ra);
                         exp_chunk(i, ra, kk2, nb2);
-                    }
-                    if constexpr (TAIL) {
-                        uint32_t rt[16];
-                        load_tail(j0, warp_full, lim, rt);
-                        uint32_t pw[8];
-    #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float2 x =
-                                __ffma2_rn(make_float2(__uint_as_float(rt[2 * e]), __uint_as_float(rt[2 * e + 1])), kk2, nb2);
-                            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                            if (e & 1)
-                                lb = __fadd2_rn(lb, make_float2(p0, p1));
-                            else
-                                la = __fadd2_rn(la, make_float2(p0, p1));
-                            pw[e] = pack2<T>(p0, p1);
-                        }
-                        tmem_st8(s_addr + 32 * NCH, pw);
                     }
                 }
                 l += (la.x + la.y) + (lb.x + lb.y);
