@@ -122,6 +122,50 @@ def test_decode_workspace_size_grows_with_length(lib):
     assert f(4, 1, 30, 8, 128, 100, 16, -1) == 0  # invalid sizes
 
 
+def test_decode_window_slightly_longer_than_a_chunk_takes_one_split(lib):
+    # the long-context shape: 32 rows per kv head give 4096-key splits, and
+    # its window of 4095 + 4 keys (plus up to 63 for tile alignment) takes one
+    # split of its own length -- no partials, no merge
+    f = lib.paged_decode_workspace_size
+    assert f(256, 4, 64, 8, 128, 32768, 64, 4095) == 0
+    # a window well beyond the chunk still splits
+    assert f(256, 4, 64, 8, 128, 32768, 64, 8191) > 0
+    # without a window the same shape needs partials for up to 8 splits of
+    # 4096 keys: B * Hkv * splits * rows * (128 + 1) floats
+    need = f(256, 4, 64, 8, 128, 32768, 64, -1)
+    assert need >= 256 * 8 * 8 * 32 * 129 * 4
+
+
+def test_prefill_fp8_rejects_bad_arguments(lib):
+    good = 0x1000
+    E4M3, BF16, F16 = 2, 1, 0
+
+    def call(**over):
+        a = dict(q=good, total_q=150, k=good, v=good, ks=8 * 32 * 128, vs=8 * 32 * 128, pages=100,
+                 scale=0.08, qs=None, kscale=None, vscale=None, ws=good, ws_bytes=1 << 30, maxq=100,
+                 maxkv=200, lq=good, lkv=good, bt=good, bt_stride=8, B=2, causal=1, hqo=32, hkv=8, dqk=128,
+                 dvo=128, S=32, layout=1, qd=E4M3, kvd=E4M3, od=BF16, out=good, lse=good, err=None,
+                 stream=None)
+        a.update(over)
+        return lib.paged_prefill_fp8(*a.values())
+
+    assert call(od=E4M3) == 2          # the output is 16-bit
+    assert call(qd=F16) == 2           # a 16-bit query must match the output type
+    assert call(bt=None) == 2          # E4M3 caches are paged
+    assert call(ks=8 * 32 * 128 + 8) == 2  # E4M3 page strides: multiples of 16 bytes
+    assert call(ws_bytes=4096) == 4    # too small for the widened inputs
+    assert call(dqk=64) == 3
+    assert call(total_q=0) == 0
+    size = lib.paged_prefill_fp8_workspace_size
+    q8 = size(2, 32, 8, 100, 200, 150, 128, 128, E4M3, BF16)
+    kv8 = size(2, 32, 8, 100, 200, 150, 128, 128, BF16, E4M3)
+    both = size(2, 32, 8, 100, 200, 150, 128, 128, E4M3, E4M3)
+    base = lib.paged_prefill_workspace_size(2, 32, 100, 200)
+    assert q8 - base >= 150 * 32 * 128 * 2                   # the widened query rows
+    assert kv8 - base >= 2 * 200 * 8 * (128 + 128) * 2       # widened K and V
+    assert both >= q8 + kv8 - base
+
+
 def test_prefill_rejects_bad_arguments(lib):
     good = 0x1000
 
