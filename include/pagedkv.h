@@ -14,8 +14,9 @@
  * ---------------------------------------
  *  - Every pointer argument is caller-owned.  Tensor arguments are DEVICE
  *    pointers on the current CUDA device; scalars are passed by value.  The
- *    library allocates and frees no memory and keeps no per-call state; the
- *    only global is a launch counter for diagnostics.
+ *    library allocates and frees no memory and keeps no per-call state; its
+ *    only globals are a launch counter for diagnostics and the fixed scratch
+ *    array of paged_decode_noalloc.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  All device work is enqueued on it and the call returns without
  *    synchronising.  Argument errors are detected on the host and returned
@@ -31,7 +32,9 @@
  *    dtype; LSE is fp32, natural log.  An 8-bit (OCP FP8 E4M3) K/V cache:
  *    PKV_E4M3 for paged_append, PKV_F16_E4M3 / PKV_BF16_E4M3 for decode (the
  *    query and output stay 16-bit; the caller folds the K and V scales into
- *    bmm1_scale / bmm2_scale, as the decode page's fused scales do).
+ *    bmm1_scale / bmm2_scale, as the decode page's fused scales do), and
+ *    paged_prefill_fp8 for the prefill (E4M3 query and/or caches with the
+ *    prefill page's q_scale / k_scale / v_scale).
  *  - Layouts (both pages list the same two):
  *      PKV_HND: a page is [num_kv_heads][page_size][head_dim];
  *      PKV_NHD: a page is [page_size][num_kv_heads][head_dim].
