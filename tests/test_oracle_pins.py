@@ -532,12 +532,13 @@ def test_prefill_fp8_equals_rescaled_16bit(qd, kvd):
     np.testing.assert_allclose(a[1], b[1], rtol=1e-12, atol=1e-14)
 
 
-def test_prefill_fp8_scales_match_library():
+@pytest.mark.parametrize("d_qk,d_vo", [(16, 16), (24, 16)])
+def test_prefill_fp8_scales_match_library(d_qk, d_vo):
     # arbitrary scales: q_scale and k_scale multiply the logits, v_scale the
     # output; against library attention on torch-dequantised tensors
     q_lens, kv_lens = [5, 4], [8, 4]
     c = _small_prefill(q_lens, kv_lens, q_dtype=wl.E4M3, kv_dtype=wl.E4M3, q_scale=0.37,
-                       k_scale=1.9, v_scale=0.61)
+                       k_scale=1.9, v_scale=0.61, d_qk=d_qk, d_vo=d_vo)
     out, lse, err = oracle_prefill(c)
     assert err == 0
     off = 0
