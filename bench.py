@@ -384,6 +384,103 @@ def make_next_parts(rank: int, dev):
     return parts
 
 
+SWEEP_BATCHES = (4, 16, 64, 256, 1024, 4096)
+
+
+def time_flushed(fn, iters: int, flush, st) -> float:
+    """Median CUDA-event time (ms) of `iters` runs of fn, each preceded by a
+    write of `flush` (twice the L2) outside the timed region, so that no run
+    finds its inputs in L2."""
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        z.record(st)
+        ms.append((a, z))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(z) for a, z in ms)
+
+
+def run_sweeps(rank: int, dev, iters: int, pk_peaks) -> dict:
+    """Every other configuration of the workloads, each timed as the median
+    of `iters` runs with L2 flushed before each: the append sweep (4 ..
+    4096 requests appending U[1,128] tokens, and one token each), the append
+    page's worked example (NHD / HND, 5-D / tuple cache), the 4-request
+    decode of 45/8/25/22 keys (HND / NHD) and the Llama-shaped decode in NHD.
+    Small ones are latency-bound: their microseconds are the figure to read."""
+    import paged_kv_cache_316_gb300 as pk
+    from paged_kv_cache_316_gb300 import workloads as wl
+    st = torch.cuda.current_stream()
+    flush = torch.empty(2 * 129 * 2 ** 20 // 4 * 4, dtype=torch.uint8, device=dev)
+    hbm = pk_peaks["hbm_gbs"]
+    out = {}
+
+    def entry(ms, nbytes, **kw):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return dict(kw, us=round(ms * 1e3, 2), bytes=int(nbytes), value=round(gbs, 2), unit="GB/s",
+                    roofline_frac=round(gbs / hbm, 4))
+
+    def append_point(c, layout_name):
+        kvi, kvp, last = (x.to(dev) for x in (c.kv_indices, c.kv_indptr, c.kv_last_page_len))
+        seq = pk.paged_seq_lens(kvp, last, c.pool.page_size)
+        nnz = c.append_key.shape[0]
+        bi, pos = pk.paged_batch_indices_positions(c.append_indptr.to(dev), seq, nnz)
+        ak, av = c.append_key.to(dev), c.append_value.to(dev)
+        kv = c.pool.storage[0] if len(c.pool.storage) == 1 else c.pool.storage
+
+        def run():
+            pk.paged_append(ak, av, bi, pos, kv, kvi, kvp, last, kv_layout=layout_name)
+        for _ in range(3):
+            run()
+        return time_flushed(run, iters, flush, st), append_bytes(c), nnz
+
+    for one in (False, True):
+        rows = []
+        for B in SWEEP_BATCHES:
+            c = wl.append_sweep(B, seed=1 + rank_seed(rank), layout=wl.NHD, one_token=one, device=dev,
+                                fill="empty")
+            ms, nb, nnz = append_point(c, "NHD")
+            rows.append(entry(ms, nb, batch=B, tokens=nnz))
+            del c
+        out["append_one_token" if one else "append"] = rows
+    ex = {}
+    for layout, lname in ((wl.NHD, "NHD"), (wl.HND, "HND")):
+        for form in ("5d", "tuple"):
+            c = wl.append_example(layout=layout, form=form, device=dev)
+            ms, nb, nnz = append_point(c, lname)
+            ex[f"{lname}_{form}"] = entry(ms, nb, tokens=nnz)
+    out["append_example"] = ex
+
+    def decode_point(c, lname):
+        B = len(c.pt.lengths)
+        ws = torch.zeros(max(1, pk.paged_decode_workspace_size(
+            B, c.q_len_per_req, c.num_qo_heads, c.num_kv_heads, 128, c.max_seq_len, c.pool.page_size,
+            c.window_left)), dtype=torch.uint8, device=dev)
+        q, kv = c.query.to(dev), c.pool.storage[0].to(dev)
+        bt, sl = c.block_tables.to(dev), c.seq_lens.to(dev)
+        o = torch.empty_like(q)
+
+        def run():
+            pk.paged_decode(q, kv, ws, bt, sl, c.max_seq_len, bmm1_scale=c.bmm1_scale, kv_layout=lname,
+                            out=o)
+        for _ in range(3):
+            run()
+        return time_flushed(run, iters, flush, st), decode_bytes(c)
+
+    pr = {}
+    for layout, lname in ((wl.HND, "HND"), (wl.NHD, "NHD")):
+        ms, nb = decode_point(wl.pr1_decode(seed=rank_seed(rank), layout=layout, device=dev), lname)
+        pr[lname] = entry(ms, nb)
+    out["decode_pr1"] = pr
+    ms, nb = decode_point(wl.llama_decode(seed=rank_seed(rank), layout=wl.NHD, device=dev), "NHD")
+    out["decode_llama_nhd"] = entry(ms, nb)
+    out["note"] = (f"median of {iters} runs, L2 flushed (a {flush.numel() >> 20} MB write) before each run; "
+                   "bytes are the algorithmic bytes of the call")
+    return out
+
+
 def traffic_for(kernel_file: str, part: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the kernel source as it is now."""
@@ -398,42 +495,91 @@ def traffic_for(kernel_file: str, part: str):
         return None
 
 
-def cpu_baseline_decode(llama_part, budget_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of the Llama-shaped
-    decode (a few requests, all heads), repeated until ~budget_s of CPU work."""
+def _repeat_for(budget_s, fn):
+    """Run fn() (returning work units) until ~budget_s of wall time; at least
+    once.  Returns (units, seconds, repetitions)."""
+    units, reps, t0 = 0, 0, time.perf_counter()
+    while True:
+        units += fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            return units, el, reps
+
+
+def cpu_baselines(llama_case, budget_s: float = 4.0):
+    """The oracle, as it stands, on bounded samples of each operation's
+    workload, timed on the host cores: single-threaded and with all the
+    threads the oracle can use (OpenMP; its append is a serial loop).  Rates
+    are work / time on the sample, in the unit of the GPU part."""
     import oracle
     from paged_kv_cache_316_gb300 import workloads as wl
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    c = llama_part.case
-    requests = [0, 1, 2, 3]
+    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    all_thr = oracle.max_threads()
+    res = {}
+    # decode: requests 0-3 of the Llama-shaped decode, all heads, full length
+    c = llama_case
     subs = []
-    for b in requests:
+    for b in range(4):
         pages = c.pt.pages[b]
         idx = torch.tensor(pages, dtype=torch.long, device=c.pool.k.device)
         k = c.pool.k.index_select(0, idx).cpu().contiguous()
         v = c.pool.v.index_select(0, idx).cpu().contiguous()
-        L = c.pt.lengths[b]
-        q = c.query[b:b + 1].cpu().contiguous()
-        bt = np.arange(len(pages), dtype=np.int32)[None, :]
-        subs.append((q, k, v, L, bt))
-    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    nbytes = 0
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
+        subs.append((c.query[b:b + 1].cpu().contiguous(), k, v, c.pt.lengths[b],
+                     np.arange(len(pages), dtype=np.int32)[None, :]))
+
+    def dec(thr):
+        nb = 0
         for q, k, v, L, bt in subs:
-            oracle.decode(u16(q), u16(k), u16(v), k[0].numel(), k.shape[0], bt,
-                          np.array([L], np.uint32), L, c.bmm1_scale, 1.0, -1, None, 1, 32, 8,
-                          128, 16, wl.HND, wl.BF16)
-            nbytes += L * 8 * 128 * 2 * 2 + 2 * 32 * 128 * 2 + ((L + 15) // 16) * 4 + 4
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 1000:
-            break
-    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": f"fp64 oracle decode of requests {requests} (all 32 heads, full kv length) "
-                      f"of the Llama-shaped decode, {reps} repetitions, {el:.1f} s"}
+            oracle.decode(u16(q), u16(k), u16(v), k[0].numel(), k.shape[0], bt, np.array([L], np.uint32),
+                          L, c.bmm1_scale, 1.0, -1, None, 1, 32, 8, 128, 16, wl.HND, wl.BF16, threads=thr)
+            nb += L * 8 * 128 * 2 * 2 + 2 * 32 * 128 * 2 + ((L + 15) // 16) * 4 + 4
+        return nb
+    for name, thr in (("single", 1), ("all", all_thr)):
+        nb, el, reps = _repeat_for(budget_s, lambda: dec(thr))
+        res.setdefault("decode_llama", {})[name] = {
+            "value": round(nb / el / 1e9, 4), "unit": "GB/s", "cores": thr, "reps": reps, "s": round(el, 2)}
+    res["decode_llama"]["sample"] = ("requests 0-3 of the Llama-shaped decode (all 32 heads, full kv "
+                                     "length, kv lengths %s)" % [s_[3] for s_ in subs])
+    # append: 64 requests of the append sweep's shape (fp16, 32 kv heads)
+    a = wl.append_sweep(64, seed=1, layout=wl.NHD)
+    sl = oracle.seq_lens(a.kv_indptr.numpy(), a.kv_last_page_len.numpy(), 16)
+    bi, pos = oracle.batch_indices_positions(a.append_indptr.numpy(), sl, a.append_key.shape[0])
+    pool = a.pool.storage[0]
+    pk_, pv_ = u16(pool[:, 0]), u16(pool[:, 1])
+
+    def app():
+        oracle.append(u16(a.append_key), u16(a.append_value), bi, pos, pk_, pv_, a.pool.k_page_stride,
+                      a.pool.num_pages, a.kv_indices.numpy(), a.kv_indptr.numpy(),
+                      a.kv_last_page_len.numpy(), 32, 128, 16, wl.NHD)
+        return append_bytes(a)
+    nb, el, reps = _repeat_for(budget_s / 2, app)
+    one = {"value": round(nb / el / 1e9, 4), "unit": "GB/s", "cores": 1, "reps": reps, "s": round(el, 2)}
+    res["append"] = {"single": one, "all": dict(one, note="the oracle's append is a serial loop"),
+                     "sample": f"64 requests of the append sweep's shape ({a.append_key.shape[0]} tokens, "
+                               "fp16, 32 kv heads, d 128, page 16, NHD)"}
+    # prefill: one request (q 1024, prefix 1024) of the ragged prefill's shape
+    # with 4 qo heads over 1 kv head (the per-head work of the 32/8 config)
+    pc = wl.prefill_case([1024], [2048], 32, 4, 1, 128, 128, wl.HND, wl.BF16, seed=5)
+    fl = prefill_flops(pc)
+
+    def pre(thr):
+        oracle.prefill(u16(pc.q), u16(pc.pool.k), u16(pc.pool.v), pc.pool.k_page_stride,
+                       pc.pool.v_page_stride, pc.pool.num_pages, pc.scale, pc.seq_lens_q.numpy(),
+                       pc.seq_lens_kv.numpy(), pc.block_tables.numpy(), True, 4, 1, 128, 128, 32, wl.HND,
+                       wl.BF16, threads=thr)
+        return fl
+    for name, thr in (("single", 1), ("all", all_thr)):
+        f, el, reps = _repeat_for(budget_s, lambda: pre(thr))
+        res.setdefault("prefill_d128", {})[name] = {
+            "value": round(f / el / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "reps": reps, "s": round(el, 2)}
+    res["prefill_d128"]["sample"] = ("one causal request (q 1024 after a 1024-token prefix) of the ragged "
+                                     "prefill's shape, 4 qo heads / 1 kv head, d 128")
+    dl = res["decode_llama"]
+    return {"value": dl["all"]["value"], "unit": "GB/s", "cores": all_thr, "kind": "oracle",
+            "sample": "fp64 oracle decode of " + dl["sample"] + "; per_op holds every operation, "
+                      "single-threaded and on all threads",
+            "per_op": res}
 
 
 def e2e_decode(part, steps: int, dev):
@@ -547,6 +693,8 @@ def run_ours(args):
     next_rows = aggregate_parts([(p.name, sum(p.ms) / len(p.ms), p.work, p.unit) for p in nxt],
                                 ws, dev, pk_peaks)
 
+    sweeps = run_sweeps(rank, dev, 50, pk_peaks) if not args.no_sweeps else None
+
     llama = next(p for p in parts if p.name == "decode_llama")
     e2e_ms, h2d, d2h = e2e_decode(llama, max(10, args.steps // 4), dev)
     e2e_ms = allreduce_max(e2e_ms, ws, dev)
@@ -556,7 +704,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{ws} (independent requests)",
-                   "l2": "no flush: every part's inputs exceed the 129 MB L2",
+                   "l2": "step parts: no flush, every part's inputs exceed the 129 MB L2; sweeps: "
+                         "L2 flushed before every timed run",
                    "headline_part": "decode_llama"},
         "parts": out_parts, "roofline": roofline,
         "next_rows": dict(next_rows, note="outside the step and its ms_per_step: variable-length "
@@ -574,8 +723,10 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
     }
+    if sweeps is not None:
+        line["sweeps"] = sweeps
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_decode(llama)
+        line["cpu_baseline"] = cpu_baselines(llama.case)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -644,6 +795,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweeps", action="store_true",
+                    help="skip the sweep / small-configuration measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -15,8 +15,9 @@
  *  - Every pointer argument is caller-owned.  Tensor arguments are DEVICE
  *    pointers on the current CUDA device; scalars are passed by value.  The
  *    library allocates and frees no memory and keeps no per-call state; its
- *    only globals are a launch counter for diagnostics and the fixed scratch
- *    array of paged_decode_noalloc.
+ *    only globals are a launch counter for diagnostics, the limit of its
+ *    bounded waits (pkv_set_wait_limit_ns) and the fixed scratch array of
+ *    paged_decode_noalloc.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  All device work is enqueued on it and the call returns without
  *    synchronising.  Argument errors are detected on the host and returned
@@ -93,6 +94,22 @@ const char *pkv_status_string(int status);
 unsigned long long pkv_kernel_launches(void);
 
 /*
+ * pkv_set_wait_limit_ns -- time limit, in nanoseconds, of every bounded
+ * pipeline wait (an mbarrier wait for copied data, for the tensor core or
+ * for another warp of the CTA) in the kernels of paged_append and
+ * paged_prefill launched after the call; 0 restores the default of one
+ * second.  Returns the previous limit.  Process-wide (every thread and
+ * device).  A wait that runs out sets PKV_DEV_ERR_TIMEOUT in the call's
+ * error word; the CTA then stops its work, waits for the copies and MMAs
+ * it had already issued, frees its tensor memory and exits, so the device
+ * stays usable and the next call runs normally, but the outputs of that
+ * call are incomplete.  It exists to detect a stalled pipeline (and to test
+ * that detection with a limit no wait can meet); the pages have no
+ * counterpart.
+ */
+unsigned long long pkv_set_wait_limit_ns(unsigned long long ns);
+
+/*
  * paged_seq_lens -- [append] worked example, `get_seq_lens` and the comments
  * "45 = (3 - 1) * 16 + 13" ...: the kv length of each request from its page
  * count and the fill of its last page,
@@ -139,7 +156,9 @@ int paged_batch_indices_positions(const int32_t *append_indptr,
  * Device errors: b outside [0, batch_size) -> PKV_DEV_ERR_BATCH; p outside
  * [0, seq_len(b)) -> PKV_DEV_ERR_POS; page outside [0, max_num_pages) ->
  * PKV_DEV_ERR_PAGE; the entry is skipped.  A copy that does not complete
- * within 1 s -> PKV_DEV_ERR_TIMEOUT.  Duplicate (b, p) pairs race.
+ * within the wait limit (1 s; pkv_set_wait_limit_ns) -> PKV_DEV_ERR_TIMEOUT
+ * and the CTA stops (its remaining entries are not written).  Duplicate
+ * (b, p) pairs race.
  * dtype: PKV_F16 / PKV_BF16 (2-byte elements) or PKV_E4M3 (1-byte).
  * Host errors: a head row (head_dim elements) not a multiple of 16 bytes or
  * page_size <= 0 -> PKV_ERR_INVALID_ARG; a head row above 8 KB ->
@@ -281,9 +300,12 @@ int paged_decode_ex(const void *query, int64_t num_tokens, const void *k_cache,
  *    copy until the process exits.  Sizes whose
  *    paged_decode_workspace_size(...) exceeds it are rejected with
  *    PKV_ERR_WORKSPACE before anything is launched (use paged_decode then).
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *  - The first call in each CUDA context (so on each device, and again after
+ *    a cudaDeviceReset, which creates a new context in which the array may
+ *    sit elsewhere) looks up the array's device address
+ *    (cudaGetSymbolAddress, with that context current) and caches it, keyed
+ *    by the context's unique id; make that first call before any stream
+ *    capture.
  *  - All calls share the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero.  Calls that overlap on the GPU
  *    (concurrent streams, or host threads on one device) race on it:
@@ -338,7 +360,8 @@ size_t paged_prefill_workspace_size(int32_t batch_size, int32_t num_qo_heads,
  * power of two in [8, 256]; num_qo_heads % num_kv_heads == 0.
  * Errors: PKV_ERR_CUDA also when the driver rejects a TMA tensor map.
  * Device errors additionally include PKV_DEV_ERR_TIMEOUT if a pipeline wait
- * gave up (the affected rows are then zero).
+ * gave up (see pkv_set_wait_limit_ns; rows of the CTAs that stopped are
+ * then left unwritten).
  * Device errors: bad page id -> PKV_DEV_ERR_PAGE; kv_b < q_b ->
  * PKV_DEV_ERR_QLEN (rows that see no key get out = 0, lse = -inf).
  * block_tables = NULL (the page's non-paged case): k_cache / v_cache are

@@ -19,4 +19,5 @@ from .binding import (  # noqa: F401
     paged_prefill_fp8_workspace_size,
     paged_prefill,
     kernel_launches,
+    set_wait_limit_ns,
 )

@@ -29,6 +29,7 @@ _sz = ctypes.c_size_t
 _SIGNATURES = {
     "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "pkv_kernel_launches": ([], ctypes.c_ulonglong),
+    "pkv_set_wait_limit_ns": ([ctypes.c_ulonglong], ctypes.c_ulonglong),
     "paged_seq_lens": ([_c_p, _c_p, _i32, _i32, _c_p, _c_p], ctypes.c_int),
     "paged_batch_indices_positions": ([_c_p, _c_p, _i32, _i64, _c_p, _c_p, _c_p],
                                       ctypes.c_int),
@@ -91,6 +92,12 @@ def load_library():
 
 def kernel_launches() -> int:
     return int(load_library().pkv_kernel_launches())
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of the bounded pipeline waits of later append / prefill
+    launches (0: the default, one second); returns the previous limit."""
+    return int(load_library().pkv_set_wait_limit_ns(int(ns)))
 
 
 def _check(status: int):
@@ -174,6 +181,10 @@ def split_cache(kv_cache, layout: int):
     return kp, vp, base.stride(0), base.shape[0], H, S, D, base
 
 
+def base_dtype(kv_cache) -> torch.dtype:
+    return (kv_cache[0] if isinstance(kv_cache, (tuple, list)) else kv_cache).dtype
+
+
 # ---- index helpers ------------------------------------------------------------------
 
 def paged_seq_lens(kv_indptr, kv_last_page_len, page_size: int, seq_lens=None,
@@ -210,6 +221,13 @@ def paged_append(append_key, append_value, batch_indices, positions, paged_kv_ca
     nnz = append_key.shape[0]
     if not (append_key.is_contiguous() and append_value.is_contiguous()):
         raise PagedKVError("append_key/append_value must be contiguous")
+    if append_value.shape != append_key.shape or tuple(append_key.shape[1:]) != (H, D):
+        raise PagedKVError(f"append_key/append_value must both be [nnz, {H}, {D}]")
+    if append_key.dtype != base_dtype(paged_kv_cache) or append_value.dtype != append_key.dtype:
+        raise PagedKVError("append_key/append_value hold the cache's element type")
+    for t in (batch_indices, positions):
+        if t.dtype != torch.int32 or t.numel() < nnz:
+            raise PagedKVError(f"batch_indices/positions must be int32 with >= {nnz} entries")
     _check(load_library().paged_append(
         _ptr(append_key), _ptr(append_value), nnz, _ptr(batch_indices),
         _ptr(positions), kp, vp, stride, P, _ptr(kv_indices), _ptr(kv_indptr),
@@ -236,6 +254,28 @@ def paged_decode_workspace_size(batch_size, q_len_per_req, num_qo_heads, num_kv_
         max_seq_len, page_size, window_left))
 
 
+def _check_decode_args(query, out, lse, block_tables, seq_lens, rows_needed: int):
+    """The C ABI of the uniform decode takes no row count: the shapes it
+    trusts are checked here, so that no kernel reads or writes past the end
+    of query, out or lse."""
+    rows, Hqo, _ = query.shape
+    if not query.is_contiguous():
+        raise PagedKVError("query must be contiguous [rows, num_qo_heads, head_dim]")
+    if rows < rows_needed:
+        raise PagedKVError(f"query has {rows} rows; the requests need {rows_needed}")
+    if out.shape != query.shape or out.dtype != query.dtype or not out.is_contiguous():
+        raise PagedKVError("out must be a contiguous tensor of the query's shape and dtype")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (rows, Hqo)
+                            or not lse.is_contiguous()):
+        raise PagedKVError(f"lse must be a contiguous float32 [{rows}, {Hqo}] tensor")
+    B = seq_lens.shape[0]
+    if seq_lens.dim() != 1 or seq_lens.element_size() != 4:
+        raise PagedKVError("seq_lens must be a 1-D tensor of 32-bit lengths")
+    if block_tables.dim() != 2 or block_tables.shape[0] < B or block_tables.dtype != torch.int32 \
+            or block_tables.stride(1) != 1:
+        raise PagedKVError("block_tables must be int32 [>= batch_size, pages] with unit column stride")
+
+
 def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len: int,
                  bmm1_scale: float = 1.0, bmm2_scale: float = 1.0, window_left: int = -1,
                  sinks=None, kv_layout="HND", q_len_per_req: int = 1, out=None,
@@ -258,6 +298,12 @@ def paged_decode(query, kv_cache, workspace, block_tables, seq_lens, max_seq_len
         out = torch.empty_like(query)
     if (cum_seq_lens_q is None) != (max_q_len is None):
         raise PagedKVError("cum_seq_lens_q and max_q_len go together")
+    if cum_seq_lens_q is not None:
+        if cum_seq_lens_q.dtype != torch.int32 or tuple(cum_seq_lens_q.shape) != (B + 1,):
+            raise PagedKVError(f"cum_seq_lens_q must be int32 [{B + 1}]")
+        _check_decode_args(query, out, lse, block_tables, seq_lens, 0)
+    else:
+        _check_decode_args(query, out, lse, block_tables, seq_lens, B * q_len_per_req)
     s1, s1_dev = _scale_arg(bmm1_scale, query.device)
     s2, s2_dev = _scale_arg(bmm2_scale, query.device)
     if s1_dev or s2_dev or enable_pdl:
@@ -306,6 +352,7 @@ def paged_decode_noalloc(query, kv_cache, block_tables, seq_lens, max_seq_len: i
     B = seq_lens.shape[0]
     if out is None:
         out = torch.empty_like(query)
+    _check_decode_args(query, out, lse, block_tables, seq_lens, B * q_len_per_req)
     _check(load_library().paged_decode_noalloc(
         _ptr(query), kp, vp, stride, P, _ptr(block_tables), block_tables.stride(0),
         _ptr(seq_lens), B, max_seq_len, bmm1_scale, bmm2_scale, window_left, _ptr(sinks),
@@ -378,6 +425,12 @@ def paged_prefill(q, k_cache, v_cache, scale: float, workspace,
         out = torch.empty((total_q, Hqo, dv), dtype=odt, device=q.device)
     if lse is None:
         lse = torch.empty((total_q, Hqo), dtype=torch.float32, device=q.device)
+    if tuple(out.shape) != (total_q, Hqo, dv) or out.dtype != odt or not out.is_contiguous():
+        raise PagedKVError(f"out must be a contiguous {odt} [{total_q}, {Hqo}, {dv}] tensor")
+    if tuple(lse.shape) != (total_q, Hqo) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise PagedKVError(f"lse must be a contiguous float32 [{total_q}, {Hqo}] tensor")
+    if not q.is_contiguous():
+        raise PagedKVError("q must be contiguous [total_q, num_qo_heads, d_qk]")
     B = actual_seq_lens_q.shape[0]
     bt_stride = 0 if block_tables is None else block_tables.stride(0)
     offsets = (batch_offsets_q, batch_offsets_o, batch_offsets_k, batch_offsets_v)

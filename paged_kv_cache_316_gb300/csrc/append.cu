@@ -63,6 +63,7 @@ struct AppendParams {
     int pieces_per_row;    // ceil(H / heads_per_piece)
     int64_t tokens_per_cta;
     int32_t *err;
+    unsigned long long wait_ns;  // limit of the bounded copy waits
 };
 
 constexpr int kApSlots = 6;            // shared-memory ring of one CTA
@@ -179,7 +180,8 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
     volatile int no_abort = 0;
     int64_t jl = 0;
     for (; jl < total && jl < kApSlots - 1; ++jl) issue_load(jl);
-    for (int64_t js = 0; js < total; ++js) {
+    int64_t js = 0;
+    for (; js < total; ++js) {
         int64_t tok;
         int row, h0, nh;
         piece(js, tok, row, h0, nh);
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
         const int64_t dst = dst_of(tok);
         const int s = static_cast<int>(js % kApSlots);
         if (lane == 0) {
-            if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((js / kApSlots) & 1), &no_abort)) {
+            if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((js / kApSlots) & 1), &no_abort, p.wait_ns)) {
                 set_err(p.err, PKV_DEV_ERR_TIMEOUT);
                 ok = false;
             } else if (dst >= 0) {
@@ -215,6 +217,12 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
             ++jl;
         }
     }
+    // A wait that gave up left the loads of pieces js .. jl-1 in flight (at
+    // most one per slot): they land in this CTA's shared memory, so wait for
+    // them before it exits; then for the stores.
+    if (lane == 0 && !ok)
+        for (int64_t j = js; j < jl; ++j)
+            mbar_wait_drain(smem_u32(&full[j % kApSlots]), static_cast<uint32_t>((j / kApSlots) & 1));
     if (lane == 0) bulk_wait_all();
 }
 
@@ -299,6 +307,7 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
     p.heads_per_piece = head_dim * esize >= kApSlotBytes ? 1 : min(num_kv_heads, kApSlotBytes / (head_dim * esize));
     p.pieces_per_row = (num_kv_heads + p.heads_per_piece - 1) / p.heads_per_piece;
     p.err = err_word;
+    p.wait_ns = wait_limit_ns();
     const int64_t ctas_max = static_cast<int64_t>(num_sms()) * kApCtasPerSm;
     p.tokens_per_cta = (nnz + ctas_max - 1) / ctas_max;
     const int64_t blocks = (nnz + p.tokens_per_cta - 1) / p.tokens_per_cta;

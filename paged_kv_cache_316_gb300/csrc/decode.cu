@@ -930,31 +930,65 @@ extern "C" int paged_decode_ex(const void *query, int64_t num_tokens, const void
 // a process that reserves all device memory up front.  The split partials
 // live in a fixed array in this library's own device image instead of a
 // caller workspace.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 namespace pkv {
 
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES);
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocCachedContexts = 64;
 
 // One copy per device that loads the library, held until the process exits.
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-// Device address of g_decode_scratch on the current device.  In host code
-// the symbol is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// Unique id of the calling thread's current CUDA context (driver entry points
+// fetched through the runtime: the library does not link libcuda).  False
+// when no context is current yet.
+static bool current_context_id(unsigned long long *id) {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_decode_scratch in the current context.  In host code
+// the symbol is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress and cached per CUDA context, keyed by the context's
+// unique id: after a device reset (or under another context of the same
+// device) the library's module is loaded again and the array may move; the
+// new context has a new id, so its address is looked up afresh.
 static void *noalloc_scratch_ptr() {
     static std::mutex mu;
-    static void *ptrs[kNoAllocMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+    static unsigned long long ids[kNoAllocCachedContexts];
+    static void *ptrs[kNoAllocCachedContexts];
+    static int used = 0, next = 0;
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return nullptr;
-        ptrs[dev] = p;
-    }
-    return ptrs[dev];
+    if (have_id)
+        for (int i = 0; i < used; ++i)
+            if (ids[i] == id) return ptrs[i];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return nullptr;
+    // (the lookup above made the primary context current if none was)
+    if (!have_id && !current_context_id(&id)) return p;  // not cached: looked up again next call
+    const int slot = used < kNoAllocCachedContexts ? used++ : (next++ % kNoAllocCachedContexts);
+    ids[slot] = id;
+    ptrs[slot] = p;
+    return p;
 }
 
 }  // namespace pkv

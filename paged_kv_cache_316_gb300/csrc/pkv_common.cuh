@@ -15,6 +15,10 @@ namespace pkv {
 // Count `n` kernel launches (diagnostics; see pkv_kernel_launches).
 void note_launches(int n);
 
+// Time limit of every bounded pipeline wait in kernels launched from now on
+// (nanoseconds; see pkv_set_wait_limit_ns).
+unsigned long long wait_limit_ns();
+
 // Programmatic dependent launch between the kernels of one call: the second
 // kernel is launched with programmatic stream serialisation, may start while
 // the first finishes, and waits (griddepcontrol.wait) for the first grid's

@@ -50,7 +50,7 @@ template <int DQK>
 struct PfCfg;
 template <>
 struct PfCfg<128> {
-    static constexpr int BN = 128, SK = 2, SV = 2, SPLIT = 2;
+    static constexpr int BN = 128, SK = 2, SV = 2, SPLIT = 1;
 };
 template <>
 struct PfCfg<192> {
@@ -60,8 +60,17 @@ template <int DQK>
 struct PfRoles {
     static constexpr int kSoftmaxWarps = 8 * PfCfg<DQK>::SPLIT;
     static constexpr int kTmaWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1, kTmaVWarp = kSoftmaxWarps + 2;
-    static constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+    // + one idle warp, so that the producer / MMA warps make a whole warpgroup
+    static constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 };
+// Register split with one softmax thread per row (384 threads): launched at
+// 168 registers a thread (65536 / 384, rounded down to a multiple of 8), the
+// producer warpgroup drops to kRegsLow and the two softmax warpgroups rise to
+// kRegsHigh: 128 x 104 + 256 x 200 = 64512 = 384 x 168, the launch's total.
+// (A row's 128 scores and the rest of the softmax fit in 200 without spills;
+// the producers spill below about 100.)
+constexpr int kRegsLow = 104, kRegsHigh = 200;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the launch's registers");
 static int pf_bn(int d_qk) { return d_qk == 128 ? PfCfg<128>::BN : PfCfg<192>::BN; }
 // Rows per TMA box: pages, or parts of pages of the largest power of two
 // dividing BN, so that no box crosses a page and the boxes tile a key tile.
@@ -96,6 +105,7 @@ struct PrefillParams {
     void *out;
     float *lse;
     int32_t *err;
+    unsigned long long wait_ns;  // limit of every bounded pipeline wait
 };
 
 // cu_q / cu_kv = exclusive prefix sums of the query / kv lengths and
@@ -261,6 +271,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 2;  // per block: P tile written (128 * SPLIT arrivals)
     const uint32_t b_odone0 = bar0 + 8u * nb; nb += 2;  // per block: last PV of an item done
     const uint32_t b_xchg0 = bar0 + 8u * nb; nb += 8;   // per (block, row quarter): partner exchange
+    const uint32_t b_drain = bar0 + 8u * nb++;          // every MMA the issuer made has completed
     auto b_item_full = [&](int i) { return b_item_full0 + 8u * i; };
     auto b_item_empty = [&](int i) { return b_item_empty0 + 8u * i; };
     auto b_kfull = [&](int s) { return b_kfull0 + 8u * s; };
@@ -299,6 +310,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             mbar_init(b_odone(x), 1);
         }
         for (int i = 0; i < 8; ++i) mbar_init(b_xchg(i), 64);
+        mbar_init(b_drain, 1);
         abort_s = 0;
         fence_mbar_init();
     }
@@ -312,6 +324,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     pdl_wait();  // the plan kernel's prefix sums and zeroed work counter
     const uint32_t tmem = tmem_base_s;
     volatile int *abort_flag = &abort_s;
+    const uint64_t wlim = p.wait_ns;
     auto give_up = [&]() {
         *abort_flag = 1;
         set_err(p.err, PKV_DEV_ERR_TIMEOUT);
@@ -320,7 +333,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     // every consumer role takes every item, in order, and releases the slot
     auto take_item = [&](int k, bool &ok) -> int4 {
         const int slot = k % NI;
-        if (!mbar_wait(b_item_full(slot), (k / NI) & 1, abort_flag)) {
+        if (!mbar_wait(b_item_full(slot), (k / NI) & 1, abort_flag, wlim)) {
             ok = false;
             return make_int4(-1, 0, 0, 0);
         }
@@ -338,260 +351,287 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     // issued after PV_X(t), which needs P_X(t), so no block can run two
     // phases ahead of its partner.
 
-    if (warp == kTmaWarp || warp == kTmaVWarp) {
-        // ------------------------------------------------------------ TMA producers
-        // Warp 8 takes items from the global counter, publishes them, loads
-        // the Q blocks and the K tiles; warp 10 loads the V tiles.  A K stage
-        // is released by the last QK that reads it and a V stage by the last
-        // PV.  Each warp looks up a tile's page ids in one coalesced load,
-        // one tile ahead; lane 0 issues the copies.
-        const bool is_k = warp == kTmaWarp;
-        if (lane == 0) {
-            if (is_k) {
-                prefetch_tmap(&tm_q);
-                prefetch_tmap(&tm_k);
-            } else {
-                prefetch_tmap(&tm_v);
-            }
-        }
-        const int S = 1 << p.page_shift;
-        // rows per TMA box: a page or part of one; a whole tile for contiguous K/V
-        const int RB = p.contiguous ? BN : pf_box_rows(S, BN);
-        const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
-        const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
-        const int NS = is_k ? SK : SV;
-        const int U = p.Hkv * p.pairs;
-        bool ok = true;
-        int t_base = 0;  // tiles of earlier items (global tile counter)
-        const int total_items = is_k ? p.cu_items[p.B] : 0;
-        int b_scan = 0;  // request of this CTA's previous item: items come in increasing order
-        for (int k = 0; ok; ++k) {
-            int4 itm = make_int4(-1, 0, 0, 0);
-            if (is_k) {
-                // take the next item from the counter, find its request with a
-                // warp-wide forward scan of cu_items, and publish it
-                int c = 0;
-                if (lane == 0) c = atomicAdd(p.work_counter, 1);
-                c = __shfl_sync(0xffffffffu, c, 0);
-                if (c < total_items) {
-                    while (true) {  // ends: cu_items[B] = total > c
-                        const int bi = b_scan + lane;
-                        const int v = bi <= p.B ? p.cu_items[bi] : 0x7fffffff;
-                        const unsigned m = __ballot_sync(0xffffffffu, v > c);
-                        if (m) {
-                            b_scan += __ffs(m) - 2;  // cu_items[b_scan] <= c always
-                            break;
-                        }
-                        b_scan += 32;
-                    }
-                    const int rem = c - p.cu_items[b_scan];
-                    const int u = rem % U, kvh = u / p.pairs;
-                    const int hA = kvh * p.group + 2 * (u % p.pairs);
-                    const int hB = hA + 1 < (kvh + 1) * p.group ? hA + 1 : -1;
-                    itm = make_int4(b_scan, hA, hB, rem / U);
-                }
-                if (lane == 0) {
-                    const int slot = k % NI;
-                    if (k >= NI && !mbar_wait(b_item_empty(slot), ((k / NI) - 1) & 1, abort_flag)) {
-                        give_up();
-                        ok = false;
-                    } else {
-                        item_ring[slot] = itm;
-                        mbar_arrive(b_item_full(slot));
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-            } else {
-                if (lane == 0) itm = take_item(k, ok);
-                itm.x = __shfl_sync(0xffffffffu, itm.x, 0);
-                itm.y = __shfl_sync(0xffffffffu, itm.y, 0);
-                itm.z = __shfl_sync(0xffffffffu, itm.z, 0);
-                itm.w = __shfl_sync(0xffffffffu, itm.w, 0);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-            }
-            if (!ok || itm.x < 0) break;
-            PfItem it;
-            pf_item(p, itm, BN, it);
-            const int32_t *bt = p.block_tables + static_cast<int64_t>(it.b) * p.bt_stride;
-            // Q blocks of this item, once the previous item's last QK is done;
-            // loaded after the item's first K tile so that the two overlap
-            auto load_q = [&]() {  // lane 0 of the K producer
-                if (k >= 1 && !mbar_wait(b_qempty, (k - 1) & 1, abort_flag)) {
-                    give_up();
-                    ok = false;
+    if (warp >= PfRoles<DQK>::kSoftmaxWarps) {
+        // warps 8-11 (one warpgroup): the producers, the MMA issuer and an idle
+        // warp give registers to the softmax warpgroups
+        if constexpr (SPLIT == 1) reg_dealloc<kRegsLow>();
+        if (warp == kTmaWarp || warp == kTmaVWarp) {
+            // ------------------------------------------------------------ TMA producers
+            // Warp 8 takes items from the global counter, publishes them, loads
+            // the Q blocks and the K tiles; warp 10 loads the V tiles.  A K stage
+            // is released by the last QK that reads it and a V stage by the last
+            // PV.  Each warp looks up a tile's page ids in one coalesced load,
+            // one tile ahead; lane 0 issues the copies.
+            const bool is_k = warp == kTmaWarp;
+            if (lane == 0) {
+                if (is_k) {
+                    prefetch_tmap(&tm_q);
+                    prefetch_tmap(&tm_k);
                 } else {
-                    mbar_expect_tx(b_qfull, it.hB >= 0 ? 2 * QB : QB);
-                    for (int c = 0; c < QA; ++c)
-                        tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hA, it.row_base);
-                    if (it.hB >= 0)
-                        for (int c = 0; c < QA; ++c)
-                            tma_load_3d(q_s + QB + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hB,
-                                        it.row_base);
+                    prefetch_tmap(&tm_v);
                 }
-            };
-            if (is_k && lane == 0 && it.n_tiles == 0) load_q();
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
-                const int key = j * BN + lane * RB;
-                int page = oob;
-                if (p.contiguous) return 0;  // one page: the whole tensor
-                if (lane < nbox && key < it.kvb) {
-                    page = bt[key >> p.page_shift];
-                    if (page < 0 || page >= p.max_num_pages) {
-                        if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
-                        page = oob;
-                    }
-                }
-                return page;
-            };
-            int pg_next = it.n_tiles > 0 ? lookup(0) : oob;
-            for (int j = 0; j < it.n_tiles; ++j) {
-                const int t = t_base + j;
-                const int pg = pg_next;
-                if (j + 1 < it.n_tiles) pg_next = lookup(j + 1);
-                int pages[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
-                if (lane == 0) {
-                    const int st = t % NS, us = t / NS;
-                    if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag)) {
-                        give_up();
-                        ok = false;
-                    } else {
-                        const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
-                        mbar_expect_tx(full, is_k ? KB : VB);
-                        const int j0 = j * BN;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (i >= nbox) break;
-                            const int r0 = i * RB;
-                            const int slot0 = p.contiguous ? (is_k ? it.kv_k : it.kv_v) + j0 + r0
-                                                           : (j0 + r0) & (S - 1);
-                            const int ca = LAYOUT == PKV_HND ? slot0 : it.kvh;
-                            const int cb = LAYOUT == PKV_HND ? it.kvh : slot0;
-                            if (is_k) {
-                                for (int c = 0; c < QA; ++c)
-                                    tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca,
-                                                cb, pages[i]);
-                            } else {
-                                for (int c = 0; c < kPfDV / 64; ++c)
-                                    tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca,
-                                                cb, pages[i]);
-                            }
-                        }
-                        if (is_k && j == 0) load_q();
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
             }
-            t_base += it.n_tiles;
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        // Per item of n tiles: QK_A(0) QK_B(0), then for every tile t:
-        // PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1).  tcgen05 MMAs execute in issue
-        // order, so QK_X(t+1), which overwrites S_X, cannot disturb PV_X(t)
-        // reading P_X from it, and a completed S_X(t+1) implies that PV_X(t)
-        // is complete (the softmax relies on both).
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
-            constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
-            const uint64_t qdesc0 = umma_sdesc_sw128(q_s, 16, 1024);
-            const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
-            const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
+            const int S = 1 << p.page_shift;
+            // rows per TMA box: a page or part of one; a whole tile for contiguous K/V
+            const int RB = p.contiguous ? BN : pf_box_rows(S, BN);
+            const int nbox = BN / RB;       // boxes (pages or page parts) per tile, <= 16
+            const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
+            const int NS = is_k ? SK : SV;
+            const int U = p.Hkv * p.pairs;
             bool ok = true;
-            int t_base = 0;   // K/V tiles of earlier items
-            int tb_base = 0;  // tiles of block B in earlier items
-            auto wait_k = [&](int t) {
-                if (!mbar_wait(b_kfull(t % SK), (t / SK) & 1, abort_flag)) return false;
-                tc_fence_after();
-                return true;
-            };
-            auto qk = [&](int x, int t) {  // S_X = Q_X K(t)^T
-                const uint64_t kd = kdesc0 + (((t % SK) * KB) >> 4);
-                const uint64_t qd = qdesc0 + ((x * QB) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < DQK / 16; ++kk)
-                    umma_ss(tmem + x * S_STRIDE, qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
-                            kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-                umma_commit(b_sfull(x));
-            };
-            // P column of keys 16kk .. 16kk+15: each softmax thread owns HC
-            // columns, and writes chunk i (32 keys, or a final 16) as 16-bit
-            // pairs at the chunk's first column
-            constexpr int HC = BN / SPLIT;
-            auto pcol = [](int kk) {
-                const int k0 = 16 * kk, c = k0 % HC;
-                return (k0 / HC) * HC + 32 * (c / 32) + (c % 32) / 2;
-            };
-            auto pv = [&](int x, int t, bool first) {  // O_X (+)= P_X V(t)
-                const uint64_t vd = vdesc0 + (((t % SV) * VB) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(tmem + O_COL + x * kPfDV, tmem + x * S_STRIDE + pcol(kk), vd + ((kk * 16 * 128) >> 4), idesc_pv,
-                            (!first || kk > 0) ? 1u : 0u);
-            };
+            int t_base = 0;  // tiles of earlier items (global tile counter)
+            int t_next = 0;  // (lane 0) tiles [0, t_next) have their copies issued
+            int q_loads = 0; // (lane 0) Q blocks of items [0, q_loads) issued
+            const int total_items = is_k ? p.cu_items[p.B] : 0;
+            int b_scan = 0;  // request of this CTA's previous item: items come in increasing order
             for (int k = 0; ok; ++k) {
-                const int4 itm = take_item(k, ok);
+                int4 itm = make_int4(-1, 0, 0, 0);
+                if (is_k) {
+                    // take the next item from the counter, find its request with a
+                    // warp-wide forward scan of cu_items, and publish it
+                    int c = 0;
+                    if (lane == 0) c = atomicAdd(p.work_counter, 1);
+                    c = __shfl_sync(0xffffffffu, c, 0);
+                    if (c < total_items) {
+                        while (true) {  // ends: cu_items[B] = total > c
+                            const int bi = b_scan + lane;
+                            const int v = bi <= p.B ? p.cu_items[bi] : 0x7fffffff;
+                            const unsigned m = __ballot_sync(0xffffffffu, v > c);
+                            if (m) {
+                                b_scan += __ffs(m) - 2;  // cu_items[b_scan] <= c always
+                                break;
+                            }
+                            b_scan += 32;
+                        }
+                        const int rem = c - p.cu_items[b_scan];
+                        const int u = rem % U, kvh = u / p.pairs;
+                        const int hA = kvh * p.group + 2 * (u % p.pairs);
+                        const int hB = hA + 1 < (kvh + 1) * p.group ? hA + 1 : -1;
+                        itm = make_int4(b_scan, hA, hB, rem / U);
+                    }
+                    if (lane == 0) {
+                        const int slot = k % NI;
+                        if (k >= NI && !mbar_wait(b_item_empty(slot), ((k / NI) - 1) & 1, abort_flag, wlim)) {
+                            give_up();
+                            ok = false;
+                        } else {
+                            item_ring[slot] = itm;
+                            mbar_arrive(b_item_full(slot));
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                } else {
+                    if (lane == 0) itm = take_item(k, ok);
+                    itm.x = __shfl_sync(0xffffffffu, itm.x, 0);
+                    itm.y = __shfl_sync(0xffffffffu, itm.y, 0);
+                    itm.z = __shfl_sync(0xffffffffu, itm.z, 0);
+                    itm.w = __shfl_sync(0xffffffffu, itm.w, 0);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                }
                 if (!ok || itm.x < 0) break;
                 PfItem it;
                 pf_item(p, itm, BN, it);
-                const bool hasB = it.hB >= 0;
-                const int n = it.n_tiles;
-                if (!mbar_wait(b_qfull, k & 1, abort_flag)) { ok = false; break; }
-                if (n == 0) {
-                    umma_commit(b_qempty);
-                    continue;
-                }
-                if (!wait_k(t_base)) { ok = false; break; }
-                qk(0, t_base);
-                if (hasB) qk(1, t_base);
-                umma_commit(b_kempty(t_base % SK));
-                if (n == 1) umma_commit(b_qempty);
-                for (int j = 0; j < n; ++j) {
-                    const int t = t_base + j, tb = tb_base + j;
-                    const bool more = j + 1 < n;
-                    // block A: PV_A(t), then QK_A(t+1).  V(t) and K(t+1) arrive
-                    // long before P_A(t): wait for them first, so that once P_A
-                    // is there the MMAs go out back to back
-                    if (!mbar_wait(b_vfull(t % SV), (t / SV) & 1, abort_flag)) { ok = false; break; }
-                    if (more && !mbar_wait(b_kfull((t + 1) % SK), ((t + 1) / SK) & 1, abort_flag)) {
+                const int32_t *bt = p.block_tables + static_cast<int64_t>(it.b) * p.bt_stride;
+                // Q blocks of this item, once the previous item's last QK is done;
+                // loaded after the item's first K tile so that the two overlap
+                auto load_q = [&]() {  // lane 0 of the K producer
+                    if (k >= 1 && !mbar_wait(b_qempty, (k - 1) & 1, abort_flag, wlim)) {
+                        give_up();
                         ok = false;
-                        break;
+                    } else {
+                        mbar_expect_tx(b_qfull, it.hB >= 0 ? 2 * QB : QB);
+                        for (int c = 0; c < QA; ++c)
+                            tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hA, it.row_base);
+                        if (it.hB >= 0)
+                            for (int c = 0; c < QA; ++c)
+                                tma_load_3d(q_s + QB + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hB,
+                                            it.row_base);
+                        q_loads = k + 1;
                     }
-                    if (!mbar_wait(b_pfull(0), t & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    pv(0, t, j == 0);
-                    if (!more) umma_commit(b_odone(0));
-                    if (more) {
-                        qk(0, t + 1);
-                        if (!hasB) {
-                            umma_commit(b_kempty((t + 1) % SK));
-                            if (j + 2 == n) umma_commit(b_qempty);
+                };
+                if (is_k && lane == 0 && it.n_tiles == 0) load_q();
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
+                    const int key = j * BN + lane * RB;
+                    int page = oob;
+                    if (p.contiguous) return 0;  // one page: the whole tensor
+                    if (lane < nbox && key < it.kvb) {
+                        page = bt[key >> p.page_shift];
+                        if (page < 0 || page >= p.max_num_pages) {
+                            if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
+                            page = oob;
                         }
                     }
-                    // block B: PV_B(t), then QK_B(t+1)
-                    if (hasB) {
-                        if (!mbar_wait(b_pfull(1), tb & 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        pv(1, t, j == 0);
-                        if (!more) umma_commit(b_odone(1));
-                        if (more) {
-                            qk(1, t + 1);
-                            umma_commit(b_kempty((t + 1) % SK));
-                            if (j + 2 == n) umma_commit(b_qempty);
+                    return page;
+                };
+                int pg_next = it.n_tiles > 0 ? lookup(0) : oob;
+                for (int j = 0; j < it.n_tiles; ++j) {
+                    const int t = t_base + j;
+                    const int pg = pg_next;
+                    if (j + 1 < it.n_tiles) pg_next = lookup(j + 1);
+                    int pages[16];
+    #pragma unroll
+                    for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
+                    if (lane == 0) {
+                        const int st = t % NS, us = t / NS;
+                        if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag, wlim)) {
+                            give_up();
+                            ok = false;
+                        } else {
+                            const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
+                            mbar_expect_tx(full, is_k ? KB : VB);
+                            const int j0 = j * BN;
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (i >= nbox) break;
+                                const int r0 = i * RB;
+                                const int slot0 = p.contiguous ? (is_k ? it.kv_k : it.kv_v) + j0 + r0
+                                                               : (j0 + r0) & (S - 1);
+                                const int ca = LAYOUT == PKV_HND ? slot0 : it.kvh;
+                                const int cb = LAYOUT == PKV_HND ? it.kvh : slot0;
+                                if (is_k) {
+                                    for (int c = 0; c < QA; ++c)
+                                        tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca,
+                                                    cb, pages[i]);
+                                } else {
+                                    for (int c = 0; c < kPfDV / 64; ++c)
+                                        tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca,
+                                                    cb, pages[i]);
+                                }
+                            }
+                            t_next = t + 1;
+                            if (is_k && j == 0) load_q();
                         }
                     }
-                    umma_commit(b_vempty(t % SV));
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
                 }
-                t_base += n;
-                if (hasB) tb_base += n;
+                t_base += it.n_tiles;
             }
-            if (!ok) give_up();
+            // Before the CTA exits -- after the last item, or after a wait gave
+            // up with copies in flight -- wait for every copy this warp issued to
+            // land: the last phase issued on each stage (the earlier ones of a
+            // stage completed before it was reused) and the last Q blocks.
+            if (lane == 0) {
+                for (int t = t_next > NS ? t_next - NS : 0; t < t_next; ++t)
+                    if (!mbar_wait_drain(is_k ? b_kfull(t % NS) : b_vfull(t % NS), (t / NS) & 1))
+                        set_err(p.err, PKV_DEV_ERR_TIMEOUT);
+                if (is_k && q_loads > 0 && !mbar_wait_drain(b_qfull, (q_loads - 1) & 1))
+                    set_err(p.err, PKV_DEV_ERR_TIMEOUT);
+            }
+            __syncwarp();
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer
+            // Per item of n tiles: QK_A(0) QK_B(0), then for every tile t:
+            // PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1).  tcgen05 MMAs execute in issue
+            // order, so QK_X(t+1), which overwrites S_X, cannot disturb PV_X(t)
+            // reading P_X from it, and a completed S_X(t+1) implies that PV_X(t)
+            // is complete (the softmax relies on both).
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
+                constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
+                const uint64_t qdesc0 = umma_sdesc_sw128(q_s, 16, 1024);
+                const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
+                const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
+                bool ok = true;
+                int t_base = 0;   // K/V tiles of earlier items
+                int tb_base = 0;  // tiles of block B in earlier items
+                auto wait_k = [&](int t) {
+                    if (!mbar_wait(b_kfull(t % SK), (t / SK) & 1, abort_flag, wlim)) return false;
+                    tc_fence_after();
+                    return true;
+                };
+                auto qk = [&](int x, int t) {  // S_X = Q_X K(t)^T
+                    const uint64_t kd = kdesc0 + (((t % SK) * KB) >> 4);
+                    const uint64_t qd = qdesc0 + ((x * QB) >> 4);
+    #pragma unroll
+                    for (int kk = 0; kk < DQK / 16; ++kk)
+                        umma_ss(tmem + x * S_STRIDE, qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
+                                kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+                    umma_commit(b_sfull(x));
+                };
+                // P column of keys 16kk .. 16kk+15: each softmax thread owns HC
+                // columns, and writes chunk i (32 keys, or a final 16) as 16-bit
+                // pairs at the chunk's first column
+                constexpr int HC = BN / SPLIT;
+                auto pcol = [](int kk) {
+                    const int k0 = 16 * kk, c = k0 % HC;
+                    return (k0 / HC) * HC + 32 * (c / 32) + (c % 32) / 2;
+                };
+                auto pv = [&](int x, int t, bool first) {  // O_X (+)= P_X V(t)
+                    const uint64_t vd = vdesc0 + (((t % SV) * VB) >> 4);
+    #pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_ts(tmem + O_COL + x * kPfDV, tmem + x * S_STRIDE + pcol(kk), vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                                (!first || kk > 0) ? 1u : 0u);
+                };
+                for (int k = 0; ok; ++k) {
+                    const int4 itm = take_item(k, ok);
+                    if (!ok || itm.x < 0) break;
+                    PfItem it;
+                    pf_item(p, itm, BN, it);
+                    const bool hasB = it.hB >= 0;
+                    const int n = it.n_tiles;
+                    if (!mbar_wait(b_qfull, k & 1, abort_flag, wlim)) { ok = false; break; }
+                    if (n == 0) {
+                        umma_commit(b_qempty);
+                        continue;
+                    }
+                    if (!wait_k(t_base)) { ok = false; break; }
+                    qk(0, t_base);
+                    if (hasB) qk(1, t_base);
+                    umma_commit(b_kempty(t_base % SK));
+                    if (n == 1) umma_commit(b_qempty);
+                    for (int j = 0; j < n; ++j) {
+                        const int t = t_base + j, tb = tb_base + j;
+                        const bool more = j + 1 < n;
+                        // block A: PV_A(t), then QK_A(t+1).  V(t) and K(t+1) arrive
+                        // long before P_A(t): wait for them first, so that once P_A
+                        // is there the MMAs go out back to back
+                        if (!mbar_wait(b_vfull(t % SV), (t / SV) & 1, abort_flag, wlim)) { ok = false; break; }
+                        if (more && !mbar_wait(b_kfull((t + 1) % SK), ((t + 1) / SK) & 1, abort_flag, wlim)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait(b_pfull(0), t & 1, abort_flag, wlim)) { ok = false; break; }
+                        tc_fence_after();
+                        pv(0, t, j == 0);
+                        if (!more) umma_commit(b_odone(0));
+                        if (more) {
+                            qk(0, t + 1);
+                            if (!hasB) {
+                                umma_commit(b_kempty((t + 1) % SK));
+                                if (j + 2 == n) umma_commit(b_qempty);
+                            }
+                        }
+                        // block B: PV_B(t), then QK_B(t+1)
+                        if (hasB) {
+                            if (!mbar_wait(b_pfull(1), tb & 1, abort_flag, wlim)) { ok = false; break; }
+                            tc_fence_after();
+                            pv(1, t, j == 0);
+                            if (!more) umma_commit(b_odone(1));
+                            if (more) {
+                                qk(1, t + 1);
+                                umma_commit(b_kempty((t + 1) % SK));
+                                if (j + 2 == n) umma_commit(b_qempty);
+                            }
+                        }
+                        umma_commit(b_vempty(t % SV));
+                    }
+                    t_base += n;
+                    if (hasB) tb_base += n;
+                }
+                if (!ok) give_up();
+                // every MMA issued (also those of an abandoned item) completes
+                // before tensor memory is freed
+                umma_commit(b_drain);
+                if (!mbar_wait_drain(b_drain, 0)) set_err(p.err, PKV_DEV_ERR_TIMEOUT);
+            }
+            __syncwarp();
         }
     } else {
+        if constexpr (SPLIT == 1) reg_alloc<kRegsHigh>();
         // ------------------------------------------------------------ softmax warps
         // Warp w (0..15): block X = (w / 4) % 2, column half hh = w / 8, TMEM
         // lane quarter w % 4, so each query row of a block is served by two
@@ -618,14 +658,14 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         const bool pos_scale = sc > 0.f;  // max on raw scores, one FFMA scales and shifts
         const float k_mul = pos_scale ? sc : 1.f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, wlim));
         };
         int ex = 0;  // exchanges with the partner thread so far (buffer and phase)
         auto exchange = [&](float v, float &other) -> bool {
             xbuf[ex & 1][X][hh][r] = v;
             mbar_arrive(b_pair);
             // the partner arrives within a few hundred cycles: spin, no sleep
-            const bool done = __all_sync(0xffffffffu, mbar_wait_spin(b_pair, ex & 1, abort_flag));
+            const bool done = __all_sync(0xffffffffu, mbar_wait_spin(b_pair, ex & 1, abort_flag, wlim));
             other = *reinterpret_cast<volatile float *>(&xbuf[ex & 1][X][hh ^ 1][r]);
             ++ex;
             return done;
@@ -837,6 +877,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             nx_items += have;
         }
         if (!ok) give_up();
+        // (a tile abandoned after its P stores: they complete before the
+        // allocation is freed; the whole warp gets here together)
+        tmem_wait_st();
+        tmem_wait_ld();
     }
 
     tc_fence_before();
@@ -850,7 +894,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
 template <int DQK>
 static size_t prefill_smem_bytes() {
     constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
-    return 1024 + 2 * kPfRows * DQK * 2 + SK * BN * DQK * 2 + SV * BN * kPfDV * 2 + 8 * (20 + 2 * SK + 2 * SV);
+    return 1024 + 2 * kPfRows * DQK * 2 + SK * BN * DQK * 2 + SV * BN * kPfDV * 2 + 8 * (21 + 2 * SK + 2 * SV);
 }
 
 template <typename T, int DQK, int LAYOUT>
@@ -861,6 +905,18 @@ static int launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
+    if constexpr (PfCfg<DQK>::SPLIT == 1) {
+        // the register split draws on the registers the CTA is launched with:
+        // refuse to launch if the compiled kernel was given fewer (the
+        // softmax warps' setmaxnreg.inc would wait for registers forever)
+        static int ok = -1;
+        if (ok < 0) {
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PKV_ERR_CUDA;
+            ok = fa.numRegs * PfRoles<DQK>::kThreads >= 128 * kRegsLow + 256 * kRegsHigh ? 1 : 0;
+        }
+        if (!ok) return PKV_ERR_UNSUPPORTED;
+    }
     // launched as the plan kernel's dependent: the prologue (barriers, tensor
     // memory, descriptor prefetch) overlaps the plan kernel
     if (launch_dependent(kern, grid, dim3(PfRoles<DQK>::kThreads), smem, st, tq, tk, tv, p) != cudaSuccess)
@@ -1177,6 +1233,7 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     p.out = out;
     p.lse = lse;
     p.err = err_word;
+    p.wait_ns = wait_limit_ns();
     const int n_qt = (max_token_per_sequence + kPfRows - 1) / kPfRows;
     const int64_t items = static_cast<int64_t>(n_qt) * num_kv_heads * pairs * batch_size;
     if (n_qt > 0) {

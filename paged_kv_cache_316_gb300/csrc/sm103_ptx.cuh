@@ -27,17 +27,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-// One bounded poll: the thread may sleep in hardware for up to
-// kSuspendHintNs (waking as soon as the phase completes), so a waiting warp
-// does not burn issue slots of the warps that do the work.
+// One bounded poll: the thread may sleep in hardware for up to `hint_ns`
+// (waking as soon as the phase completes), so a waiting warp does not burn
+// issue slots of the warps that do the work.
 constexpr uint32_t kSuspendHintNs = 200000;
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -48,23 +48,33 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives
-// up (returns false) after about one second, or as soon as *abort is set by
-// another thread of the CTA that gave up first.
+// up (returns false) after `limit_ns` (by default one second; the host can
+// change it per launch, see pkv_set_wait_limit_ns), or as soon as *abort is
+// set by another thread of the CTA that gave up first.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity);
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_test_wait(bar, parity)) return true;  // already complete: no potentially blocking poll
-    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = limit_ns < kSuspendHintNs ? static_cast<uint32_t>(limit_ns) + 1u : kSuspendHintNs;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
+// Wait for a phase that completes without any other thread's help (a copy
+// this thread issued landing, or its MMAs finishing), before the CTA exits
+// after another wait gave up: no abort flag, the default one-second limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    volatile int no_abort = 0;
+    return mbar_wait(bar, parity, &no_abort, kWaitLimitNs);
+}
 
-// The same wait without the sleep hint: for phases expected within a few
-// hundred cycles.  Checks the abort flag and the time limit every 256 polls.
+// One non-blocking poll: true when the phase with parity `parity` of `bar`
+// has completed.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -75,18 +85,34 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *abort) {
+// The wait of mbar_wait without the sleep hint: for phases expected within a
+// few hundred cycles.  Checks the abort flag and the time limit every 256
+// polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_test_wait(bar, parity)) return true;
-        if ((i & 255) == 0 && (*abort || global_ns() - t0 > kWaitLimitNs)) return false;
+        if ((i & 255) == 0 && (*abort || global_ns() - t0 > limit_ns)) return false;
     }
 }
 
 // Barrier `id` (1..15) among `count` threads of the CTA (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
+// Per-warpgroup register budget (setmaxnreg): every warp of a warpgroup
+// executes the same one.  `dealloc` returns registers to the CTA's pool,
+// `alloc` takes them (waiting until the pool holds enough).
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
 }
 
 // ---- TMA (tensor loads into shared memory, completion on an mbarrier) -----------

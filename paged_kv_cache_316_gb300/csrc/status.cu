@@ -6,7 +6,15 @@
 namespace pkv {
 static std::atomic<unsigned long long> g_launches{0};
 void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+static std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(); }
 }  // namespace pkv
+
+extern "C" unsigned long long pkv_set_wait_limit_ns(unsigned long long ns) {
+    return pkv::g_wait_limit_ns.exchange(ns ? ns : pkv::kDefaultWaitLimitNs);
+}
 
 extern "C" const char *pkv_status_string(int status) {
     switch (status) {

@@ -47,6 +47,15 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libpagedkv.so does not export {name}"
 
 
+def test_wait_limit_is_set_and_restored(lib):
+    # host state only: the limit later launches pass to their kernels
+    lib.pkv_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.pkv_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    assert lib.pkv_set_wait_limit_ns(5000) == 1000000000  # the default: one second
+    assert lib.pkv_set_wait_limit_ns(0) == 5000           # 0 restores the default
+    assert lib.pkv_set_wait_limit_ns(0) == 1000000000
+
+
 def test_status_strings(lib):
     assert lib.pkv_status_string(0) == b"ok"
     assert b"workspace" in lib.pkv_status_string(4)

@@ -287,3 +287,82 @@ def test_fp8_cache_full_size_sampled():
     c = wl.llama_decode(device=DEV, kv_dtype=wl.E4M3)
     lengths = np.array(c.pt.lengths)
     _sampled_full_size(c, sorted({int(lengths.argmin()), int(lengths.argmax()), 9, 40}))
+
+
+def _key_factor(j: int) -> float:
+    """Scale of key j: steps up at keys 100, 600 and 2500, so that each
+    row's running max (base 2) rises by more than 2^8 several times after
+    its first tile, in the first split and in later ones."""
+    return 1.0 if j < 100 else 4.0 if j < 600 else 12.0 if j < 2500 else 24.0
+
+
+def _rising_keys(c):
+    """Multiply the keys of every request by _key_factor(position) (CPU pool,
+    in place); returns the largest rise of a row's base-2 max over its first
+    64-key tile, for checking that the case does what it is for."""
+    rise = 0.0
+    Q = c.q_len_per_req
+    group = c.num_qo_heads // c.num_kv_heads
+    for b, L in enumerate(c.pt.lengths):
+        k, v = wl.read_tokens(c.pool, c.pt, b)
+        f = torch.tensor([_key_factor(j) for j in range(L)], dtype=torch.float32).view(-1, 1, 1)
+        k = (k.float() * f).to(k.dtype)
+        wl.write_tokens(c.pool, c.pt, b, k, v)
+        q = c.query[b * Q:(b + 1) * Q].double()                        # [Q, Hqo, D]
+        kk = k.double().repeat_interleave(group, dim=1)                # [L, Hqo, D]
+        s = torch.einsum("qhd,khd->qhk", q, kk) * c.bmm1_scale * 1.4426950408889634
+        if L > 64:
+            rise = max(rise, float((s[..., 64:].amax(-1) - s[..., :64].amax(-1)).max()))
+    return rise
+
+
+RISING = [
+    # lengths, page, Hqo, Hkv, Q, window, sinks, layout, kv dtype, seed
+    ([3000, 700, 5000, 129], 16, 32, 8, 1, -1, False, wl.HND, None, 61),     # 4 rows, 1..5 splits
+    ([900, 2600], 64, 64, 8, 4, -1, True, wl.NHD, None, 62),                 # 32 rows
+    ([1100, 4000], 32, 32, 4, 8, 3000, True, wl.HND, None, 63),              # 64 rows, window
+    ([3000, 700, 129], 16, 32, 8, 1, -1, True, wl.NHD, wl.E4M3, 64),         # E4M3, 4 rows
+    ([2600, 900], 64, 64, 8, 4, 2000, False, wl.HND, wl.E4M3, 65),           # E4M3, 32 rows
+]
+
+
+@pytest.mark.parametrize("case", RISING, ids=[f"r{i}" for i in range(len(RISING))])
+def test_running_max_rises_far_after_first_tile(case):
+    # the decode raises its running max only when a tile's exceeds it by more
+    # than 2^8 and rescales O only then; these keys make that happen many
+    # times (the rescale of O, and the (m, l) update across tiles and splits)
+    L, S, hq, hk, Q, w, sk, lay, kvd, seed = case
+    c = wl.decode_case(L, S, hq, hk, 128, lay, q_len_per_req=Q, window_left=w, with_sinks=sk,
+                       seed=seed, slack=0.2, kv_dtype=kvd)
+    assert _rising_keys(c) > 16.0
+    err = err_word()
+    _check(c, err_word=err)
+    assert int(err.item()) == 0
+
+
+def test_binding_refuses_shapes_the_abi_cannot_check():
+    # the uniform decode's C entry points take no row count: the binding
+    # checks query rows, out and lse against the requests before the call
+    c = wl.decode_case([100, 50], 16, 32, 8, 128, wl.HND, q_len_per_req=2, seed=66)
+    kv, bt, sl = c.pool.storage[0].to(DEV), c.block_tables.to(DEV), c.seq_lens.to(DEV)
+    q = c.query.to(DEV)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=DEV)
+    bad = [
+        dict(query=q[:3]),                                                    # 3 rows for 2 x 2
+        dict(out=torch.empty((3, 32, 128), dtype=q.dtype, device=DEV)),
+        dict(out=torch.empty_like(q, dtype=torch.float16)),
+        dict(lse=torch.empty((4, 32), dtype=torch.float64, device=DEV)),
+        dict(lse=torch.empty((4, 31), dtype=torch.float32, device=DEV)),
+        dict(block_tables=bt[:1]),
+    ]
+    for kw in bad:
+        args = dict(query=q, block_tables=bt)
+        args.update(kw)
+        with pytest.raises(pk.PagedKVError):
+            pk.paged_decode(args.pop("query"), kv, ws, args.pop("block_tables"), sl, c.max_seq_len,
+                            q_len_per_req=2, **args)
+        with pytest.raises(pk.PagedKVError):
+            a2 = dict(query=q, block_tables=bt)
+            a2.update(kw)
+            pk.paged_decode_noalloc(a2.pop("query"), kv, a2.pop("block_tables"), sl, c.max_seq_len,
+                                    q_len_per_req=2, **a2)
