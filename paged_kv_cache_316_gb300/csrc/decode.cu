@@ -121,7 +121,9 @@ __device__ __forceinline__ void store4(T *dst, float a, float b, float c, float 
     *reinterpret_cast<uint2 *>(dst) = v;
 }
 
-template <typename T, int MT, int LAYOUT, bool KV8>
+// SW (an E4M3 cache and at most 8 query rows): the MMAs take the keys as
+// their 16-row side, S^T = K Q^T and O^T = V^T P^T (see the tile loop).
+template <typename T, int MT, int LAYOUT, bool KV8, bool SW = false>
 __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_split_kernel(const DecodeParams p) {
     constexpr int kDecStages = DecCfg<MT, KV8>::STAGES;
     constexpr int STAGE_BYTES = DecSmem<KV8>::STAGE;
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     // fp16 in one instruction; a bf16 query is brought to fp16 exactly, see
     // below)
     using TM = typename std::conditional<KV8, __half, T>::type;
+    static_assert(!SW || (KV8 && MT == 1), "swapped operands: E4M3 cache, one row tile");
     constexpr int NKG = 4 / MT;          // warps that split the keys of a tile
     constexpr int KPW = kDecTile / NKG;  // keys per warp per tile
     constexpr int NT = KPW / 8;          // 8-key score tiles per warp
@@ -364,7 +367,19 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     }
 
     uint32_t qa[8][4];
-    if constexpr (KV8) {
+    if constexpr (SW) {
+        // B operand of the swapped QK (Q^T, k = head dim, n = query row):
+        // lane (g, c) holds row g, dims 32c + 4kk + {0, 1} and {2, 3} of
+        // k-step kk (the permuted order of the K rows, below)
+        const int gq = lane >> 2, cq = lane & 3;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int dim = cq * 32 + kk * 4;
+            const uint2 lo = *reinterpret_cast<const uint2 *>(q_s + swz(gq, dim >> 3, kDecRowBytes) + (dim & 7) * 2);
+            qa[kk][0] = lo.x;
+            qa[kk][1] = lo.y;
+        }
+    } else if constexpr (KV8) {
         // Over an E4M3 cache the head dimension is taken in a permuted order,
         // the same for Q and K (a dot product does not depend on it): the k
         // pairs {2c, 2c+1} and {2c+8, 2c+9} of k-step kk are the dims
@@ -397,6 +412,11 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     const int lo1 = p.window_left >= 0 ? max(0, pos1 - p.window_left) : 0;
     const int lo_max = p.window_left >= 0 ? max(0, L - 1 - p.window_left) : 0;
     const int hi_min = min(L - Q, k_end - 1);
+    // (swapped operands: lane (g, c) holds query rows 2c and 2c + 1)
+    const int sr0 = 2 * (lane & 3), sr1 = sr0 + 1;
+    const int spos0 = L - Q + min(sr0 / p.group, Q - 1), spos1 = L - Q + min(sr1 / p.group, Q - 1);
+    const int slo0 = p.window_left >= 0 ? max(0, spos0 - p.window_left) : 0;
+    const int slo1 = p.window_left >= 0 ? max(0, spos1 - p.window_left) : 0;
 
     float o[16][4];
 #pragma unroll
@@ -418,129 +438,231 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         const uint8_t *k8 = smem + stage * STAGE_BYTES;  // E4M3 K rows (KV8)
         const uint8_t *v8 = k8 + kDec8TileBytes;         // E4M3 V rows (KV8)
 
-        float sc[NT][4];
+        if constexpr (SW) {
+            // Swapped operands for at most 8 query rows: S^T (the warp's 16
+            // keys x 8 rows) = K Q^T and O^T (128 dims x 8 rows) += V^T P^T,
+            // so that the keys fill the MMA's 16-row side and half as many
+            // MMAs cover a tile.  Lane (g, c) = (lane / 4, lane % 4) holds
+            // the scores of keys kw0 + g and kw0 + g + 8 for query rows 2c
+            // and 2c + 1; rows at or beyond R are padding, masked out.
+            const int g = lane >> 2, c = lane & 3;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps
+            {
+                // A = K rows kw0 + g and kw0 + g + 8: the word at byte
+                // 32c + 4kk of a row holds dims 32c + 4kk .. + 3, both halves
+                // of the lane's A fragment of k-step kk (the permuted order
+                // the Q fragments follow)
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(k8 + swz8(kw0 + g, 2 * c));
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(k8 + swz8(kw0 + g, 2 * c + 1));
+                const uint4 v0 = *reinterpret_cast<const uint4 *>(k8 + swz8(kw0 + g + 8, 2 * c));
+                const uint4 v1 = *reinterpret_cast<const uint4 *>(k8 + swz8(kw0 + g + 8, 2 * c + 1));
+                const uint32_t wa[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                const uint32_t wb[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-        if constexpr (KV8) {
-            // key kw0 + 8nt + g: its 32 bytes at dims 32c .. 32c + 31 hold the
-            // B fragments of all eight k-steps (see the Q fragments)
-            const int g8 = lane >> 2, c8 = lane & 3;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int row = kw0 + nt * 8 + g8;
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(k8 + swz8(row, 2 * c8));
-                const uint4 u1 = *reinterpret_cast<const uint4 *>(k8 + swz8(row, 2 * c8 + 1));
-                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma16816<TM>(sc[nt], qa[kk], widen_e4m3x2<TM>(w[kk] & 0xffffu), widen_e4m3x2<TM>(w[kk] >> 16));
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a[4] = {widen_e4m3x2<TM>(wa[kk] & 0xffffu), widen_e4m3x2<TM>(wb[kk] & 0xffffu),
+                                           widen_e4m3x2<TM>(wa[kk] >> 16), widen_e4m3x2<TM>(wb[kk] >> 16)};
+                    if (kk & 1)
+                        mma16816<TM>(sb, a, qa[kk][0], qa[kk][1]);
+                    else
+                        mma16816<TM>(sa, a, qa[kk][0], qa[kk][1]);
+                }
             }
-        } else {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t bf[4];
-                int key = kw0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(bf, kb + swz(key, 2 * kk + ((lane >> 3) & 1), kDecRowBytes));
-                mma16816<TM>(sc[2 * np], qa[kk], bf[0], bf[1]);
-                mma16816<TM>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
-            }
-        }
-        }
-
-        const bool interior = !any_bad[kg] && j0 >= lo_max && j0 + kDecTile - 1 <= hi_min;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+            // element e: key kw0 + g + 8 (e / 2), query row 2c + (e % 2)
+            float sv[4];
+            const bool interior = !any_bad[kg] && j0 >= lo_max && j0 + kDecTile - 1 <= hi_min;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float x = sc[nt][e] * scale_log2;
-                if (!interior) {
-                    int jj = kw0 + nt * 8 + 2 * (lane & 3) + (e & 1);
-                    int j = j0 + jj;
-                    bool vis = kvalid[stage * kDecTile + jj] &&
-                               (e < 2 ? (j >= lo0 && j <= pos0) : (j >= lo1 && j <= pos1));
-                    if (!vis) x = -INFINITY;
+                float x = (sa[e] + sb[e]) * scale_log2;
+                const int jj = kw0 + g + 8 * (e >> 1), j = j0 + jj;
+                bool vis = (e & 1 ? sr1 : sr0) < R;
+                if (!interior)
+                    vis = vis && kvalid[stage * kDecTile + jj] &&
+                          (e & 1 ? (j >= slo1 && j <= spos1) : (j >= slo0 && j <= spos0));
+                sv[e] = vis ? x : -INFINITY;
+            }
+            // row maxima over the warp's 16 keys (the lanes of one c)
+            float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+            for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
+            }
+            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
+            const float p0 = fast_exp2(sv[0] - base0), p1 = fast_exp2(sv[1] - base1);
+            const float p2 = fast_exp2(sv[2] - base0), p3 = fast_exp2(sv[3] - base1);
+            l0 = l0 * al0 + (p0 + p2);  // (this lane's keys; summed over g at the end)
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[i][0] *= al0;
+                    o[i][2] *= al0;
+                    o[i][1] *= al1;
+                    o[i][3] *= al1;
                 }
-                sc[nt][e] = x;
             }
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+            // B = P^T (k = the warp's 16 keys, n = query row): lane (g, c)
+            // needs row g's P of keys 2c, 2c + 1, 2c + 8, 2c + 9, held by
+            // lanes (2c, g / 2) and (2c + 1, g / 2) as their row-2c' or
+            // row-2c'+1 pair
+            const uint32_t he = pack2<TM>(p0, p2), ho = pack2<TM>(p1, p3);
+            const int srcA = 8 * c + (g >> 1), srcB = srcA + 4;
+            const uint32_t eA = __shfl_sync(0xffffffffu, he, srcA), oA = __shfl_sync(0xffffffffu, ho, srcA);
+            const uint32_t eB = __shfl_sync(0xffffffffu, he, srcB), oB = __shfl_sync(0xffffffffu, ho, srcB);
+            const uint32_t vA = (g & 1) ? oA : eA, vB = (g & 1) ? oB : eB;
+            const uint32_t pb0 = __byte_perm(vA, vB, 0x5410), pb1 = __byte_perm(vA, vB, 0x7632);
+            // A = V^T (m = head dim, k = key) of m-tile i: its row m is dim
+            // 16 (m % 8) + 2i + m / 8, so that a lane's 16 dims of a V row are
+            // one 16-byte chunk (g) and the two keys of an A register are
+            // byte-interleaved from two rows
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(v8 + swz8(kw0 + 2 * c, g));
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(v8 + swz8(kw0 + 2 * c + 1, g));
+            const uint4 y0 = *reinterpret_cast<const uint4 *>(v8 + swz8(kw0 + 2 * c + 8, g));
+            const uint4 y1 = *reinterpret_cast<const uint4 *>(v8 + swz8(kw0 + 2 * c + 9, g));
+            const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
+            const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        // the running max rises only when a tile's exceeds it by more than 8
-        // (a factor 2^8; from -inf at the first key): P stays below 2^8 and
-        // O is rarely rescaled
-        const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
-        float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            sc[nt][0] = fast_exp2(sc[nt][0] - base0);
-            sc[nt][1] = fast_exp2(sc[nt][1] - base0);
-            sc[nt][2] = fast_exp2(sc[nt][2] - base1);
-            sc[nt][3] = fast_exp2(sc[nt][3] - base1);
-            rs0 += sc[nt][0] + sc[nt][1];
-            rs1 += sc[nt][2] + sc[nt][3];
-        }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-        m0 = mn0;
-        m1 = mn1;
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                o[i][0] *= al0;
-                o[i][1] *= al0;
-                o[i][2] *= al1;
-                o[i][3] *= al1;
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t x01 = __byte_perm(X0[i], X1[i], 0x5140), x23 = __byte_perm(X0[i], X1[i], 0x7362);
+                const uint32_t y01 = __byte_perm(Y0[i], Y1[i], 0x5140), y23 = __byte_perm(Y0[i], Y1[i], 0x7362);
+                const uint32_t a0[4] = {widen_e4m3x2<TM>(x01 & 0xffffu), widen_e4m3x2<TM>(x01 >> 16),
+                                        widen_e4m3x2<TM>(y01 & 0xffffu), widen_e4m3x2<TM>(y01 >> 16)};
+                const uint32_t a1[4] = {widen_e4m3x2<TM>(x23 & 0xffffu), widen_e4m3x2<TM>(x23 >> 16),
+                                        widen_e4m3x2<TM>(y23 & 0xffffu), widen_e4m3x2<TM>(y23 >> 16)};
+                mma16816<TM>(o[2 * i], a0, pb0, pb1);
+                mma16816<TM>(o[2 * i + 1], a1, pb0, pb1);
             }
-        }
+        } else {
+            float sc[NT][4];
 #pragma unroll
-        for (int ks = 0; ks < NT / 2; ++ks) {
-            uint32_t a[4];
-            a[0] = pack2<TM>(sc[2 * ks][0], sc[2 * ks][1]);
-            a[1] = pack2<TM>(sc[2 * ks][2], sc[2 * ks][3]);
-            a[2] = pack2<TM>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-            a[3] = pack2<TM>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+            for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
             if constexpr (KV8) {
-                // The output dims are permuted too: column g of n-tile nt is
-                // dim 16g + nt, so the lane's 16 bytes of the keys 2c, 2c+1,
-                // 2c+8, 2c+9 feed all 16 n-tiles, the two keys of a B
-                // register interleaved byte by byte.
-                const int g8 = lane >> 2, rb = kw0 + ks * 16 + 2 * (lane & 3);
-                const uint4 x0 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb, g8));
-                const uint4 x1 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 1, g8));
-                const uint4 y0 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 8, g8));
-                const uint4 y1 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 9, g8));
-                const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
-                const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
+                // key kw0 + 8nt + g: its 32 bytes at dims 32c .. 32c + 31 hold the
+                // B fragments of all eight k-steps (see the Q fragments)
+                const int g8 = lane >> 2, c8 = lane & 3;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t p01 = __byte_perm(X0[i], X1[i], 0x5140), p23 = __byte_perm(X0[i], X1[i], 0x7362);
-                    const uint32_t q01 = __byte_perm(Y0[i], Y1[i], 0x5140), q23 = __byte_perm(Y0[i], Y1[i], 0x7362);
-                    mma16816<TM>(o[4 * i], a, widen_e4m3x2<TM>(p01 & 0xffffu), widen_e4m3x2<TM>(q01 & 0xffffu));
-                    mma16816<TM>(o[4 * i + 1], a, widen_e4m3x2<TM>(p01 >> 16), widen_e4m3x2<TM>(q01 >> 16));
-                    mma16816<TM>(o[4 * i + 2], a, widen_e4m3x2<TM>(p23 & 0xffffu), widen_e4m3x2<TM>(q23 & 0xffffu));
-                    mma16816<TM>(o[4 * i + 3], a, widen_e4m3x2<TM>(p23 >> 16), widen_e4m3x2<TM>(q23 >> 16));
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int row = kw0 + nt * 8 + g8;
+                    const uint4 u0 = *reinterpret_cast<const uint4 *>(k8 + swz8(row, 2 * c8));
+                    const uint4 u1 = *reinterpret_cast<const uint4 *>(k8 + swz8(row, 2 * c8 + 1));
+                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma16816<TM>(sc[nt], qa[kk], widen_e4m3x2<TM>(w[kk] & 0xffffu), widen_e4m3x2<TM>(w[kk] >> 16));
                 }
             } else {
-                const int key = kw0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-                for (int dp = 0; dp < 8; ++dp) {
-                    uint32_t vf[4];
-                    ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), kDecRowBytes));
-                    mma16816<TM>(o[2 * dp], a, vf[0], vf[1]);
-                    mma16816<TM>(o[2 * dp + 1], a, vf[2], vf[3]);
+            for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t bf[4];
+                    int key = kw0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    ldsm_x4(bf, kb + swz(key, 2 * kk + ((lane >> 3) & 1), kDecRowBytes));
+                    mma16816<TM>(sc[2 * np], qa[kk], bf[0], bf[1]);
+                    mma16816<TM>(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
+                }
+            }
+            }
+
+            const bool interior = !any_bad[kg] && j0 >= lo_max && j0 + kDecTile - 1 <= hi_min;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float x = sc[nt][e] * scale_log2;
+                    if (!interior) {
+                        int jj = kw0 + nt * 8 + 2 * (lane & 3) + (e & 1);
+                        int j = j0 + jj;
+                        bool vis = kvalid[stage * kDecTile + jj] &&
+                                   (e < 2 ? (j >= lo0 && j <= pos0) : (j >= lo1 && j <= pos1));
+                        if (!vis) x = -INFINITY;
+                    }
+                    sc[nt][e] = x;
+                }
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+                mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            // the running max rises only when a tile's exceeds it by more than 8
+            // (a factor 2^8; from -inf at the first key): P stays below 2^8 and
+            // O is rarely rescaled
+            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                sc[nt][0] = fast_exp2(sc[nt][0] - base0);
+                sc[nt][1] = fast_exp2(sc[nt][1] - base0);
+                sc[nt][2] = fast_exp2(sc[nt][2] - base1);
+                sc[nt][3] = fast_exp2(sc[nt][3] - base1);
+                rs0 += sc[nt][0] + sc[nt][1];
+                rs1 += sc[nt][2] + sc[nt][3];
+            }
+            l0 = l0 * al0 + rs0;
+            l1 = l1 * al1 + rs1;
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    o[i][0] *= al0;
+                    o[i][1] *= al0;
+                    o[i][2] *= al1;
+                    o[i][3] *= al1;
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < NT / 2; ++ks) {
+                uint32_t a[4];
+                a[0] = pack2<TM>(sc[2 * ks][0], sc[2 * ks][1]);
+                a[1] = pack2<TM>(sc[2 * ks][2], sc[2 * ks][3]);
+                a[2] = pack2<TM>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+                a[3] = pack2<TM>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+                if constexpr (KV8) {
+                    // The output dims are permuted too: column g of n-tile nt is
+                    // dim 16g + nt, so the lane's 16 bytes of the keys 2c, 2c+1,
+                    // 2c+8, 2c+9 feed all 16 n-tiles, the two keys of a B
+                    // register interleaved byte by byte.
+                    const int g8 = lane >> 2, rb = kw0 + ks * 16 + 2 * (lane & 3);
+                    const uint4 x0 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb, g8));
+                    const uint4 x1 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 1, g8));
+                    const uint4 y0 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 8, g8));
+                    const uint4 y1 = *reinterpret_cast<const uint4 *>(v8 + swz8(rb + 9, g8));
+                    const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
+                    const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t p01 = __byte_perm(X0[i], X1[i], 0x5140), p23 = __byte_perm(X0[i], X1[i], 0x7362);
+                        const uint32_t q01 = __byte_perm(Y0[i], Y1[i], 0x5140), q23 = __byte_perm(Y0[i], Y1[i], 0x7362);
+                        mma16816<TM>(o[4 * i], a, widen_e4m3x2<TM>(p01 & 0xffffu), widen_e4m3x2<TM>(q01 & 0xffffu));
+                        mma16816<TM>(o[4 * i + 1], a, widen_e4m3x2<TM>(p01 >> 16), widen_e4m3x2<TM>(q01 >> 16));
+                        mma16816<TM>(o[4 * i + 2], a, widen_e4m3x2<TM>(p23 & 0xffffu), widen_e4m3x2<TM>(q23 & 0xffffu));
+                        mma16816<TM>(o[4 * i + 3], a, widen_e4m3x2<TM>(p23 >> 16), widen_e4m3x2<TM>(q23 >> 16));
+                    }
+                } else {
+                    const int key = kw0 + ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+                    for (int dp = 0; dp < 8; ++dp) {
+                        uint32_t vf[4];
+                        ldsm_x4_t(vf, vb + swz(key, 2 * dp + (lane >> 4), kDecRowBytes));
+                        mma16816<TM>(o[2 * dp], a, vf[0], vf[1]);
+                        mma16816<TM>(o[2 * dp + 1], a, vf[2], vf[3]);
+                    }
                 }
             }
         }
@@ -550,12 +672,39 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     pdl_launch_dependents();  // the merge kernel may get ready; it waits for this grid
 
     // combine the key groups of this CTA through shared memory
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if constexpr (SW) {  // a row's keys are spread over the lanes of one c
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+        }
+    } else {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    }
     float *comb_o = reinterpret_cast<float *>(smem);  // [NKG][ROWS][128]
-    if constexpr (KV8) {
+    if constexpr (SW) {
+        // lane (g, c) holds rows 2c and 2c + 1 at dims 16g .. 16g + 15:
+        // o[i][0 / 1] at dim 16g + 2i, o[i][2 / 3] at dim 16g + 2i + 1
+        const int g = lane >> 2;
+        float *w0 = &comb_o[(kg * ROWS + sr0) * kDecD + 16 * g];
+        float *w1 = &comb_o[(kg * ROWS + sr1) * kDecD + 16 * g];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            *reinterpret_cast<float4 *>(w0 + 4 * q) =
+                make_float4(o[2 * q][0], o[2 * q][2], o[2 * q + 1][0], o[2 * q + 1][2]);
+            *reinterpret_cast<float4 *>(w1 + 4 * q) =
+                make_float4(o[2 * q][1], o[2 * q][3], o[2 * q + 1][1], o[2 * q + 1][3]);
+        }
+        if (g == 0) {
+            comb_m[kg * ROWS + sr0] = m0;
+            comb_l[kg * ROWS + sr0] = l0;
+            comb_m[kg * ROWS + sr1] = m1;
+            comb_l[kg * ROWS + sr1] = l1;
+        }
+    } else if constexpr (KV8) {
         // undo the output permutation: o[nt][e] is dim 16 (2c + (e & 1)) + nt
         const int d0 = 32 * (lane & 3);
 #pragma unroll
@@ -575,7 +724,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
             *reinterpret_cast<float2 *>(&comb_o[(kg * ROWS + r1) * kDecD + d]) = make_float2(o[nd][2], o[nd][3]);
         }
     }
-    if ((lane & 3) == 0) {
+    if (!SW && (lane & 3) == 0) {
         comb_m[kg * ROWS + r0] = m0;
         comb_l[kg * ROWS + r0] = l0;
         comb_m[kg * ROWS + r1] = m1;
@@ -690,7 +839,7 @@ struct DecodePlan {
 };
 
 static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, int page_size,
-                       int window_left, DecodePlan &pl) {
+                       int window_left, DecodePlan &pl, bool kv8 = false) {
     if (B < 0 || Q < 1 || Hqo < 1 || Hkv < 1 || max_seq_len < 0 || window_left < -1)
         return PKV_ERR_INVALID_ARG;
     if (Hqo % Hkv) return PKV_ERR_INVALID_ARG;
@@ -711,6 +860,9 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     // while the grid would leave SMs idle.
     int chunk = 128 * pl.R;
     chunk = chunk < 1024 ? 1024 : (chunk > 4096 ? 4096 : chunk);
+    // an E4M3 cache moves half the bytes per key: twice the keys per split
+    // keep the per-CTA set-up and partial traffic at the same share
+    if (kv8) chunk = 2 * chunk > 4096 ? 4096 : 2 * chunk;
     chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
     // a window a little longer than the chunk (its first key need not sit on
     // a tile edge: up to 63 keys more) takes one split rather than a second,
@@ -736,13 +888,13 @@ static int plan_decode(int B, int Q, int Hqo, int Hkv, int D, int max_seq_len, i
     return PKV_OK;
 }
 
-template <typename T, int MT, int LAYOUT, bool KV8>
+template <typename T, int MT, int LAYOUT, bool KV8, bool SW = false>
 static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
     constexpr int ROWS = 16 * MT, NKG = 4 / MT;
     constexpr int kDecStages = DecCfg<MT, KV8>::STAGES;
     const size_t smem = kDecStages * DecSmem<KV8>::STAGE + ROWS * kDecRowBytes +
                         kDecStages * kDecTile + 2 * NKG * ROWS * sizeof(float) + kDecMaxPages * sizeof(int);
-    auto kern = decode_split_kernel<T, MT, LAYOUT, KV8>;
+    auto kern = decode_split_kernel<T, MT, LAYOUT, KV8, SW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -753,6 +905,9 @@ static int launch_split(const DecodeParams &p, dim3 grid, cudaStream_t st, bool 
 
 template <typename T, int LAYOUT, bool KV8>
 static int launch_split_mt(int MT, const DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
+    if constexpr (KV8) {
+        if (p.R <= 8) return launch_split<T, 1, LAYOUT, true, true>(p, grid, st, pdl);  // swapped operands
+    }
     if (MT == 1) return launch_split<T, 1, LAYOUT, KV8>(p, grid, st, pdl);
     if (MT == 2) return launch_split<T, 2, LAYOUT, KV8>(p, grid, st, pdl);
     return launch_split<T, 4, LAYOUT, KV8>(p, grid, st, pdl);
@@ -815,6 +970,15 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
     int rc = plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
                          max_seq_len, page_size, window_left, pl);
     if (rc != PKV_OK) return rc;
+    if (kv8) {
+        // the E4M3 plan's longer splits, whenever they fit the workspace that
+        // paged_decode_workspace_size (which knows no element type) sized
+        DecodePlan p8;
+        if (plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim, max_seq_len,
+                        page_size, window_left, p8, true) == PKV_OK &&
+            p8.ws_bytes <= pl.ws_bytes)
+            pl = p8;
+    }
     if (page_stride < static_cast<int64_t>(num_kv_heads) * page_size * head_dim || max_num_pages < 0 ||
         static_cast<int64_t>(block_table_stride) * page_size < max_seq_len)
         return PKV_ERR_INVALID_ARG;

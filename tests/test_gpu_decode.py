@@ -268,6 +268,11 @@ FP8 = [
     ([2100, 777, 40], 64, 64, 8, 4, 300, True, wl.BF16, wl.NHD, 52),     # 32 rows
     ([900, 130], 32, 16, 16, 1, -1, True, wl.F16, wl.HND, 53),           # MHA, fp16 query
     ([1025, 64], 16, 32, 4, 8, 100, False, wl.BF16, wl.HND, 54),         # 64 rows
+    # at most 8 query rows take the swapped-operand MMAs: 8, 6 and 2 rows,
+    # padding rows, windows, sinks, both layouts
+    ([900, 130, 2500], 16, 32, 4, 1, 200, True, wl.BF16, wl.NHD, 55),    # 8 rows
+    ([700, 3000], 32, 24, 8, 2, -1, True, wl.F16, wl.HND, 56),           # group 3 x 2 tokens
+    ([513, 77, 4100], 64, 8, 8, 2, 100, False, wl.BF16, wl.HND, 57),     # 2 rows
 ]
 
 
