@@ -33,6 +33,8 @@
 // other roles stop, tensor memory is freed and the CTA returns.
 #include <math.h>
 
+#include <type_traits>
+
 #include "pkv_common.cuh"
 #include "sm103_ptx.cuh"
 
@@ -50,15 +52,15 @@ template <int DQK>
 struct PfCfg;
 template <>
 struct PfCfg<128> {
-    static constexpr int BN = 128, SK = 2, SV = 2, SPLIT = 1;
+    static constexpr int BN = 128, SK = 2, SV = 2;
 };
 template <>
 struct PfCfg<192> {
-    static constexpr int BN = 96, SK = 2, SV = 2, SPLIT = 1;
+    static constexpr int BN = 96, SK = 2, SV = 2;
 };
 template <int DQK>
 struct PfRoles {
-    static constexpr int kSoftmaxWarps = 8 * PfCfg<DQK>::SPLIT;
+    static constexpr int kSoftmaxWarps = 8;
     static constexpr int kTmaWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1, kTmaVWarp = kSoftmaxWarps + 2;
     // + one idle warp, so that the producer / MMA warps make a whole warpgroup
     static constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
@@ -228,18 +230,29 @@ __device__ __forceinline__ void pf_item(const PrefillParams &p, const int4 itm, 
     it.n_tiles = (k_hi + bn - 1) / bn;
 }
 
-template <typename T, int DQK, int LAYOUT>
+// F8: the query and the caches hold E4M3 (one byte per element; d_qk 128):
+// QK runs as kind::f8f6f4 MMAs straight from the E4M3 tiles, and the E4M3 V
+// tiles are widened (exactly) to fp16 in shared memory by warp 11 for the
+// 16-bit PV, whose P is then fp16.  T is the output type.
+template <typename T, int DQK, int LAYOUT, bool F8 = false>
 __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     constexpr int BN = PfCfg<DQK>::BN;
-    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV, SPLIT = PfCfg<DQK>::SPLIT;
+    // (F8: a third V stage, so that the widening of a tile has a whole tile
+    // period of slack before its PV)
+    constexpr int SK = PfCfg<DQK>::SK, SV = F8 ? 3 : PfCfg<DQK>::SV;
     constexpr int kTmaWarp = PfRoles<DQK>::kTmaWarp, kMmaWarp = PfRoles<DQK>::kMmaWarp,
                   kTmaVWarp = PfRoles<DQK>::kTmaVWarp;
-    constexpr int QA = DQK / 64;                 // 64-column atoms of a Q / K row
-    constexpr uint32_t QB = kPfRows * DQK * 2;   // bytes of one Q block
-    constexpr uint32_t KB = BN * DQK * 2;        // bytes of one K stage
-    constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one V stage
+    static_assert(!F8 || DQK == 128, "E4M3 tiles: d_qk 128");
+    using TP = typename std::conditional<F8, __half, T>::type;  // element type of P (and V)
+    constexpr int ES = F8 ? 1 : 2;               // bytes per Q / K element
+    constexpr int QA = DQK * ES / 128;           // 128-byte atoms of a Q / K row
+    constexpr uint32_t QB = kPfRows * DQK * ES;  // bytes of one Q block
+    constexpr uint32_t KB = BN * DQK * ES;       // bytes of one K stage
+    constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one 16-bit V stage
+    constexpr uint32_t V8B = F8 ? BN * kPfDV : 0;  // bytes of one E4M3 V stage (F8)
+    constexpr int KSTEPS = DQK * ES / 32;        // 32-byte K-steps of a QK MMA
     constexpr int NI = 2;                        // slots of the work-item ring
     // TMEM columns (every region starts at a multiple of 128): S of block X
     // at X * S_STRIDE (BN columns; P of a chunk, 16-bit pairs,
@@ -256,8 +269,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     const uint32_t q_s = smem_u32(smem);  // block A, then block B
     const uint32_t k_s = q_s + 2 * QB;
     const uint32_t v_s = k_s + SK * KB;
-    const uint32_t bar0 = v_s + SV * VB;
+    const uint32_t v8_s = v_s + SV * VB;       // E4M3 V stages (F8)
+    const uint32_t bar0 = v8_s + SV * V8B;
     uint8_t *v_gen = smem + 2 * QB + SK * KB;  // generic pointer to the V stages
+    const uint8_t *v8_gen = v_gen + SV * VB;   // and to the E4M3 V stages
     uint32_t nb = 0;
     const uint32_t b_qfull = bar0 + 8u * nb++;   // Q blocks of the current item landed
     const uint32_t b_qempty = bar0 + 8u * nb++;  // last QK of an item done: Q buffers free
@@ -268,10 +283,11 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     const uint32_t b_vfull0 = bar0 + 8u * nb; nb += SV;
     const uint32_t b_vempty0 = bar0 + 8u * nb; nb += SV;
     const uint32_t b_sfull0 = bar0 + 8u * nb; nb += 2;  // per block: S tile written
-    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 2;  // per block: P tile written (128 * SPLIT arrivals)
+    const uint32_t b_pfull0 = bar0 + 8u * nb; nb += 2;  // per block: P tile written
     const uint32_t b_odone0 = bar0 + 8u * nb; nb += 2;  // per block: last PV of an item done
-    const uint32_t b_xchg0 = bar0 + 8u * nb; nb += 8;   // per (block, row quarter): partner exchange
     const uint32_t b_drain = bar0 + 8u * nb++;          // every MMA the issuer made has completed
+    const uint32_t b_v8full0 = bar0 + 8u * nb; nb += F8 ? SV : 0;   // E4M3 V stage landed (F8)
+    const uint32_t b_v8empty0 = bar0 + 8u * nb; nb += F8 ? SV : 0;  // E4M3 V stage widened (F8)
     auto b_item_full = [&](int i) { return b_item_full0 + 8u * i; };
     auto b_item_empty = [&](int i) { return b_item_empty0 + 8u * i; };
     auto b_kfull = [&](int s) { return b_kfull0 + 8u * s; };
@@ -281,11 +297,12 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     auto b_sfull = [&](int x) { return b_sfull0 + 8u * x; };
     auto b_pfull = [&](int x) { return b_pfull0 + 8u * x; };
     auto b_odone = [&](int x) { return b_odone0 + 8u * x; };
-    auto b_xchg = [&](int i) { return b_xchg0 + 8u * i; };
+    auto b_v8full = [&](int s) { return b_v8full0 + 8u * s; };
+    auto b_v8empty = [&](int s) { return b_v8empty0 + 8u * s; };
+    constexpr int kConvWarp = PfRoles<DQK>::kSoftmaxWarps + 3;  // (F8) the V widening warp
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ int4 item_ring[NI];  // (request, head A, head B, x); request -1: no more work
-    __shared__ float xbuf[2][2][2][kPfRows];  // [exchange parity][block][column half][row]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -294,22 +311,26 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
         mbar_init(b_qempty, 1);
         for (int i = 0; i < NI; ++i) {
             mbar_init(b_item_full(i), 1);
-            mbar_init(b_item_empty(i), 2 + 256 * SPLIT);  // MMA thread, V producer, softmax threads
+            // MMA thread, V producer, softmax threads (and the V widening warp)
+            mbar_init(b_item_empty(i), 2 + 256 + (F8 ? 1 : 0));
         }
         for (int s = 0; s < SK; ++s) {
             mbar_init(b_kfull(s), 1);
             mbar_init(b_kempty(s), 1);
         }
         for (int s = 0; s < SV; ++s) {
-            mbar_init(b_vfull(s), 1);
+            mbar_init(b_vfull(s), F8 ? 32 : 1);  // (F8: the widening warp's lanes)
             mbar_init(b_vempty(s), 1);
+            if (F8) {
+                mbar_init(b_v8full(s), 1);
+                mbar_init(b_v8empty(s), 32);
+            }
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(b_sfull(x), 1);
-            mbar_init(b_pfull(x), 128 * SPLIT);
+            mbar_init(b_pfull(x), 128);
             mbar_init(b_odone(x), 1);
         }
-        for (int i = 0; i < 8; ++i) mbar_init(b_xchg(i), 64);
         mbar_init(b_drain, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -354,7 +375,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     if (warp >= PfRoles<DQK>::kSoftmaxWarps) {
         // warps 8-11 (one warpgroup): the producers, the MMA issuer and an idle
         // warp give registers to the softmax warpgroups
-        if constexpr (SPLIT == 1) reg_dealloc<kRegsLow>();
+        reg_dealloc<kRegsLow>();
         if (warp == kTmaWarp || warp == kTmaVWarp) {
             // ------------------------------------------------------------ TMA producers
             // Warp 8 takes items from the global counter, publishes them, loads
@@ -378,6 +399,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             const int oob = static_cast<int>(p.max_num_pages);  // page coordinate past the pool: zero fill
             const int NS = is_k ? SK : SV;
             const int U = p.Hkv * p.pairs;
+            // the V producer's ring: the 16-bit V stages, or (F8) the E4M3
+            // stages the widening warp reads
+            auto v_full = [&](int st) { return F8 ? b_v8full(st) : b_vfull(st); };
+            auto v_empty = [&](int st) { return F8 ? b_v8empty(st) : b_vempty(st); };
             bool ok = true;
             int t_base = 0;  // tiles of earlier items (global tile counter)
             int t_next = 0;  // (lane 0) tiles [0, t_next) have their copies issued
@@ -441,10 +466,11 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     } else {
                         mbar_expect_tx(b_qfull, it.hB >= 0 ? 2 * QB : QB);
                         for (int c = 0; c < QA; ++c)
-                            tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hA, it.row_base);
+                            tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * (128 / ES), it.hA,
+                                        it.row_base);
                         if (it.hB >= 0)
                             for (int c = 0; c < QA; ++c)
-                                tma_load_3d(q_s + QB + c * (kPfRows * 128), &tm_q, b_qfull, c * 64, it.hB,
+                                tma_load_3d(q_s + QB + c * (kPfRows * 128), &tm_q, b_qfull, c * (128 / ES), it.hB,
                                             it.row_base);
                         q_loads = k + 1;
                     }
@@ -475,12 +501,12 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
                     if (lane == 0) {
                         const int st = t % NS, us = t / NS;
-                        if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : b_vempty(st), (us - 1) & 1, abort_flag, wlim)) {
+                        if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : v_empty(st), (us - 1) & 1, abort_flag, wlim)) {
                             give_up();
                             ok = false;
                         } else {
-                            const uint32_t full = is_k ? b_kfull(st) : b_vfull(st);
-                            mbar_expect_tx(full, is_k ? KB : VB);
+                            const uint32_t full = is_k ? b_kfull(st) : v_full(st);
+                            mbar_expect_tx(full, is_k ? KB : (F8 ? V8B : VB));
                             const int j0 = j * BN;
     #pragma unroll
                             for (int i = 0; i < 16; ++i) {
@@ -492,8 +518,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                                 const int cb = LAYOUT == PKV_HND ? it.kvh : slot0;
                                 if (is_k) {
                                     for (int c = 0; c < QA; ++c)
-                                        tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full, c * 64, ca,
-                                                    cb, pages[i]);
+                                        tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full,
+                                                    c * (128 / ES), ca, cb, pages[i]);
+                                } else if (F8) {  // one 128-byte atom: a whole E4M3 row
+                                    tma_load_4d(v8_s + st * V8B + r0 * 128, &tm_v, full, 0, ca, cb, pages[i]);
                                 } else {
                                     for (int c = 0; c < kPfDV / 64; ++c)
                                         tma_load_4d(v_s + st * VB + c * (BN * 128) + r0 * 128, &tm_v, full, c * 64, ca,
@@ -515,7 +543,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             // stage completed before it was reused) and the last Q blocks.
             if (lane == 0) {
                 for (int t = t_next > NS ? t_next - NS : 0; t < t_next; ++t)
-                    if (!mbar_wait_drain(is_k ? b_kfull(t % NS) : b_vfull(t % NS), (t / NS) & 1))
+                    if (!mbar_wait_drain(is_k ? b_kfull(t % NS) : v_full(t % NS), (t / NS) & 1))
                         set_err(p.err, PKV_DEV_ERR_TIMEOUT);
                 if (is_k && q_loads > 0 && !mbar_wait_drain(b_qfull, (q_loads - 1) & 1))
                     set_err(p.err, PKV_DEV_ERR_TIMEOUT);
@@ -529,8 +557,9 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             // reading P_X from it, and a completed S_X(t+1) implies that PV_X(t)
             // is complete (the softmax relies on both).
             if (lane == 0) {
-                constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, IsBf16<T>::value, false);
-                constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<T>::value, true);
+                // (F8: kind::f8f6f4 with E4M3 A and B, whose format code is 0)
+                constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, !F8 && IsBf16<T>::value, false);
+                constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<TP>::value, true);
                 const uint64_t qdesc0 = umma_sdesc_sw128(q_s, 16, 1024);
                 const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
                 const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
@@ -546,19 +575,20 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     const uint64_t kd = kdesc0 + (((t % SK) * KB) >> 4);
                     const uint64_t qd = qdesc0 + ((x * QB) >> 4);
     #pragma unroll
-                    for (int kk = 0; kk < DQK / 16; ++kk)
-                        umma_ss(tmem + x * S_STRIDE, qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4),
-                                kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < KSTEPS; ++kk) {  // 32-byte steps, four per 128-byte atom
+                        const uint64_t qa = qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4);
+                        const uint64_t ka = kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+                        if constexpr (F8)
+                            umma_ss_f8(tmem + x * S_STRIDE, qa, ka, idesc_qk, kk > 0 ? 1u : 0u);
+                        else
+                            umma_ss(tmem + x * S_STRIDE, qa, ka, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                     umma_commit(b_sfull(x));
                 };
-                // P column of keys 16kk .. 16kk+15: each softmax thread owns HC
-                // columns, and writes chunk i (32 keys, or a final 16) as 16-bit
-                // pairs at the chunk's first column
-                constexpr int HC = BN / SPLIT;
-                auto pcol = [](int kk) {
-                    const int k0 = 16 * kk, c = k0 % HC;
-                    return (k0 / HC) * HC + 32 * (c / 32) + (c % 32) / 2;
-                };
+                // P column of keys 16kk .. 16kk+15: the softmax writes chunk c
+                // (keys 32c .. 32c + 31) as 16-bit pairs at the chunk's first
+                // column
+                auto pcol = [](int kk) { return 32 * (kk / 2) + 8 * (kk % 2); };
                 auto pv = [&](int x, int t, bool first) {  // O_X (+)= P_X V(t)
                     const uint64_t vd = vdesc0 + (((t % SV) * VB) >> 4);
     #pragma unroll
@@ -629,56 +659,105 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 if (!mbar_wait_drain(b_drain, 0)) set_err(p.err, PKV_DEV_ERR_TIMEOUT);
             }
             __syncwarp();
+        } else if (F8 && warp == kConvWarp) {
+            // ------------------------------------------------------------ V widening (F8)
+            // Every E4M3 V stage is widened, exactly, into the matching fp16
+            // stage in the layout the TMA gives a 16-bit tile (two 64-dim
+            // atoms, 128-byte swizzle), once PV has released that stage; then
+            // each lane makes its writes visible to the tensor core and arrives.
+            bool ok = true;
+            int t_base = 0;
+            for (int k = 0; ok; ++k) {
+                int4 itm = make_int4(-1, 0, 0, 0);
+                if (lane == 0) itm = take_item(k, ok);
+                itm.x = __shfl_sync(0xffffffffu, itm.x, 0);
+                itm.y = __shfl_sync(0xffffffffu, itm.y, 0);
+                itm.z = __shfl_sync(0xffffffffu, itm.z, 0);
+                itm.w = __shfl_sync(0xffffffffu, itm.w, 0);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok || itm.x < 0) break;
+                PfItem it;
+                pf_item(p, itm, BN, it);
+                for (int j = 0; j < it.n_tiles; ++j) {
+                    const int t = t_base + j, st = t % SV, us = t / SV;
+                    bool w = mbar_wait(b_v8full(st), us & 1, abort_flag, wlim);
+                    if (us > 0) w = w && mbar_wait(b_vempty(st), (us - 1) & 1, abort_flag, wlim);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                    const uint8_t *__restrict__ src = v8_gen + st * V8B;
+                    uint8_t *__restrict__ dst = v_gen + st * VB;
+                    // 16-byte chunk q: row q / 8, dims 16c .. 16c + 15 (c = q % 8);
+                    // four chunks per lane loaded before any is widened and stored
+                    constexpr int kBatch = 4;
+#pragma unroll 1
+                    for (int q0 = lane; q0 < BN * 8; q0 += 32 * kBatch) {
+                        uint4 raw[kBatch];
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int q = q0 + 32 * u, row = q >> 3, c = q & 7;
+                            raw[u] = *reinterpret_cast<const uint4 *>(src + row * 128 + ((c ^ (row & 7)) << 4));
+                        }
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int q = q0 + 32 * u, row = q >> 3, c = q & 7;
+                            const uint32_t x[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+                            uint32_t h[8];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                h[2 * i] = widen_e4m3x2<__half>(x[i] & 0xffffu);
+                                h[2 * i + 1] = widen_e4m3x2<__half>(x[i] >> 16);
+                            }
+                            // dims 16c .. 16c + 7 and 16c + 8 .. 16c + 15: 16-byte
+                            // chunks 2(c % 4) and 2(c % 4) + 1 of 64-dim atom c / 4
+                            uint8_t *d0 = dst + (c >> 2) * (BN * 128) + row * 128;
+                            const int ch = 2 * (c & 3);
+                            *reinterpret_cast<uint4 *>(d0 + ((ch ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<uint4 *>(d0 + (((ch + 1) ^ (row & 7)) << 4)) =
+                                make_uint4(h[4], h[5], h[6], h[7]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(b_vfull(st));
+                    mbar_arrive(b_v8empty(st));
+                }
+                t_base += it.n_tiles;
+            }
+            if (!ok) give_up();
+            __syncwarp();
         }
     } else {
-        if constexpr (SPLIT == 1) reg_alloc<kRegsHigh>();
         // ------------------------------------------------------------ softmax warps
-        // Warp w (0..15): block X = (w / 4) % 2, column half hh = w / 8, TMEM
-        // lane quarter w % 4, so each query row of a block is served by two
-        // threads (warps w and w + 8), each owning HC = BN / 2 of the tile's
-        // columns.  Per tile a thread takes the max over its columns, trades
-        // it with its partner (a 64-thread mbarrier per row quarter), and
-        // both continue with the same running max m: it only rises when the
-        // tile max exceeds it by more than 8 (a factor 2^8), and then the
-        // row sum and O (each thread its half of O's columns) are rescaled.
-        // P, 16-bit pairs, overwrites the first half of each consumed 32-column
-        // chunk of S.  The partners' row sums are added at the end of the item.
-        constexpr int HC = BN / SPLIT;  // columns per thread
-        constexpr int NCH = HC / 32;    // 32-column chunks per thread
-        static_assert(HC % 32 == 0, "columns per thread");
-        const int X = (warp >> 2) & 1;
-        const int hh = warp >> 3;
-        const int qd = warp & 3;
+        // One thread per query row, one warpgroup per block: warp w serves
+        // block X = w / 4, TMEM lane quarter w % 4.  The row's scores are held
+        // in registers (the softmax warpgroups' larger register budget); per
+        // tile the thread takes their max, keeps a running max m in base 2
+        // that rises only when a tile's max exceeds it by more than 8 (a
+        // factor 2^8; P then stays below 2^8; the row sum and O are rescaled
+        // then), and writes P, 16-bit pairs, over the first half of each
+        // consumed 32-column chunk of S: the A operand of the block's PV MMA.
+        reg_alloc<kRegsHigh>();
+        constexpr int NCH = BN / 32;  // 32-column chunks of a row
+        static_assert(BN % 32 == 0, "score tile in 32-column chunks");
+        const int X = warp >> 2, qd = warp & 3;
         const int r = 32 * qd + lane;  // query row inside the tile
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-        const uint32_t s_addr = t_lane + X * S_STRIDE + hh * HC;
-        const uint32_t o_addr = t_lane + O_COL + X * kPfDV + hh * (kPfDV / SPLIT);
-        const uint32_t b_pair = b_xchg(X * 4 + qd);
+        const uint32_t s_addr = t_lane + X * S_STRIDE;
+        const uint32_t o_addr = t_lane + O_COL + X * kPfDV;
         const float sc = p.scale_log2 * (p.q_scale ? __ldg(p.q_scale) : 1.f) * (p.k_scale ? __ldg(p.k_scale) : 1.f);
         const bool pos_scale = sc > 0.f;  // max on raw scores, one FFMA scales and shifts
         const float k_mul = pos_scale ? sc : 1.f;
+        const float2 kk2 = make_float2(k_mul, k_mul);
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, wlim));
         };
-        int ex = 0;  // exchanges with the partner thread so far (buffer and phase)
-        auto exchange = [&](float v, float &other) -> bool {
-            xbuf[ex & 1][X][hh][r] = v;
-            mbar_arrive(b_pair);
-            // the partner arrives within a few hundred cycles: spin, no sleep
-            const bool done = __all_sync(0xffffffffu, mbar_wait_spin(b_pair, ex & 1, abort_flag, wlim));
-            other = *reinterpret_cast<volatile float *>(&xbuf[ex & 1][X][hh ^ 1][r]);
-            ++ex;
-            return done;
-        };
-        // scores of chunk i of this thread's columns at tile offset j0:
-        // scaled if the scale is not positive, masked past the row's last key
+        // scores of chunk i of the tile at key offset j0: scaled if the scale
+        // is not positive, masked past the row's last key
         auto scale_mask = [&](int i, int j0, bool warp_full, int lim, uint32_t(&ra)[32]) {
             if (!pos_scale) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) ra[c] = __float_as_uint(__uint_as_float(ra[c]) * sc);
             }
             if (!warp_full) {
-                const int lr = lim - (j0 + hh * HC + 32 * i);  // last visible column of the chunk
+                const int lr = lim - (j0 + 32 * i);  // last visible column of the chunk
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
                     if (c > lr) ra[c] = __float_as_uint(-INFINITY);
@@ -696,18 +775,20 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             }
             return fmax3(fmaxf(m3[0], m3[1]), m3[2], m3[3]);
         };
-        auto load_chunk = [&](int i, int j0, bool warp_full, int lim, uint32_t(&ra)[32]) {
-            tmem_ld32(s_addr + 32 * i, ra);
-            tmem_wait_ld_regs(ra);
-            if (!pos_scale) {
+        // P of a 32-key chunk, 2^(s k - base): 16-bit pairs into pw, sums
+        // into la / lb
+        auto exp_chunk = [&](const uint32_t(&ra)[32], float base, float2 &la, float2 &lb, uint32_t(&pw)[16]) {
+            const float2 nb2 = make_float2(-base, -base);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) ra[c] = __float_as_uint(__uint_as_float(ra[c]) * sc);
-            }
-            if (!warp_full) {
-                const int lr = lim - (j0 + hh * HC + 32 * i);  // last visible column of the chunk
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c > lr) ra[c] = __float_as_uint(-INFINITY);
+            for (int e = 0; e < 16; ++e) {
+                const float2 x =
+                    __ffma2_rn(make_float2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), kk2, nb2);
+                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                if (e & 1)
+                    lb = __fadd2_rn(lb, make_float2(p0, p1));
+                else
+                    la = __fadd2_rn(la, make_float2(p0, p1));
+                pw[e] = pack2<TP>(p0, p1);  // P column: keys 2e, 2e+1 of the chunk
             }
         };
         bool ok = true;
@@ -736,70 +817,31 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 if (!wait_warp(b_sfull(X), tx & 1)) { ok = false; break; }
                 tc_fence_after();
                 const bool warp_full = __all_sync(0xffffffffu, j0 + BN - 1 <= lim);
-                float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+                uint32_t rs[NCH][32];
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) tmem_ld32(s_addr + 32 * i, rs[i]);
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) tmem_wait_ld_regs(rs[i]);  // (the first waits for all)
+                float mh = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) {
+                    scale_mask(i, j0, warp_full, lim, rs[i]);
+                    mh = fmaxf(mh, chunk_max(rs[i]));
+                }
+                const float mt = pos_scale ? mh * sc : mh;
                 float alpha = 1.f;
-                // P of chunk i from its scores, relative to the running max
-                auto exp_chunk = [&](int i, const uint32_t(&ra)[32], float2 kk2, float2 nb2) {
+                if (mt > m_used + 8.f) {  // (first tile: from -inf)
+                    alpha = fast_exp2(m_used - mt);
+                    m_used = mt;
+                    l *= alpha;
+                }
+                float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+                const float base = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) {
                     uint32_t pw[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 x =
-                            __ffma2_rn(make_float2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), kk2, nb2);
-                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                        if (e & 1)
-                            lb = __fadd2_rn(lb, make_float2(p0, p1));
-                        else
-                            la = __fadd2_rn(la, make_float2(p0, p1));
-                        pw[e] = pack2<T>(p0, p1);  // P column: keys 2e, 2e+1 of the chunk
-                    }
+                    exp_chunk(rs[i], base, la, lb, pw);
                     tmem_st16(s_addr + 32 * i, pw);
-                };
-                auto raise_max = [&](float mt) {  // (first tile: from -inf)
-                    if (mt > m_used + 8.f) {
-                        alpha = fast_exp2(m_used - mt);
-                        m_used = mt;
-                        l *= alpha;
-                    }
-                };
-                if constexpr (SPLIT == 1) {
-                    // one thread per row: the whole row of scores in registers,
-                    // one pass over TMEM, no partner
-                    uint32_t rs[NCH][32];
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) tmem_ld32(s_addr + 32 * i, rs[i]);
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) tmem_wait_ld_regs(rs[i]);  // (the first waits for all)
-                    float mh = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) {
-                        scale_mask(i, j0, warp_full, lim, rs[i]);
-                        mh = fmaxf(mh, chunk_max(rs[i]));
-                    }
-                    raise_max(pos_scale ? mh * sc : mh);
-                    const float base = m_used == -INFINITY ? 0.f : m_used;
-                    const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) exp_chunk(i, rs[i], kk2, nb2);
-                } else {
-                    uint32_t ra[32];
-                    float mh = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) {
-                        load_chunk(i, j0, warp_full, lim, ra);
-                        mh = fmaxf(mh, chunk_max(ra));
-                    }
-                    if (pos_scale) mh *= sc;
-                    float mo = -INFINITY;
-                    if (SPLIT == 2 && !exchange(mh, mo)) { ok = false; break; }
-                    const float mt = fmaxf(mh, mo);  // the tile's row max (scaled)
-                    raise_max(mt);
-                    const float base = m_used == -INFINITY ? 0.f : m_used;
-                    const float2 kk2 = make_float2(k_mul, k_mul), nb2 = make_float2(-base, -base);
-#pragma unroll
-                    for (int i = 0; i < NCH; ++i) {
-                        load_chunk(i, j0, warp_full, lim, ra);
-                        exp_chunk(i, ra, kk2, nb2);
-                    }
                 }
                 l += (la.x + la.y) + (lb.x + lb.y);
                 // rows of V past the sequence end may hold anything (even NaN):
@@ -810,19 +852,19 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     if (!wait_warp(b_vfull(sv), uv & 1)) { ok = false; break; }
                     const int zs = max(it.kvb - j0, 0);
                     uint8_t *vbase = v_gen + sv * VB;
-                    for (int q = hh * 128 + r; q < (BN - zs) * 16; q += 128 * SPLIT) {
+                    for (int q = r; q < (BN - zs) * 16; q += 128) {
                         const int row = zs + (q >> 4), chunk = q & 15;
                         *reinterpret_cast<uint4 *>(vbase + (chunk >> 3) * (BN * 128) + row * 128 + (chunk & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                 }
-                // O_X *= alpha (this thread's half of the columns) when the
-                // running max moved; PV_X(t-1) is complete (S_X(t) is), and at
-                // the item's first tile O is about to be overwritten anyway
+                // O_X *= alpha when the running max moved; PV_X(t-1) is
+                // complete (S_X(t) is), and at the item's first tile O is
+                // about to be overwritten anyway
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < kPfDV / 32 / SPLIT; ++c) {
+                    for (int c = 0; c < kPfDV / 32; ++c) {
                         uint32_t ro[32];
                         tmem_ld32(o_addr + c * 32, ro);
                         tmem_wait_ld_regs(ro);
@@ -836,22 +878,18 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 mbar_arrive(b_pfull(X));
             }
             if (!ok) break;
-            // epilogue: after the block's last PV of the item, add the
-            // partners' row sums, normalise this thread's half of O and write
-            // it; the column-half-0 thread writes the LSE
+            // epilogue: after the block's last PV of the item, normalise O and
+            // write it with the LSE
             const bool have = n > 0;
             if (have && !wait_warp(b_odone(X), nx_items & 1)) { ok = false; break; }
-            float lo = 0.f;
-            if (SPLIT == 2 && !exchange(l, lo)) { ok = false; break; }
-            const float lt = l + lo;
             tc_fence_after();
             const int qi = it.i0 + r;
             const int64_t grow = static_cast<int64_t>(it.orow_base) + r;
             const bool valid = qi < it.qb && grow >= 0 && grow < p.total_q;
-            const float inv = lt > 0.f ? (p.v_scale ? __ldg(p.v_scale) : 1.f) / lt : 0.f;
-            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV + hh * (kPfDV / SPLIT);
+            const float inv = l > 0.f ? (p.v_scale ? __ldg(p.v_scale) : 1.f) / l : 0.f;
+            T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV;
 #pragma unroll
-            for (int c = 0; c < kPfDV / 32 / SPLIT; ++c) {
+            for (int c = 0; c < kPfDV / 32; ++c) {
                 uint32_t ro[32];
                 if (have) {
                     tmem_ld32(o_addr + c * 32, ro);
@@ -870,7 +908,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     }
                 }
             }
-            if (valid && hh == 0) p.lse[grow * p.Hqo + h] = lt > 0.f ? (m_used + fast_log2(lt)) * kLn2 : -INFINITY;
+            if (valid) p.lse[grow * p.Hqo + h] = l > 0.f ? (m_used + fast_log2(l)) * kLn2 : -INFINITY;
             tc_fence_before();  // O read before the next item's first PV_X overwrites it
             t_base += n;
             tx_base += n;
@@ -891,21 +929,22 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     }
 }
 
-template <int DQK>
+template <int DQK, bool F8>
 static size_t prefill_smem_bytes() {
-    constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
-    return 1024 + 2 * kPfRows * DQK * 2 + SK * BN * DQK * 2 + SV * BN * kPfDV * 2 + 8 * (21 + 2 * SK + 2 * SV);
+    constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = F8 ? 3 : PfCfg<DQK>::SV, ES = F8 ? 1 : 2;
+    return 1024 + 2 * kPfRows * DQK * ES + SK * BN * DQK * ES + SV * BN * kPfDV * 2 + (F8 ? SV * BN * kPfDV : 0) +
+           8 * (13 + 2 * SK + 2 * SV + (F8 ? 2 * SV : 0));
 }
 
-template <typename T, int DQK, int LAYOUT>
+template <typename T, int DQK, int LAYOUT, bool F8 = false>
 static int launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const PrefillParams &p, dim3 grid, cudaStream_t st) {
-    const size_t smem = prefill_smem_bytes<DQK>();
-    auto kern = prefill_tc_kernel<T, DQK, LAYOUT>;
+    const size_t smem = prefill_smem_bytes<DQK, F8>();
+    auto kern = prefill_tc_kernel<T, DQK, LAYOUT, F8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PKV_ERR_CUDA;
-    if constexpr (PfCfg<DQK>::SPLIT == 1) {
+    {
         // the register split draws on the registers the CTA is launched with:
         // refuse to launch if the compiled kernel was given fewer (the
         // softmax warps' setmaxnreg.inc would wait for registers forever)
@@ -1010,6 +1049,7 @@ __global__ void __launch_bounds__(256) widen_rows_kernel(const uint8_t *__restri
 // What an E4M3 call adds to the 16-bit path.
 struct PrefillFp8 {
     const float *q_scale = nullptr, *k_scale = nullptr, *v_scale = nullptr;
+    bool direct = false;             // E4M3 query and caches read as they are (kind::f8f6f4 QK)
     const uint8_t *q_src = nullptr;  // E4M3 query rows, widened into the call's `q` first
     bool kv8 = false;                // widen the paged caches after the plan kernel
     WidenKvParams widen{};           // (cu_kv and err filled in by prefill_impl)
@@ -1018,7 +1058,11 @@ struct PrefillFp8 {
 
 template <typename T>
 static int dispatch_prefill(int d_qk, int layout, const CUtensorMap &tq, const CUtensorMap &tk,
-                            const CUtensorMap &tv, const PrefillParams &p, dim3 grid, cudaStream_t st) {
+                            const CUtensorMap &tv, const PrefillParams &p, dim3 grid, cudaStream_t st,
+                            bool f8_direct) {
+    if (f8_direct)  // (d_qk 128)
+        return layout == PKV_HND ? launch_prefill<T, 128, PKV_HND, true>(tq, tk, tv, p, grid, st)
+                                 : launch_prefill<T, 128, PKV_NHD, true>(tq, tk, tv, p, grid, st);
     if (d_qk == 128)
         return layout == PKV_HND ? launch_prefill<T, 128, PKV_HND>(tq, tk, tv, p, grid, st)
                                  : launch_prefill<T, 128, PKV_NHD>(tq, tk, tv, p, grid, st);
@@ -1026,31 +1070,32 @@ static int dispatch_prefill(int d_qk, int layout, const CUtensorMap &tq, const C
                              : launch_prefill<T, 192, PKV_NHD>(tq, tk, tv, p, grid, st);
 }
 
-// K or V cache as a 4-D tensor map whose box is one 64-element d-atom of
-// `rows` consecutive slots of one (page, kv head).
+// K or V cache as a 4-D tensor map whose box is one 128-byte d-atom (64
+// 16-bit or 128 one-byte elements, es bytes each) of `rows` consecutive
+// slots of one (page, kv head).
 static bool cache_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int layout, int d,
                        int page_size, int num_kv_heads, int64_t page_stride, int64_t num_pages,
-                       int rows) {
+                       int rows, int es = 2) {
     uint64_t dims[4], strides[3];
     uint32_t box[4];
     dims[0] = d;
-    box[0] = 64;
-    strides[0] = static_cast<uint64_t>(d) * 2;
+    box[0] = 128 / es;
+    strides[0] = static_cast<uint64_t>(d) * es;
     if (layout == PKV_HND) {
         dims[1] = page_size;
         dims[2] = num_kv_heads;
-        strides[1] = static_cast<uint64_t>(page_size) * d * 2;
+        strides[1] = static_cast<uint64_t>(page_size) * d * es;
         box[1] = rows;
         box[2] = 1;
     } else {
         dims[1] = num_kv_heads;
         dims[2] = page_size;
-        strides[1] = static_cast<uint64_t>(num_kv_heads) * d * 2;
+        strides[1] = static_cast<uint64_t>(num_kv_heads) * d * es;
         box[1] = 1;
         box[2] = rows;
     }
     dims[3] = static_cast<uint64_t>(num_pages);
-    strides[2] = static_cast<uint64_t>(page_stride) * 2;
+    strides[2] = static_cast<uint64_t>(page_stride) * es;
     box[3] = 1;
     return encode_tmap(m, base, dt, 4, dims, strides, box);
 }
@@ -1136,20 +1181,30 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
         (reinterpret_cast<uintptr_t>(workspace) & 255))
         return PKV_ERR_WORKSPACE;
 
-    const CUtensorMapDataType tdt =
-        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // (the E4M3 query and caches read as they are: one-byte elements)
+    const bool f8d = f8 && f8->direct;
+    const int es = f8d ? 1 : 2;
+    const CUtensorMapDataType tdt = f8d ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                        : (dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     const int bn = pf_bn(d_qk);
     const int rows = pf_box_rows(page_size, bn);
     CUtensorMap tq, tk, tv;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),
                             static_cast<uint64_t>(total_q)};
-        uint64_t strides[2] = {static_cast<uint64_t>(d_qk) * 2,
-                               static_cast<uint64_t>(num_qo_heads) * d_qk * 2};
-        uint32_t box[3] = {64, 1, static_cast<uint32_t>(kPfRows)};
+        uint64_t strides[2] = {static_cast<uint64_t>(d_qk) * es,
+                               static_cast<uint64_t>(num_qo_heads) * d_qk * es};
+        uint32_t box[3] = {static_cast<uint32_t>(128 / es), 1, static_cast<uint32_t>(kPfRows)};
         if (!encode_tmap(&tq, q, tdt, 3, dims, strides, box)) return PKV_ERR_CUDA;
     }
-    if (contiguous) {
+    if (f8d) {
+        if (contiguous || !cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride,
+                                      max_num_pages, rows, 1) ||
+            !cache_tmap(&tv, v_cache, tdt, layout, d_vo, page_size, num_kv_heads, v_page_stride, max_num_pages,
+                        rows, 1))
+            return PKV_ERR_CUDA;
+    } else if (contiguous) {
         if (!contiguous_tmap(&tk, k_cache, tdt, d_qk, num_kv_heads, k_page_stride, max_num_pages, bn) ||
             !contiguous_tmap(&tv, v_cache, tdt, d_vo, num_kv_heads, v_page_stride, max_num_pages, bn))
             return PKV_ERR_CUDA;
@@ -1240,8 +1295,8 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
         // persistent: one CTA per SM (the shared-memory footprint allows one)
         const int64_t ctas = items < num_sms() ? items : num_sms();
         dim3 grid(static_cast<unsigned>(ctas));
-        int rc = dtype == PKV_BF16 ? dispatch_prefill<__nv_bfloat16>(d_qk, layout, tq, tk, tv, p, grid, st)
-                                   : dispatch_prefill<__half>(d_qk, layout, tq, tk, tv, p, grid, st);
+        int rc = dtype == PKV_BF16 ? dispatch_prefill<__nv_bfloat16>(d_qk, layout, tq, tk, tv, p, grid, st, f8d)
+                                   : dispatch_prefill<__half>(d_qk, layout, tq, tk, tv, p, grid, st, f8d);
         if (rc != PKV_OK) return rc;
         ++launches;
     }
@@ -1291,9 +1346,17 @@ extern "C" int paged_prefill_ex(const void *q, int64_t total_q, const void *k_ca
 // Workspace of paged_prefill_fp8: the 16-bit path's, then the widened query
 // rows (E4M3 query) and the widened, packed K and V (E4M3 caches; room for
 // batch_size * max_sequence_kv keys, the most the lengths allow).
+// An E4M3 query with E4M3 caches at d_qk = d_vo = 128 is read as it is (the
+// kind::f8f6f4 kernel): nothing is widened into the workspace.
+static bool prefill_fp8_direct(bool q8, bool kv8, int d_qk, int d_vo) { return q8 && kv8 && d_qk == 128 && d_vo == 128; }
+
 static size_t prefill_fp8_ws_bytes(int B, int Hqo, int Hkv, int max_kv, int64_t total_q, int d_qk, int d_vo,
                                    bool q8, bool kv8, size_t *q_off, size_t *k_off, size_t *v_off) {
     size_t off = prefill_ws_bytes(B);
+    if (prefill_fp8_direct(q8, kv8, d_qk, d_vo)) {
+        *q_off = *k_off = *v_off = off;
+        return off;
+    }
     *q_off = off;
     if (q8) off += round_up(static_cast<size_t>(total_q) * Hqo * d_qk * 2, 256);
     *k_off = off;
@@ -1360,6 +1423,14 @@ extern "C" int paged_prefill_fp8(const void *q, int64_t total_q, const void *k_c
     f8.q_scale = q_scale;
     f8.k_scale = k_scale;
     f8.v_scale = v_scale;
+    if (prefill_fp8_direct(q8, kv8, d_qk, d_vo)) {
+        f8.direct = true;
+        return prefill_impl(q, total_q, k_cache, v_cache, k_page_stride, v_page_stride, max_num_pages, scale,
+                            workspace, workspace_bytes, max_token_per_sequence, max_sequence_kv, actual_seq_lens_q,
+                            actual_seq_lens_kv, block_tables, block_table_stride, batch_size, causal, num_qo_heads,
+                            num_kv_heads, d_qk, d_vo, page_size, layout, out_dtype, out, lse, err_word, stream,
+                            nullptr, nullptr, nullptr, nullptr, &f8);
+    }
     const void *qq = q;
     if (q8) {
         f8.q_src = static_cast<const uint8_t *>(q);

@@ -172,6 +172,16 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T for kind::f8f6f4 (8-bit floats in, fp32
+// accumulate; K = 32 per instruction).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // D[tmem] (+)= A[tmem] * B[smem]^T for kind::f16: A is M x K with row m in
 // TMEM lane m and K packed two 16-bit elements per 32-bit column.
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -191,6 +201,8 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B
 // of the same 16-bit type, A K-major, B K-major or MN-major, shape M x N.
+// With `bf16` false the A/B format code is 0, which kind::f8f6f4 reads as
+// E4M3: the same descriptor serves E4M3 x E4M3 MMAs.
 __host__ __device__ constexpr uint32_t umma_idesc(int M, int N, bool bf16, bool b_mn_major) {
     return (1u << 4)                                   // D: f32
            | ((bf16 ? 1u : 0u) << 7)                   // A: f16 / bf16

@@ -1,6 +1,6 @@
 """Run one operation of the library on its named synthetic workload.
 
-    python -m paged_kv_cache_316_gb300.run_case --op prefill [--d-qk 128] [--iters 3]
+    python -m paged_kv_cache_316_gb300.run_case --op prefill [--d-qk 128] [--iters 3] [--kv-dtype e4m3]
     python -m paged_kv_cache_316_gb300.run_case --op decode_llama | decode_long | decode_varlen | append
                                                 [--batch N] [--iters 3] [--kv-dtype e4m3]
 
@@ -27,22 +27,28 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--kv-dtype", choices=["same", "e4m3"], default="same",
-                    help="decode: the cache in the query's dtype, or E4M3 (FP8)")
+                    help="the cache in the query's dtype, or E4M3 (FP8; prefill: query and caches)")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     from . import build
     build.build()
 
     if a.op == "prefill":
-        c = wl.ragged_prefill(d_qk=a.d_qk, device=dev)
+        e4 = a.kv_dtype == "e4m3"  # E4M3 query and caches, unit device scales
+        kw = dict(q_dtype=wl.E4M3, kv_dtype=wl.E4M3) if e4 else {}
+        c = wl.ragged_prefill(d_qk=a.d_qk, device=dev, **kw)
         B = c.seq_lens_q.shape[0]
-        ws = torch.zeros(pk.paged_prefill_workspace_size(B, c.num_qo_heads, c.max_q, c.max_kv),
-                         dtype=torch.uint8, device=dev)
+        nbytes = (pk.paged_prefill_fp8_workspace_size(B, c.num_qo_heads, c.num_kv_heads, c.max_q, c.max_kv,
+                                                      c.q.shape[0], c.d_qk, c.d_vo, c.q.dtype, c.pool.k.dtype)
+                  if e4 else pk.paged_prefill_workspace_size(B, c.num_qo_heads, c.max_q, c.max_kv))
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         lq, lkv, bt = c.seq_lens_q.to(dev), c.seq_lens_kv.to(dev), c.block_tables.to(dev)
+        scales = dict(q_scale=torch.ones(1, device=dev), k_scale=torch.ones(1, device=dev),
+                      v_scale=torch.ones(1, device=dev)) if e4 else {}
 
         def run():
             pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv,
-                             bt, causal=True, kv_layout="HND")
+                             bt, causal=True, kv_layout="HND", **scales)
     elif a.op in ("decode_llama", "decode_long", "decode_varlen"):
         kvd = dict(kv_dtype=wl.E4M3) if a.kv_dtype == "e4m3" else {}
         if a.op == "decode_varlen":

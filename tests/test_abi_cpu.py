@@ -162,17 +162,20 @@ def test_prefill_fp8_rejects_bad_arguments(lib):
     assert call(qd=F16) == 2           # a 16-bit query must match the output type
     assert call(bt=None) == 2          # E4M3 caches are paged
     assert call(ks=8 * 32 * 128 + 8) == 2  # E4M3 page strides: multiples of 16 bytes
-    assert call(ws_bytes=4096) == 4    # too small for the widened inputs
+    assert call(ws_bytes=4096, kvd=BF16) == 4  # too small for the widened query rows
+    assert call(ws_bytes=4096, dqk=192, ks=8 * 32 * 192) == 4  # d_qk 192: everything widened
     assert call(dqk=64) == 3
     assert call(total_q=0) == 0
     size = lib.paged_prefill_fp8_workspace_size
     q8 = size(2, 32, 8, 100, 200, 150, 128, 128, E4M3, BF16)
     kv8 = size(2, 32, 8, 100, 200, 150, 128, 128, BF16, E4M3)
     both = size(2, 32, 8, 100, 200, 150, 128, 128, E4M3, E4M3)
+    both192 = size(2, 32, 8, 100, 200, 150, 192, 128, E4M3, E4M3)
     base = lib.paged_prefill_workspace_size(2, 32, 100, 200)
     assert q8 - base >= 150 * 32 * 128 * 2                   # the widened query rows
     assert kv8 - base >= 2 * 200 * 8 * (128 + 128) * 2       # widened K and V
-    assert both >= q8 + kv8 - base
+    assert both == base  # E4M3 query and caches at d_qk 128 are read as they are
+    assert both192 - base >= 150 * 32 * 192 * 2 + 2 * 200 * 8 * (192 + 128) * 2
 
 
 def test_prefill_rejects_bad_arguments(lib):

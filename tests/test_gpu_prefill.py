@@ -187,6 +187,10 @@ FP8_CASES = [
     ([64, 200], [500, 200], 64, 16, 2, 192, False, wl.BF16, wl.NHD, True, True, 14),
     ([77, 300], [500, 300], 16, 16, 4, 192, True, wl.F16, wl.HND, True, True, 15),
     ([200], [333], 8, 6, 2, 128, True, wl.BF16, wl.HND, False, True, 16),
+    # E4M3 query and caches at d_qk 128 take the kind::f8f6f4 kernel
+    ([257, 33], [600, 33], 16, 16, 4, 128, True, wl.F16, wl.NHD, True, True, 20),
+    ([129], [129], 64, 8, 2, 128, False, wl.BF16, wl.HND, True, True, 21),
+    ([1, 700, 64], [1, 1300, 64], 256, 6, 2, 128, True, wl.BF16, wl.NHD, True, True, 22),   # odd group
 ]
 
 
@@ -201,9 +205,10 @@ def test_fp8_small_shapes(case):
 
 
 def test_fp8_with_unit_scales_equals_16bit_on_widened_values():
-    # every E4M3 value is a bf16 value: the E4M3 prefill with unit scales
-    # gives bit for bit the 16-bit prefill over the same values
-    c8 = wl.prefill_case([130, 7, 300], [400, 7, 300], 32, 32, 8, 128, 128, wl.HND, wl.BF16, seed=17,
+    # every E4M3 value is a bf16 value: where the E4M3 inputs are widened to
+    # 16 bits first (d_qk 192), the E4M3 prefill with unit scales gives bit
+    # for bit the 16-bit prefill over the same values
+    c8 = wl.prefill_case([130, 7, 300], [400, 7, 300], 32, 32, 8, 192, 128, wl.HND, wl.BF16, seed=17,
                          slack=0.2, q_dtype=wl.E4M3, kv_dtype=wl.E4M3)
     o8, l8 = prefill_on_gpu(c8)
     k16, v16 = c8.pool.k.to(torch.bfloat16), c8.pool.v.to(torch.bfloat16)

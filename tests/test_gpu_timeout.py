@@ -29,10 +29,11 @@ def _default_limit_afterwards():
     pk.set_wait_limit_ns(0)
 
 
-@pytest.mark.parametrize("d_qk", [128, 192])
-def test_prefill_wait_runs_out_then_next_call_is_right(d_qk):
+@pytest.mark.parametrize("d_qk,e4m3", [(128, False), (192, False), (128, True)])
+def test_prefill_wait_runs_out_then_next_call_is_right(d_qk, e4m3):
+    # (E4M3 query and caches at d_qk 128: the kernel with the V widening warp)
     c = wl.prefill_case([300, 130, 700], [500, 130, 1400], 32, 32, 8, d_qk, 128, wl.HND, wl.BF16,
-                        seed=81)
+                        seed=81, **(dict(q_dtype=wl.E4M3, kv_dtype=wl.E4M3, k_scale=1.5) if e4m3 else {}))
     prev = pk.set_wait_limit_ns(TINY_NS)
     assert prev == 10 ** 9
     err = err_word()
