@@ -11,26 +11,31 @@
 // is one 128-row query tile of a request for TWO qo heads of the same kv
 // head (blocks A and B; B is absent when the group size is odd and the
 // heads run out), so every K/V tile brought into shared memory feeds two
-// 128 x BN score tiles.  Warp roles (S = softmax threads per query row, 2
-// for d_qk 128 and 1 for d_qk 192):
-//   warps 0 .. 8S-1  the softmax: block X = (w / 4) % 2, TMEM lane quarter
-//           w % 4, column share w / 8; each thread reads its part of a score
-//           row from TMEM 32 columns at a time, masks, takes the row max
-//           (traded with its partner when S = 2), runs the online softmax in
-//           base 2 against a running max that is raised only when the tile
-//           max exceeds it by more than 2^8, and writes P (bf16/fp16) over
-//           the consumed S columns as the A operand of the block's PV MMA,
-//           which accumulates into the block's O in TMEM; at the end of the
-//           item it normalises its share of O and writes it with the LSE;
-//   warp 8S     TMA producer: takes the items, loads both Q blocks and the K
+// 128 x BN score tiles.  Twelve warps:
+//   warps 0-7   the softmax, one thread per query row: block X = w / 4, TMEM
+//           lane quarter w % 4.  Each thread reads its score row from TMEM
+//           32 columns at a time, masks, takes the row max, runs the online
+//           softmax in base 2 against a running max that is raised only
+//           when the tile max exceeds it by more than 2^8, and writes P
+//           (bf16/fp16) over the consumed S columns as the A operand of the
+//           block's PV MMA, which accumulates into the block's O in TMEM; at
+//           the end of the item it normalises O and writes it with the LSE;
+//   warp 8      TMA producer: takes the items, loads both Q blocks and the K
 //           tiles page by page through a ring of shared-memory stages;
-//   warp 8S+1   allocates tensor memory and issues the tcgen05 MMAs from one
+//   warp 9      allocates tensor memory and issues the tcgen05 MMAs from one
 //           thread in the order QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t)
 //           QK_B(t+1) | ..., so that while one block's softmax runs the
 //           tensor core works for the other block (ping-pong);
-//   warp 8S+2   TMA producer of the V tiles (a second ring).
-// Every wait is bounded; a wait that gives up sets PKV_DEV_ERR_TIMEOUT, the
-// other roles stop, tensor memory is freed and the CTA returns.
+//   warp 10     TMA producer of the V tiles (a second ring);
+//   warp 11     idle for 16-bit inputs.  With an E4M3 query and E4M3 caches
+//           the QK MMAs are kind::f8f6f4 straight from the E4M3 Q and K
+//           tiles, V tiles arrive as E4M3 in a byte ring and this warp widens
+//           each one exactly to fp16 in the 16-bit V stage layout, so that
+//           PV stays a 16-bit MMA with P in fp16.
+// The softmax warps run with 200 registers and the others with 104
+// (setmaxnreg).  Every wait is bounded; a wait that gives up sets
+// PKV_DEV_ERR_TIMEOUT, the other roles stop, the copies in flight are
+// waited for, tensor memory is freed and the CTA returns.
 #include <math.h>
 
 #include <type_traits>
@@ -43,11 +48,10 @@ namespace pkv {
 constexpr int kPfRows = 128;     // query rows per block
 constexpr int kPfDV = 128;
 
-// Keys per tile (BN), ring depths and softmax threads per query row
-// (SPLIT).  TMEM holds S of both blocks (BN columns each) and O of both
-// blocks (128 columns each); shared memory holds both Q blocks, SK K stages
-// and SV V stages.  Warps 0 .. 8*SPLIT-1 run the softmax, then come the
-// K-load, MMA and V-load warps.
+// Keys per tile (BN) and ring depths.  TMEM holds S of both blocks (BN
+// columns each) and O of both blocks (128 columns each); shared memory holds
+// both Q blocks, SK K stages and SV V stages (three 16-bit V stages plus an
+// E4M3 V ring on the E4M3 path).
 template <int DQK>
 struct PfCfg;
 template <>
