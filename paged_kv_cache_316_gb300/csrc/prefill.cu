@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     constexpr int BN = PfCfg<DQK>::BN;
     // (F8: a third V stage, so that the widening of a tile has a whole tile
     // period of slack before its PV)
-    constexpr int SK = PfCfg<DQK>::SK, SV = F8 ? 3 : PfCfg<DQK>::SV;
+    constexpr int SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV;
     constexpr int kTmaWarp = PfRoles<DQK>::kTmaWarp, kMmaWarp = PfRoles<DQK>::kMmaWarp,
                   kTmaVWarp = PfRoles<DQK>::kTmaVWarp;
     static_assert(!F8 || DQK == 128, "E4M3 tiles: d_qk 128");
@@ -560,7 +560,17 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             // order, so QK_X(t+1), which overwrites S_X, cannot disturb PV_X(t)
             // reading P_X from it, and a completed S_X(t+1) implies that PV_X(t)
             // is complete (the softmax relies on both).
-            if (lane == 0) {
+            // The whole warp runs the loop (warp-uniform descriptor arithmetic);
+            // one elected lane issues every MMA and commit, so that each commit
+            // tracks all the MMAs before it.
+            {
+                const bool leader = elect_one();
+                auto mwait = [&](uint32_t bar, uint32_t parity) {
+                    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, wlim));
+                };
+                auto commit = [&](uint32_t bar) {
+                    if (leader) umma_commit(bar);
+                };
                 // (F8: kind::f8f6f4 with E4M3 A and B, whose format code is 0)
                 constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, !F8 && IsBf16<T>::value, false);
                 constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<TP>::value, true);
@@ -571,7 +581,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 int t_base = 0;   // K/V tiles of earlier items
                 int tb_base = 0;  // tiles of block B in earlier items
                 auto wait_k = [&](int t) {
-                    if (!mbar_wait(b_kfull(t % SK), (t / SK) & 1, abort_flag, wlim)) return false;
+                    if (!mwait(b_kfull(t % SK), (t / SK) & 1)) return false;
                     tc_fence_after();
                     return true;
                 };
@@ -582,12 +592,13 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     for (int kk = 0; kk < KSTEPS; ++kk) {  // 32-byte steps, four per 128-byte atom
                         const uint64_t qa = qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4);
                         const uint64_t ka = kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+                        if (!leader) continue;
                         if constexpr (F8)
                             umma_ss_f8(tmem + x * S_STRIDE, qa, ka, idesc_qk, kk > 0 ? 1u : 0u);
                         else
                             umma_ss(tmem + x * S_STRIDE, qa, ka, idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    umma_commit(b_sfull(x));
+                    commit(b_sfull(x));
                 };
                 // P column of keys 16kk .. 16kk+15: the softmax writes chunk c
                 // (keys 32c .. 32c + 31) as 16-bit pairs at the chunk's first
@@ -597,70 +608,77 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     const uint64_t vd = vdesc0 + (((t % SV) * VB) >> 4);
     #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        umma_ts(tmem + O_COL + x * kPfDV, tmem + x * S_STRIDE + pcol(kk), vd + ((kk * 16 * 128) >> 4), idesc_pv,
-                                (!first || kk > 0) ? 1u : 0u);
+                        if (leader)
+                            umma_ts(tmem + O_COL + x * kPfDV, tmem + x * S_STRIDE + pcol(kk), vd + ((kk * 16 * 128) >> 4),
+                                    idesc_pv, (!first || kk > 0) ? 1u : 0u);
                 };
                 for (int k = 0; ok; ++k) {
-                    const int4 itm = take_item(k, ok);
+                    int4 itm = make_int4(-1, 0, 0, 0);
+                    if (lane == 0) itm = take_item(k, ok);
+                    itm.x = __shfl_sync(0xffffffffu, itm.x, 0);
+                    itm.y = __shfl_sync(0xffffffffu, itm.y, 0);
+                    itm.z = __shfl_sync(0xffffffffu, itm.z, 0);
+                    itm.w = __shfl_sync(0xffffffffu, itm.w, 0);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok || itm.x < 0) break;
                     PfItem it;
                     pf_item(p, itm, BN, it);
                     const bool hasB = it.hB >= 0;
                     const int n = it.n_tiles;
-                    if (!mbar_wait(b_qfull, k & 1, abort_flag, wlim)) { ok = false; break; }
+                    if (!mwait(b_qfull, k & 1)) { ok = false; break; }
                     if (n == 0) {
-                        umma_commit(b_qempty);
+                        commit(b_qempty);
                         continue;
                     }
                     if (!wait_k(t_base)) { ok = false; break; }
                     qk(0, t_base);
                     if (hasB) qk(1, t_base);
-                    umma_commit(b_kempty(t_base % SK));
-                    if (n == 1) umma_commit(b_qempty);
+                    commit(b_kempty(t_base % SK));
+                    if (n == 1) commit(b_qempty);
                     for (int j = 0; j < n; ++j) {
                         const int t = t_base + j, tb = tb_base + j;
                         const bool more = j + 1 < n;
                         // block A: PV_A(t), then QK_A(t+1).  V(t) and K(t+1) arrive
                         // long before P_A(t): wait for them first, so that once P_A
                         // is there the MMAs go out back to back
-                        if (!mbar_wait(b_vfull(t % SV), (t / SV) & 1, abort_flag, wlim)) { ok = false; break; }
-                        if (more && !mbar_wait(b_kfull((t + 1) % SK), ((t + 1) / SK) & 1, abort_flag, wlim)) {
+                        if (!mwait(b_vfull(t % SV), (t / SV) & 1)) { ok = false; break; }
+                        if (more && !mwait(b_kfull((t + 1) % SK), ((t + 1) / SK) & 1)) {
                             ok = false;
                             break;
                         }
-                        if (!mbar_wait(b_pfull(0), t & 1, abort_flag, wlim)) { ok = false; break; }
+                        if (!mwait(b_pfull(0), t & 1)) { ok = false; break; }
                         tc_fence_after();
                         pv(0, t, j == 0);
-                        if (!more) umma_commit(b_odone(0));
+                        if (!more) commit(b_odone(0));
                         if (more) {
                             qk(0, t + 1);
                             if (!hasB) {
-                                umma_commit(b_kempty((t + 1) % SK));
-                                if (j + 2 == n) umma_commit(b_qempty);
+                                commit(b_kempty((t + 1) % SK));
+                                if (j + 2 == n) commit(b_qempty);
                             }
                         }
                         // block B: PV_B(t), then QK_B(t+1)
                         if (hasB) {
-                            if (!mbar_wait(b_pfull(1), tb & 1, abort_flag, wlim)) { ok = false; break; }
+                            if (!mwait(b_pfull(1), tb & 1)) { ok = false; break; }
                             tc_fence_after();
                             pv(1, t, j == 0);
-                            if (!more) umma_commit(b_odone(1));
+                            if (!more) commit(b_odone(1));
                             if (more) {
                                 qk(1, t + 1);
-                                umma_commit(b_kempty((t + 1) % SK));
-                                if (j + 2 == n) umma_commit(b_qempty);
+                                commit(b_kempty((t + 1) % SK));
+                                if (j + 2 == n) commit(b_qempty);
                             }
                         }
-                        umma_commit(b_vempty(t % SV));
+                        commit(b_vempty(t % SV));
                     }
                     t_base += n;
                     if (hasB) tb_base += n;
                 }
-                if (!ok) give_up();
+                if (!ok && leader) give_up();
                 // every MMA issued (also those of an abandoned item) completes
                 // before tensor memory is freed
-                umma_commit(b_drain);
-                if (!mbar_wait_drain(b_drain, 0)) set_err(p.err, PKV_DEV_ERR_TIMEOUT);
+                commit(b_drain);
+                if (leader && !mbar_wait_drain(b_drain, 0)) set_err(p.err, PKV_DEV_ERR_TIMEOUT);
             }
             __syncwarp();
         } else if (F8 && warp == kConvWarp) {
@@ -935,7 +953,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
 
 template <int DQK, bool F8>
 static size_t prefill_smem_bytes() {
-    constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = F8 ? 3 : PfCfg<DQK>::SV, ES = F8 ? 1 : 2;
+    constexpr int BN = PfCfg<DQK>::BN, SK = PfCfg<DQK>::SK, SV = PfCfg<DQK>::SV, ES = F8 ? 1 : 2;
     return 1024 + 2 * kPfRows * DQK * ES + SK * BN * DQK * ES + SV * BN * kPfDV * 2 + (F8 ? SV * BN * kPfDV : 0) +
            8 * (13 + 2 * SK + 2 * SV + (F8 ? 2 * SV : 0));
 }
