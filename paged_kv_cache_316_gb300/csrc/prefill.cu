@@ -22,8 +22,9 @@
 //           the end of the item it normalises O and writes it with the LSE;
 //   warp 8      TMA producer: takes the items, loads both Q blocks and the K
 //           tiles page by page through a ring of shared-memory stages;
-//   warp 9      allocates tensor memory and issues the tcgen05 MMAs from one
-//           thread in the order QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t)
+//   warp 9      allocates tensor memory and runs the MMA issue loop (the
+//           whole warp; an elect.sync leader issues the tcgen05 MMAs and
+//           commits) in the order QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t)
 //           QK_B(t+1) | ..., so that while one block's softmax runs the
 //           tensor core works for the other block (ping-pong);
 //   warp 10     TMA producer of the V tiles (a second ring);
@@ -50,8 +51,8 @@ constexpr int kPfDV = 128;
 
 // Keys per tile (BN) and ring depths.  TMEM holds S of both blocks (BN
 // columns each) and O of both blocks (128 columns each); shared memory holds
-// both Q blocks, SK K stages and SV V stages (three 16-bit V stages plus an
-// E4M3 V ring on the E4M3 path).
+// both Q blocks, SK K stages and SV V stages (plus SV E4M3 V stages on the
+// E4M3 path).
 template <int DQK>
 struct PfCfg;
 template <>
