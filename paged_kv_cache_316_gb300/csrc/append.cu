@@ -121,7 +121,7 @@ __device__ __forceinline__ int64_t append_dst(const AppendParams &p, int64_t tok
 // head for HND).  Loads run kApSlots-1 pieces ahead of the stores; a slot is
 // reloaded once the store that read it has finished reading.  The lanes
 // resolve the destinations of 32 tokens at a time (lane i: token i), two
-// groups ahead of need; lane 0 issues every copy.
+// groups ahead of need; one elect.sync leader issues every copy.
 template <int LAYOUT>
 __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
     extern __shared__ __align__(128) uint8_t ring[];
@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * p.tokens_per_cta;
     const int64_t t1 = min(p.nnz, t0 + p.tokens_per_cta);
     if (t0 >= t1) return;
-    if (lane == 0) {
+    const bool leader = elect_one();
+    const int leader_lane = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
+    if (leader) {
         for (int s = 0; s < kApSlots; ++s) mbar_init(smem_u32(&full[s]), 1);
         fence_mbar_init();
     }
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
         const int64_t dst = dst_of(tok);
         const int s = static_cast<int>(j % kApSlots);
         const uint32_t bar = smem_u32(&full[s]);
-        if (lane == 0) {
+        if (leader) {
             if (dst >= 0) {
                 const uint32_t bytes = static_cast<uint32_t>(nh) * p.D * p.esize;
                 mbar_expect_tx(bar, bytes);
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
         }
         const int64_t dst = dst_of(tok);
         const int s = static_cast<int>(js % kApSlots);
-        if (lane == 0) {
+        if (leader) {
             if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((js / kApSlots) & 1), &no_abort, p.wait_ns)) {
                 set_err(p.err, PKV_DEV_ERR_TIMEOUT);
                 ok = false;
@@ -210,9 +212,9 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
             }
             bulk_commit();
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (!__shfl_sync(0xffffffffu, ok, leader_lane)) break;
         if (jl < total) {
-            if (lane == 0) bulk_wait_read1();  // the store that last read slot jl % kApSlots is done reading
+            if (leader) bulk_wait_read1();  // the store that last read slot jl % kApSlots is done reading
             issue_load(jl);
             ++jl;
         }
@@ -220,10 +222,10 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
     // A wait that gave up left the loads of pieces js .. jl-1 in flight (at
     // most one per slot): they land in this CTA's shared memory, so wait for
     // them before it exits; then for the stores.
-    if (lane == 0 && !ok)
+    if (leader && !ok)
         for (int64_t j = js; j < jl; ++j)
             mbar_wait_drain(smem_u32(&full[j % kApSlots]), static_cast<uint32_t>((j / kApSlots) & 1));
-    if (lane == 0) bulk_wait_all();
+    if (leader) bulk_wait_all();
 }
 
 }  // namespace pkv

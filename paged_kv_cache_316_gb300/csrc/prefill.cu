@@ -387,9 +387,11 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             // the Q blocks and the K tiles; warp 10 loads the V tiles.  A K stage
             // is released by the last QK that reads it and a V stage by the last
             // PV.  Each warp looks up a tile's page ids in one coalesced load,
-            // one tile ahead; lane 0 issues the copies.
+            // one tile ahead; an elect.sync leader issues the copies.
             const bool is_k = warp == kTmaWarp;
-            if (lane == 0) {
+            const bool leader = elect_one();
+            const int leader_lane = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
+            if (leader) {
                 if (is_k) {
                     prefetch_tmap(&tm_q);
                     prefetch_tmap(&tm_k);
@@ -410,8 +412,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             auto v_empty = [&](int st) { return F8 ? b_v8empty(st) : b_vempty(st); };
             bool ok = true;
             int t_base = 0;  // tiles of earlier items (global tile counter)
-            int t_next = 0;  // (lane 0) tiles [0, t_next) have their copies issued
-            int q_loads = 0; // (lane 0) Q blocks of items [0, q_loads) issued
+            int t_next = 0;  // (leader) tiles [0, t_next) have their copies issued
+            int q_loads = 0; // (leader) Q blocks of items [0, q_loads) issued
             const int total_items = is_k ? p.cu_items[p.B] : 0;
             int b_scan = 0;  // request of this CTA's previous item: items come in increasing order
             for (int k = 0; ok; ++k) {
@@ -420,8 +422,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     // take the next item from the counter, find its request with a
                     // warp-wide forward scan of cu_items, and publish it
                     int c = 0;
-                    if (lane == 0) c = atomicAdd(p.work_counter, 1);
-                    c = __shfl_sync(0xffffffffu, c, 0);
+                    if (leader) c = atomicAdd(p.work_counter, 1);
+                    c = __shfl_sync(0xffffffffu, c, leader_lane);
                     if (c < total_items) {
                         while (true) {  // ends: cu_items[B] = total > c
                             const int bi = b_scan + lane;
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         const int hB = hA + 1 < (kvh + 1) * p.group ? hA + 1 : -1;
                         itm = make_int4(b_scan, hA, hB, rem / U);
                     }
-                    if (lane == 0) {
+                    if (leader) {
                         const int slot = k % NI;
                         if (k >= NI && !mbar_wait(b_item_empty(slot), ((k / NI) - 1) & 1, abort_flag, wlim)) {
                             give_up();
@@ -449,14 +451,14 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                             mbar_arrive(b_item_full(slot));
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    ok = __shfl_sync(0xffffffffu, ok, leader_lane);
                 } else {
-                    if (lane == 0) itm = take_item(k, ok);
-                    itm.x = __shfl_sync(0xffffffffu, itm.x, 0);
-                    itm.y = __shfl_sync(0xffffffffu, itm.y, 0);
-                    itm.z = __shfl_sync(0xffffffffu, itm.z, 0);
-                    itm.w = __shfl_sync(0xffffffffu, itm.w, 0);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (leader) itm = take_item(k, ok);
+                    itm.x = __shfl_sync(0xffffffffu, itm.x, leader_lane);
+                    itm.y = __shfl_sync(0xffffffffu, itm.y, leader_lane);
+                    itm.z = __shfl_sync(0xffffffffu, itm.z, leader_lane);
+                    itm.w = __shfl_sync(0xffffffffu, itm.w, leader_lane);
+                    ok = __shfl_sync(0xffffffffu, ok, leader_lane);
                 }
                 if (!ok || itm.x < 0) break;
                 PfItem it;
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 const int32_t *bt = p.block_tables + static_cast<int64_t>(it.b) * p.bt_stride;
                 // Q blocks of this item, once the previous item's last QK is done;
                 // loaded after the item's first K tile so that the two overlap
-                auto load_q = [&]() {  // lane 0 of the K producer
+                auto load_q = [&]() {  // the K producer's leader
                     if (k >= 1 && !mbar_wait(b_qempty, (k - 1) & 1, abort_flag, wlim)) {
                         give_up();
                         ok = false;
@@ -480,8 +482,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         q_loads = k + 1;
                     }
                 };
-                if (is_k && lane == 0 && it.n_tiles == 0) load_q();
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (is_k && leader && it.n_tiles == 0) load_q();
+                ok = __shfl_sync(0xffffffffu, ok, leader_lane);
                 if (!ok) break;
                 auto lookup = [&](int j) {  // lane i < nbox: page of box i of tile j
                     const int key = j * BN + lane * RB;
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     int pages[16];
     #pragma unroll
                     for (int i = 0; i < 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
-                    if (lane == 0) {
+                    if (leader) {
                         const int st = t % NS, us = t / NS;
                         if (us > 0 && !mbar_wait(is_k ? b_kempty(st) : v_empty(st), (us - 1) & 1, abort_flag, wlim)) {
                             give_up();
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                             if (is_k && j == 0) load_q();
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    ok = __shfl_sync(0xffffffffu, ok, leader_lane);
                     if (!ok) break;
                 }
                 t_base += it.n_tiles;
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             // up with copies in flight -- wait for every copy this warp issued to
             // land: the last phase issued on each stage (the earlier ones of a
             // stage completed before it was reused) and the last Q blocks.
-            if (lane == 0) {
+            if (leader) {
                 for (int t = t_next > NS ? t_next - NS : 0; t < t_next; ++t)
                     if (!mbar_wait_drain(is_k ? b_kfull(t % NS) : v_full(t % NS), (t / NS) & 1))
                         set_err(p.err, PKV_DEV_ERR_TIMEOUT);
