@@ -150,15 +150,22 @@ def test_bad_page_flagged_and_treated_as_absent():
 
 
 def test_workspace_reused_across_sizes():
-    # one workspace serves calls of different sizes in turn, the split
-    # partials of a larger call staying behind
+    # one workspace serves calls of different sizes and split counts in
+    # turn, the split partials of a larger call staying behind: each result
+    # is within tolerance of the oracle and bit for bit the result with a
+    # freshly zeroed workspace.
     big = wl.decode_case([3000, 2500, 4100, 900, 5000, 1800], 16, 32, 8, 128, wl.HND, seed=11,
                          window_left=-1, slack=0.2)
     small = wl.decode_case([2100, 4000], 32, 64, 8, 128, wl.HND, seed=12, q_len_per_req=2,
                            with_sinks=True, slack=0.2)
+    fp8 = wl.decode_case([6000, 70, 2900], 16, 32, 8, 128, wl.HND, seed=14, kv_dtype=wl.E4M3,
+                         bmm1_scale=0.07, bmm2_scale=0.6, slack=0.2)
     ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
-    for c in (big, small, big, small):
-        _check(c, ws=ws)
+    for c in (big, small, fp8, big, fp8, small):
+        out, lse = _check(c, ws=ws)
+        fresh_out, fresh_lse = decode_on_gpu(c)
+        assert torch.equal(out.view(torch.int16), fresh_out.view(torch.int16))
+        assert torch.equal(lse, fresh_lse)
 
 
 def test_hundreds_of_splits():
