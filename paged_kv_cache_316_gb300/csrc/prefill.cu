@@ -482,6 +482,14 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         q_loads = k + 1;
                     }
                 };
+                // the item's Q blocks into L2 now: their load waits for the
+                // previous item's last QK, and from HBM (128 rows 8 KB apart per
+                // head and atom) it would take several thousand cycles
+                if (is_k && leader && it.n_tiles > 0)
+                    for (int c = 0; c < QA; ++c) {
+                        tma_prefetch_l2_3d(&tm_q, c * (128 / ES), it.hA, it.row_base);
+                        if (it.hB >= 0) tma_prefetch_l2_3d(&tm_q, c * (128 / ES), it.hB, it.row_base);
+                    }
                 if (is_k && leader && it.n_tiles == 0) load_q();
                 ok = __shfl_sync(0xffffffffu, ok, leader_lane);
                 if (!ok) break;
