@@ -36,6 +36,8 @@ CASES = [
     ([77, 300], [500, 300], 16, 16, 4, 192, True, wl.BF16, wl.HND, 6),    # 96-key tiles, 16-slot pages
     ([130, 45], [900, 45], 256, 8, 2, 192, True, wl.F16, wl.NHD, 7),     # tiles inside 256-slot pages
     ([200], [333], 8, 6, 2, 192, False, wl.BF16, wl.HND, 8),             # odd group: block B absent
+    ([0, 300, 0, 17], [40, 1000, 0, 17], 128, 8, 2, 128, True, wl.BF16, wl.NHD, 9),   # requests without queries
+    ([129, 1], [2049, 1], 256, 16, 4, 128, False, wl.F16, wl.HND, 10),  # 256-slot pages, one-key request
 ]
 
 
