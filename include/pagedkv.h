@@ -424,9 +424,13 @@ int paged_prefill_ex(const void *q, int64_t total_q, const void *k_cache,
  *  - Paged caches only (block_tables non-NULL); packed rows (no batch
  *    offsets).
  *  - workspace: >= paged_prefill_fp8_workspace_size(...) bytes, 256-byte
- *    aligned.  E4M3 inputs are widened (exactly: every E4M3 value is an fp16
- *    and a bf16 value) into it before the attention kernel: the query rows,
- *    and the caches packed request by request, for which it reserves
+ *    aligned.  With an E4M3 query and E4M3 caches at d_qk = d_vo = 128 the
+ *    attention kernel reads the E4M3 bytes as they are (QK as E4M3 x E4M3
+ *    tensor-core MMAs, V tiles widened exactly to fp16 in shared memory, P
+ *    in fp16) and the workspace is the plain prefill's.  Otherwise the E4M3
+ *    inputs are widened (exactly: every E4M3 value is an fp16 and a bf16
+ *    value) into it before the attention kernel: the query rows, and the
+ *    caches packed request by request, for which it reserves
  *    batch_size * max_sequence_kv keys.
  * Device errors as paged_prefill (a page id outside the pool flags
  * PKV_DEV_ERR_PAGE and its keys read as zeros).  Host errors: a dtype other
