@@ -145,6 +145,30 @@ def test_full_size_sweep_properties():
     assert torch.equal(changed, expect)
 
 
+@pytest.mark.parametrize("heads,page,layout,dtype,seed",
+                         [(64, 32, wl.HND, wl.BF16, 11),   # 16 KB rows: two 8 KB pieces each
+                          (48, 16, wl.NHD, wl.F16, 12),    # 12 KB rows: pieces of 32 and 16 heads
+                          (4, 8, wl.HND, wl.BF16, 13),     # 1 KB rows, 8-slot pages
+                          (48, 64, wl.HND, wl.E4M3, 14)],  # 6 KB E4M3 rows, 64-slot pages
+                         ids=["h64", "h48", "h4", "h48-e4m3"])
+def test_append_head_counts_and_pages(heads, page, layout, dtype, seed):
+    # rows cut into several whole-head pieces, an uneven last piece, small
+    # rows and other page sizes: the pool after the append bit-exact against
+    # the oracle (untouched slots and pages included)
+    g = np.random.default_rng(seed)
+    n = [int(x) for x in g.integers(1, 90, size=23)]
+    prefix = [int(x) for x in g.integers(0, 200, size=23)]
+    c = wl.append_case(n, prefix, page, heads, 128, layout, dtype, seed=seed, slack=0.2)
+    seq, bi, pos = _gpu_helpers(c)
+    got = _run_append(c, bi, pos)
+    sl = oracle.seq_lens(c.kv_indptr.numpy(), c.kv_last_page_len.numpy(), page)
+    obi, opos = oracle.batch_indices_positions(c.append_indptr.numpy(), sl, c.append_key.shape[0])
+    assert np.array_equal(bi.cpu().numpy(), obi) and np.array_equal(pos.cpu().numpy(), opos)
+    assert oracle_append(c, obi, opos) == 0
+    for gt, r in zip(got, c.pool.storage):
+        assert torch.equal(gt.view(torch.uint8), r.view(torch.uint8))
+
+
 @pytest.mark.parametrize("layout", [wl.NHD, wl.HND])
 def test_fp8_append_bit_exact(layout):
     # 8-bit (E4M3) cache elements are copied byte for byte

@@ -59,6 +59,20 @@ def test_bmm_scales_and_window_zero():
     _check(c)
 
 
+@pytest.mark.parametrize("bmm1", [-0.06, 0.0], ids=["negative", "zero"])
+def test_non_positive_logit_scale(bmm1):
+    # a negative bmm1_scale favours the keys least aligned with q; zero makes
+    # every visible key equally likely (out = bmm2 * mean of V, lse = log n,
+    # plus the sink): both against the oracle, one and several splits, an
+    # E4M3 cache on the swapped-operand path
+    c = wl.decode_case([2500, 7, 900], 16, 32, 8, 128, wl.HND, seed=15, with_sinks=True,
+                       bmm1_scale=bmm1, bmm2_scale=1.3, slack=0.2)
+    _check(c)
+    c8 = wl.decode_case([2500, 7, 900], 16, 32, 8, 128, wl.NHD, seed=16, kv_dtype=wl.E4M3,
+                        bmm1_scale=bmm1, bmm2_scale=0.7, slack=0.2)
+    _check(c8)
+
+
 SCALE_CASES = [
     # uniform queries, split and single-split requests, sinks, window
     dict(L=[1500, 3, 1029, 5000], Q=2, w=700, sinks=True, q_lens=None),

@@ -206,6 +206,22 @@ def test_fp8_small_shapes(case):
     _check(c)
 
 
+@pytest.mark.parametrize("scale", [-0.07, 0.0], ids=["negative", "zero"])
+@pytest.mark.parametrize("dqk", [128, 192])
+def test_non_positive_logit_scale(scale, dqk):
+    # the softmax takes the row max after scaling when the scale is not
+    # positive (a positive one is applied after the max of the raw scores);
+    # zero gives every visible key the same weight
+    c = wl.prefill_case([300, 90], [700, 90], 32, 16, 4, dqk, 128, wl.HND, wl.BF16, causal=True,
+                        seed=31 + dqk, scale=scale, slack=0.2)
+    _check(c)
+    if dqk == 128:  # and on the E4M3 kernel
+        c8 = wl.prefill_case([300, 90], [700, 90], 32, 16, 4, 128, 128, wl.NHD, wl.BF16, causal=True,
+                             seed=33, scale=scale, slack=0.2, q_dtype=wl.E4M3, kv_dtype=wl.E4M3,
+                             k_scale=1.5)
+        _check(c8)
+
+
 def test_fp8_with_unit_scales_equals_16bit_on_widened_values():
     # every E4M3 value is a bf16 value: where the E4M3 inputs are widened to
     # 16 bits first (d_qk 192), the E4M3 prefill with unit scales gives bit
