@@ -1,6 +1,7 @@
 """Run one operation of the library on its named synthetic workload.
 
     python -m paged_kv_cache_316_gb300.run_case --op prefill [--d-qk 128] [--iters 3] [--kv-dtype e4m3]
+                                                [--contiguous]
     python -m paged_kv_cache_316_gb300.run_case --op decode_llama | decode_long | decode_varlen | append
                                                 [--batch N] [--iters 3] [--kv-dtype e4m3]
 
@@ -28,6 +29,8 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--kv-dtype", choices=["same", "e4m3"], default="same",
                     help="the cache in the query's dtype, or E4M3 (FP8; prefill: query and caches)")
+    ap.add_argument("--contiguous", action="store_true",
+                    help="prefill: the same keys as contiguous (non-paged) K/V, no block table")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     from . import build
@@ -46,13 +49,21 @@ def main():
         scales = dict(q_scale=torch.ones(1, device=dev), k_scale=torch.ones(1, device=dev),
                       v_scale=torch.ones(1, device=dev)) if e4 else {}
 
-        def run():
-            pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv,
-                             bt, causal=True, kv_layout="HND", **scales)
+        if a.contiguous:  # each request's keys gathered into [rows, Hkv, d] tensors
+            ks, vs = zip(*(wl.read_tokens(c.pool, c.pt, b) for b in range(B)))
+            kc, vc = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+
+            def run():
+                pk.paged_prefill(c.q, kc, vc, c.scale, ws, c.max_q, c.max_kv, lq, lkv, None, causal=True,
+                                 **scales)
+        else:
+            def run():
+                pk.paged_prefill(c.q, c.pool.k, c.pool.v, c.scale, ws, c.max_q, c.max_kv, lq, lkv,
+                                 bt, causal=True, kv_layout="HND", **scales)
     elif a.op in ("decode_llama", "decode_long", "decode_varlen"):
         kvd = dict(kv_dtype=wl.E4M3) if a.kv_dtype == "e4m3" else {}
-        if a.op == "decode_varlen":
-            c = wl.long_decode_varlen(device=dev, **kvd)
+        if a.op == "decode_varlen":  # (batch: the first requests of the same draws)
+            c = wl.long_decode_varlen(device=dev, batch=a.batch or 256, **kvd)
         elif not a.batch:
             c = (wl.llama_decode(device=dev, **kvd) if a.op == "decode_llama"
                  else wl.long_decode(device=dev, **kvd))
@@ -79,7 +90,8 @@ def main():
                             window_left=c.window_left, sinks=sinks, kv_layout=c.pool.layout,
                             q_len_per_req=c.q_len_per_req, **vl)
     else:
-        c = wl.append_sweep(a.batch or 4096, seed=1, layout=wl.NHD, device=dev, fill="empty")
+        c = wl.append_sweep(a.batch or 4096, seed=1, layout=wl.NHD, device=dev, fill="empty",
+                            **(dict(dtype=wl.E4M3) if a.kv_dtype == "e4m3" else {}))
         kvi, kvp, last = (x.to(dev) for x in (c.kv_indices, c.kv_indptr, c.kv_last_page_len))
         seq = pk.paged_seq_lens(kvp, last, 16)
         nnz = c.append_key.shape[0]

@@ -392,11 +392,13 @@ def long_decode(seed: int = 0, layout: int = HND, device="cpu", **kw) -> DecodeC
                        device=device, bt_width=32768 // 64, **kw)
 
 
-def long_decode_varlen(seed: int = 0, layout: int = HND, device="cpu", **kw) -> DecodeCase:
+def long_decode_varlen(seed: int = 0, layout: int = HND, device="cpu", batch: int = 256,
+                       **kw) -> DecodeCase:
     """The long-context decode with variable-length queries: each of the 256
-    requests has 1 to 4 query tokens (uniform), max_q_len 4."""
-    L = lognormal_lengths(generator(seed), 256, 4096.0, 1.0, 4, 32768)
-    ql = uniform_lengths(generator(seed + 101), 256, 1, 4)
+    requests has 1 to 4 query tokens (uniform), max_q_len 4.  `batch` keeps
+    the first requests of the same draws (a smaller case of the same shape)."""
+    L = lognormal_lengths(generator(seed), 256, 4096.0, 1.0, 4, 32768)[:batch]
+    ql = uniform_lengths(generator(seed + 101), 256, 1, 4)[:batch]
     return decode_case(L, 64, 64, 8, 128, layout, BF16, q_lens=ql, window_left=4095,
                        with_sinks=True, seed=seed, device=device, bt_width=32768 // 64, **kw)
 
