@@ -86,12 +86,27 @@ enum {
 #define PKV_DEV_ERR_QLEN 8    /* kv length shorter than the query length            */
 #define PKV_DEV_ERR_TIMEOUT 16 /* a bounded pipeline wait gave up; output invalid   */
 #define PKV_DEV_ERR_LEN 32    /* a length exceeds the stated maximum; it is clamped  */
+#define PKV_DEV_ERR_BOUNDS 64 /* debug build only: a derived offset left its buffer  */
 
 /* Human-readable name of a pkv_status value (static string). */
 const char *pkv_status_string(int status);
 
 /* Number of kernels this library has launched in this process. */
 unsigned long long pkv_kernel_launches(void);
+
+/*
+ * pkv_debug_bounds -- 1 for the debug build of the library (compiled with
+ * -DPKV_DEBUG_BOUNDS=1: libpagedkv_debug.so), 0 for the release build.  Both
+ * check every index they read from device memory (page ids, batch indices,
+ * positions, lengths; the PKV_DEV_ERR_* bits above).  The debug build also
+ * range-checks every offset the kernels derive from those indices -- cache
+ * rows, query and output rows, workspace partials, block-table entries,
+ * tensor-map coordinates and shared-memory page lists -- before the access;
+ * a violation sets PKV_DEV_ERR_BOUNDS and the access is skipped.  The
+ * results of both builds are otherwise identical.  A diagnostic aid of this
+ * library (the pages have none), in place of a memory checker.
+ */
+int pkv_debug_bounds(void);
 
 /*
  * pkv_set_wait_limit_ns -- time limit, in nanoseconds, of every bounded
@@ -392,7 +407,8 @@ int paged_prefill(const void *q, int64_t total_q, const void *k_cache,
  * batch_offsets_o[b] + i of out / lse, and (contiguous K/V only) its keys /
  * values rows batch_offsets_k[b] + j / batch_offsets_v[b] + j.  A NULL array
  * keeps the packed placement of paged_prefill.  Output rows outside
- * [0, total_q) are not written.  Host errors: K/V offsets together with a
+ * [0, total_q) are not written (the debug build, pkv_debug_bounds, also sets
+ * PKV_DEV_ERR_BOUNDS for them).  Host errors: K/V offsets together with a
  * block table -> PKV_ERR_INVALID_ARG; the rest as paged_prefill.
  */
 int paged_prefill_ex(const void *q, int64_t total_q, const void *k_cache,

@@ -29,6 +29,7 @@ _sz = ctypes.c_size_t
 _SIGNATURES = {
     "pkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "pkv_kernel_launches": ([], ctypes.c_ulonglong),
+    "pkv_debug_bounds": ([], ctypes.c_int),
     "pkv_set_wait_limit_ns": ([ctypes.c_ulonglong], ctypes.c_ulonglong),
     "paged_seq_lens": ([_c_p, _c_p, _i32, _i32, _c_p, _c_p], ctypes.c_int),
     "paged_batch_indices_positions": ([_c_p, _c_p, _i32, _i64, _c_p, _c_p, _c_p],
@@ -72,11 +73,14 @@ def library_path() -> str:
     return os.path.join(_HERE, _LIB_NAME)
 
 
-def load_library():
-    """Load libpagedkv.so from the package directory (raises if missing)."""
+def load_library(path: str | None = None):
+    """Load libpagedkv.so from the package directory (raises if missing).
+    With `path`, load that build of the library instead and route every later
+    call to it (e.g. the range-checking libpagedkv_debug.so; passing
+    library_path() switches back)."""
     global _lib
-    if _lib is None:
-        path = library_path()
+    if _lib is None or path is not None:
+        path = path or library_path()
         if not os.path.exists(path):
             raise PagedKVError(
                 f"{path} is not built: run `python -m paged_kv_cache_316_gb300.build` "
@@ -88,6 +92,11 @@ def load_library():
             fn.restype = res
         _lib = lib
     return _lib
+
+
+def debug_bounds() -> bool:
+    """True when the loaded library is the range-checking debug build."""
+    return bool(load_library().pkv_debug_bounds())
 
 
 def kernel_launches() -> int:

@@ -55,6 +55,7 @@ struct AppendParams {
     int esize;  // bytes per element: 2 (fp16 / bf16) or 1 (e4m3)
     int64_t page_stride;  // elements
     int64_t max_num_pages;
+    int64_t kv_extent;  // elements a cache pointer spans: (max_num_pages - 1) * page_stride + one page
     const int32_t *kv_indices;
     const int32_t *kv_indptr;
     const int32_t *kv_last_page_len;
@@ -105,12 +106,18 @@ __device__ __forceinline__ int64_t append_dst(const AppendParams &p, int64_t tok
         set_err(p.err, PKV_DEV_ERR_POS);
         return -1;
     }
+    if (kDebugBounds && !dbg_in(first + pos / p.page_size, 1, p.kv_indptr[p.B], p.err)) return -1;
     const int64_t page = p.kv_indices[first + pos / p.page_size];
     if (page < 0 || page >= p.max_num_pages) {
         set_err(p.err, PKV_DEV_ERR_PAGE);
         return -1;
     }
-    return kv_row_offset<LAYOUT>(page, p.page_stride, 0, pos % p.page_size, p.H, p.page_size, p.D);
+    const int64_t dst = kv_row_offset<LAYOUT>(page, p.page_stride, 0, pos % p.page_size, p.H, p.page_size, p.D);
+    // the token's whole row: H * D contiguous elements (NHD) or H head rows
+    // page_size * D apart (HND)
+    const int64_t span = LAYOUT == PKV_NHD ? static_cast<int64_t>(p.H) * p.D
+                                           : static_cast<int64_t>(p.H - 1) * p.page_size * p.D + p.D;
+    return dbg_in(dst, span, p.kv_extent, p.err) ? dst : -1;
 }
 
 // One warp per CTA copies a contiguous run of tokens with the bulk-copy
@@ -160,6 +167,11 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
         h0 = (r % npr) * p.heads_per_piece;
         nh = min(p.heads_per_piece, p.H - h0);
     };
+    // (debug build) the piece's heads lie inside the row and its bytes fit a
+    // ring slot; both sides skip a piece that fails
+    auto piece_in = [&](int h0, int nh) {
+        return dbg_in(h0, nh, p.H, p.err) && dbg_in(0, static_cast<int64_t>(nh) * p.D * p.esize, kApSlotBytes, p.err);
+    };
     auto issue_load = [&](int64_t j) {
         int64_t tok;
         int row, h0, nh;
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
         const int s = static_cast<int>(j % kApSlots);
         const uint32_t bar = smem_u32(&full[s]);
         if (leader) {
-            if (dst >= 0) {
+            if (dst >= 0 && piece_in(h0, nh)) {
                 const uint32_t bytes = static_cast<uint32_t>(nh) * p.D * p.esize;
                 mbar_expect_tx(bar, bytes);
                 const uint8_t *src = (row ? p.value : p.key) + (tok * row_elems + static_cast<int64_t>(h0) * p.D) * p.esize;
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(32) append_kernel(AppendParams p) {
             if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((js / kApSlots) & 1), &no_abort, p.wait_ns)) {
                 set_err(p.err, PKV_DEV_ERR_TIMEOUT);
                 ok = false;
-            } else if (dst >= 0) {
+            } else if (dst >= 0 && piece_in(h0, nh)) {
                 uint8_t *cache = row ? p.v_cache : p.k_cache;
                 const uint32_t src = ring_s + s * kApSlotBytes;
                 const uint32_t hb = static_cast<uint32_t>(p.D) * p.esize;
@@ -235,6 +247,7 @@ using namespace pkv;
 extern "C" int paged_seq_lens(const int32_t *kv_indptr, const int32_t *kv_last_page_len,
                               int32_t batch_size, int32_t page_size, int32_t *seq_lens,
                               void *stream) {
+    const CallRange nvtx_range("paged_seq_lens");
     if (batch_size < 0 || page_size <= 0) return PKV_ERR_INVALID_ARG;
     if (batch_size == 0) return PKV_OK;
     if (!kv_indptr || !kv_last_page_len || !seq_lens) return PKV_ERR_NULL;
@@ -249,6 +262,7 @@ extern "C" int paged_batch_indices_positions(const int32_t *append_indptr,
                                              const int32_t *seq_lens, int32_t batch_size,
                                              int64_t nnz, int32_t *batch_indices,
                                              int32_t *positions, void *stream) {
+    const CallRange nvtx_range("paged_batch_indices_positions");
     if (batch_size < 0 || nnz < 0) return PKV_ERR_INVALID_ARG;
     if (nnz == 0) return PKV_OK;
     if (!append_indptr || !seq_lens || !batch_indices || !positions) return PKV_ERR_NULL;
@@ -270,6 +284,7 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
                             int32_t batch_size, int32_t num_kv_heads, int32_t head_dim,
                             int32_t page_size, int32_t layout, int32_t dtype,
                             int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_append");
     if (layout != PKV_NHD && layout != PKV_HND) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_E4M3) return PKV_ERR_INVALID_ARG;
     const int esize = dtype == PKV_E4M3 ? 1 : 2;  // bytes per element; bits are copied unchanged
@@ -299,6 +314,9 @@ extern "C" int paged_append(const void *append_key, const void *append_value, in
     p.esize = esize;
     p.page_stride = page_stride;
     p.max_num_pages = max_num_pages;
+    p.kv_extent = max_num_pages > 0 ? (max_num_pages - 1) * page_stride +
+                                          static_cast<int64_t>(num_kv_heads) * page_size * head_dim
+                                    : 0;
     p.kv_indices = kv_indices;
     p.kv_indptr = kv_indptr;
     p.kv_last_page_len = kv_last_page_len;

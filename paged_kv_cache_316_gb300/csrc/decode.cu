@@ -74,6 +74,8 @@ struct DecodeParams {
     int Q, Hqo, Hkv, group, R;  // Q: query tokens per request (the largest, with cu_q)
     const int32_t *cu_q;        // [B+1] variable-length query rows, or NULL (rows b*Q + t)
     int64_t num_tokens;         // query / out rows the caller holds
+    int64_t kv_extent;  // elements a cache pointer spans: (max_num_pages - 1) * page_stride + one page
+    int64_t ws_rows;    // partial rows of the workspace (B * Hkv * n_split_max * R)
     int page_shift;
     int chunk;        // keys per split
     int n_split_max;  // split slots per (request, kv head) in the workspace
@@ -196,12 +198,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
     const int first_page = k_begin >> p.page_shift;
     const int n_pages = k_end > k_begin ? ((k_end - 1) >> p.page_shift) - first_page + 1 : 0;
     for (int i = tid; i < n_pages; i += kDecThreads) {
-        int page = bt[first_page + i];
-        if (page < 0 || page >= p.max_num_pages) {
+        const bool in_bt = dbg_in(first_page + i, 1, (p.max_seq_len + S - 1) >> p.page_shift, p.err);
+        int page = in_bt ? bt[first_page + i] : -1;
+        if (in_bt && (page < 0 || page >= p.max_num_pages)) {
             set_err(p.err, PKV_DEV_ERR_PAGE);
             page = -1;
         }
-        pages_s[i] = page;
+        if (dbg_in(i, 1, kDecMaxPages, p.err)) pages_s[i] = page;
     }
     __syncthreads();
 
@@ -223,8 +226,10 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         {
             const int r0 = kw0 + gtid / LPR, c = gtid % LPR;
             const int jA = j0 + r0, jZ = jA + (NLOAD - 1) * RSTEP;
-            const int page = jA >= k_begin && jZ < k_end && (jA >> p.page_shift) == (jZ >> p.page_shift)
-                                 ? pages_s[(jA >> p.page_shift) - first_page]
+            const int pi = (jA >> p.page_shift) - first_page;
+            const int page = jA >= k_begin && jZ < k_end && (jA >> p.page_shift) == (jZ >> p.page_shift) &&
+                                     dbg_in(pi, 1, kDecMaxPages, p.err)
+                                 ? pages_s[pi]
                                  : -1;
             if (__all_sync(0xffffffffu, page >= 0)) {
                 const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, jA & (S - 1), p.Hkv, S, kDecD);
@@ -233,12 +238,16 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                     const int r = r0 + k * RSTEP;
                     if (c == 0) kvalid[stage * kDecTile + r] = 1;
                     if constexpr (KV8) {
-                        cp_async_16(dst + swz8(r, c), kc8 + off + k * row_step + c * 16, true);
-                        cp_async_16(dst + kDec8TileBytes + swz8(r, c), vc8 + off + k * row_step + c * 16, true);
+                        const int64_t e = off + k * row_step + c * 16;
+                        const bool in = dbg_in(e, 16, p.kv_extent, p.err);
+                        cp_async_16(dst + swz8(r, c), in ? kc8 + e : kc8, in);
+                        cp_async_16(dst + kDec8TileBytes + swz8(r, c), in ? vc8 + e : vc8, in);
                     } else {
                         const uint32_t o = swz(r, c, kDecRowBytes);
-                        cp_async_16(dst + o, kc + off + k * row_step + c * 8, true);
-                        cp_async_16(dst + kDecTileBytes + o, vc + off + k * row_step + c * 8, true);
+                        const int64_t e = off + k * row_step + c * 8;
+                        const bool in = dbg_in(e, 8, p.kv_extent, p.err);
+                        cp_async_16(dst + o, in ? kc + e : kc, in);
+                        cp_async_16(dst + kDecTileBytes + o, in ? vc + e : vc, in);
                     }
                 }
                 return;
@@ -254,15 +263,19 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                 bool ok = j >= k_begin && j < k_end;
                 const uint8_t *ks = kc8, *vs = vc8;
                 if (ok) {
-                    const int page = pages_s[(j >> p.page_shift) - first_page];
+                    const int pi = (j >> p.page_shift) - first_page;
+                    const int page = dbg_in(pi, 1, kDecMaxPages, p.err) ? pages_s[pi] : -1;
                     if (page < 0) {
                         ok = false;
                         any_bad[kg] = 1;
                     } else {
                         const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
                                                                   S, kDecD) + c * 16;
-                        ks = kc8 + off;
-                        vs = vc8 + off;
+                        ok = dbg_in(off, 16, p.kv_extent, p.err);
+                        if (ok) {
+                            ks = kc8 + off;
+                            vs = vc8 + off;
+                        }
                     }
                 }
                 if (c == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
@@ -278,15 +291,19 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
             bool ok = j >= k_begin && j < k_end;
             const T *ks = kc, *vs = vc;
             if (ok) {
-                const int page = pages_s[(j >> p.page_shift) - first_page];
+                const int pi = (j >> p.page_shift) - first_page;
+                const int page = dbg_in(pi, 1, kDecMaxPages, p.err) ? pages_s[pi] : -1;
                 if (page < 0) {
                     ok = false;
                     any_bad[kg] = 1;
                 } else {
                     const int64_t off = kv_row_offset<LAYOUT>(page, p.page_stride, kvh, j & (S - 1), p.Hkv,
                                                               S, kDecD) + c * 8;
-                    ks = kc + off;
-                    vs = vc + off;
+                    ok = dbg_in(off, 8, p.kv_extent, p.err);
+                    if (ok) {
+                        ks = kc + off;
+                        vs = vc + off;
+                    }
                 }
             }
             if (c == 0) kvalid[stage * kDecTile + r] = ok ? 1 : 0;
@@ -305,7 +322,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
         const T *src = qp;
         if (ok) {
             int t = r / p.group, i = r - t * p.group;
-            src = qp + ((qrow0 + t) * p.Hqo + kvh * p.group + i) * kDecD + c * 8;
+            const int64_t e = ((qrow0 + t) * p.Hqo + kvh * p.group + i) * kDecD + c * 8;
+            ok = dbg_in(e, 8, p.num_tokens * p.Hqo * kDecD, p.err);
+            if (ok) src = qp + e;
         }
         cp_async_16(smem_u32(q_s) + swz(r, c, kDecRowBytes), src, ok);
     }
@@ -767,15 +786,18 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<MT, KV8>::CTAS) decode_spl
                 lse_v = -INFINITY;
             }
             const int64_t orow = (qrow0 + t) * p.Hqo + h;
-            store4(static_cast<T *>(p.out) + orow * kDecD + d, a0 * sc_o, a1 * sc_o, a2 * sc_o, a3 * sc_o);
+            if (dbg_in(orow * kDecD + d, 4, p.num_tokens * p.Hqo * kDecD, p.err))
+                store4(static_cast<T *>(p.out) + orow * kDecD + d, a0 * sc_o, a1 * sc_o, a2 * sc_o, a3 * sc_o);
             if (p.lse && d == 0) p.lse[orow] = lse_v;
         } else {
             const int64_t prow =
                 (static_cast<int64_t>(b * p.Hkv + kvh) * p.n_split_max + s) * p.R + r;
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            *reinterpret_cast<float4 *>(p.ws_o + prow * kDecD + d) =
-                make_float4(a0 * inv, a1 * inv, a2 * inv, a3 * inv);
-            if (d == 0) p.ws_lse[prow] = lsum > 0.f ? M + fast_log2(lsum) : -INFINITY;
+            if (dbg_in(prow, 1, p.ws_rows, p.err)) {
+                *reinterpret_cast<float4 *>(p.ws_o + prow * kDecD + d) =
+                    make_float4(a0 * inv, a1 * inv, a2 * inv, a3 * inv);
+                if (d == 0) p.ws_lse[prow] = lsum > 0.f ? M + fast_log2(lsum) : -INFINITY;
+            }
         }
     }
 }
@@ -809,6 +831,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     const int r = t * p.group + (h - kvh * p.group);
     const int64_t base = static_cast<int64_t>(b * p.Hkv + kvh) * p.n_split_max * p.R + r;
     float M = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
+    if (!dbg_in(base, static_cast<int64_t>(n_split - 1) * p.R + 1, p.ws_rows, p.err) ||
+        !dbg_in(n_split, 0, p.n_split_max, p.err))
+        return;
     for (int s = 0; s < n_split; ++s) M = fmaxf(M, p.ws_lse[base + static_cast<int64_t>(s) * p.R]);
     const int d = lane * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -829,6 +854,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     const float bmm2 = p.bmm2_dev ? __ldg(p.bmm2_dev) : p.bmm2;
     const float sc = den > 0.f ? bmm2 / den : 0.f;
     const int64_t orow = (qrow0 + t) * p.Hqo + h;
+    if (!dbg_in(orow * kDecD + d, 4, p.num_tokens * p.Hqo * kDecD, p.err)) return;
     store4(static_cast<T *>(p.out) + orow * kDecD + d, acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
     if (p.lse && lane == 0) p.lse[orow] = den > 0.f ? (M + fast_log2(den)) * kLn2 : -INFINITY;
 }
@@ -1012,6 +1038,10 @@ static int decode_impl(const void *query, const void *k_cache, const void *v_cac
     p.Q = q_len_per_req;
     p.cu_q = cum_seq_lens_q;
     p.num_tokens = num_tokens;
+    p.kv_extent = max_num_pages > 0 ? (max_num_pages - 1) * page_stride +
+                                          static_cast<int64_t>(num_kv_heads) * page_size * head_dim
+                                    : 0;
+    p.ws_rows = static_cast<int64_t>(batch_size) * num_kv_heads * pl.n_split_max * pl.R;
     p.Hqo = num_qo_heads;
     p.Hkv = num_kv_heads;
     p.group = num_qo_heads / num_kv_heads;
@@ -1039,6 +1069,7 @@ extern "C" int paged_decode(const void *query, const void *k_cache, const void *
                             int32_t q_len_per_req, int32_t num_qo_heads, int32_t num_kv_heads,
                             int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
                             void *out, float *lse, int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_decode");
     return decode_impl(query, k_cache, v_cache, page_stride, max_num_pages, workspace, workspace_bytes,
                        block_tables, block_table_stride, seq_lens, batch_size, max_seq_len, bmm1_scale,
                        bmm2_scale, window_left, sinks, q_len_per_req, nullptr,
@@ -1055,6 +1086,7 @@ extern "C" int paged_decode_varlen(const void *query, int64_t num_tokens, const 
                                    const int32_t *cum_seq_lens_q, int32_t num_qo_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t page_size, int32_t layout, int32_t dtype,
                                    void *out, float *lse, int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_decode_varlen");
     if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
     if (batch_size > 0 && num_tokens > 0 && !cum_seq_lens_q) return PKV_ERR_NULL;
     if (num_tokens == 0) return PKV_OK;
@@ -1074,6 +1106,7 @@ extern "C" int paged_decode_ex(const void *query, int64_t num_tokens, const void
                                int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                                int32_t layout, int32_t dtype, int32_t enable_pdl, void *out, float *lse,
                                int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_decode_ex");
     if (num_tokens < 0 || max_q_len < 1) return PKV_ERR_INVALID_ARG;
     if (!cum_seq_lens_q && num_tokens < static_cast<int64_t>(batch_size) * max_q_len) return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0) return PKV_OK;
@@ -1167,6 +1200,7 @@ extern "C" int paged_decode_noalloc(const void *query, const void *k_cache, cons
                                     int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                                     int32_t layout, int32_t dtype, void *out, float *lse,
                                     int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_decode_noalloc");
     DecodePlan pl;
     int rc = plan_decode(batch_size, q_len_per_req, num_qo_heads, num_kv_heads, head_dim,
                          max_seq_len, page_size, window_left, pl);

@@ -44,6 +44,18 @@ static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 blo
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// An NVTX range named after one entry point, in the "pagedkv" domain, open
+// for the whole call: a profiler's timeline nests the call's launches inside
+// it, and ncu --nvtx can select them by it.  With no tool attached, the push
+// and the pop are each a call through a no-op pointer.
+class CallRange {
+  public:
+    explicit CallRange(const char *name);
+    ~CallRange();
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
+
 // PKV_OK if the launches just made succeeded, PKV_ERR_CUDA otherwise.
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -74,6 +86,25 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ void set_err(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
+}
+
+// Range checks of derived offsets, compiled in by -DPKV_DEBUG_BOUNDS=1 (the
+// debug build of the library).  dbg_in(off, n, extent, err) is true when the
+// elements [off, off + n) lie inside [0, extent); otherwise it sets
+// PKV_DEV_ERR_BOUNDS and the caller skips the access.  In the release build
+// it is the constant true and costs nothing: there only the indices read
+// from device memory (page ids, batch indices, positions, lengths) are
+// checked, since every offset derived from a checked index is in range by
+// construction -- which the debug build verifies.
+#ifndef PKV_DEBUG_BOUNDS
+#define PKV_DEBUG_BOUNDS 0
+#endif
+constexpr bool kDebugBounds = PKV_DEBUG_BOUNDS != 0;
+__device__ __forceinline__ bool dbg_in(int64_t off, int64_t n, int64_t extent, int32_t *err) {
+    if constexpr (!kDebugBounds) return true;
+    if (off >= 0 && n >= 0 && off + n <= extent) return true;
+    set_err(err, PKV_DEV_ERR_BOUNDS);
+    return false;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

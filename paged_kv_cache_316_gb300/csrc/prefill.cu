@@ -472,6 +472,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         ok = false;
                     } else {
                         mbar_expect_tx(b_qfull, it.hB >= 0 ? 2 * QB : QB);
+                        if (kDebugBounds && it.qb > 0) dbg_in(it.row_base, 1, p.total_q, p.err);
                         for (int c = 0; c < QA; ++c)
                             tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * (128 / ES), it.hA,
                                         it.row_base);
@@ -497,7 +498,8 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                     const int key = j * BN + lane * RB;
                     int page = oob;
                     if (p.contiguous) return 0;  // one page: the whole tensor
-                    if (lane < nbox && key < it.kvb) {
+                    if (lane < nbox && key < it.kvb &&
+                        dbg_in(key >> p.page_shift, 1, (p.max_kv + S - 1) >> p.page_shift, p.err)) {
                         page = bt[key >> p.page_shift];
                         if (page < 0 || page >= p.max_num_pages) {
                             if (is_k) set_err(p.err, PKV_DEV_ERR_PAGE);
@@ -531,6 +533,14 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                                                                : (j0 + r0) & (S - 1);
                                 const int ca = LAYOUT == PKV_HND ? slot0 : it.kvh;
                                 const int cb = LAYOUT == PKV_HND ? it.kvh : slot0;
+                                // (debug build) a box starts on a pool page or on the
+                                // zero-fill page and stays inside its page; the tensor
+                                // map bounds every copy in hardware, so the copy is
+                                // issued regardless and the barrier's byte count holds
+                                if (kDebugBounds && !p.contiguous) {
+                                    dbg_in(pages[i], 1, p.max_num_pages + 1, p.err);
+                                    dbg_in(slot0, RB, S, p.err);
+                                }
                                 if (is_k) {
                                     for (int c = 0; c < QA; ++c)
                                         tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full,
@@ -919,6 +929,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
             const int qi = it.i0 + r;
             const int64_t grow = static_cast<int64_t>(it.orow_base) + r;
             const bool valid = qi < it.qb && grow >= 0 && grow < p.total_q;
+            if (kDebugBounds && qi < it.qb) dbg_in(grow, 1, p.total_q, p.err);
             const float inv = l > 0.f ? (p.v_scale ? __ldg(p.v_scale) : 1.f) / l : 0.f;
             T *orow = static_cast<T *>(p.out) + (grow * p.Hqo + h) * kPfDV;
 #pragma unroll
@@ -1347,6 +1358,7 @@ extern "C" int paged_prefill(const void *q, int64_t total_q, const void *k_cache
                              int32_t num_qo_heads, int32_t num_kv_heads, int32_t d_qk,
                              int32_t d_vo, int32_t page_size, int32_t layout, int32_t dtype,
                              void *out, float *lse, int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_prefill");
     return prefill_impl(q, total_q, k_cache, v_cache, k_page_stride, v_page_stride, max_num_pages, scale,
                         workspace, workspace_bytes, max_token_per_sequence, max_sequence_kv, actual_seq_lens_q,
                         actual_seq_lens_kv, block_tables, block_table_stride, batch_size, causal, num_qo_heads,
@@ -1366,6 +1378,7 @@ extern "C" int paged_prefill_ex(const void *q, int64_t total_q, const void *k_ca
                                 void *out, float *lse, const int32_t *batch_offsets_q,
                                 const int32_t *batch_offsets_o, const int32_t *batch_offsets_k,
                                 const int32_t *batch_offsets_v, int32_t *err_word, void *stream) {
+    const CallRange nvtx_range("paged_prefill_ex");
     if (block_tables && (batch_offsets_k || batch_offsets_v)) return PKV_ERR_INVALID_ARG;  // pages place K/V
     return prefill_impl(q, total_q, k_cache, v_cache, k_page_stride, v_page_stride, max_num_pages, scale,
                         workspace, workspace_bytes, max_token_per_sequence, max_sequence_kv, actual_seq_lens_q,
@@ -1422,6 +1435,7 @@ extern "C" int paged_prefill_fp8(const void *q, int64_t total_q, const void *k_c
                                  int32_t d_vo, int32_t page_size, int32_t layout, int32_t q_dtype,
                                  int32_t kv_dtype, int32_t out_dtype, void *out, float *lse, int32_t *err_word,
                                  void *stream) {
+    const CallRange nvtx_range("paged_prefill_fp8");
     if (out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
     const bool q8 = q_dtype == PKV_E4M3, kv8 = kv_dtype == PKV_E4M3;
     if ((!q8 && q_dtype != out_dtype) || (!kv8 && kv_dtype != out_dtype)) return PKV_ERR_INVALID_ARG;

@@ -1,4 +1,6 @@
 // status.cu -- status strings and the launch counter of libpagedkv.
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 
 #include "pkv_common.cuh"
@@ -10,6 +12,20 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
 static std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+static nvtxDomainHandle_t nvtx_domain() {
+    static nvtxDomainHandle_t d = nvtxDomainCreateA("pagedkv");
+    return d;
+}
+CallRange::CallRange(const char *name) {
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(nvtx_domain(), &a);
+}
+CallRange::~CallRange() { nvtxDomainRangePop(nvtx_domain()); }
 }  // namespace pkv
 
 extern "C" unsigned long long pkv_set_wait_limit_ns(unsigned long long ns) {
@@ -29,6 +45,8 @@ extern "C" const char *pkv_status_string(int status) {
 }
 
 extern "C" unsigned long long pkv_kernel_launches(void) { return pkv::g_launches.load(); }
+
+extern "C" int pkv_debug_bounds(void) { return pkv::kDebugBounds ? 1 : 0; }
 
 // ---- tensor-map encoding through the driver entry point (no libcuda link) ----
 #include <mutex>

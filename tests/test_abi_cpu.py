@@ -47,6 +47,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libpagedkv.so does not export {name}"
 
 
+def test_debug_build_exports_the_same_abi(lib):
+    # the range-checking variant (-DPKV_DEBUG_BOUNDS=1) builds for sm_103a,
+    # exports every declared entry point and says which build it is
+    from paged_kv_cache_316_gb300 import build
+    dbg = ctypes.CDLL(build.build(debug_bounds=True))
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"libpagedkv_debug.so does not export {name}"
+    assert dbg.pkv_debug_bounds() == 1
+    assert lib.pkv_debug_bounds() == 0
+
+
 def test_wait_limit_is_set_and_restored(lib):
     # host state only: the limit later launches pass to their kernels
     lib.pkv_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
