@@ -9,7 +9,8 @@ plain paths, one and several splits with the merge, variable-length
 queries; prefill d_qk 128/192, both layouts, pages 8..256, the E4M3
 kind::f8f6f4 and widening paths, contiguous K/V; append with whole-row and
 per-head pieces) no check may fire: the error word stays 0 and the results
-match the oracle as in the release build's tests.  One input the release
+match the oracle as in the release build's tests; nor over the benchmark's
+workloads at full size.  One input the release
 build tolerates silently -- output rows placed past the end of `out`, which
 are documented as not written -- is reported by the debug build.
 
@@ -188,3 +189,35 @@ def test_append_no_check_fires(case):
     assert oracle_append(c, obi, opos) == 0
     for g_, r in zip(storage, c.pool.storage):
         assert torch.equal(g_.cpu().view(torch.uint8), r.view(torch.uint8))
+
+
+FULL = ["decode_llama", "decode_llama_e4m3", "decode_long", "decode_varlen", "prefill_d128",
+        "prefill_d192", "prefill_d128_e4m3", "append_4096", "append_4096_e4m3"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_no_check_fires(name):
+    # the benchmark's workloads at full size (the largest offsets: a 4096-
+    # request append pool of several GB, 256-request long-context decode,
+    # the ragged prefill): no derived offset leaves its buffer.  Their
+    # results are checked against the oracle on sampled requests elsewhere.
+    err = err_word()
+    if name.startswith("decode"):
+        kv8 = dict(kv_dtype=wl.E4M3) if name.endswith("e4m3") else {}
+        c = {"decode_llama": wl.llama_decode, "decode_llama_e4m3": wl.llama_decode,
+             "decode_long": wl.long_decode, "decode_varlen": wl.long_decode_varlen}[name](device=DEV, **kv8)
+        decode_on_gpu(c, err_word=err)
+    elif name.startswith("prefill"):
+        kw = dict(q_dtype=wl.E4M3, kv_dtype=wl.E4M3) if name.endswith("e4m3") else {}
+        c = wl.ragged_prefill(d_qk=192 if "192" in name else 128, device=DEV, **kw)
+        prefill_on_gpu(c, err_word=err)
+    else:
+        c = wl.append_sweep(4096, seed=1, layout=wl.NHD, device=DEV, fill="empty",
+                            **(dict(dtype=wl.E4M3) if name.endswith("e4m3") else {}))
+        kvi, kvp, last = (x.to(DEV) for x in (c.kv_indices, c.kv_indptr, c.kv_last_page_len))
+        seq = pk.paged_seq_lens(kvp, last, 16)
+        bi, pos = pk.paged_batch_indices_positions(c.append_indptr.to(DEV), seq, c.append_key.shape[0])
+        pk.paged_append(c.append_key, c.append_value, bi, pos, c.pool.storage[0], kvi, kvp, last,
+                        kv_layout="NHD", err_word=err)
+        torch.cuda.synchronize()
+    assert int(err.item()) == 0
