@@ -54,6 +54,16 @@ MUTANTS = {
                             "o[d] += w * orc_elem(v_cache, off, kv_dtype);"),
     "k_scale_used_for_q": ("dot += (q_mul * orc_elem(q, q_off + d, dtype)) * (k_mul * orc_elem(k_cache, off, kv_dtype));",
                            "dot += (k_mul * orc_elem(q, q_off + d, dtype)) * (k_mul * orc_elem(k_cache, off, kv_dtype));"),
+    "decode_excludes_own_key": ("int64_t lo = 0, hi = p;", "int64_t lo = 0, hi = p - 1;"),
+    "prefill_always_causal": ("int64_t hi = causal ? (pos < kvb - 1 ? pos : kvb - 1) : kvb - 1;",
+                              "int64_t hi = pos < kvb - 1 ? pos : kvb - 1;"),
+    "prefill_excludes_own_key": ("int64_t hi = causal ? (pos < kvb - 1 ? pos : kvb - 1) : kvb - 1;",
+                                 "int64_t hi = causal ? (pos - 1 < kvb - 1 ? pos - 1 : kvb - 1) : kvb - 1;"),
+    "bf16_decoded_as_fp16": ("return dtype == ORC_BF16 ? orc_from_bf16(h[i]) : orc_from_fp16(h[i]);",
+                             "return orc_from_fp16(h[i]);"),
+    "sink_scaled_by_logit_scale": ("sinks != NULL, sinks ? (double)sinks[h] : 0.0,",
+                                   "sinks != NULL, sinks ? bmm1_scale * (double)sinks[h] : 0.0,"),
+    "lse_in_base_two": ("*lse = m + log(den);", "*lse = m + log2(den);"),
     "prefill_query_read_as_cache_type": (
         "err |= orc_attend_row(q, r * d_qk, q_dtype, q_scale, k_scale, v_scale, k_cache, v_cache, kv_dtype,",
         "err |= orc_attend_row(q, r * d_qk, kv_dtype, q_scale, k_scale, v_scale, k_cache, v_cache, kv_dtype,"),
