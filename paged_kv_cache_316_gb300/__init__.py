@@ -20,4 +20,5 @@ from .binding import (  # noqa: F401
     paged_prefill,
     kernel_launches,
     set_wait_limit_ns,
+    debug_bounds,
 )
