@@ -113,6 +113,11 @@ struct PrefillParams {
     float *lse;
     int32_t *err;
     unsigned long long wait_ns;  // limit of every bounded pipeline wait
+    // K tiles through the 5-D map of cache_tmap5 (one copy per page part for
+    // all of a row's 128-byte atoms; stages laid out [8-row group][atom][8
+    // rows][128 B]) with the coordinate page * k5_ratio + kv head, or (0)
+    // through the 4-D map, one copy per atom ([atom][row][128 B] stages)
+    int k5, k5_ratio;
 };
 
 // cu_q / cu_kv = exclusive prefix sums of the query / kv lengths and
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     constexpr uint32_t VB = BN * kPfDV * 2;      // bytes of one 16-bit V stage
     constexpr uint32_t V8B = F8 ? BN * kPfDV : 0;  // bytes of one E4M3 V stage (F8)
     constexpr int KSTEPS = DQK * ES / 32;        // 32-byte K-steps of a QK MMA
+    constexpr bool K5 = DQK == 192 && !F8;       // K tiles may come through the 5-D map (p.k5)
     constexpr int NI = 2;                        // slots of the work-item ring
     // TMEM columns (every region starts at a multiple of 128): S of block X
     // at X * S_STRIDE (BN columns; P of a chunk, 16-bit pairs,
@@ -541,7 +547,10 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                                     dbg_in(pages[i], 1, p.max_num_pages + 1, p.err);
                                     dbg_in(slot0, RB, S, p.err);
                                 }
-                                if (is_k) {
+                                if (is_k && K5 && p.k5) {  // every atom of the page part in one copy
+                                    tma_load_5d(k_s + st * KB + r0 * (QA * 128), &tm_k, full, 0, 0, 0, slot0 >> 3,
+                                                pages[i] * p.k5_ratio + it.kvh);
+                                } else if (is_k) {
                                     for (int c = 0; c < QA; ++c)
                                         tma_load_4d(k_s + st * KB + c * (BN * 128) + r0 * 128, &tm_k, full,
                                                     c * (128 / ES), ca, cb, pages[i]);
@@ -596,7 +605,9 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                 constexpr uint32_t idesc_qk = umma_idesc(kPfRows, BN, !F8 && IsBf16<T>::value, false);
                 constexpr uint32_t idesc_pv = umma_idesc(kPfRows, kPfDV, IsBf16<TP>::value, true);
                 const uint64_t qdesc0 = umma_sdesc_sw128(q_s, 16, 1024);
-                const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, 1024);
+                const bool k5 = K5 && p.k5;
+                const uint64_t kdesc0 = umma_sdesc_sw128(k_s, 16, k5 ? QA * 1024 : 1024);
+                const uint32_t k_atom = k5 ? 1024u : static_cast<uint32_t>(BN * 128);
                 const uint64_t vdesc0 = umma_sdesc_sw128(v_s, BN * 128, 1024);
                 bool ok = true;
                 int t_base = 0;   // K/V tiles of earlier items
@@ -612,7 +623,7 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
     #pragma unroll
                     for (int kk = 0; kk < KSTEPS; ++kk) {  // 32-byte steps, four per 128-byte atom
                         const uint64_t qa = qd + (((kk >> 2) * (kPfRows * 128) + (kk & 3) * 32) >> 4);
-                        const uint64_t ka = kd + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+                        const uint64_t ka = kd + (((kk >> 2) * k_atom + (kk & 3) * 32) >> 4);
                         if (!leader) continue;
                         if constexpr (F8)
                             umma_ss_f8(tmem + x * S_STRIDE, qa, ka, idesc_qk, kk > 0 ? 1u : 0u);
@@ -1144,6 +1155,45 @@ static bool cache_tmap(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
     return encode_tmap(m, base, dt, 4, dims, strides, box);
 }
 
+// A paged cache as a 5-D map whose box holds every 128-byte atom of `rows`
+// slots of one page: dims (64 elements, 8 slots, d / 64 atoms, page_size / 8
+// slot groups, u = page * ratio + kv head), so one copy fills
+// [group][atom][8 rows][128 B] of shared memory -- a 128-byte-swizzled
+// K-major layout with 8-row groups QA * 1024 bytes apart.  The atom
+// dimension's stride (128 B) is below the slot dimension's; the driver
+// accepts the map.  Possible when the page stride is a multiple of
+// page_size * d (HND) or d (NHD) elements, so that (page, head) is one index
+// u, and u fits an int32 coordinate.  Used for d_qk 192 (three atoms, one
+// copy instead of three): at d_qk 128 the two-atom box measured slower.
+static bool cache_tmap5_ok(int layout, int d, int S, int hkv, int64_t P, int64_t pages, int rows, int &ratio) {
+    if (d != 192 || S % 8 || rows % 8) return false;
+    const int64_t unit = layout == PKV_HND ? static_cast<int64_t>(S) * d : d;
+    if (P % unit) return false;
+    const int64_t r = P / unit;
+    if ((pages + 1) * r + hkv >= (1LL << 31)) return false;
+    ratio = static_cast<int>(r);
+    return true;
+}
+static bool cache_tmap5(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int layout, int d, int S, int hkv,
+                        int ratio, int64_t pages, int rows) {
+    uint64_t dims[5] = {64, 8, static_cast<uint64_t>(d / 64), static_cast<uint64_t>(S / 8),
+                        static_cast<uint64_t>(pages > 0 ? pages * ratio : 1)};
+    uint64_t strides[4];
+    if (layout == PKV_HND) {
+        strides[0] = static_cast<uint64_t>(d) * 2;
+        strides[1] = 128;
+        strides[2] = 8ull * d * 2;
+        strides[3] = static_cast<uint64_t>(S) * d * 2;
+    } else {
+        strides[0] = static_cast<uint64_t>(hkv) * d * 2;
+        strides[1] = 128;
+        strides[2] = 8ull * hkv * d * 2;
+        strides[3] = static_cast<uint64_t>(d) * 2;
+    }
+    uint32_t box[5] = {64, 8, static_cast<uint32_t>(d / 64), static_cast<uint32_t>(rows / 8), 1};
+    return encode_tmap(m, base, dt, 5, dims, strides, box);
+}
+
 // Contiguous K or V ([rows, num_kv_heads, d], row stride in elements) as the
 // NHD map of a single page holding every row; a box is one 64-element d-atom
 // of `box_rows` consecutive rows of one kv head.
@@ -1234,6 +1284,7 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     const int bn = pf_bn(d_qk);
     const int rows = pf_box_rows(page_size, bn);
     CUtensorMap tq, tk, tv;
+    int k5 = 0, k5_ratio = 0;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),
                             static_cast<uint64_t>(total_q)};
@@ -1252,11 +1303,14 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
         if (!contiguous_tmap(&tk, k_cache, tdt, d_qk, num_kv_heads, k_page_stride, max_num_pages, bn) ||
             !contiguous_tmap(&tv, v_cache, tdt, d_vo, num_kv_heads, v_page_stride, max_num_pages, bn))
             return PKV_ERR_CUDA;
-    } else if (!cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride,
-                           max_num_pages, rows) ||
-               !cache_tmap(&tv, v_cache, tdt, layout, d_vo, page_size, num_kv_heads, v_page_stride,
-                           max_num_pages, rows)) {
-        return PKV_ERR_CUDA;
+    } else {
+        k5 = cache_tmap5_ok(layout, d_qk, page_size, num_kv_heads, k_page_stride, max_num_pages, rows, k5_ratio) ? 1
+                                                                                                                   : 0;
+        if (!(k5 ? cache_tmap5(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k5_ratio, max_num_pages, rows)
+                 : cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride, max_num_pages,
+                              rows)) ||
+            !cache_tmap(&tv, v_cache, tdt, layout, d_vo, page_size, num_kv_heads, v_page_stride, max_num_pages, rows))
+            return PKV_ERR_CUDA;
     }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1333,6 +1387,8 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     p.lse = lse;
     p.err = err_word;
     p.wait_ns = wait_limit_ns();
+    p.k5 = k5;
+    p.k5_ratio = k5_ratio;
     const int n_qt = (max_token_per_sequence + kPfRows - 1) / kPfRows;
     const int64_t items = static_cast<int64_t>(n_qt) * num_kv_heads * pairs * batch_size;
     if (n_qt > 0) {
