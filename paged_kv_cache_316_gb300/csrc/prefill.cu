@@ -477,26 +477,18 @@ __global__ void __launch_bounds__(PfRoles<DQK>::kThreads, 1)
                         give_up();
                         ok = false;
                     } else {
-                        mbar_expect_tx(b_qfull, it.hB >= 0 ? 2 * QB : QB);
+                        mbar_expect_tx(b_qfull, 2 * QB);
                         if (kDebugBounds && it.qb > 0) dbg_in(it.row_base, 1, p.total_q, p.err);
-                        for (int c = 0; c < QA; ++c)
-                            tma_load_3d(q_s + c * (kPfRows * 128), &tm_q, b_qfull, c * (128 / ES), it.hA,
-                                        it.row_base);
-                        if (it.hB >= 0)
-                            for (int c = 0; c < QA; ++c)
-                                tma_load_3d(q_s + QB + c * (kPfRows * 128), &tm_q, b_qfull, c * (128 / ES), it.hB,
-                                            it.row_base);
+                        // both blocks' Q in one copy (heads hA and hA + 1; when block B
+                        // is absent the second head's rows land in its unused buffer)
+                        tma_load_4d(q_s, &tm_q, b_qfull, 0, it.row_base, 0, it.hA);
                         q_loads = k + 1;
                     }
                 };
                 // the item's Q blocks into L2 now: their load waits for the
                 // previous item's last QK, and from HBM (128 rows 8 KB apart per
                 // head and atom) it would take several thousand cycles
-                if (is_k && leader && it.n_tiles > 0)
-                    for (int c = 0; c < QA; ++c) {
-                        tma_prefetch_l2_3d(&tm_q, c * (128 / ES), it.hA, it.row_base);
-                        if (it.hB >= 0) tma_prefetch_l2_3d(&tm_q, c * (128 / ES), it.hB, it.row_base);
-                    }
+                if (is_k && leader && it.n_tiles > 0) tma_prefetch_l2_4d(&tm_q, 0, it.row_base, 0, it.hA);
                 if (is_k && leader && it.n_tiles == 0) load_q();
                 ok = __shfl_sync(0xffffffffu, ok, leader_lane);
                 if (!ok) break;
@@ -1286,12 +1278,15 @@ static int prefill_impl(const void *q, int64_t total_q, const void *k_cache,
     CUtensorMap tq, tk, tv;
     int k5 = 0, k5_ratio = 0;
     {
-        uint64_t dims[3] = {static_cast<uint64_t>(d_qk), static_cast<uint64_t>(num_qo_heads),
-                            static_cast<uint64_t>(total_q)};
-        uint64_t strides[2] = {static_cast<uint64_t>(d_qk) * es,
-                               static_cast<uint64_t>(num_qo_heads) * d_qk * es};
-        uint32_t box[3] = {static_cast<uint32_t>(128 / es), 1, static_cast<uint32_t>(kPfRows)};
-        if (!encode_tmap(&tq, q, tdt, 3, dims, strides, box)) return PKV_ERR_CUDA;
+        // (128-byte atom elements, token rows, atoms, qo heads): one box is the
+        // two heads' Q blocks, [head][atom][row][128 B]
+        uint64_t dims[4] = {static_cast<uint64_t>(128 / es), static_cast<uint64_t>(total_q > 0 ? total_q : 1),
+                            static_cast<uint64_t>(d_qk * es / 128), static_cast<uint64_t>(num_qo_heads)};
+        uint64_t strides[3] = {static_cast<uint64_t>(num_qo_heads) * d_qk * es, 128,
+                               static_cast<uint64_t>(d_qk) * es};
+        uint32_t box[4] = {static_cast<uint32_t>(128 / es), static_cast<uint32_t>(kPfRows),
+                           static_cast<uint32_t>(d_qk * es / 128), 2};
+        if (!encode_tmap(&tq, q, tdt, 4, dims, strides, box)) return PKV_ERR_CUDA;
     }
     if (f8d) {
         if (contiguous || !cache_tmap(&tk, k_cache, tdt, layout, d_qk, page_size, num_kv_heads, k_page_stride,
